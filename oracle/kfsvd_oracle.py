@@ -1,0 +1,278 @@
+"""fp64 CPU oracle for curvature-whitened truncated SVD with global rank allocation.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or execute
+this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it.  It shares no code with the CUDA library; the only thing both sides
+use is the seeded input generator in ``synth`` (which holds no method arithmetic).
+
+Every function is a plain, slow, directly checkable statement of what the pages define,
+in float64 (numpy/LAPACK routines serve as textbook steps).  Sources:
+
+  [LASER]   "LASER: Loss-Aware Singular-value Decomposition and Rank Allocation for
+            Efficient Low-Precision Vision-Language Models", technical summary,
+            Methodology 1 (K-FAC surrogate, curvature-weighted transformation,
+            quantisation-aware whitening) and 2 (global greedy rank allocation).
+  [UniRank] "UniRank: Unified Rank Allocation for Low-Rank LLM Compression",
+            section 2.1 (sort all scores descending, accumulate the m+n cost of each kept
+            singular pair until the parameter budget is reached).
+  [Swift]   "Swift-SVD: Theoretical Optimality Meets Practical Efficiency in Low-Rank LLM
+            Compression", section 2A (closed form W_k = W V_k V_k^T; incremental
+            covariance aggregation; one eigendecomposition of the aggregated covariance).
+
+Readings where the pages are silent (all listed in the design doc): W is d_in x d_out (y = x W);
+X = A^T A / N and G = Gr^T Gr / N uncentred, each damped by lam * mean(diag); the
+Cholesky factors are S_x = chol_lower(X)^T and S_g = chol_lower(G), which is the choice
+that makes ||S_x dW S_g||_F^2 equal the K-FAC form with column-major vec; the score of a
+component is half its squared whitened singular value; the greedy cut keeps the longest
+prefix of the sorted list whose cumulative cost stays within the budget.
+
+Parity status: every function here is pinned by tests/test_oracle_pins.py against
+closed forms, the pages' identities, brute force or hand-worked values; none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, List, Optional, Sequence
+
+import numpy as np
+import scipy.linalg as sla
+
+KEY_HALF_SIGMA2 = "half_sigma2"
+KEY_PER_PARAM = "per_param"
+FIXED_RANK = "fixed_rank"
+
+
+# --------------------------------------------------------------- step 1: covariances
+def covariance_sum(A: np.ndarray) -> np.ndarray:
+    """Running second-moment sum A^T A of a block of calibration rows (tokens x channels).
+
+    [Swift] 2A, incremental aggregation: the covariance is a sum over tokens of outer
+    products, so it can be accumulated batch by batch.
+    """
+    A = np.asarray(A, dtype=np.float64)
+    return A.T @ A
+
+
+def finalize_covariance(S: np.ndarray, n_tokens: int, lam: float) -> np.ndarray:
+    """X = S / N, then X + lam * mean(diag(X)) * I.  [LASER] 1: covariance over the
+    calibration set; normalisation and damping follow the statement of the hot path."""
+    C = np.asarray(S, dtype=np.float64) / float(n_tokens)
+    return C + lam * np.mean(np.diag(C)) * np.eye(C.shape[0])
+
+
+def fake_quant_int8_token(A: np.ndarray) -> np.ndarray:
+    """Quantisation-aware whitening input: per-token symmetric INT8 fake quantisation.
+
+    [LASER] 1 (QAW): the K-FAC factors are estimated from quantised calibration
+    activations.  The page gives no quantiser; this is the plain symmetric per-row one:
+    scale s_t = max_j |A_tj| / 127, code q = clamp(rint(A_tj / s_t), -127, 127) with
+    round-half-even, output s_t * q rounded to bfloat16 (a zero row stays zero).  The
+    scale and the code decide integers, so this step runs in float32 exactly as the
+    kernel does (IEEE division and multiplication), not in float64.
+    """
+    A = np.asarray(A, dtype=np.float32)
+    amax = np.max(np.abs(A), axis=1, keepdims=True).astype(np.float32)
+    s = (amax / np.float32(127.0)).astype(np.float32)
+    safe = np.where(s > 0, s, np.float32(1.0)).astype(np.float32)
+    q = np.clip(np.rint((A / safe).astype(np.float32)), -127, 127).astype(np.float32)
+    y = (s * q).astype(np.float32)
+    y = np.where(s > 0, y, np.float32(0.0)).astype(np.float32)
+    u = y.view(np.uint32)
+    with np.errstate(over="ignore"):
+        r = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return (r.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# -------------------------------------------------------------- step 2: factors
+def cholesky_factors(X: np.ndarray, G: np.ndarray):
+    """S_x = chol_lower(X)^T (upper), S_g = chol_lower(G) (lower).  [LASER] 1: S_x, S_g
+    are Cholesky factors of X and G; this orientation gives S_x^T S_x = X, S_g S_g^T = G."""
+    Lx = np.linalg.cholesky(np.asarray(X, dtype=np.float64))
+    Lg = np.linalg.cholesky(np.asarray(G, dtype=np.float64))
+    return Lx.T.copy(), Lg
+
+
+# --------------------------------------------------------------- step 3: whitening
+def whiten(W: np.ndarray, Sx: np.ndarray, Sg: np.ndarray) -> np.ndarray:
+    """[LASER] 1: curvature-weighted weight W~ = S_x W S_g."""
+    return Sx @ np.asarray(W, dtype=np.float64) @ Sg
+
+
+# ------------------------------------------------------------- step 4: spectrum
+def whitened_svd(Wt: np.ndarray):
+    """[LASER] 1: SVD of W~ (LAPACK gesdd).  Returns (U~, sigma descending, V~)."""
+    U, s, Vt = np.linalg.svd(Wt, full_matrices=False)
+    return U, s, Vt.T
+
+
+def gram_eigenvalues(Wt: np.ndarray) -> np.ndarray:
+    """[Swift] 2A: one eigendecomposition of the Gram matrix of the smaller side."""
+    m, n = Wt.shape
+    C = Wt.T @ Wt if n <= m else Wt @ Wt.T
+    w = np.linalg.eigh(C)[0]
+    return np.sort(w)[::-1]
+
+
+# ----------------------------------------------------------- step 5: allocation
+def component_scores(sigma: np.ndarray, cost: int, mode: str, precision: str):
+    """Score of each component: half its squared whitened singular value (the K-FAC
+    estimate of the loss increase when it is dropped, [LASER] 1), or that divided by the
+    m+n parameters the pair costs ([LASER] 2, "score per parameter cost").
+
+    ``precision="f32"`` evaluates 0.5 * (sigma * sigma) [/ cost] in float32 with one
+    rounding per operation, the order the GPU uses, so that both sides rank identical
+    float32 sigma identically.
+    """
+    if precision == "f32":
+        s = np.asarray(sigma, dtype=np.float32)
+        sc = (np.float32(0.5) * (s * s)).astype(np.float32)
+        if mode == KEY_PER_PARAM:
+            sc = (sc / np.float32(cost)).astype(np.float32)
+        return sc
+    s = np.asarray(sigma, dtype=np.float64)
+    sc = 0.5 * s * s
+    if mode == KEY_PER_PARAM:
+        sc = sc / float(cost)
+    return sc
+
+
+@dataclass
+class Allocation:
+    ranks: np.ndarray          # int64 per unit
+    cut_score: float           # score of the last kept component (nan if none kept)
+    next_score: float          # score of the first dropped component (nan if none)
+    used: int                  # parameters used by the kept components
+    order_unit: np.ndarray     # sorted list: unit of each component
+    order_comp: np.ndarray     # sorted list: index of each component inside its unit
+    order_score: np.ndarray
+
+
+def allocate(sigmas: Sequence[np.ndarray], costs: Sequence[int], budget: int,
+             mode: str = KEY_HALF_SIGMA2, fixed_ranks: Optional[Sequence[int]] = None,
+             precision: str = "f64") -> Allocation:
+    """Global sort-and-truncate rank allocation.
+
+    [UniRank] 2.1 and [LASER] 2: pool the scores of every component of every unit, sort
+    them descending (ties: lower unit index first, then lower component index), walk the
+    list accumulating each component's parameter cost m+n, and keep the longest prefix
+    whose cumulative cost does not exceed the budget.  The rank of a unit is the number
+    of its components in that prefix.
+    """
+    n_units = len(sigmas)
+    if mode == FIXED_RANK:
+        ranks = np.array([min(int(fixed_ranks[u]), len(sigmas[u])) for u in range(n_units)])
+        used = int(sum(int(ranks[u]) * int(costs[u]) for u in range(n_units)))
+        e = np.zeros(0, dtype=np.int64)
+        return Allocation(ranks, float("nan"), float("nan"), used, e, e, np.zeros(0))
+    units, comps, scores = [], [], []
+    for u, s in enumerate(sigmas):
+        sc = component_scores(s, costs[u], mode, precision)
+        units.append(np.full(len(sc), u, dtype=np.int64))
+        comps.append(np.arange(len(sc), dtype=np.int64))
+        scores.append(sc.astype(np.float64))
+    units = np.concatenate(units)
+    comps = np.concatenate(comps)
+    scores = np.concatenate(scores)
+    order = np.lexsort((comps, units, -scores))
+    cost_sorted = np.asarray(costs, dtype=np.int64)[units[order]]
+    prefix = np.cumsum(cost_sorted)
+    n_keep = int(np.searchsorted(prefix, budget, side="right"))
+    ranks = np.bincount(units[order[:n_keep]], minlength=n_units).astype(np.int64)
+    cut = float(scores[order[n_keep - 1]]) if n_keep > 0 else float("nan")
+    nxt = float(scores[order[n_keep]]) if n_keep < len(order) else float("nan")
+    used = int(prefix[n_keep - 1]) if n_keep > 0 else 0
+    return Allocation(ranks, cut, nxt, used, units[order], comps[order], scores[order])
+
+
+# --------------------------------------------------------- step 5: map back
+def unwhiten(Sx: np.ndarray, Sg: np.ndarray, Ut: np.ndarray, sigma: np.ndarray,
+             Vt: np.ndarray, r: int):
+    """[LASER] 1: map the rank-r factors of W~ back to the original space:
+    U = S_x^-1 U~_r Sigma_r (d_in x r) and V = V~_r^T S_g^-1 (r x d_out), by triangular
+    solves (S_x upper, S_g lower)."""
+    B = Ut[:, :r] * sigma[:r][None, :]
+    U = sla.solve_triangular(Sx, B, lower=False)
+    V = sla.solve_triangular(Sg.T, Vt[:, :r], lower=False).T
+    return U, V
+
+
+# --------------------------------------------------------------- the objective
+def kfac_quadratic(dW: np.ndarray, X: np.ndarray, G: np.ndarray) -> float:
+    """[LASER] 1, K-FAC surrogate: 1/2 vec(dW)^T (G kron X) vec(dW), built explicitly
+    (tiny shapes only), vec stacking the columns of dW (d_in x d_out)."""
+    v = np.asarray(dW, dtype=np.float64).reshape(-1, order="F")
+    K = np.kron(np.asarray(G, dtype=np.float64), np.asarray(X, dtype=np.float64))
+    return 0.5 * float(v @ K @ v)
+
+
+def whitened_error(W: np.ndarray, U: np.ndarray, V: np.ndarray, Sx: np.ndarray,
+                   Sg: np.ndarray) -> float:
+    """||S_x (W - U V) S_g||_F^2, twice the K-FAC loss estimate of replacing W by U V."""
+    D = Sx @ (np.asarray(W, dtype=np.float64) - np.asarray(U, np.float64) @ np.asarray(V, np.float64)) @ Sg
+    return float(np.sum(D * D))
+
+
+# ------------------------------------------------------------ whole workloads
+@dataclass
+class UnitResult:
+    name: str
+    m: int
+    n: int
+    X: np.ndarray
+    G: np.ndarray
+    Sx: np.ndarray
+    Sg: np.ndarray
+    Wt: np.ndarray
+    U_t: np.ndarray
+    sigma: np.ndarray
+    V_t: np.ndarray
+    rank: int = 0
+    U: Optional[np.ndarray] = None
+    V: Optional[np.ndarray] = None
+
+
+def site_covariance_sum(wl, site, chunk: int = 8192) -> np.ndarray:
+    """Sum of A^T A over all calibration tokens of one site, streamed in token chunks."""
+    from synth import recipes
+    S = np.zeros((site.d, site.d), dtype=np.float64)
+    for t0 in range(0, wl.n_tokens, chunk):
+        A = recipes.gen_stream(wl, site, t0, min(wl.n_tokens, t0 + chunk))
+        if wl.quant == "int8_token" and site.kind == "act":
+            A = fake_quant_int8_token(A)
+        S += covariance_sum(A)
+    return S
+
+
+def compress_workload(wl, units: Optional[List[int]] = None) -> Dict:
+    """Runs the whole path on a synthetic workload: covariances of every site, factors,
+    whitening and SVD of every unit, global allocation (or fixed rank), factors U, V."""
+    from synth import recipes
+    idx = list(range(len(wl.units))) if units is None else list(units)
+    covs: Dict[str, np.ndarray] = {}
+
+    def cov(name):
+        if name not in covs:
+            covs[name] = finalize_covariance(site_covariance_sum(wl, wl.sites[name]),
+                                             wl.n_tokens, wl.lam)
+        return covs[name]
+
+    res: List[UnitResult] = []
+    for i in idx:
+        u = wl.units[i]
+        X, G = cov(u.x_site), cov(u.g_site)
+        Sx, Sg = cholesky_factors(X, G)
+        W = recipes.gen_weight(wl, u).astype(np.float64)
+        Wt = whiten(W, Sx, Sg)
+        Ut, s, Vt = whitened_svd(Wt)
+        res.append(UnitResult(u.name, u.m, u.n, X, G, Sx, Sg, Wt, Ut, s, Vt))
+    costs = [r.m + r.n for r in res]
+    if wl.fixed_rank is not None:
+        alloc = allocate([r.sigma for r in res], costs, 0, FIXED_RANK,
+                         [wl.fixed_rank] * len(res))
+    else:
+        alloc = allocate([r.sigma for r in res], costs, wl.budget)
+    for r, k in zip(res, alloc.ranks):
+        r.rank = int(k)
+        r.U, r.V = unwhiten(r.Sx, r.Sg, r.U_t, r.sigma, r.V_t, r.rank)
+    return {"units": res, "alloc": alloc, "covs": covs}

@@ -1,0 +1,271 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix (CPU only).
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a transposed
+factor, the wrong vec order, a wrong damping or normalisation, a wrong cut rule) fails.
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(20260602)
+
+
+def _tiny_problem(m=5, n=7, N=50, lam=1e-2, seed=0):
+    r = np.random.default_rng(seed)
+    A = r.standard_normal((N, m)) * (1.0 / np.sqrt(np.arange(1, m + 1)))
+    Gr = r.standard_normal((N, n)) * 1e-3
+    W = r.standard_normal((m, n)) * 0.02
+    X = O.finalize_covariance(O.covariance_sum(A), N, lam)
+    G = O.finalize_covariance(O.covariance_sum(Gr), N, lam)
+    return A, Gr, W, X, G
+
+
+def test_covariance_hand_values():
+    g = json.load(open(os.path.join(GOLD, "cov_hand.json")))
+    A = np.array(g["A"], dtype=np.float64)
+    np.testing.assert_array_equal(O.covariance_sum(A), np.array(g["sum"]))
+    np.testing.assert_allclose(O.finalize_covariance(O.covariance_sum(A), A.shape[0], g["lam"]),
+                               np.array(g["X"]), rtol=0, atol=1e-14)
+
+
+def test_covariance_is_streamable():
+    """Swift-SVD 2A: aggregating batch by batch equals one pass over all tokens."""
+    A = rng.standard_normal((97, 6))
+    S = O.covariance_sum(A[:40]) + O.covariance_sum(A[40:71]) + O.covariance_sum(A[71:])
+    brute = np.zeros((6, 6))
+    for t in range(A.shape[0]):
+        brute += np.outer(A[t], A[t])
+    np.testing.assert_allclose(S, brute, rtol=1e-13)
+
+
+def test_cholesky_reconstruction_and_orientation():
+    _, _, _, X, G = _tiny_problem(m=9, n=11)
+    Sx, Sg = O.cholesky_factors(X, G)
+    assert np.allclose(np.tril(Sx, -1), 0) and np.all(np.diag(Sx) > 0)   # upper
+    assert np.allclose(np.triu(Sg, 1), 0) and np.all(np.diag(Sg) > 0)    # lower
+    assert np.linalg.norm(Sx.T @ Sx - X) / np.linalg.norm(X) <= 1e-13
+    assert np.linalg.norm(Sg @ Sg.T - G) / np.linalg.norm(G) <= 1e-13
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_kronecker_identity(seed):
+    """LASER 1: 1/2 vec(dW)^T (G kron X) vec(dW) (explicit Kronecker, column-major vec)
+    equals 1/2 ||S_x dW S_g||_F^2 for the oracle's factors and whitening."""
+    _, _, W, X, G = _tiny_problem(seed=seed)
+    Sx, Sg = O.cholesky_factors(X, G)
+    for dW in (rng.standard_normal(W.shape), W):
+        lhs = O.kfac_quadratic(dW, X, G)
+        rhs = 0.5 * np.sum(O.whiten(dW, Sx, Sg) ** 2)
+        assert abs(lhs - rhs) <= 1e-12 * abs(lhs)
+
+
+@pytest.mark.parametrize("r", [0, 1, 3, 5])
+def test_truncation_loss_equals_discarded_spectrum(r):
+    """The K-FAC loss of W - U V equals half the sum of the discarded sigma^2 (LASER 1:
+    truncating the smallest components gives the smallest estimated loss increase), and
+    Swift-SVD's stability claim: the achieved loss is the theoretical minimum."""
+    _, _, W, X, G = _tiny_problem(seed=7)
+    Sx, Sg = O.cholesky_factors(X, G)
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, r)
+    assert U.shape == (W.shape[0], r) and V.shape == (r, W.shape[1])
+    dl = O.kfac_quadratic(W - U @ V, X, G)
+    scale = 0.5 * np.sum(s ** 2)          # full energy: the reference size for rounding
+    assert abs(dl - 0.5 * np.sum(s[r:] ** 2)) <= 1e-10 * scale
+    assert abs(O.whitened_error(W, U, V, Sx, Sg) - 2 * dl) <= 1e-10 * scale
+
+
+def test_eckart_young_beats_random_factorisations():
+    _, _, W, X, G = _tiny_problem(m=6, n=8, seed=3)
+    Sx, Sg = O.cholesky_factors(X, G)
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    for r in (1, 2, 4):
+        U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, r)
+        e_opt = O.whitened_error(W, U, V, Sx, Sg)
+        for k in range(1000):
+            if k % 2 == 0:
+                P, Q = rng.standard_normal((6, r)) * 0.03, rng.standard_normal((r, 8))
+            else:
+                eps = 10.0 ** rng.uniform(-6, -1)
+                P = U + eps * rng.standard_normal(U.shape) * np.abs(U).max()
+                Q = V + eps * rng.standard_normal(V.shape) * np.abs(V).max()
+            assert O.whitened_error(W, P, Q, Sx, Sg) >= e_opt * (1 - 1e-12)
+
+
+def test_swift_svd_closed_form_special_case():
+    """Swift-SVD 2A: with G = I and no damping, the optimum of ||A W - A W_k|| is
+    W_k = W V_k V_k^T with V_k the top right singular vectors of Y = A W, and the
+    whitened spectrum is the spectrum of A W / sqrt(N)."""
+    N, m, n = 200, 12, 9
+    A = rng.standard_normal((N, m)) * np.linspace(2.0, 0.2, m)
+    W = rng.standard_normal((m, n))
+    X = O.finalize_covariance(O.covariance_sum(A), N, 0.0)
+    G = np.eye(n)
+    Sx, Sg = O.cholesky_factors(X, G)
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    sy = np.linalg.svd(A @ W, compute_uv=False)
+    np.testing.assert_allclose(s * s * N, sy * sy, rtol=1e-10)
+    _, _, VyT = np.linalg.svd(A @ W)
+    for k in (1, 3, 6):
+        U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, k)
+        Vk = VyT[:k].T
+        np.testing.assert_allclose(U @ V, W @ Vk @ Vk.T, atol=1e-10)
+
+
+def test_identity_covariances_give_textbook_truncation():
+    """X = G = I: the method is the plain truncated SVD of W (built from a known SVD)."""
+    m, n = 10, 7
+    P = np.linalg.qr(rng.standard_normal((m, m)))[0][:, :n]
+    Q = np.linalg.qr(rng.standard_normal((n, n)))[0]
+    d = np.array([9.0, 7.5, 5.0, 2.0, 1.0, 0.5, 0.25])
+    W = P @ np.diag(d) @ Q.T
+    Sx, Sg = O.cholesky_factors(np.eye(m), np.eye(n))
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    np.testing.assert_allclose(s, d, rtol=1e-13)
+    for r in (1, 3, 7):
+        U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, r)
+        np.testing.assert_allclose(U @ V, P[:, :r] @ np.diag(d[:r]) @ Q[:, :r].T, atol=1e-12)
+
+
+def test_diagonal_covariances_closed_form():
+    """Diagonal X, G and a diagonal W: W~ = sqrt(x) W sqrt(g) entry by entry, so the
+    whitened singular values are |sqrt(x_i) w_i sqrt(g_i)| sorted."""
+    x = np.array([4.0, 1.0, 9.0, 0.25])
+    g = np.array([1.0, 16.0, 0.5, 2.0])
+    w = np.array([0.5, -1.0, 0.1, 3.0])
+    Sx, Sg = O.cholesky_factors(np.diag(x), np.diag(g))
+    Wt = O.whiten(np.diag(w), Sx, Sg)
+    np.testing.assert_allclose(Wt, np.diag(np.sqrt(x) * w * np.sqrt(g)), atol=1e-15)
+    s = O.whitened_svd(Wt)[1]
+    np.testing.assert_allclose(s, np.sort(np.abs(np.sqrt(x) * w * np.sqrt(g)))[::-1], rtol=1e-14)
+
+
+def test_gram_route_equals_svd_route():
+    for shape in ((13, 7), (7, 13), (9, 9)):
+        Wt = rng.standard_normal(shape)
+        s = np.linalg.svd(Wt, compute_uv=False)
+        lam = O.gram_eigenvalues(Wt)
+        np.testing.assert_allclose(lam, s * s, rtol=1e-10, atol=1e-12)
+
+
+def test_full_rank_roundtrip():
+    _, _, W, X, G = _tiny_problem(m=6, n=4, seed=11)
+    Sx, Sg = O.cholesky_factors(X, G)
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, 4)
+    np.testing.assert_allclose(U @ V, W, atol=1e-12)
+
+
+# ------------------------------------------------------------------ allocation
+def test_allocation_hand_cases():
+    g = json.load(open(os.path.join(GOLD, "alloc_hand.json")))
+    for c in g["cases"]:
+        sig = [np.array(s, dtype=np.float64) for s in c["sigmas"]]
+        costs = [a + b for a, b in c["mn"]]
+        for prec in ("f64", "f32"):
+            al = O.allocate(sig, costs, c["budget"], c["mode"], precision=prec)
+            assert list(al.ranks) == c["ranks"], c
+            assert al.used == c["used"]
+            for got, want in ((al.cut_score, c["cut"]), (al.next_score, c["next"])):
+                if want is None:
+                    assert np.isnan(got)
+                else:
+                    assert got == want
+
+
+def _walk(sigmas, costs, budget, mode):
+    """Independent pure-Python statement of the sort-and-truncate walk."""
+    items = []
+    for u, s in enumerate(sigmas):
+        for i, v in enumerate(s):
+            sc = 0.5 * float(v) * float(v)
+            if mode == O.KEY_PER_PARAM:
+                sc /= costs[u]
+            items.append((-sc, u, i))
+    items.sort()
+    ranks = [0] * len(sigmas)
+    spent = 0
+    for _, u, _ in items:
+        if spent + costs[u] > budget:
+            break
+        spent += costs[u]
+        ranks[u] += 1
+    return ranks, spent
+
+
+@pytest.mark.parametrize("trial", range(40))
+def test_allocation_brute_force_and_invariants(trial):
+    r = np.random.default_rng(trial)
+    n_units = int(r.integers(1, 5))
+    sig = [np.sort(r.uniform(0, 3, size=int(r.integers(1, 7))))[::-1] for _ in range(n_units)]
+    if trial % 5 == 0:  # exact ties across units
+        sig = [np.round(s, 1) for s in sig]
+    costs = [int(r.integers(2, 12)) for _ in range(n_units)]
+    total = sum(len(s) * c for s, c in zip(sig, costs))
+    budget = int(r.integers(0, total + 3))
+    for mode in (O.KEY_HALF_SIGMA2, O.KEY_PER_PARAM):
+        al = O.allocate(sig, costs, budget, mode)
+        ranks, spent = _walk(sig, costs, budget, mode)
+        assert list(al.ranks) == ranks and al.used == spent
+        assert spent <= budget
+        kept = sum(al.ranks)
+        if kept < sum(len(s) for s in sig):   # the next sorted item would overflow
+            assert spent + costs[int(al.order_unit[kept])] > budget
+        if mode == O.KEY_HALF_SIGMA2:
+            dropped = sum(0.5 * np.sum(s[k:] ** 2) for s, k in zip(sig, al.ranks))
+            assert abs(dropped - float(np.sum(al.order_score[kept:]))) <= 1e-12 * (1 + dropped)
+    # information only: the greedy prefix never needs to beat the knapsack optimum
+    best = 0.0
+    for choice in itertools.product(*[range(len(s) + 1) for s in sig]):
+        if sum(k * c for k, c in zip(choice, costs)) <= budget:
+            best = max(best, sum(0.5 * np.sum(s[:k] ** 2) for s, k in zip(sig, choice)))
+    al = O.allocate(sig, costs, budget, O.KEY_HALF_SIGMA2)
+    greedy = sum(0.5 * np.sum(s[:k] ** 2) for s, k in zip(sig, al.ranks))
+    assert greedy <= best + 1e-12
+
+
+def test_allocation_sum_of_dropped_scores_is_kfac_loss():
+    """Across units, the dropped scores add up to the K-FAC loss of the truncation."""
+    total_dl, total_dropped = 0.0, 0.0
+    res = []
+    for seed in range(3):
+        _, _, W, X, G = _tiny_problem(m=4 + seed, n=6 - seed, seed=seed + 20)
+        Sx, Sg = O.cholesky_factors(X, G)
+        Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+        res.append((W, X, G, Sx, Sg, Ut, s, Vt))
+    costs = [W.shape[0] + W.shape[1] for W, *_ in res]
+    al = O.allocate([t[6] for t in res], costs, 25)
+    for (W, X, G, Sx, Sg, Ut, s, Vt), k in zip(res, al.ranks):
+        U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, int(k))
+        total_dl += O.kfac_quadratic(W - U @ V, X, G)
+    total_dropped = float(np.sum(al.order_score[int(np.sum(al.ranks)):]))
+    assert abs(total_dl - total_dropped) <= 1e-10 * total_dl
+
+
+def test_fixed_rank_mode():
+    al = O.allocate([np.ones(5), np.ones(3)], [10, 10], 0, O.FIXED_RANK, [4, 4])
+    assert list(al.ranks) == [4, 3]
+
+
+# ------------------------------------------------------------------------- QAW
+def test_fake_quant_hand_rows():
+    g = json.load(open(os.path.join(GOLD, "qaw_hand.json")))
+    out = O.fake_quant_int8_token(np.array(g["rows_in"], dtype=np.float32))
+    np.testing.assert_array_equal(out, np.array(g["rows_out"], dtype=np.float32))
+
+
+def test_fake_quant_properties():
+    A = (rng.standard_normal((64, 33)) * rng.uniform(0.01, 50, size=(64, 1))).astype(np.float32)
+    Q = O.fake_quant_int8_token(A)
+    s = np.abs(A).max(axis=1) / 127.0
+    assert np.all(np.abs(Q - A) <= 0.5 * s[:, None] * 1.01 + np.abs(A) * 2 ** -8)
+    # at most 255 levels per row, symmetric grid
+    for row, sc in zip(Q, s):
+        lv = np.unique(np.round(row / sc))
+        assert lv.min() >= -127 and lv.max() <= 127
