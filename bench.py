@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Benchmark: one Llama-7B-shaped decoder block (q, k, v, o 4096x4096; gate, up 4096x11008;
+down 11008x4096; bf16), 131072 calibration tokens per site, compressed to 50% of the
+block's parameters under global allocation.  One step = the whole path over one batch:
+K-FAC factors of the 11 calibration sites (tcgen05 SYRK), Cholesky factors and whitening of
+the 7 weights, their spectra (Gram + blocked Jacobi), global sort-and-truncate allocation,
+and the rank-r factors U, V.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kfsvd|reference]
+
+Prints one JSON line.  `value` is calibration tokens per second through the whole step with
+inputs resident in HBM (17.2 GB of synthetic bf16 rows, larger than L2, so no L2 flush is
+needed between steps); `e2e` is the same metric when every step also copies its inputs
+from pinned host memory and reads the factors back.  --impl reference times the fp64 CPU
+oracle on a bounded sample of the same workload.  Under torchrun each rank runs its own
+replica of the workload (the path has no data exchange): scaling is weak, value sums ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "calib tokens/s into K-FAC covariances; whitened-SVD layers/s; % bf16/HBM roof"
+WORKLOAD = "llama7b_block: q,k,v,o 4096x4096, gate,up 4096x11008, down 11008x4096 bf16; N=131072; rho=0.5 global"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kfsvd", choices=["kfsvd", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join(tempfile.gettempdir(), "kfsvd_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        reasons = set()
+        for r in rows:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[2:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------- workload
+def cost_tail(m, n):
+    s = min(m, n)
+    return m * n * s + (m ** 3 + n ** 3) / 3.0 + m * m * n + m * n * n
+
+
+def syrk_flops(n_tokens, d):
+    return 2.0 * n_tokens * d * (d + 1) / 2.0
+
+
+def run_kfsvd(args):
+    import torch
+    import torch.distributed as dist
+
+    from synth import device as sdev, recipes
+    from vlm_compression_fac_b300 import kfsvd as K, pipeline
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    wl = recipes.llama7b_block()
+    ctx = K.Context(local)
+    K.kf_svd_profile_enable(ctx, True)
+    units = [pipeline.UnitSpec(u.name, u.m, u.n, u.x_site, u.g_site) for u in wl.units]
+    acts = {n: sdev.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
+    grads = {n: sdev.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
+    weights = {u.name: sdev.weight_on_device(wl, u, torch) for u in wl.units}
+    torch.cuda.synchronize()
+    in_bytes = sum(t.numel() * t.element_size() for t in list(acts.values()) + list(grads.values()))
+    w_bytes = sum(t.numel() * t.element_size() for t in weights.values())
+
+    stream = torch.cuda.current_stream()
+    rec = []
+
+    def mark(tag):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        rec.append((tag, e))
+
+    def one_step(a, g, w):
+        return pipeline.compress(ctx, units, w, a, g, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                                 sync_timer=mark)
+
+    for _ in range(args.warmup):
+        rec.clear()
+        res = one_step(acts, grads, weights)
+    ctx.sync_status()
+    torch.cuda.synchronize()
+
+    # ---------------- timed region (device-resident inputs)
+    phases = {k: 0.0 for k in ("kfac", "whiten", "svd", "allocate", "unwhiten")}
+    syrk_ms, jac_ms, jac_flops, svd_prof = 0.0, 0.0, 0.0, None
+    n_syrk = 0
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    l0 = K.kf_launch_count()
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    per_step_marks = []
+    for _ in range(args.steps):
+        rec.clear()
+        mark("start")
+        res = one_step(acts, grads, weights)
+        per_step_marks.append(list(rec))
+        p = K.kf_svd_profile_read(ctx)
+        jac_ms += p["jacobi_ms"]
+        jac_flops += p["jacobi_apply_flops"]
+        svd_prof = p
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = K.kf_launch_count() - l0
+    ctx.sync_status()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    for marks in per_step_marks:
+        prev = marks[0][1]
+        open_syrk = None
+        for tag, e in marks[1:]:
+            if tag == "syrk<":
+                open_syrk = e
+                continue
+            if tag == "syrk>":
+                syrk_ms += open_syrk.elapsed_time(e)
+                n_syrk += 1
+                continue
+            phases[tag] += prev.elapsed_time(e)
+            prev = e
+    K_ = args.steps
+    ms_step = total_ms / K_
+    tokens = wl.n_tokens * world
+    value = tokens / (ms_step / 1e3)
+
+    # ---------------- end to end through host buffers
+    e2e = None
+    if not args.no_e2e:
+        h_acts = {k: v.cpu().pin_memory() for k, v in acts.items()}
+        h_grads = {k: v.cpu().pin_memory() for k, v in grads.items()}
+        h_w = {k: v.cpu().pin_memory() for k, v in weights.items()}
+        torch.cuda.synchronize()
+        out_bytes = 0
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K_):
+            a = {k: v.to("cuda", non_blocking=True) for k, v in h_acts.items()}
+            g = {k: v.to("cuda", non_blocking=True) for k, v in h_grads.items()}
+            w = {k: v.to("cuda", non_blocking=True) for k, v in h_w.items()}
+            r = pipeline.compress(ctx, units, w, a, g, wl.n_tokens, lam=wl.lam, budget=wl.budget)
+            outs = [u.U.cpu() for u in r.units] + [u.V.cpu() for u in r.units] + [r.ranks.cpu()]
+            out_bytes = sum(o.numel() * o.element_size() for o in outs)
+            del a, g, w, r
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device="cuda")
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = float(tt.item())
+        e2e = {"value": tokens / (e2e_ms / K_ / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": in_bytes + w_bytes,
+               "d2h_bytes_per_step": out_bytes}
+        del h_acts, h_grads, h_w
+
+    # ---------------- roofline of the dominant kernel
+    pk = peaks() or {}
+    bf16_peak = pk.get("bf16_tflops_sustained", 1400.0)
+    sm_max = (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2032.0)
+    fp32_peak = 148 * 128 * 2 * sm_max * 1e6 / 1e12
+    sites = list(acts.values()) + list(grads.values())
+    syrk_total_flops = sum(syrk_flops(wl.n_tokens, t.shape[1]) for t in sites) * K_
+    syrk_tf = syrk_total_flops / (syrk_ms / 1e3) / 1e12 if syrk_ms > 0 else 0.0
+    jac_tf = jac_flops / (jac_ms / 1e3) / 1e12 if jac_ms > 0 else 0.0
+    kern = {
+        "syrk_tcgen05": {"bound": "tensor", "achieved": round(syrk_tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": round(syrk_tf / bf16_peak, 4), "ms_per_step": round(syrk_ms / K_, 3),
+                         "launches_per_step": n_syrk // K_, "peak_kind": "bf16 sustained, of measured"},
+        "jacobi_solve_apply": {"bound": "alu", "achieved": round(jac_tf, 2), "peak": round(fp32_peak, 1),
+                               "unit": "TFLOP/s", "frac": round(jac_tf / fp32_peak, 4),
+                               "ms_per_step": round(jac_ms / K_, 3),
+                               "peak_kind": "FP32 FFMA 148 SM x 128 lanes x 2 x max SM clock (derived)"},
+    }
+    dom = "syrk_tcgen05" if syrk_ms >= jac_ms else "jacobi_solve_apply"
+    roof = dict(kern[dom])
+    roof["kernel"] = dom
+    roof["traffic"] = None
+
+    # ---------------- CPU baseline (oracle on a bounded sample), rank 0 only at N=1
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = oracle_sample(wl, sample_tokens=1024)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K_,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox; see DESIGN.md)",
+        "config": {"workload": WORKLOAD, "global_batch": wl.n_tokens * world, "seq_len": wl.n_tokens,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs (%.1f GB) larger than L2; no flush" % (in_bytes / 1e9)},
+        "layers_per_s": round(len(units) * world / ((phases["whiten"] + phases["svd"]) / K_ / 1e3), 3),
+        "kfac_tokens_per_s": round(tokens / ((phases["kfac"]) / K_ / 1e3), 1),
+        "phases_ms": {k: round(v / K_, 3) for k, v in phases.items()},
+        "svd_profile": svd_prof, "ranks": [int(x) for x in res.ranks.cpu().tolist()],
+        "roofline": roof, "kernels": kern, "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- oracle arm
+def oracle_sample(wl, sample_tokens=1024, tail_unit="q"):
+    """fp64 oracle on a bounded sample of the workload, extrapolated to one full step:
+    covariance sums of `sample_tokens` rows of every site (scaled by N / sample_tokens) plus
+    the per-unit tail (factors, whitening, SVD, factors U V) of one unit, scaled to all
+    units by m n min(m,n) + (m^3 + n^3)/3 + m^2 n + m n^2."""
+    import numpy as np
+    import oracle as O
+    from synth import recipes
+
+    cores = os.cpu_count()
+    t0 = time.perf_counter()
+    for s in wl.sites.values():
+        A = recipes.gen_stream(wl, s, 0, sample_tokens).astype(np.float64)
+        O.covariance_sum(A)
+    t_cov = time.perf_counter() - t0
+    u = [x for x in wl.units if x.name == tail_unit][0]
+    r = np.random.default_rng(0)
+    t1 = time.perf_counter()
+    Ax = recipes.gen_stream(wl, wl.sites[u.x_site], 0, 256).astype(np.float64)
+    Ag = recipes.gen_stream(wl, wl.sites[u.g_site], 0, 256).astype(np.float64)
+    t_gen = time.perf_counter() - t1
+    X = O.finalize_covariance(O.covariance_sum(Ax), 256, wl.lam)
+    G = O.finalize_covariance(O.covariance_sum(Ag), 256, wl.lam)
+    W = recipes.gen_weight(wl, u).astype(np.float64)
+    t2 = time.perf_counter()
+    Sx, Sg = O.cholesky_factors(X, G)
+    Wt = O.whiten(W, Sx, Sg)
+    Ut, s, Vt = O.whitened_svd(Wt)
+    O.unwhiten(Sx, Sg, Ut, s, Vt, min(u.m, u.n) // 2)
+    t_tail = time.perf_counter() - t2
+    scale = sum(cost_tail(x.m, x.n) for x in wl.units) / cost_tail(u.m, u.n)
+    est = t_cov * (wl.n_tokens / sample_tokens) + t_tail * scale
+    return {"value": round(wl.n_tokens / est, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "covariance sums of %d of %d tokens on all %d sites (%.1f s, scaled by N) + factor/whiten/"
+                      "SVD/unwhiten tail of unit %s (%.1f s, scaled by the tail cost model to all %d units); "
+                      "extrapolated step %.1f s" % (sample_tokens, wl.n_tokens, len(wl.sites), t_cov, tail_unit,
+                                                    t_tail, len(wl.units), est)}
+
+
+def run_reference(args):
+    rank, local, world = dist_env()
+    if rank != 0:
+        return
+    from synth import recipes
+    wl = recipes.llama7b_block()
+    for _ in range(args.warmup):
+        oracle_sample(wl, sample_tokens=64)
+    t = []
+    res = None
+    for _ in range(args.steps):
+        res = oracle_sample(wl, sample_tokens=256)
+        t.append(wl.n_tokens / res["value"])
+    ms = 1e3 * sum(t) / len(t)
+    v = wl.n_tokens / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": wl.n_tokens, "seq_len": wl.n_tokens,
+                       "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(v, 2), "unit": "tokens/s", "cores": res["cores"], "kind": "oracle",
+                             "sample": res["sample"]},
+            "e2e": {"value": round(v, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_kfsvd(a)

@@ -1,0 +1,244 @@
+/*
+ * kfsvd.h - C ABI of libkfsvd.so: curvature-whitened truncated SVD of linear layers with
+ * global rank allocation, on one NVIDIA Blackwell GPU (sm_103a).
+ *
+ * The calls follow the statement of the problem in
+ *   LASER: Loss-Aware Singular-value Decomposition and Rank Allocation for Efficient
+ *   Low-Precision Vision-Language Models (technical summary, Methodology 1 and 2),
+ *   UniRank: Unified Rank Allocation for Low-Rank LLM Compression (section 2.1), and
+ *   Swift-SVD: Theoretical Optimality Meets Practical Efficiency in Low-Rank LLM
+ *   Compression (section 2A):
+ * given a weight W (d_in x d_out, y = x W) and calibration activations A and output
+ * gradients Gr, estimate the K-FAC factors X = A^T A / N and G = Gr^T Gr / N, whiten
+ * W~ = S_x W S_g with S_x^T S_x = X and S_g S_g^T = G, take the spectrum of W~, keep the
+ * components with the largest estimated loss increase 1/2 sigma^2 under a global parameter
+ * budget (each kept pair costs d_in + d_out), and map the kept factors back:
+ * U = S_x^-1 U~_r Sigma_r, V = V~_r^T S_g^-1, so that W ~= U V.
+ *
+ * Conventions shared by every call:
+ *  - All matrix pointers are DEVICE pointers to caller-owned memory; matrices are
+ *    row-major with an explicit leading dimension in elements (ld >= columns).
+ *  - Every call is asynchronous on the caller's CUDA stream (`stream`, a cudaStream_t;
+ *    NULL is the legacy default stream).  Nothing is copied between host and device
+ *    except by kf_sync_status.
+ *  - Argument errors (null pointers, sizes, leading dimensions, alignment, workspace too
+ *    small) are detected on the host before any launch and returned synchronously; the
+ *    text is available from kf_last_error().
+ *  - Numerical failures found on the device (a Cholesky pivot <= 0, Jacobi not converged,
+ *    a device-side wait that gave up) are recorded in the context's device status word;
+ *    the first one wins.  kf_sync_status() synchronises the stream and returns it.
+ *  - Scratch memory is passed in by the caller as `workspace` / `workspace_bytes`; each
+ *    call has a *_workspace_size() query.  The library allocates nothing per call; the
+ *    context owns a few bytes of device status only.
+ *  - A context may be used by one host thread at a time.
+ */
+#ifndef KFSVD_H
+#define KFSVD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KF_API __attribute__((visibility("default")))
+#else
+#define KF_API
+#endif
+
+typedef struct CUstream_st* kf_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  KF_OK = 0,
+  KF_ERR_INVALID = 1,         /* bad argument: null pointer, size, ld, alignment, mode   */
+  KF_ERR_WORKSPACE = 2,       /* workspace_bytes smaller than the matching *_size query  */
+  KF_ERR_CUDA = 3,            /* a CUDA runtime call or kernel launch failed            */
+  KF_ERR_NOT_SPD = 4,         /* Cholesky met a pivot <= 0 or not finite (info = index)  */
+  KF_ERR_NO_CONVERGENCE = 5,  /* Jacobi did not converge within max_sweeps (info = unit) */
+  KF_ERR_TIMEOUT = 6,         /* a bounded device-side wait gave up (info = site code)   */
+  KF_ERR_UNSUPPORTED = 7      /* device is not compute capability 10.x/11.x, or size cap */
+} kf_status;
+
+typedef enum { KF_BF16 = 0, KF_F32 = 1 } kf_dtype;
+typedef enum { KF_QUANT_NONE = 0, KF_QUANT_INT8_TOKEN = 1 } kf_quant;
+typedef enum { KF_KEY_HALF_SIGMA2 = 0, KF_KEY_PER_PARAM = 1, KF_FIXED_RANK = 2 } kf_alloc_mode;
+typedef enum { KF_SIDE_RIGHT = 0, KF_SIDE_LEFT = 1 } kf_side;
+
+/* whiten() flags: reuse factors that an earlier whiten() call already wrote into the
+ * same buffers (e.g. q, k and v share the input factor S_x). */
+#define KF_REUSE_SX 1u
+#define KF_REUSE_SG 2u
+#define KF_REUSE_SINV 4u
+
+typedef struct kf_ctx kf_ctx;
+
+/* Creates a context on `device` (made current for the call).  Fails with
+ * KF_ERR_UNSUPPORTED on GPUs older than compute capability 10.0. */
+KF_API kf_status kf_create(int device, kf_ctx** out);
+KF_API void kf_destroy(kf_ctx* ctx);
+
+/* Message of the last failing call made on this host thread ("" if none). */
+KF_API const char* kf_last_error(void);
+
+/* Number of CUDA kernels this library has launched in the process so far (all contexts,
+ * all streams); differences of two readings count the launches of the calls between. */
+KF_API uint64_t kf_launch_count(void);
+
+/* Synchronises `stream`, then returns and clears the device status word.  *info (may be
+ * NULL) receives the detail: the global pivot index for KF_ERR_NOT_SPD, the unit index
+ * for KF_ERR_NO_CONVERGENCE, the wait site for KF_ERR_TIMEOUT. */
+KF_API kf_status kf_sync_status(kf_ctx* ctx, kf_stream_t stream, int32_t* info);
+
+/* Side whose Gram matrix the spectrum is taken from: KF_SIDE_RIGHT (W~^T W~, n x n) when
+ * d_out <= d_in, else KF_SIDE_LEFT (W~ W~^T, m x m). */
+KF_API kf_side kf_gram_side(int64_t m, int64_t n);
+
+/* ------------------------------------------------------------------------------------
+ * (1) kfac_accumulate - step 1: stream calibration rows into a K-FAC factor.
+ * LASER Methodology 1 (X, G are activation and gradient covariances estimated on a
+ * calibration set; quantisation-aware whitening estimates them from quantised
+ * activations); Swift-SVD 2A (the covariance is aggregated batch by batch).
+ *
+ * act:     n_tokens x d rows (one token per row), dtype KF_BF16 or KF_F32, leading
+ *          dimension ld; 16-byte aligned, ld * sizeof(dtype) a multiple of 16.
+ * quant:   KF_QUANT_INT8_TOKEN fake-quantises every row first: s = max|row| / 127,
+ *          q = clamp(rint(x / s), -127, 127), value s * q rounded to bfloat16 (float32
+ *          arithmetic, a zero row stays zero).
+ * cov_sum: d x d float32 (ldc), caller-initialised (zero before the first chunk).  The
+ *          lower triangle including the diagonal (i >= j) is incremented by
+ *          sum_t a_ti a_tj; entries above the diagonal are neither read nor written.
+ * Products of bfloat16 values are exact and accumulate in float32 on the tensor cores;
+ * float32 rows are split into two bfloat16 terms (three products: hi*hi + hi*lo + lo*hi).
+ * ---------------------------------------------------------------------------------- */
+KF_API size_t kfac_accumulate_workspace_size(kf_dtype dtype, kf_quant quant, int64_t d);
+KF_API kf_status kfac_accumulate(kf_ctx* ctx, const void* act, kf_dtype dtype, int64_t n_tokens,
+                          int64_t d, int64_t ld, kf_quant quant, float* cov_sum, int64_t ldc,
+                          void* workspace, size_t workspace_bytes, kf_stream_t stream);
+
+/* Step 1, tail: turns a finished sum into the damped factor, in place:
+ * C = sum / n_tokens (lower triangle mirrored to the full matrix), then
+ * C += lambda * mean(diag(C)) * I.  Call once per site after its last kfac_accumulate. */
+KF_API kf_status kf_finalize_covariance(kf_ctx* ctx, float* cov, int64_t ldc, int64_t d,
+                                 int64_t n_tokens, float lambda, kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (2)+(3) whiten - Cholesky factors and the curvature-weighted weight.
+ * LASER Methodology 1: W~ = S_x W S_g with S_x, S_g Cholesky factors of X and G.
+ *
+ * X:     m x m damped input factor (ldx), G: n x n damped output factor (ldg); may point
+ *        at a diagonal block of a larger factor (per-head units).
+ * W:     m x n weight (d_in x d_out), KF_BF16 or KF_F32, leading dimension ldw.
+ * Sx:    m x m out, S_x = chol_lower(X)^T (upper triangular, zeros below the diagonal).
+ * Sg:    n x n out, S_g = chol_lower(G) (lower triangular, zeros above).
+ * Sinv:  s x s out, inverse of the Gram-side factor (S_g^-1 for KF_SIDE_RIGHT, S_x^-1 for
+ *        KF_SIDE_LEFT; see kf_gram_side), needed by unwhiten().
+ * Wt:    m x n float32 out, W~ = S_x W S_g.
+ * flags: KF_REUSE_* skip recomputing a factor already present in its buffer.
+ * A pivot <= 0 sets KF_ERR_NOT_SPD on the device (raise lambda and retry).
+ * ---------------------------------------------------------------------------------- */
+KF_API size_t whiten_workspace_size(int64_t m, int64_t n);
+KF_API kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const float* G,
+                 int64_t ldg, int64_t n, const void* W, kf_dtype w_dtype, int64_t ldw,
+                 uint32_t flags, float* Sx, int64_t ldsx, float* Sg, int64_t ldsg, float* Sinv,
+                 int64_t ldsi, float* Wt, int64_t ldwt, void* workspace,
+                 size_t workspace_bytes, kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (4) whitened_svd - spectrum of W~ through its Gram matrix.
+ * LASER Methodology 1 (SVD of W~); Swift-SVD 2A (one eigendecomposition of the Gram of
+ * the aggregated output instead of repeated SVDs).
+ *
+ * Batched: all problems of one call must have the same s = min(m, n) (s <= 16384).
+ * For each problem: C = W~^T W~ (KF_SIDE_RIGHT) or W~ W~^T (KF_SIDE_LEFT) in float32;
+ * C = Q Lambda Q^T by blocked parallel cyclic Jacobi (32-wide blocks, round-robin pairing,
+ * every 64 x 64 pair problem diagonalised in shared memory) until every block pair has
+ * |c_pq| <= tol * sqrt(c_pp c_qq) (or below a float32 rounding floor); then
+ * sigma_i = ||W~ q_i|| / ||q_i|| (Rayleigh quotient evaluated on W~ itself, not on C).
+ * sigma:  s floats out, descending.
+ * vecs:   s x s out (ldv): column i is the unit-norm Gram-side singular vector of sigma[i]
+ *         (a right singular vector of W~ for KF_SIDE_RIGHT, a left one otherwise).
+ * sweeps: device int out (may be NULL): sweeps used.  Not converged within max_sweeps
+ *         sets KF_ERR_NO_CONVERGENCE (results are still written).
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  const float* Wt;   /* m x n, ldw */
+  int64_t m, n, ldw;
+  float* sigma;      /* s */
+  float* vecs;       /* s x s, ldv */
+  int64_t ldv;
+  int32_t* sweeps;   /* device, may be NULL */
+} kf_svd_problem;
+
+/* Optional timing of whitened_svd's phases, measured with CUDA events recorded on the
+ * caller's stream, plus the rotation-application work the Jacobi kernel executed (pairs
+ * whose coupling fell below the threshold are skipped and do no work). */
+typedef struct {
+  float gram_ms, jacobi_ms, rayleigh_ms, sort_ms;
+  int64_t jacobi_steps;          /* solve + apply launch pairs issued */
+  double jacobi_apply_flops;     /* executed multiply-add flops of the rotation products */
+} kf_svd_profile;
+
+/* Enables (1) or disables (0) recording of the profile by later whitened_svd calls. */
+KF_API kf_status kf_svd_profile_enable(kf_ctx* ctx, int enable);
+/* Synchronises the stream of the last profiled whitened_svd call and returns its profile. */
+KF_API kf_status kf_svd_profile_read(kf_ctx* ctx, kf_svd_profile* out);
+
+KF_API size_t whitened_svd_workspace_size(int32_t n_problems, int64_t m_max, int64_t n_max, int64_t s);
+KF_API kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_problem* problems,
+                       float tol, int32_t max_sweeps, void* workspace, size_t workspace_bytes,
+                       kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (5a) score_and_allocate - global sort-and-truncate rank allocation.
+ * UniRank 2.1 (all scores pooled and sorted descending; kept singular pairs each cost
+ * m + n parameters; accumulate until the budget is reached) and LASER Methodology 2
+ * (greedy global selection, score per parameter cost).
+ *
+ * sigma:      device, the units' spectra concatenated; unit u owns
+ *             sigma[seg_offset[u] .. seg_offset[u+1]) in descending order.
+ * seg_offset: device int64[n_units + 1]; cost: device int64[n_units] (m_u + n_u).
+ * mode:       KF_KEY_HALF_SIGMA2: key 0.5f * (sigma * sigma);
+ *             KF_KEY_PER_PARAM:  that divided by (float)cost[u];
+ *             KF_FIXED_RANK:     ranks[u] = min(fixed_rank[u], length of unit u).
+ * The keys are sorted descending (ties: lower unit, then lower component index first) by
+ * a device LSD radix sort on 64-bit (~key_bits << 32 | component id) words; the prefix
+ * sum of costs in that order is cut at the longest prefix with sum <= budget.
+ * ranks:      device int32[n_units] out: kept components per unit.
+ * cut:        device float[2] out (may be NULL): score of the last kept and of the first
+ *             dropped component (NaN where there is none).
+ * used:       device int64 out (may be NULL): parameters of the kept components.
+ * Integer results are deterministic and bit-identical for identical sigma input.
+ * ---------------------------------------------------------------------------------- */
+KF_API size_t score_and_allocate_workspace_size(int64_t n_components, int32_t n_units);
+KF_API kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset,
+                             const int64_t* cost, int32_t n_units, int64_t n_components,
+                             int64_t budget, kf_alloc_mode mode, const int32_t* fixed_rank,
+                             int32_t* ranks, float* cut, int64_t* used, void* workspace,
+                             size_t workspace_bytes, kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * (5b) unwhiten - rank-r factors in the original space.
+ * LASER Methodology 1: the low-rank factors of W~ are mapped back to the original space.
+ *
+ * The r leading columns of vecs are re-orthonormalised (CholeskyQR2) first.
+ * KF_SIDE_RIGHT (vecs = V~): U = W (S_g V~_r)          (= S_x^-1 U~_r Sigma_r),
+ *                            V = V~_r^T S_g^-1.
+ * KF_SIDE_LEFT  (vecs = U~): U = S_x^-1 U~_r Sigma_r,
+ *                            V = Sigma_r^-1 (U~_r^T S_x) W   (= V~_r^T S_g^-1).
+ * Sx, Sg, Sinv as written by whiten(); sigma, vecs as written by whitened_svd().
+ * U: m x r float32 out (ldu); V: r x n float32 out (ldvo).  0 <= r <= min(m, n).
+ * ---------------------------------------------------------------------------------- */
+KF_API size_t unwhiten_workspace_size(int64_t m, int64_t n, int32_t r);
+KF_API kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m,
+                   int64_t n, const float* Sx, int64_t ldsx, const float* Sg, int64_t ldsg,
+                   const float* Sinv, int64_t ldsi, const float* sigma, const float* vecs,
+                   int64_t ldv, int32_t r, float* U, int64_t ldu, float* V, int64_t ldvo,
+                   void* workspace, size_t workspace_bytes, kf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KFSVD_H */

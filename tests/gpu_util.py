@@ -1,0 +1,41 @@
+"""Helpers shared by the GPU parity tests (no method arithmetic here)."""
+import numpy as np
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def lower(a):
+    return np.tril(np.asarray(a, dtype=np.float64))
+
+
+def to_dev(x, torch, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def bf16_dev(x, torch):
+    """float32 values that are exactly bfloat16 -> a bfloat16 device tensor (exact)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).cuda()
+
+
+def rank_parity(ranks_gpu, alloc_oracle, sig_oracle, tie_rel):
+    """Ranks equal except where every differing component has an oracle score within
+    tie_rel (relative) of the oracle's cut score.  Returns (ok, n_components_moved)."""
+    moved = 0
+    cut = alloc_oracle.cut_score if np.isfinite(alloc_oracle.cut_score) else alloc_oracle.next_score
+    for u, (rg, ro) in enumerate(zip(ranks_gpu, alloc_oracle.ranks)):
+        rg, ro = int(rg), int(ro)
+        if rg == ro:
+            continue
+        lo, hi = min(rg, ro), max(rg, ro)
+        sc = 0.5 * np.asarray(sig_oracle[u][lo:hi], dtype=np.float64) ** 2
+        if np.any(np.abs(sc - cut) > tie_rel * abs(cut)):
+            return False, hi - lo
+        moved += hi - lo
+    return True, moved

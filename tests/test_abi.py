@@ -1,0 +1,66 @@
+"""The C ABI library loads on a host without a GPU, exports every declared symbol, and
+rejects bad arguments synchronously (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kfsvd.h")
+
+
+def declared_symbols():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"^KF_API [^(]*?\b([a-z_]+)\(", txt, flags=re.M)))
+
+
+def test_header_declares_the_five_steps():
+    syms = declared_symbols()
+    for s in ("kfac_accumulate", "whiten", "whitened_svd", "score_and_allocate", "unwhiten"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol():
+    from vlm_compression_fac_b300 import kfsvd as K
+    L = K.lib()
+    missing = [s for s in declared_symbols() if not hasattr(L, s)]
+    assert not missing, missing
+    assert sorted(K.EXPORTED) == declared_symbols()
+
+
+def test_library_has_no_driver_link_dependency():
+    # the .so must load without libcuda (driver entry points are resolved at run time)
+    from vlm_compression_fac_b300 import kfsvd as K
+    out = os.popen("ldd %s" % K.LIB_PATH).read()
+    assert "libcuda.so" not in out and "libtorch" not in out
+
+
+def test_workspace_queries_are_host_only():
+    from vlm_compression_fac_b300 import kfsvd as K
+    assert K.kfac_accumulate_workspace_size(K.KF_BF16, K.KF_QUANT_NONE, 4096) == 0
+    assert K.kfac_accumulate_workspace_size(K.KF_F32, K.KF_QUANT_NONE, 256) >= 2 * 8192 * 256 * 2
+    assert K.whiten_workspace_size(4096, 11008) >= 4096 * 11008 * 4
+    assert K.whitened_svd_workspace_size(7, 11008, 11008, 4096) >= 7 * 2 * 4096 * 4096 * 4
+    assert K.score_and_allocate_workspace_size(1 << 20, 7) >= 3 * 8 * (1 << 20)
+    assert K.unwhiten_workspace_size(4096, 4096, 0) == 0
+    assert K.kf_gram_side(4096, 4096) == K.KF_SIDE_RIGHT
+    assert K.kf_gram_side(4096, 11008) == K.KF_SIDE_LEFT
+    assert K.kf_gram_side(11008, 4096) == K.KF_SIDE_RIGHT
+
+
+def test_invalid_arguments_fail_before_any_launch():
+    from vlm_compression_fac_b300 import kfsvd as K
+    L = K.lib()
+    st = L.kfac_accumulate(None, None, 0, 10, 8, 8, 0, None, 8, None, 0, None)
+    assert st == K.KF_ERR_INVALID
+    assert b"null context" in L.kf_last_error()
+    st = L.score_and_allocate(None, None, None, None, 1, 0, 0, 0, None, None, None, None, None, 0, None)
+    assert st == K.KF_ERR_INVALID
+    assert L.kf_sync_status(None, None, None) == K.KF_ERR_INVALID
+    h = ctypes.c_void_p()
+    st = L.kf_create(0, ctypes.byref(h))
+    if st != K.KF_OK:          # no GPU on this host: a clean error, no crash
+        assert st in (K.KF_ERR_CUDA, K.KF_ERR_UNSUPPORTED, K.KF_ERR_INVALID)
+    else:
+        L.kf_destroy(h)

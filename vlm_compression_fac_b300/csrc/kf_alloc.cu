@@ -1,0 +1,342 @@
+// Global sort-and-truncate rank allocation (UniRank 2.1; LASER Methodology 2).
+//   keys:  k = (~bits(score) << 32) | component id, score = 0.5f * (sigma * sigma) [/ cost];
+//          ascending k is score descending, then lower unit, then lower component index
+//          (ids are assigned in unit order), which makes the order total and deterministic;
+//   sort:  LSD radix sort, 8 passes of 8 bits; each pass = per-tile digit histogram,
+//          one exclusive scan over (digit, tile), stable scatter (warp match + per-warp
+//          digit counters keep the original order inside a tile);
+//   cut:   inclusive prefix sum of the kept pairs' cost m+n in sorted order; the kept
+//          prefix is every position whose prefix sum is <= budget (costs are positive, so
+//          the walk stops at the first overflow); ranks = kept count per unit.
+#include "kf_internal.cuh"
+
+namespace kf {
+namespace {
+
+constexpr int RT = 256;            // threads per tile
+constexpr int RI = 16;             // keys per thread
+constexpr int TILE = RT * RI;      // 4096 keys per tile
+constexpr int SCAN_T = 1024;
+
+__device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_units, int64_t g) {
+  int lo = 0, hi = n_units;  // off[lo] <= g < off[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (off[mid] <= g) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+__global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off,
+                                  const int64_t* __restrict__ cost, int n_units, int64_t n, int mode,
+                                  unsigned long long* __restrict__ keys) {
+  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += int64_t(gridDim.x) * blockDim.x) {
+    const int u = unit_of(off, n_units, g);
+    const float s = sigma[g];
+    float sc = 0.5f * __fmul_rn(s, s);
+    if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
+    const unsigned bits = ~__float_as_uint(sc);
+    keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(uint32_t(g));
+  }
+}
+
+__global__ void __launch_bounds__(RT) hist_kernel(const unsigned long long* __restrict__ keys, int64_t n, int shift,
+                                                  int ntiles, unsigned* __restrict__ hist) {
+  __shared__ unsigned h[256];
+  h[threadIdx.x] = 0;
+  __syncthreads();
+  const int64_t base = int64_t(blockIdx.x) * TILE;
+  for (int i = 0; i < RI; ++i) {
+    const int64_t g = base + int64_t(i) * RT + threadIdx.x;
+    if (g < n) atomicAdd(&h[(keys[g] >> shift) & 255u], 1u);
+  }
+  __syncthreads();
+  hist[int64_t(threadIdx.x) * ntiles + blockIdx.x] = h[threadIdx.x];
+}
+
+// Exclusive scan of a uint array of length len (one CTA, sequential over chunks).
+__global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__ a, int64_t len) {
+  __shared__ unsigned ws[32];
+  __shared__ unsigned carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int64_t c0 = 0; c0 < len; c0 += SCAN_T) {
+    const int64_t i = c0 + threadIdx.x;
+    const unsigned v = i < len ? a[i] : 0u;
+    unsigned x = v;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      unsigned z = ws[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, z, o);
+        if (lane >= o) z += y;
+      }
+      ws[lane] = z;
+    }
+    __syncthreads();
+    const unsigned incl = x + (w > 0 ? ws[w - 1] : 0u) + carry;
+    if (i < len) a[i] = incl - v;
+    __syncthreads();
+    if (threadIdx.x == SCAN_T - 1) carry = incl;
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(RT) scatter_kernel(const unsigned long long* __restrict__ in,
+                                                     unsigned long long* __restrict__ out, int64_t n, int shift,
+                                                     int ntiles, const unsigned* __restrict__ hist) {
+  __shared__ unsigned base[256];
+  __shared__ unsigned run[256];
+  __shared__ unsigned wcnt[RT / 32][256];
+  __shared__ unsigned woff[RT / 32][256];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  base[t] = hist[int64_t(t) * ntiles + blockIdx.x];
+  run[t] = 0;
+  const int64_t tile0 = int64_t(blockIdx.x) * TILE;
+  for (int r = 0; r < RI; ++r) {
+    for (int x = lane; x < 256; x += 32) wcnt[w][x] = 0;
+    __syncthreads();
+    const int64_t g = tile0 + int64_t(r) * RT + t;
+    const bool valid = g < n;
+    const unsigned long long k = valid ? in[g] : 0ull;
+    const unsigned d = valid ? unsigned((k >> shift) & 255u) : 256u;
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    const unsigned lt = peers & ((1u << lane) - 1u);
+    const unsigned rank = __popc(lt);
+    if (valid && lt == 0) wcnt[w][d] = __popc(peers);
+    __syncthreads();
+    {  // per digit: offsets of each warp within this round, in warp order
+      unsigned acc = run[t];
+      for (int ww = 0; ww < RT / 32; ++ww) {
+        woff[ww][t] = acc;
+        acc += wcnt[ww][t];
+      }
+      run[t] = acc;
+    }
+    __syncthreads();
+    if (valid) out[base[d] + woff[w][d] + rank] = k;
+    __syncthreads();
+  }
+}
+
+// Inclusive prefix sums of the sorted components' costs, per 1024-item block.
+__global__ void __launch_bounds__(SCAN_T) cost_block_sum_kernel(const unsigned long long* __restrict__ keys,
+                                                                const int64_t* __restrict__ off,
+                                                                const int64_t* __restrict__ cost, int n_units,
+                                                                int64_t n, long long* __restrict__ bsum) {
+  __shared__ long long red[SCAN_T / 32];
+  const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
+  long long c = 0;
+  if (i < n) c = cost[unit_of(off, n_units, int64_t(uint32_t(keys[i])))];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long s = 0;
+    for (int w = 0; w < SCAN_T / 32; ++w) s += red[w];
+    bsum[blockIdx.x] = s;
+  }
+}
+
+__global__ void __launch_bounds__(SCAN_T) scan_i64_kernel(long long* __restrict__ a, int64_t len) {
+  __shared__ long long ws[32];
+  __shared__ long long carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  for (int64_t c0 = 0; c0 < len; c0 += SCAN_T) {
+    const int64_t i = c0 + threadIdx.x;
+    const long long v = i < len ? a[i] : 0;
+    long long x = v;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) ws[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      long long z = ws[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, z, o);
+        if (lane >= o) z += y;
+      }
+      ws[lane] = z;
+    }
+    __syncthreads();
+    const long long incl = x + (w > 0 ? ws[w - 1] : 0) + carry;
+    if (i < len) a[i] = incl - v;
+    __syncthreads();
+    if (threadIdx.x == SCAN_T - 1) carry = incl;
+    __syncthreads();
+  }
+}
+
+// Per item: inclusive prefix; items within budget are kept (kcount = max kept index + 1).
+__global__ void __launch_bounds__(SCAN_T) cut_kernel(const unsigned long long* __restrict__ keys,
+                                                     const int64_t* __restrict__ off, const int64_t* __restrict__ cost,
+                                                     int n_units, int64_t n, const long long* __restrict__ bexcl,
+                                                     long long budget, long long* __restrict__ prefix,
+                                                     unsigned long long* __restrict__ kcount) {
+  __shared__ long long ws[32];
+  const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
+  long long c = 0;
+  if (i < n) c = cost[unit_of(off, n_units, int64_t(uint32_t(keys[i])))];
+  long long x = c;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[w] = x;
+  __syncthreads();
+  if (w == 0) {
+    long long z = ws[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, z, o);
+      if (lane >= o) z += y;
+    }
+    ws[lane] = z;
+  }
+  __syncthreads();
+  const long long incl = x + (w > 0 ? ws[w - 1] : 0) + bexcl[blockIdx.x];
+  if (i < n) {
+    prefix[i] = incl;
+    if (incl <= budget) atomicMax(kcount, static_cast<unsigned long long>(i + 1));
+  }
+}
+
+__global__ void ranks_kernel(const unsigned long long* __restrict__ keys, const int64_t* __restrict__ off,
+                             int n_units, const unsigned long long* __restrict__ kcount, int* __restrict__ ranks) {
+  const int64_t k = int64_t(*kcount);
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x)
+    atomicAdd(&ranks[unit_of(off, n_units, int64_t(uint32_t(keys[i])))], 1);
+}
+
+__device__ __forceinline__ float key_score(unsigned long long k) { return __uint_as_float(~unsigned(k >> 32)); }
+
+__global__ void finish_kernel(const unsigned long long* __restrict__ keys, const long long* __restrict__ prefix,
+                              int64_t n, const unsigned long long* __restrict__ kcount, float* __restrict__ cut,
+                              long long* __restrict__ used) {
+  const int64_t k = int64_t(*kcount);
+  if (cut) {
+    cut[0] = k > 0 ? key_score(keys[k - 1]) : __int_as_float(0x7fc00000);
+    cut[1] = k < n ? key_score(keys[k]) : __int_as_float(0x7fc00000);
+  }
+  if (used) *used = k > 0 ? prefix[k - 1] : 0;
+}
+
+__global__ void fixed_rank_kernel(const int64_t* __restrict__ off, const int64_t* __restrict__ cost, int n_units,
+                                  const int* __restrict__ fixed, int* __restrict__ ranks, float* __restrict__ cut,
+                                  long long* __restrict__ used) {
+  __shared__ long long red[256];
+  long long acc = 0;
+  for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
+    const long long len = off[u + 1] - off[u];
+    long long r = fixed[u] < 0 ? 0 : fixed[u];
+    if (r > len) r = len;
+    ranks[u] = int(r);
+    acc += r * cost[u];
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (used) *used = red[0];
+    if (cut) cut[0] = cut[1] = __int_as_float(0x7fc00000);
+  }
+}
+
+unsigned grid_cap(int64_t n, int per) {
+  int64_t b = (n + per - 1) / per;
+  if (b > 148 * 16) b = 148 * 16;
+  return unsigned(b < 1 ? 1 : b);
+}
+
+struct AllocBufs {
+  unsigned long long *ka, *kb, *kcount;
+  unsigned* hist;
+  long long *bsum, *prefix;
+};
+
+size_t alloc_carve(Carve& cv, int64_t n, AllocBufs& b) {
+  const int64_t ntiles = (n + TILE - 1) / TILE;
+  const int64_t nb = (n + SCAN_T - 1) / SCAN_T;
+  b.ka = cv.take<unsigned long long>(n > 0 ? n : 1);
+  b.kb = cv.take<unsigned long long>(n > 0 ? n : 1);
+  b.hist = cv.take<unsigned>(size_t(256) * (ntiles > 0 ? ntiles : 1));
+  b.bsum = cv.take<long long>(nb > 0 ? nb : 1);
+  b.prefix = cv.take<long long>(n > 0 ? n : 1);
+  b.kcount = cv.take<unsigned long long>(1);
+  return cv.off;
+}
+
+}  // namespace
+
+size_t alloc_workspace(int64_t n) {
+  Carve cv(nullptr, 0, true);
+  AllocBufs b;
+  return alloc_carve(cv, n, b) + 256;
+}
+
+kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
+                    int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, int32_t* ranks, float* cut,
+                    int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st) {
+  (void)ctx;
+  KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
+  if (mode == KF_FIXED_RANK) {
+    fixed_rank_kernel<<<1, 256, 0, st>>>(off, cost, n_units, fixed, ranks, cut, (long long*)used); note_launch();
+    return check_cuda(cudaGetLastError(), "fixed_rank launch");
+  }
+  Carve cv(ws, ws_bytes, false);
+  AllocBufs b;
+  alloc_carve(cv, n, b);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "score_and_allocate: workspace too small");
+  const int ntiles = int((n + TILE - 1) / TILE);
+  build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), b.ka); note_launch();
+  KF_CUDA(cudaGetLastError());
+  unsigned long long* src = b.ka;
+  unsigned long long* dst = b.kb;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = pass * 8;
+    hist_kernel<<<ntiles, RT, 0, st>>>(src, n, shift, ntiles, b.hist); note_launch();
+    KF_CUDA(cudaGetLastError());
+    scan_u32_kernel<<<1, SCAN_T, 0, st>>>(b.hist, int64_t(256) * ntiles); note_launch();
+    KF_CUDA(cudaGetLastError());
+    scatter_kernel<<<ntiles, RT, 0, st>>>(src, dst, n, shift, ntiles, b.hist); note_launch();
+    KF_CUDA(cudaGetLastError());
+    unsigned long long* tmp = src;
+    src = dst;
+    dst = tmp;
+  }
+  // src now holds the sorted keys.
+  const int64_t nb = (n + SCAN_T - 1) / SCAN_T;
+  cost_block_sum_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum); note_launch();
+  KF_CUDA(cudaGetLastError());
+  scan_i64_kernel<<<1, SCAN_T, 0, st>>>(b.bsum, nb); note_launch();
+  KF_CUDA(cudaGetLastError());
+  KF_CUDA(cudaMemsetAsync(b.kcount, 0, sizeof(unsigned long long), st));
+  cut_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, budget, b.prefix, b.kcount); note_launch();
+  KF_CUDA(cudaGetLastError());
+  ranks_kernel<<<grid_cap(n, 256), 256, 0, st>>>(src, off, n_units, b.kcount, ranks); note_launch();
+  KF_CUDA(cudaGetLastError());
+  finish_kernel<<<1, 1, 0, st>>>(src, b.prefix, n, b.kcount, cut, (long long*)used); note_launch();
+  return check_cuda(cudaGetLastError(), "allocation launch");
+}
+
+}  // namespace kf

@@ -1,0 +1,423 @@
+// C ABI entry points of libkfsvd.so (declared in include/kfsvd.h): argument validation on
+// the host, workspace carving, and the launch sequence of each step of the path.
+#include "kf_internal.cuh"
+
+#include <cstring>
+#include <string>
+
+namespace kf {
+const char* last_error_cstr();
+unsigned long long launch_count();
+size_t svd_workspace(int32_t nu, int64_t m_max, int64_t n_max, int64_t s);
+kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, int32_t max_sweeps, void* ws,
+                  size_t ws_bytes, cudaStream_t st);
+kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out);
+size_t alloc_workspace(int64_t n);
+kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
+                    int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, int32_t* ranks, float* cut,
+                    int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st);
+}  // namespace kf
+
+using namespace kf;
+
+namespace {
+
+constexpr int64_t ACC_CHUNK = 8192;  // tokens per preprocessing chunk (float32 / QAW input)
+constexpr int FINAL_SLOTS = 1024;
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+kf_status need(bool cond, const char* msg) { return cond ? KF_OK : fail(KF_ERR_INVALID, msg); }
+
+size_t elem_size(kf_dtype d) { return d == KF_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+const char* kf_last_error(void) { return last_error_cstr(); }
+
+uint64_t kf_launch_count(void) { return launch_count(); }
+
+kf_side kf_gram_side(int64_t m, int64_t n) { return n <= m ? KF_SIDE_RIGHT : KF_SIDE_LEFT; }
+
+kf_status kf_create(int device, kf_ctx** out) {
+  if (!out) return fail(KF_ERR_INVALID, "kf_create: out is null");
+  *out = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) return fail(KF_ERR_CUDA, "kf_create: no CUDA device");
+  if (device < 0 || device >= count) return fail(KF_ERR_INVALID, "kf_create: bad device index");
+  KF_CUDA(cudaSetDevice(device));
+  kf_ctx* c = new kf_ctx();
+  c->device = device;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+    delete c;
+    return fail(KF_ERR_CUDA, "kf_create: cudaGetDeviceProperties failed");
+  }
+  c->sm_count = prop.multiProcessorCount;
+  c->cc_major = prop.major;
+  c->cc_minor = prop.minor;
+  if (!(prop.major == 10 && prop.minor == 3)) {
+    delete c;
+    return fail(KF_ERR_UNSUPPORTED, "kf_create: libkfsvd is built for sm_103a (compute capability 10.3)");
+  }
+  // status int32[4] followed by the finalisation scratch ring
+  const size_t bytes = 64 + sizeof(float) * FINAL_SLOTS;
+  if (cudaMalloc(&c->d_status, bytes) != cudaSuccess) {
+    delete c;
+    return fail(KF_ERR_CUDA, "kf_create: cudaMalloc of the status word failed");
+  }
+  cudaMemset(c->d_status, 0, bytes);
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaFree(c->d_status);
+    delete c;
+    return fail(KF_ERR_CUDA, "kf_create: cuTensorMapEncodeTiled entry point not found");
+  }
+  c->encode = reinterpret_cast<PFN_encodeTiled>(fn);
+  *out = c;
+  return KF_OK;
+}
+
+void kf_destroy(kf_ctx* ctx) {
+  if (!ctx) return;
+  for (int e = 0; e < 5; ++e)
+    if (ctx->prof_ev[e]) cudaEventDestroy(ctx->prof_ev[e]);
+  if (ctx->d_status) cudaFree(ctx->d_status);
+  delete ctx;
+}
+
+kf_status kf_sync_status(kf_ctx* ctx, kf_stream_t stream, int32_t* info) {
+  if (!ctx) return fail(KF_ERR_INVALID, "kf_sync_status: null context");
+  KF_CUDA(cudaStreamSynchronize(stream));
+  int h[2] = {0, 0};
+  KF_CUDA(cudaMemcpy(h, ctx->d_status, sizeof(h), cudaMemcpyDeviceToHost));
+  KF_CUDA(cudaMemset(ctx->d_status, 0, sizeof(h)));
+  if (info) *info = h[1];
+  if (h[0] == 0) return KF_OK;
+  const char* what = h[0] == KF_ERR_NOT_SPD ? "Cholesky pivot <= 0 (factor not positive definite)"
+                     : h[0] == KF_ERR_NO_CONVERGENCE ? "Jacobi did not converge within max_sweeps"
+                     : h[0] == KF_ERR_TIMEOUT ? "a device-side wait timed out"
+                                              : "device error";
+  return fail(kf_status(h[0]), std::string("device status: ") + what + " (info " + std::to_string(h[1]) + ")");
+}
+
+// ----------------------------------------------------------------------- (1)
+size_t kfac_accumulate_workspace_size(kf_dtype dtype, kf_quant quant, int64_t d) {
+  const int64_t dp = round_up(d > 0 ? d : 1, 8);
+  if (dtype == KF_BF16 && quant == KF_QUANT_NONE) return 0;
+  if (quant == KF_QUANT_INT8_TOKEN) return size_t(ACC_CHUNK) * dp * 2 + 256;
+  return size_t(2) * ACC_CHUNK * dp * 2 + 512;  // float32: hi and lo planes
+}
+
+kf_status kfac_accumulate(kf_ctx* ctx, const void* act, kf_dtype dtype, int64_t n_tokens, int64_t d, int64_t ld,
+                          kf_quant quant, float* cov_sum, int64_t ldc, void* workspace, size_t workspace_bytes,
+                          kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "kfac_accumulate: null context"));
+  KF_TRY(need(dtype == KF_BF16 || dtype == KF_F32, "kfac_accumulate: dtype"));
+  KF_TRY(need(quant == KF_QUANT_NONE || quant == KF_QUANT_INT8_TOKEN, "kfac_accumulate: quant"));
+  KF_TRY(need(n_tokens >= 0 && d > 0 && ld >= d && ldc >= d, "kfac_accumulate: sizes"));
+  if (n_tokens == 0) return KF_OK;
+  KF_TRY(need(act && cov_sum, "kfac_accumulate: null pointer"));
+  if (workspace_bytes < kfac_accumulate_workspace_size(dtype, quant, d))
+    return fail(KF_ERR_WORKSPACE, "kfac_accumulate: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TcGemm g{};
+  g.M = d; g.N = d; g.D = cov_sum; g.ldd = ldc; g.accumulate = true; g.sched = TC_LOWER; g.krange = KR_FULL;
+  if (dtype == KF_BF16 && quant == KF_QUANT_NONE) {
+    KF_TRY(need((reinterpret_cast<uintptr_t>(act) & 15) == 0 && (ld * 2) % 16 == 0,
+                "kfac_accumulate: bf16 rows need a 16-byte aligned base and ld a multiple of 8"));
+    g.K = n_tokens; g.npass = 1;
+    g.a[0] = TcOperand{(const __nv_bfloat16*)act, ld, true};
+    g.b[0] = g.a[0];
+    return tc_gemm(ctx, g, st);
+  }
+  const int64_t dp = round_up(d, 8);
+  Carve cv(workspace, workspace_bytes, false);
+  __nv_bfloat16* p0 = cv.take<__nv_bfloat16>(size_t(ACC_CHUNK) * dp);
+  __nv_bfloat16* p1 = quant == KF_QUANT_NONE ? cv.take<__nv_bfloat16>(size_t(ACC_CHUNK) * dp) : nullptr;
+  for (int64_t t0 = 0; t0 < n_tokens; t0 += ACC_CHUNK) {
+    const int64_t rows = n_tokens - t0 < ACC_CHUNK ? n_tokens - t0 : ACC_CHUNK;
+    const char* src = static_cast<const char*>(act) + size_t(t0) * ld * elem_size(dtype);
+    g.K = rows;
+    if (quant == KF_QUANT_INT8_TOKEN) {
+      KF_TRY(launch_fake_quant(src, dtype, rows, d, ld, p0, st));
+      // fake-quant writes rows with leading dimension d; re-pad when d is not a multiple of 8
+      if (dp != d) return fail(KF_ERR_INVALID, "kfac_accumulate: quantised rows need d a multiple of 8");
+      g.npass = 1;
+      g.a[0] = TcOperand{p0, dp, true};
+      g.b[0] = g.a[0];
+    } else {
+      KF_TRY(launch_split_bf16(reinterpret_cast<const float*>(src), rows, d, ld, p0, p1, dp, st));
+      g.npass = 3;  // hi*hi + hi*lo + lo*hi
+      g.a[0] = TcOperand{p0, dp, true}; g.b[0] = TcOperand{p0, dp, true};
+      g.a[1] = TcOperand{p0, dp, true}; g.b[1] = TcOperand{p1, dp, true};
+      g.a[2] = TcOperand{p1, dp, true}; g.b[2] = TcOperand{p0, dp, true};
+    }
+    KF_TRY(tc_gemm(ctx, g, st));
+  }
+  return KF_OK;
+}
+
+kf_status kf_finalize_covariance(kf_ctx* ctx, float* cov, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
+                                 kf_stream_t stream) {
+  KF_TRY(need(ctx && cov, "kf_finalize_covariance: null pointer"));
+  KF_TRY(need(d > 0 && ldc >= d && n_tokens > 0 && lambda >= 0.f, "kf_finalize_covariance: sizes"));
+  static unsigned slot = 0;
+  float* scratch = reinterpret_cast<float*>(reinterpret_cast<char*>(ctx->d_status) + 64) + (slot++ % FINAL_SLOTS);
+  return launch_finalize(cov, ldc, d, n_tokens, lambda, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// --------------------------------------------------------------------- (2)+(3)
+namespace {
+size_t whiten_carve(Carve& cv, int64_t m, int64_t n, float** dinv, float** T, float** tt) {
+  const int64_t mx = m > n ? m : n;
+  *dinv = cv.take<float>(size_t(round_up(mx, CHOL_NB)) * CHOL_NB);
+  *T = cv.take<float>(size_t(m) * n);
+  *tt = cv.take<float>(trtri_tmp_floats(mx));
+  return cv.off;
+}
+}  // namespace
+
+size_t whiten_workspace_size(int64_t m, int64_t n) {
+  if (m <= 0 || n <= 0) return 0;
+  Carve cv(nullptr, 0, true);
+  float *a, *b, *c;
+  return whiten_carve(cv, m, n, &a, &b, &c) + 256;
+}
+
+kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const float* G, int64_t ldg, int64_t n,
+                 const void* W, kf_dtype w_dtype, int64_t ldw, uint32_t flags, float* Sx, int64_t ldsx, float* Sg,
+                 int64_t ldsg, float* Sinv, int64_t ldsi, float* Wt, int64_t ldwt, void* workspace,
+                 size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "whiten: null context"));
+  KF_TRY(need(m > 0 && n > 0, "whiten: sizes"));
+  KF_TRY(need(X && G && W && Sx && Sg && Sinv && Wt, "whiten: null pointer"));
+  KF_TRY(need(ldx >= m && ldg >= n && ldw >= n && ldsx >= m && ldsg >= n && ldwt >= n, "whiten: leading dimension"));
+  KF_TRY(need(w_dtype == KF_BF16 || w_dtype == KF_F32, "whiten: dtype"));
+  const kf_side side = kf_gram_side(m, n);
+  const int64_t s = side == KF_SIDE_RIGHT ? n : m;
+  KF_TRY(need(ldsi >= s, "whiten: ldsi"));
+  Carve cv(workspace, workspace_bytes, false);
+  float *dinv, *T, *tt;
+  whiten_carve(cv, m, n, &dinv, &T, &tt);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "whiten: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  // S_x = chol_lower(X)^T  (and S_x^-1 for the left Gram side)
+  if (!(flags & KF_REUSE_SX)) {
+    KF_TRY(launch_copy(X, ldx, Sx, ldsx, m, m, false, st));
+    KF_TRY(cholesky_lower(ctx, Sx, ldsx, m, dinv, st));
+    if (side == KF_SIDE_LEFT && !(flags & KF_REUSE_SINV)) {
+      KF_TRY(trtri_lower(ctx, Sx, ldsx, m, dinv, Sinv, ldsi, tt, st));   // L_x^-1
+      KF_TRY(launch_transpose_inplace(Sinv, ldsi, m, st));               // S_x^-1 = L_x^-T
+    }
+    KF_TRY(launch_transpose_inplace(Sx, ldsx, m, st));                   // S_x = L_x^T
+  }
+  // S_g = chol_lower(G)  (and S_g^-1 for the right Gram side)
+  if (!(flags & KF_REUSE_SG)) {
+    KF_TRY(launch_copy(G, ldg, Sg, ldsg, n, n, false, st));
+    KF_TRY(cholesky_lower(ctx, Sg, ldsg, n, dinv, st));
+    if (side == KF_SIDE_RIGHT && !(flags & KF_REUSE_SINV)) {
+      KF_TRY(trtri_lower(ctx, Sg, ldsg, n, dinv, Sinv, ldsi, tt, st));
+    }
+  }
+  // T = W S_g  (S_g lower: column j needs k >= j), then W~ = S_x T (S_x upper: k >= i).
+  GemmDesc g{};
+  g.M = m; g.N = n; g.K = n; g.batch = 1;
+  g.A = W; g.lda = ldw; g.a_bf16 = w_dtype == KF_BF16;
+  g.B = Sg; g.ldb = ldsg;
+  g.C = T; g.ldc = n; g.alpha = 1.f; g.beta = 0.f; g.krange = KR_GE_COL;
+  KF_TRY(simt_gemm(g, st));
+  GemmDesc h{};
+  h.M = m; h.N = n; h.K = m; h.batch = 1;
+  h.A = Sx; h.lda = ldsx;
+  h.B = T; h.ldb = n;
+  h.C = Wt; h.ldc = ldwt; h.alpha = 1.f; h.beta = 0.f; h.krange = KR_GE_ROW;
+  return simt_gemm(h, st);
+}
+
+// ------------------------------------------------------------------------ (4)
+size_t whitened_svd_workspace_size(int32_t n_problems, int64_t m_max, int64_t n_max, int64_t s) {
+  if (n_problems <= 0 || s <= 0) return 0;
+  return svd_workspace(n_problems, m_max, n_max, s);
+}
+
+kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_problem* problems, float tol,
+                       int32_t max_sweeps, void* workspace, size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "whitened_svd: null context"));
+  if (n_problems == 0) return KF_OK;
+  KF_TRY(need(n_problems > 0 && problems, "whitened_svd: problems"));
+  KF_TRY(need(n_problems <= 65535, "whitened_svd: at most 65535 problems per call"));
+  KF_TRY(need(tol > 0.f && max_sweeps > 0, "whitened_svd: tol and max_sweeps must be positive"));
+  int64_t s0 = -1, m_max = 0, n_max = 0;
+  for (int i = 0; i < n_problems; ++i) {
+    const kf_svd_problem& p = problems[i];
+    KF_TRY(need(p.Wt && p.sigma && p.vecs && p.m > 0 && p.n > 0 && p.ldw >= p.n, "whitened_svd: problem fields"));
+    const int64_t s = p.m < p.n ? p.m : p.n;
+    KF_TRY(need(p.ldv >= s, "whitened_svd: ldv"));
+    if (s0 < 0) s0 = s;
+    KF_TRY(need(s == s0, "whitened_svd: all problems of a call need the same min(m, n)"));
+    m_max = p.m > m_max ? p.m : m_max;
+    n_max = p.n > n_max ? p.n : n_max;
+  }
+  if (s0 > 16384) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: min(m, n) > 16384");
+  if (workspace_bytes < svd_workspace(n_problems, m_max, n_max, s0))
+    return fail(KF_ERR_WORKSPACE, "whitened_svd: workspace too small");
+  return svd_run(ctx, n_problems, problems, tol, max_sweeps, workspace, workspace_bytes,
+                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+kf_status kf_svd_profile_enable(kf_ctx* ctx, int enable) {
+  KF_TRY(need(ctx != nullptr, "kf_svd_profile_enable: null context"));
+  ctx->prof_enabled = enable != 0;
+  return KF_OK;
+}
+
+kf_status kf_svd_profile_read(kf_ctx* ctx, kf_svd_profile* out) {
+  KF_TRY(need(ctx && out, "kf_svd_profile_read: null pointer"));
+  return svd_profile_read(ctx, out);
+}
+
+// ----------------------------------------------------------------------- (5a)
+size_t score_and_allocate_workspace_size(int64_t n_components, int32_t n_units) {
+  (void)n_units;
+  return alloc_workspace(n_components > 0 ? n_components : 1);
+}
+
+kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset, const int64_t* cost,
+                             int32_t n_units, int64_t n_components, int64_t budget, kf_alloc_mode mode,
+                             const int32_t* fixed_rank, int32_t* ranks, float* cut, int64_t* used, void* workspace,
+                             size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "score_and_allocate: null context"));
+  KF_TRY(need(n_units > 0 && n_components >= 0, "score_and_allocate: sizes"));
+  KF_TRY(need(n_components < (int64_t(1) << 32), "score_and_allocate: at most 2^32 - 1 components"));
+  KF_TRY(need(seg_offset && cost && ranks, "score_and_allocate: null pointer"));
+  KF_TRY(need(mode == KF_KEY_HALF_SIGMA2 || mode == KF_KEY_PER_PARAM || mode == KF_FIXED_RANK,
+              "score_and_allocate: mode"));
+  if (mode == KF_FIXED_RANK) KF_TRY(need(fixed_rank != nullptr, "score_and_allocate: fixed_rank is null"));
+  else KF_TRY(need(sigma != nullptr || n_components == 0, "score_and_allocate: sigma is null"));
+  if (mode != KF_FIXED_RANK && workspace_bytes < alloc_workspace(n_components > 0 ? n_components : 1))
+    return fail(KF_ERR_WORKSPACE, "score_and_allocate: workspace too small");
+  if (mode != KF_FIXED_RANK && n_components == 0) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
+    if (used) KF_CUDA(cudaMemsetAsync(used, 0, sizeof(int64_t), st));
+    if (cut) KF_CUDA(cudaMemsetAsync(cut, 0xFF, 2 * sizeof(float), st));  // NaN
+    return KF_OK;
+  }
+  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, ranks, cut, used,
+                   workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ----------------------------------------------------------------------- (5b)
+namespace {
+size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, float** q0, float** q1, float** gm, float** li,
+                      float** dinv, float** tt, float** P) {
+  const int64_t s = m < n ? m : n, mx = m > n ? m : n;
+  *q0 = cv.take<float>(size_t(s) * r);
+  *q1 = cv.take<float>(size_t(s) * r);
+  *gm = cv.take<float>(size_t(r) * r);
+  *li = cv.take<float>(size_t(r) * r);
+  *dinv = cv.take<float>(size_t(round_up(r, CHOL_NB)) * CHOL_NB);
+  *tt = cv.take<float>(trtri_tmp_floats(r));
+  *P = cv.take<float>(size_t(mx) * r);
+  return cv.off;
+}
+}  // namespace
+
+size_t unwhiten_workspace_size(int64_t m, int64_t n, int32_t r) {
+  if (m <= 0 || n <= 0 || r <= 0) return 0;
+  Carve cv(nullptr, 0, true);
+  float *a, *b, *c, *d, *e, *f, *g;
+  return unwhiten_carve(cv, m, n, r, &a, &b, &c, &d, &e, &f, &g) + 256;
+}
+
+kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m, int64_t n, const float* Sx,
+                   int64_t ldsx, const float* Sg, int64_t ldsg, const float* Sinv, int64_t ldsi, const float* sigma,
+                   const float* vecs, int64_t ldv, int32_t r, float* U, int64_t ldu, float* V, int64_t ldvo,
+                   void* workspace, size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "unwhiten: null context"));
+  KF_TRY(need(m > 0 && n > 0, "unwhiten: sizes"));
+  const int64_t s = m < n ? m : n;
+  KF_TRY(need(r >= 0 && r <= s, "unwhiten: r must be in [0, min(m, n)]"));
+  if (r == 0) return KF_OK;
+  KF_TRY(need(W && Sx && Sg && Sinv && sigma && vecs && U && V, "unwhiten: null pointer"));
+  KF_TRY(need(ldw >= n && ldsx >= m && ldsg >= n && ldsi >= s && ldv >= s && ldu >= r && ldvo >= n,
+              "unwhiten: leading dimension"));
+  Carve cv(workspace, workspace_bytes, false);
+  float *q0, *q1, *gm, *li, *dinv, *tt, *P;
+  unwhiten_carve(cv, m, n, r, &q0, &q1, &gm, &li, &dinv, &tt, &P);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "unwhiten: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  // CholeskyQR2 of the r leading Gram-side vectors: twice Q <- Q R^-1 with R^T R = Q^T Q.
+  KF_TRY(launch_copy(vecs, ldv, q0, r, s, r, false, st));
+  float* cur = q0;
+  float* nxt = q1;
+  for (int it = 0; it < 2; ++it) {
+    GemmDesc g{};
+    g.M = r; g.N = r; g.K = s; g.batch = 1;
+    g.A = cur; g.lda = r; g.trans_a = true;
+    g.B = cur; g.ldb = r;
+    g.C = gm; g.ldc = r; g.alpha = 1.f; g.beta = 0.f; g.out_mask = OUT_LOWER;
+    KF_TRY(simt_gemm(g, st));
+    KF_TRY(cholesky_lower(ctx, gm, r, r, dinv, st));
+    KF_TRY(trtri_lower(ctx, gm, r, r, dinv, li, r, tt, st));
+    GemmDesc h{};
+    h.M = s; h.N = r; h.K = r; h.batch = 1;
+    h.A = cur; h.lda = r;
+    h.B = li; h.ldb = r; h.trans_b = true; h.krange = KR_LE_COL;  // (L^-1)^T is upper
+    h.C = nxt; h.ldc = r; h.alpha = 1.f; h.beta = 0.f;
+    KF_TRY(simt_gemm(h, st));
+    float* tmp = cur; cur = nxt; nxt = tmp;
+  }
+  const bool wbf = w_dtype == KF_BF16;
+  if (kf_gram_side(m, n) == KF_SIDE_RIGHT) {
+    // P = S_g V~_r (S_g lower: row i needs k <= i);  U = W P;  V = V~_r^T S_g^-1.
+    GemmDesc a{};
+    a.M = n; a.N = r; a.K = n; a.batch = 1;
+    a.A = Sg; a.lda = ldsg; a.krange = KR_LE_ROW;
+    a.B = cur; a.ldb = r;
+    a.C = P; a.ldc = r; a.alpha = 1.f; a.beta = 0.f;
+    KF_TRY(simt_gemm(a, st));
+    GemmDesc b{};
+    b.M = m; b.N = r; b.K = n; b.batch = 1;
+    b.A = W; b.lda = ldw; b.a_bf16 = wbf;
+    b.B = P; b.ldb = r;
+    b.C = U; b.ldc = ldu; b.alpha = 1.f; b.beta = 0.f;
+    KF_TRY(simt_gemm(b, st));
+    GemmDesc c{};
+    c.M = r; c.N = n; c.K = n; c.batch = 1;
+    c.A = cur; c.lda = r; c.trans_a = true;
+    c.B = Sinv; c.ldb = ldsi; c.krange = KR_GE_COL;  // S_g^-1 lower
+    c.C = V; c.ldc = ldvo; c.alpha = 1.f; c.beta = 0.f;
+    return simt_gemm(c, st);
+  }
+  // Left side: U = S_x^-1 U~_r Sigma_r;  V = Sigma_r^-1 (U~_r^T S_x) W.
+  GemmDesc a{};
+  a.M = m; a.N = r; a.K = m; a.batch = 1;
+  a.A = Sinv; a.lda = ldsi; a.krange = KR_GE_ROW;  // S_x^-1 upper
+  a.B = cur; a.ldb = r;
+  a.C = U; a.ldc = ldu; a.alpha = 1.f; a.beta = 0.f;
+  KF_TRY(simt_gemm(a, st));
+  KF_TRY(launch_scale_cols(U, ldu, m, r, sigma, false, st));
+  GemmDesc b{};
+  b.M = r; b.N = m; b.K = m; b.batch = 1;
+  b.A = cur; b.lda = r; b.trans_a = true;
+  b.B = Sx; b.ldb = ldsx; b.krange = KR_LE_COL;  // S_x upper: B[k][j] needs k <= j
+  b.C = P; b.ldc = m; b.alpha = 1.f; b.beta = 0.f;
+  KF_TRY(simt_gemm(b, st));
+  GemmDesc c{};
+  c.M = r; c.N = n; c.K = m; c.batch = 1;
+  c.A = P; c.lda = m;
+  c.B = W; c.ldb = ldw; c.b_bf16 = wbf;
+  c.C = V; c.ldc = ldvo; c.alpha = 1.f; c.beta = 0.f;
+  KF_TRY(simt_gemm(c, st));
+  return launch_scale_rows(V, ldvo, r, n, sigma, true, st);
+}
+
+}  // extern "C"

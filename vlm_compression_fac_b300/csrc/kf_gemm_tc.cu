@@ -1,0 +1,400 @@
+// Tensor-core GEMM / SYRK engine for sm_103a: tcgen05.mma (kind::f16, bfloat16 operands,
+// float32 accumulation in tensor memory), operands staged by TMA (cp.async.bulk.tensor,
+// 128-byte swizzle) through a 4-stage mbarrier pipeline, accumulators read back with
+// tcgen05.ld.  One 128 x 256 output tile per CTA of 4 warps:
+//   warp 0 lane 0  TMA producer           warp 1 lane 0  MMA issuer (single thread)
+//   warp 0         TMEM alloc / dealloc    warps 0-3      epilogue (TMEM lanes 32w..32w+31)
+// Several "passes" (A_p, B_p) accumulate into the same tile, which is how float32 operands
+// enter as bfloat16 hi/lo splits.  TC_LOWER visits only the tiles that touch the lower
+// triangle (the covariance SYRK X += A^T A) and writes only i >= j.
+//
+// Every mbarrier wait is bounded (wall-clock limit read from %globaltimer); on expiry the
+// thread records KF_ERR_TIMEOUT in the device status word, the CTA drains what it issued
+// (again bounded), frees its tensor memory and returns.
+#include "kf_internal.cuh"
+
+#include <cstring>
+
+namespace kf {
+namespace {
+
+constexpr int TBM = 128, TBN = 256, TBK = 64, STAGES = 4;
+constexpr uint32_t A_BYTES = TBM * TBK * 2;  // 16 KB
+constexpr uint32_t B_BYTES = TBN * TBK * 2;  // 32 KB
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s
+constexpr int SUPER_M = 8, SUPER_N = 4;
+
+struct TcMaps {
+  CUtensorMap a[3];
+  CUtensorMap b[3];
+};
+
+struct TcArgs {
+  int64_t M, N, K;
+  int npass;
+  float* D;
+  int64_t ldd;
+  int accumulate, sched, krange;
+  int64_t ntm, ntn;
+  int* status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the limit expired.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  uint32_t spins = 0;
+  while (!mbar_try(bar, parity)) {
+    if ((++spins & 255u) == 0 && now_ns() - t0 > WAIT_LIMIT_NS) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
+                                            int32_t y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading / stride byte offsets
+// (all >> 4), descriptor version 1 at bit 46, 128-byte swizzle (value 2 at bits 61..63).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= uint64_t((addr & 0x3FFFFu) >> 4);
+  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D float32, A and B bfloat16, M = 128, N = 256.
+__host__ __device__ constexpr uint32_t make_idesc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+         (uint32_t(TBN >> 3) << 17) | (uint32_t(TBM >> 4) << 24);
+}
+
+__device__ __forceinline__ int64_t lower_limit(int64_t tm) {  // last valid n-tile of row tm
+  return (tm * TBM + TBM - 1) / TBN;
+}
+
+// Maps a linear tile index to (tm, tn): super-tiles of SUPER_M x SUPER_N tiles in
+// row-major order, tiles row-major inside a super-tile; TC_LOWER skips the tiles that lie
+// entirely above the diagonal.
+__device__ bool decode_tile(int64_t idx, const TcArgs& g, int64_t& tm, int64_t& tn) {
+  const int64_t sm_rows = (g.ntm + SUPER_M - 1) / SUPER_M, sm_cols = (g.ntn + SUPER_N - 1) / SUPER_N;
+  for (int64_t sr = 0; sr < sm_rows; ++sr) {
+    for (int64_t sc = 0; sc < sm_cols; ++sc) {
+      const int64_t m_lo = sr * SUPER_M, m_hi = min(g.ntm, m_lo + SUPER_M);
+      const int64_t n_lo = sc * SUPER_N, n_hi = min(g.ntn, n_lo + SUPER_N);
+      if (g.sched == TC_LOWER && n_lo > lower_limit(m_hi - 1)) break;  // rest of row is above
+      for (int64_t r = m_lo; r < m_hi; ++r) {
+        const int64_t lim = g.sched == TC_LOWER ? min(n_hi, lower_limit(r) + 1) : n_hi;
+        const int64_t cnt = lim > n_lo ? lim - n_lo : 0;
+        if (idx < cnt) {
+          tm = r;
+          tn = n_lo + idx;
+          return true;
+        }
+        idx -= cnt;
+      }
+    }
+  }
+  return false;
+}
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
+                                                         const TcArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), done = smem_u32(bars + 2 * STAGES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int64_t tm, tn;
+  if (!decode_tile(blockIdx.x, g, tm, tn)) return;  // uniform over the CTA
+  const int64_t m0 = tm * TBM, n0 = tn * TBN;
+
+  int64_t klo = 0, khi = g.K;
+  if (g.krange == KR_GE_ROW) klo = m0;
+  else if (g.krange == KR_LE_ROW) khi = min(g.K, m0 + TBM);
+  else if (g.krange == KR_GE_COL) klo = n0;
+  else if (g.krange == KR_LE_COL) khi = min(g.K, n0 + TBN);
+  const int64_t nkb = khi > klo ? (khi - klo + TBK - 1) / TBK : 0;
+  const int64_t iters = nkb * g.npass;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    int64_t issued = 0;
+    for (int64_t it = 0; it < iters; ++it) {
+      const int s = int(it % STAGES);
+      const uint32_t ph = uint32_t((it / STAGES) & 1);
+      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
+        raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_EMPTY);
+        atomicExch(&abort_flag, 1);
+        break;
+      }
+      if (*(volatile int*)&abort_flag) break;
+      const int p = int(it / nkb);
+      const int32_t k0 = int32_t(klo + (it % nkb) * TBK);
+      const uint32_t sa = smem_u32(smem + s * STAGE_BYTES), sb = sa + A_BYTES;
+      const uint32_t fb = full0 + 8 * s;
+      mbar_expect_tx(fb, STAGE_BYTES);
+      if (A_MN) {
+        tma_load_2d(sa, &maps.a[p], int32_t(m0), k0, fb);
+        tma_load_2d(sa + 8192, &maps.a[p], int32_t(m0 + 64), k0, fb);
+      } else {
+        tma_load_2d(sa, &maps.a[p], k0, int32_t(m0), fb);
+      }
+      if (B_MN) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) tma_load_2d(sb + 8192 * h, &maps.b[p], int32_t(n0 + 64 * h), k0, fb);
+      } else {
+        tma_load_2d(sb, &maps.b[p], k0, int32_t(n0), fb);
+      }
+      issued = it + 1;
+    }
+    // Drain: every issued stage must have landed before the CTA may exit.
+    for (int64_t it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it) {
+      const int s = int(it % STAGES);
+      const uint32_t ph = uint32_t((it / STAGES) & 1);
+      if (*(volatile int*)&abort_flag) {
+        if (!mbar_wait(full0 + 8 * s, ph)) raise_status(g.status, KF_ERR_TIMEOUT, WAIT_DRAIN);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = make_idesc(A_MN, B_MN);
+    for (int64_t it = 0; it < iters; ++it) {
+      const int s = int(it % STAGES);
+      const uint32_t ph = uint32_t((it / STAGES) & 1);
+      if (!mbar_wait(full0 + 8 * s, ph)) {
+        raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_FULL);
+        atomicExch(&abort_flag, 1);
+        break;
+      }
+      if (*(volatile int*)&abort_flag) break;
+      tc_fence_after();
+      const uint32_t sa = smem_u32(smem + s * STAGE_BYTES), sb = sa + A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < TBK / 16; ++kk) {
+        // A: K-major SW128 (rows of 128 B, 8-row groups 1024 B apart, k-step 32 B) or
+        //    MN-major SW128 (64-wide MN chunks 8 KB apart, 8-row k groups 1024 B apart).
+        const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
+        const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, 8192, 1024) : smem_desc(sb + kk * 32, 16, 1024);
+        tc_mma(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc_commit(empty0 + 8 * s);
+    }
+    tc_commit(done);
+  }
+  __syncwarp();
+
+  // ---------------- epilogue: TMEM -> registers -> global (float32, optional accumulate)
+  bool ok = true;
+  if (!mbar_wait(done, 0)) {
+    raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
+    ok = false;
+  }
+  if (*(volatile int*)&abort_flag) ok = false;
+  tc_fence_after();
+  const int64_t row = m0 + warp * 32 + lane;
+  const bool vec_ok = (g.ldd % 4) == 0;
+#pragma unroll 1
+  for (int c = 0; c < TBN / 32; ++c) {
+    uint32_t v[32];
+    const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + uint32_t(c * 32);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    if (!ok || row >= g.M) continue;
+    const int64_t c0 = n0 + c * 32;
+    if (c0 >= g.N) continue;
+    float* dst = g.D + row * g.ldd + c0;
+    const bool full = c0 + 32 <= g.N && (g.sched != TC_LOWER || c0 + 31 <= row);
+    if (full && vec_ok && iters > 0) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 o = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+        if (g.accumulate) {
+          const float4 old = *reinterpret_cast<const float4*>(dst + j);
+          o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
+        }
+        *reinterpret_cast<float4*>(dst + j) = o;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int64_t col = c0 + j;
+        if (col >= g.N || (g.sched == TC_LOWER && col > row)) continue;
+        const float val = iters > 0 ? __uint_as_float(v[j]) : 0.f;
+        dst[j] = g.accumulate ? dst[j] + val : val;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  }
+}
+
+kf_status encode_operand(kf_ctx* ctx, CUtensorMap* map, const TcOperand& op, int64_t rows_mn,
+                         int64_t k, bool is_b) {
+  // Global tensor: MN-major -> {MN (inner), K}; K-major -> {K (inner), MN}.
+  cuuint64_t dims[2], strides[1];
+  cuuint32_t box[2], estr[2] = {1, 1};
+  if (op.mn_major) {
+    dims[0] = cuuint64_t(rows_mn); dims[1] = cuuint64_t(k);
+    box[0] = 64; box[1] = TBK;
+  } else {
+    dims[0] = cuuint64_t(k); dims[1] = cuuint64_t(rows_mn);
+    box[0] = TBK; box[1] = is_b ? TBN : TBM;
+  }
+  strides[0] = cuuint64_t(op.ld) * 2;
+  if ((reinterpret_cast<uintptr_t>(op.ptr) & 15) != 0 || (strides[0] & 15) != 0)
+    return fail(KF_ERR_INVALID, "tensor-core operand: base must be 16-byte aligned and ld*2 a multiple of 16");
+  if (dims[0] == 0 || dims[1] == 0) return fail(KF_ERR_INVALID, "tensor-core operand: empty");
+  CUresult r = ctx->encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(op.ptr), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KF_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string(int(r)) + ")");
+  return KF_OK;
+}
+
+int64_t count_tiles(const TcGemm& g, int64_t ntm, int64_t ntn) {
+  if (g.sched != TC_LOWER) return ntm * ntn;
+  int64_t c = 0;
+  for (int64_t tm = 0; tm < ntm; ++tm) {
+    const int64_t lim = (tm * TBM + TBM - 1) / TBN + 1;
+    c += lim < ntn ? lim : ntn;
+  }
+  return c;
+}
+
+template <bool AM, bool BM_>
+kf_status launch_tc(const TcMaps& maps, const TcArgs& a, int64_t ntiles, cudaStream_t st) {
+  static bool attr_set = false;  // per instantiation; benign race (idempotent)
+  if (!attr_set) {
+    KF_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<AM, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(SMEM_BYTES)));
+    attr_set = true;
+  }
+  tc_gemm_kernel<AM, BM_><<<unsigned(ntiles), 128, SMEM_BYTES, st>>>(maps, a); note_launch();
+  return check_cuda(cudaGetLastError(), "tc_gemm launch");
+}
+
+}  // namespace
+
+kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return KF_OK;
+  if (g.npass < 1 || g.npass > 3) return fail(KF_ERR_INVALID, "tc_gemm: 1..3 passes");
+  if (!ctx->encode) return fail(KF_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  TcMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  for (int p = 0; p < g.npass; ++p) {
+    if (g.a[p].mn_major != g.a[0].mn_major || g.b[p].mn_major != g.b[0].mn_major)
+      return fail(KF_ERR_INVALID, "tc_gemm: all passes need the same operand majors");
+    KF_TRY(encode_operand(ctx, &maps.a[p], g.a[p], g.M, g.K, false));
+    KF_TRY(encode_operand(ctx, &maps.b[p], g.b[p], g.N, g.K, true));
+  }
+  TcArgs a{};
+  a.M = g.M; a.N = g.N; a.K = g.K; a.npass = g.npass;
+  a.D = g.D; a.ldd = g.ldd;
+  a.accumulate = g.accumulate ? 1 : 0; a.sched = g.sched; a.krange = g.krange;
+  a.ntm = (g.M + TBM - 1) / TBM; a.ntn = (g.N + TBN - 1) / TBN;
+  a.status = ctx->d_status;
+  const int64_t ntiles = count_tiles(g, a.ntm, a.ntn);
+  if (ntiles > 0x7fffffff) return fail(KF_ERR_UNSUPPORTED, "tc_gemm: too many tiles");
+  const bool am = g.a[0].mn_major, bm = g.b[0].mn_major;
+  if (am && bm) return launch_tc<true, true>(maps, a, ntiles, st);
+  if (am) return launch_tc<true, false>(maps, a, ntiles, st);
+  if (bm) return launch_tc<false, true>(maps, a, ntiles, st);
+  return launch_tc<false, false>(maps, a, ntiles, st);
+}
+
+}  // namespace kf

@@ -1,0 +1,141 @@
+// Internal declarations shared by the libkfsvd translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include <string>
+
+#include "../../include/kfsvd.h"
+
+namespace kf {
+
+// Device status word layout (int32[4]): [0] error code (first one wins), [1] detail.
+enum : int { ST_CODE = 0, ST_INFO = 1 };
+
+// Wait-site codes reported with KF_ERR_TIMEOUT.
+enum : int { WAIT_TMA_EMPTY = 1, WAIT_TMA_FULL = 2, WAIT_MMA_DONE = 3, WAIT_DRAIN = 4 };
+
+__device__ __forceinline__ void raise_status(int* st, int code, int info) {
+  if (atomicCAS(st + ST_CODE, 0, code) == 0) st[ST_INFO] = info;
+}
+
+typedef CUresult (*PFN_encodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+}  // namespace kf
+
+struct kf_ctx {
+  int device = 0;
+  int sm_count = 148;
+  int cc_major = 0, cc_minor = 0;
+  int* d_status = nullptr;          // int32[4] on the device
+  kf::PFN_encodeTiled encode = nullptr;
+  // whitened_svd profile (events on the caller's stream; flop counter at d_status + 4)
+  bool prof_enabled = false;
+  bool prof_valid = false;
+  cudaEvent_t prof_ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  int64_t prof_steps = 0;
+  unsigned long long* prof_flops() { return reinterpret_cast<unsigned long long*>(d_status + 4); }
+};
+
+namespace kf {
+
+// Counts kernel launches made by the library (reported by kf_launch_count).
+void note_launch();
+
+// Host-side error reporting (thread-local message).
+kf_status fail(kf_status st, const std::string& msg);
+kf_status check_cuda(cudaError_t e, const char* what);
+#define KF_TRY(expr)                        \
+  do {                                      \
+    kf_status _s = (expr);                  \
+    if (_s != KF_OK) return _s;             \
+  } while (0)
+#define KF_CUDA(expr) KF_TRY(::kf::check_cuda((expr), #expr))
+
+// Bump allocator over a caller workspace (256-byte aligned slices).
+struct Carve {
+  char* base;
+  size_t cap, off = 0;
+  bool dry;  // sizing pass: base may be null
+  Carve(void* b, size_t c, bool dry_run) : base((char*)b), cap(c), dry(dry_run) {}
+  template <typename T>
+  T* take(size_t count) {
+    off = (off + 255) & ~size_t(255);
+    T* p = dry ? nullptr : (T*)(base + off);
+    off += count * sizeof(T);
+    return p;
+  }
+  bool fits() const { return off <= cap; }
+};
+
+// ---------------------------------------------------------------- SIMT GEMM
+// C[M x N] = alpha * op(A) * op(B) + beta * C, float32 accumulation.
+// op(A) is M x K: stored row-major M x K (trans_a = false) or K x M (trans_a = true).
+// op(B) is K x N: stored row-major K x N (trans_b = false) or N x K (trans_b = true).
+enum KRange { KR_FULL = 0, KR_GE_ROW, KR_LE_ROW, KR_GE_COL, KR_LE_COL };
+enum OutMask { OUT_ALL = 0, OUT_LOWER = 1 };
+struct GemmDesc {
+  int64_t M, N, K;
+  const void* A; int64_t lda; int64_t sA; bool a_bf16; bool trans_a;
+  const void* B; int64_t ldb; int64_t sB; bool b_bf16; bool trans_b;
+  float* C; int64_t ldc; int64_t sC;
+  float alpha, beta;
+  int krange, out_mask, batch;
+};
+kf_status simt_gemm(const GemmDesc& g, cudaStream_t st);
+
+// --------------------------------------------------------- tcgen05 GEMM / SYRK
+// D[M x N] (float32, ldd) (+)= sum over passes p of A_p * B_p with bfloat16 operands in
+// global memory.  A_p: M x K, K-major (row-major M x K) or MN-major (row-major K x M).
+// B_p: K x N, K-major (row-major N x K) or MN-major (row-major K x N).
+struct TcOperand {
+  const __nv_bfloat16* ptr;
+  int64_t ld;      // elements
+  bool mn_major;
+};
+enum TcSched { TC_FULL = 0, TC_LOWER = 1 };
+struct TcGemm {
+  int64_t M, N, K;
+  int npass;
+  TcOperand a[3], b[3];
+  float* D; int64_t ldd;
+  bool accumulate;   // D += result (else D = result)
+  int sched;         // TC_LOWER: only tiles touching i >= j, only i >= j written
+  int krange;        // KR_FULL / KR_GE_ROW / KR_LE_ROW / KR_GE_COL / KR_LE_COL
+};
+kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st);
+
+// ------------------------------------------------------------ small kernels
+kf_status launch_fake_quant(const void* in, kf_dtype dt, int64_t rows, int64_t d, int64_t ld,
+                            __nv_bfloat16* out, cudaStream_t st);
+kf_status launch_split_bf16(const float* in, int64_t rows, int64_t d, int64_t ld,
+                            __nv_bfloat16* hi, __nv_bfloat16* lo, int64_t ldo, cudaStream_t st);
+kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
+                          float* scratch, cudaStream_t st);
+kf_status launch_copy(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
+                      int64_t cols, bool transpose, cudaStream_t st);
+kf_status launch_transpose_inplace(float* A, int64_t lda, int64_t n, cudaStream_t st);
+kf_status launch_scale_cols(float* A, int64_t lda, int64_t rows, int64_t cols,
+                            const float* s, bool invert, cudaStream_t st);
+kf_status launch_scale_rows(float* A, int64_t lda, int64_t rows, int64_t cols,
+                            const float* s, bool invert, cudaStream_t st);
+
+// Cholesky: A (n x n, lda) lower triangle in, L out in place (zeros above), and the
+// inverses of the nb x nb diagonal blocks into dinv (n x 64 scratch, row-major).
+constexpr int CHOL_NB = 64;
+kf_status cholesky_lower(kf_ctx* ctx, float* A, int64_t lda, int64_t n, float* dinv,
+                         cudaStream_t st);
+// Inverse of a lower triangular L (n x n) into M (lower, zeros above), using the diagonal
+// block inverses produced by cholesky_lower.
+kf_status trtri_lower(kf_ctx* ctx, const float* L, int64_t ldl, int64_t n, const float* dinv,
+                      float* M, int64_t ldm, float* tmp, cudaStream_t st);
+size_t trtri_tmp_floats(int64_t n);
+
+}  // namespace kf

@@ -1,0 +1,244 @@
+// Memory-bound helper kernels: per-token INT8 fake quantisation (quantisation-aware
+// whitening), float32 -> bfloat16 hi/lo split, covariance finalisation (1/N, mirror,
+// damping), copies/transposes and row/column scaling.
+#include "kf_internal.cuh"
+
+#include <cstdio>
+#include <atomic>
+
+namespace kf {
+
+namespace {
+thread_local std::string g_last_error;
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+unsigned long long launch_count() { return g_launches.load(std::memory_order_relaxed); }
+
+kf_status fail(kf_status st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+kf_status check_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return KF_OK;
+  return fail(KF_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+const char* last_error_cstr() { return g_last_error.c_str(); }
+
+namespace {
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f(T v);
+template <>
+__device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+// LASER Methodology 1 (quantisation-aware whitening): symmetric per-token INT8 fake
+// quantisation.  One CTA per token row; float32 arithmetic with IEEE division.
+template <typename T>
+__global__ void __launch_bounds__(256) fake_quant_kernel(const T* __restrict__ in, int64_t d,
+                                                         int64_t ld, __nv_bfloat16* __restrict__ out) {
+  __shared__ float red[8];
+  const int64_t row = blockIdx.x;
+  const T* x = in + row * ld;
+  float m = 0.f;
+  for (int64_t j = threadIdx.x; j < d; j += blockDim.x) m = fmaxf(m, fabsf(to_f(x[j])));
+  m = warp_max(m);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_max(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float s = __fdiv_rn(red[0], 127.0f);
+  __nv_bfloat16* y = out + row * d;
+  for (int64_t j = threadIdx.x; j < d; j += blockDim.x) {
+    float v = 0.f;
+    if (s > 0.f) {
+      float q = rintf(__fdiv_rn(to_f(x[j]), s));
+      q = fminf(fmaxf(q, -127.f), 127.f);
+      v = __fmul_rn(s, q);
+    }
+    y[j] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void split_kernel(const float* __restrict__ in, int64_t rows, int64_t d, int64_t ld,
+                             __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo,
+                             int64_t ldo) {
+  const int64_t n = rows * d;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / d, c = i - r * d;
+    const float v = in[r * ld + c];
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[r * ldo + c] = h;
+    lo[r * ldo + c] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
+// Sum of the diagonal in float64, fixed order (one CTA).
+__global__ void diag_mean_kernel(const float* __restrict__ C, int64_t ldc, int64_t d,
+                                 int64_t n_tokens, float lambda, float* __restrict__ out) {
+  __shared__ double red[256];
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < d; i += blockDim.x) acc += double(C[i * ldc + i]);
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double mean = red[0] / double(d) / double(n_tokens);
+    out[0] = float(double(lambda) * mean);
+  }
+}
+
+// C[i][j] (i >= j) <- C[i][j] / N (+ damping on the diagonal), mirrored to C[j][i].
+__global__ void finalize_kernel(float* __restrict__ C, int64_t ldc, int64_t d, float inv_n_unused,
+                                float n_tokens_f, const float* __restrict__ damp) {
+  const int64_t i = int64_t(blockIdx.y) * 16 + threadIdx.y;
+  const int64_t j = int64_t(blockIdx.x) * 16 + threadIdx.x;
+  if (i >= d || j > i) return;
+  float v = __fdiv_rn(C[i * ldc + j], n_tokens_f);
+  if (i == j) v += damp[0];
+  C[i * ldc + j] = v;
+  if (i != j) C[j * ldc + i] = v;
+}
+
+__global__ void copy_kernel(const float* __restrict__ src, int64_t lds, float* __restrict__ dst,
+                            int64_t ldd, int64_t rows, int64_t cols, bool transpose) {
+  __shared__ float tile[32][33];
+  const int64_t r0 = int64_t(blockIdx.y) * 32, c0 = int64_t(blockIdx.x) * 32;
+  if (!transpose) {
+    for (int k = threadIdx.y; k < 32; k += 8) {
+      const int64_t r = r0 + k, c = c0 + threadIdx.x;
+      if (r < rows && c < cols) dst[r * ldd + c] = src[r * lds + c];
+    }
+    return;
+  }
+  // dst (rows x cols) = src^T, src is cols x rows.
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int64_t sr = c0 + k, sc = r0 + threadIdx.x;  // src row = dst col
+    if (sr < cols && sc < rows) tile[k][threadIdx.x] = src[sr * lds + sc];
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int64_t r = r0 + k, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) dst[r * ldd + c] = tile[threadIdx.x][k];
+  }
+}
+
+// In-place transpose of a square matrix: one CTA swaps tile (bi, bj) with (bj, bi), bi <= bj.
+__global__ void transpose_inplace_kernel(float* __restrict__ A, int64_t lda, int64_t n, int64_t nt) {
+  __shared__ float ta[32][33], tb[32][33];
+  int64_t l = blockIdx.x, bi = 0;
+  while (l >= nt - bi) { l -= nt - bi; ++bi; }
+  const int64_t bj = bi + l;
+  const int64_t r0 = bi * 32, c0 = bj * 32;
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int64_t r = r0 + k, c = c0 + threadIdx.x;
+    if (r < n && c < n) ta[k][threadIdx.x] = A[r * lda + c];
+    const int64_t r2 = c0 + k, c2 = r0 + threadIdx.x;
+    if (r2 < n && c2 < n) tb[k][threadIdx.x] = A[r2 * lda + c2];
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int64_t r = r0 + k, c = c0 + threadIdx.x;   // (bi, bj) <- tile (bj, bi)^T
+    if (r < n && c < n) A[r * lda + c] = tb[threadIdx.x][k];
+    const int64_t r2 = c0 + k, c2 = r0 + threadIdx.x;  // (bj, bi) <- tile (bi, bj)^T
+    if (r2 < n && c2 < n) A[r2 * lda + c2] = ta[threadIdx.x][k];
+  }
+}
+
+__global__ void scale_kernel(float* __restrict__ A, int64_t lda, int64_t rows, int64_t cols,
+                             const float* __restrict__ s, bool by_col, bool invert) {
+  const int64_t n = rows * cols;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / cols, c = i - r * cols;
+    float f = s[by_col ? c : r];
+    if (invert) f = f > 0.f ? 1.0f / f : 0.f;
+    A[r * lda + c] *= f;
+  }
+}
+
+unsigned grid_for(int64_t n, int per = 256) {
+  int64_t b = (n + per - 1) / per;
+  if (b > 148 * 32) b = 148 * 32;
+  if (b < 1) b = 1;
+  return unsigned(b);
+}
+
+}  // namespace
+
+kf_status launch_fake_quant(const void* in, kf_dtype dt, int64_t rows, int64_t d, int64_t ld,
+                            __nv_bfloat16* out, cudaStream_t st) {
+  if (rows <= 0) return KF_OK;
+  if (dt == KF_BF16)
+    fake_quant_kernel<__nv_bfloat16><<<unsigned(rows), 256, 0, st>>>((const __nv_bfloat16*)in, d, ld, out);
+  else
+    fake_quant_kernel<float><<<unsigned(rows), 256, 0, st>>>((const float*)in, d, ld, out);
+  note_launch();
+  return check_cuda(cudaGetLastError(), "fake_quant launch");
+}
+
+kf_status launch_split_bf16(const float* in, int64_t rows, int64_t d, int64_t ld,
+                            __nv_bfloat16* hi, __nv_bfloat16* lo, int64_t ldo, cudaStream_t st) {
+  if (rows <= 0 || d <= 0) return KF_OK;
+  split_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, hi, lo, ldo); note_launch();
+  return check_cuda(cudaGetLastError(), "split launch");
+}
+
+kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
+                          float* scratch, cudaStream_t st) {
+  diag_mean_kernel<<<1, 256, 0, st>>>(C, ldc, d, n_tokens, lambda, scratch); note_launch();
+  KF_CUDA(cudaGetLastError());
+  dim3 grid(unsigned((d + 15) / 16), unsigned((d + 15) / 16));
+  finalize_kernel<<<grid, dim3(16, 16), 0, st>>>(C, ldc, d, 0.f, float(n_tokens), scratch); note_launch();
+  return check_cuda(cudaGetLastError(), "finalize launch");
+}
+
+kf_status launch_copy(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,
+                      int64_t cols, bool transpose, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  dim3 grid(unsigned((cols + 31) / 32), unsigned((rows + 31) / 32));
+  copy_kernel<<<grid, dim3(32, 8), 0, st>>>(src, lds, dst, ldd, rows, cols, transpose); note_launch();
+  return check_cuda(cudaGetLastError(), "copy launch");
+}
+
+kf_status launch_transpose_inplace(float* A, int64_t lda, int64_t n, cudaStream_t st) {
+  if (n <= 0) return KF_OK;
+  const int64_t nt = (n + 31) / 32;
+  transpose_inplace_kernel<<<unsigned(nt * (nt + 1) / 2), dim3(32, 8), 0, st>>>(A, lda, n, nt); note_launch();
+  return check_cuda(cudaGetLastError(), "transpose launch");
+}
+
+kf_status launch_scale_cols(float* A, int64_t lda, int64_t rows, int64_t cols, const float* s,
+                            bool invert, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  scale_kernel<<<grid_for(rows * cols), 256, 0, st>>>(A, lda, rows, cols, s, true, invert); note_launch();
+  return check_cuda(cudaGetLastError(), "scale launch");
+}
+
+kf_status launch_scale_rows(float* A, int64_t lda, int64_t rows, int64_t cols, const float* s,
+                            bool invert, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  scale_kernel<<<grid_for(rows * cols), 256, 0, st>>>(A, lda, rows, cols, s, false, invert); note_launch();
+  return check_cuda(cudaGetLastError(), "scale launch");
+}
+
+}  // namespace kf

@@ -1,0 +1,266 @@
+"""Thin ctypes binding of libkfsvd.so (include/kfsvd.h): argument marshalling only.
+
+Every function has the name of the C entry point it calls and takes torch tensors for the
+device buffers (PyTorch provides device memory and streams; every step of the path runs in
+the library's CUDA kernels).  Workspace tensors are allocated here with torch when the
+caller does not pass one.  A non-OK status raises KfsvdError.  There is no fallback: if the
+shared library is missing the import fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkfsvd.so")
+
+KF_OK, KF_ERR_INVALID, KF_ERR_WORKSPACE, KF_ERR_CUDA = 0, 1, 2, 3
+KF_ERR_NOT_SPD, KF_ERR_NO_CONVERGENCE, KF_ERR_TIMEOUT, KF_ERR_UNSUPPORTED = 4, 5, 6, 7
+KF_BF16, KF_F32 = 0, 1
+KF_QUANT_NONE, KF_QUANT_INT8_TOKEN = 0, 1
+KF_KEY_HALF_SIGMA2, KF_KEY_PER_PARAM, KF_FIXED_RANK = 0, 1, 2
+KF_SIDE_RIGHT, KF_SIDE_LEFT = 0, 1
+KF_REUSE_SX, KF_REUSE_SG, KF_REUSE_SINV = 1, 2, 4
+
+STATUS_NAMES = {0: "KF_OK", 1: "KF_ERR_INVALID", 2: "KF_ERR_WORKSPACE", 3: "KF_ERR_CUDA",
+                4: "KF_ERR_NOT_SPD", 5: "KF_ERR_NO_CONVERGENCE", 6: "KF_ERR_TIMEOUT",
+                7: "KF_ERR_UNSUPPORTED"}
+
+EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_sync_status", "kf_gram_side",
+            "kfac_accumulate_workspace_size", "kfac_accumulate", "kf_finalize_covariance",
+            "whiten_workspace_size", "whiten", "kf_svd_profile_enable", "kf_svd_profile_read",
+            "whitened_svd_workspace_size", "whitened_svd",
+            "score_and_allocate_workspace_size", "score_and_allocate",
+            "unwhiten_workspace_size", "unwhiten"]
+
+
+class KfsvdError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, str(status)), msg))
+        self.status = status
+
+
+class SvdProblem(ctypes.Structure):
+    _fields_ = [("Wt", ctypes.c_void_p), ("m", ctypes.c_int64), ("n", ctypes.c_int64),
+                ("ldw", ctypes.c_int64), ("sigma", ctypes.c_void_p), ("vecs", ctypes.c_void_p),
+                ("ldv", ctypes.c_int64), ("sweeps", ctypes.c_void_p)]
+
+
+class SvdProfile(ctypes.Structure):
+    _fields_ = [("gram_ms", ctypes.c_float), ("jacobi_ms", ctypes.c_float), ("rayleigh_ms", ctypes.c_float),
+                ("sort_ms", ctypes.c_float), ("jacobi_steps", ctypes.c_int64),
+                ("jacobi_apply_flops", ctypes.c_double)]
+
+
+_P, _I64, _I32, _U32, _F, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
+                                 ctypes.c_float, ctypes.c_size_t)
+_SIGS = {
+    "kf_create": (_I32, [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)]),
+    "kf_destroy": (None, [_P]),
+    "kf_last_error": (ctypes.c_char_p, []),
+    "kf_launch_count": (ctypes.c_uint64, []),
+    "kf_sync_status": (_I32, [_P, _P, ctypes.POINTER(ctypes.c_int32)]),
+    "kf_gram_side": (_I32, [_I64, _I64]),
+    "kfac_accumulate_workspace_size": (_SZ, [_I32, _I32, _I64]),
+    "kfac_accumulate": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _I32, _P, _I64, _P, _SZ, _P]),
+    "kf_finalize_covariance": (_I32, [_P, _P, _I64, _I64, _I64, _F, _P]),
+    "whiten_workspace_size": (_SZ, [_I64, _I64]),
+    "whiten": (_I32, [_P, _P, _I64, _I64, _P, _I64, _I64, _P, _I32, _I64, _U32, _P, _I64, _P, _I64,
+                      _P, _I64, _P, _I64, _P, _SZ, _P]),
+    "kf_svd_profile_enable": (_I32, [_P, ctypes.c_int]),
+    "kf_svd_profile_read": (_I32, [_P, ctypes.POINTER(SvdProfile)]),
+    "whitened_svd_workspace_size": (_SZ, [_I32, _I64, _I64, _I64]),
+    "whitened_svd": (_I32, [_P, _I32, ctypes.POINTER(SvdProblem), _F, _I32, _P, _SZ, _P]),
+    "score_and_allocate_workspace_size": (_SZ, [_I64, _I32]),
+    "score_and_allocate": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "unwhiten_workspace_size": (_SZ, [_I64, _I64, _I32]),
+    "unwhiten": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _I64,
+                        _I32, _P, _I64, _P, _I64, _P, _SZ, _P]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libkfsvd.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libkfsvd.so not found at %s; run __graft_entry__.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(st: int):
+    if st != KF_OK:
+        raise KfsvdError(st, (lib().kf_last_error() or b"").decode())
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _ws(nbytes: int, workspace, device):
+    import torch
+    if nbytes == 0:
+        return None, 0
+    if workspace is not None:
+        return workspace, workspace.numel() * workspace.element_size()
+    return torch.empty(int(nbytes), dtype=torch.uint8, device=device), int(nbytes)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return KF_BF16
+    if t.dtype == torch.float32:
+        return KF_F32
+    raise TypeError("expected bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ld(t) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D row-major tensor with unit column stride")
+    return int(t.stride(0))
+
+
+class Context:
+    """A libkfsvd context on one device (kf_create / kf_destroy / kf_sync_status)."""
+
+    def __init__(self, device: int = 0):
+        h = ctypes.c_void_p()
+        _check(lib().kf_create(int(device), ctypes.byref(h)))
+        self.handle = h.value
+        self.device = device
+
+    def close(self):
+        if self.handle:
+            lib().kf_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def sync_status(self, stream=None) -> int:
+        info = ctypes.c_int32(0)
+        st = lib().kf_sync_status(self.handle, _stream(stream), ctypes.byref(info))
+        if st != KF_OK:
+            raise KfsvdError(st, (lib().kf_last_error() or b"").decode())
+        return info.value
+
+
+def kf_launch_count() -> int:
+    return int(lib().kf_launch_count())
+
+
+def kf_gram_side(m: int, n: int) -> int:
+    return int(lib().kf_gram_side(m, n))
+
+
+def kfac_accumulate_workspace_size(dtype: int, quant: int, d: int) -> int:
+    return int(lib().kfac_accumulate_workspace_size(dtype, quant, d))
+
+
+def kfac_accumulate(ctx: Context, act, cov_sum, quant: int = KF_QUANT_NONE, workspace=None, stream=None):
+    """cov_sum (d x d float32, lower triangle) += act^T act over the rows of act."""
+    n, d = act.shape
+    dt = _dtype_code(act)
+    ws, wsb = _ws(kfac_accumulate_workspace_size(dt, quant, d), workspace, act.device)
+    _check(lib().kfac_accumulate(ctx.handle, _ptr(act), dt, n, d, _ld(act), quant, _ptr(cov_sum),
+                                 _ld(cov_sum), _ptr(ws), wsb, _stream(stream)))
+
+
+def kf_finalize_covariance(ctx: Context, cov, n_tokens: int, lam: float, stream=None):
+    d = cov.shape[0]
+    _check(lib().kf_finalize_covariance(ctx.handle, _ptr(cov), _ld(cov), d, int(n_tokens), float(lam),
+                                        _stream(stream)))
+
+
+def whiten_workspace_size(m: int, n: int) -> int:
+    return int(lib().whiten_workspace_size(m, n))
+
+
+def whiten(ctx: Context, X, G, W, Sx, Sg, Sinv, Wt, flags: int = 0, workspace=None, stream=None):
+    """Cholesky factors S_x (upper), S_g (lower), the Gram-side inverse, and W~ = S_x W S_g."""
+    m, n = W.shape
+    ws, wsb = _ws(whiten_workspace_size(m, n), workspace, W.device)
+    _check(lib().whiten(ctx.handle, _ptr(X), _ld(X), m, _ptr(G), _ld(G), n, _ptr(W), _dtype_code(W), _ld(W),
+                        int(flags), _ptr(Sx), _ld(Sx), _ptr(Sg), _ld(Sg), _ptr(Sinv), _ld(Sinv), _ptr(Wt),
+                        _ld(Wt), _ptr(ws), wsb, _stream(stream)))
+
+
+def kf_svd_profile_enable(ctx: Context, enable: bool = True):
+    _check(lib().kf_svd_profile_enable(ctx.handle, 1 if enable else 0))
+
+
+def kf_svd_profile_read(ctx: Context) -> dict:
+    p = SvdProfile()
+    _check(lib().kf_svd_profile_read(ctx.handle, ctypes.byref(p)))
+    return {k: getattr(p, k) for k, _ in SvdProfile._fields_}
+
+
+def whitened_svd_workspace_size(n_problems: int, m_max: int, n_max: int, s: int) -> int:
+    return int(lib().whitened_svd_workspace_size(n_problems, m_max, n_max, s))
+
+
+def whitened_svd(ctx: Context, Wts: Sequence, sigmas: Sequence, vecs: Sequence, sweeps=None,
+                 tol: float = 1e-6, max_sweeps: int = 30, workspace=None, stream=None):
+    """Batched spectrum of whitened weights of equal min(m, n): sigma descending, vecs the
+    Gram-side singular vectors as columns.  ``sweeps`` is an int32 device tensor (one per
+    problem) or None."""
+    k = len(Wts)
+    probs = (SvdProblem * k)()
+    m_max = n_max = 0
+    for i, (Wt, sg, V) in enumerate(zip(Wts, sigmas, vecs)):
+        m, n = Wt.shape
+        m_max, n_max = max(m_max, m), max(n_max, n)
+        probs[i] = SvdProblem(_ptr(Wt), m, n, _ld(Wt), _ptr(sg), _ptr(V), _ld(V),
+                              0 if sweeps is None else int(sweeps.data_ptr()) + 4 * i)
+    s = min(Wts[0].shape)
+    ws, wsb = _ws(whitened_svd_workspace_size(k, m_max, n_max, s), workspace, Wts[0].device)
+    _check(lib().whitened_svd(ctx.handle, k, probs, float(tol), int(max_sweeps), _ptr(ws), wsb,
+                              _stream(stream)))
+
+
+def score_and_allocate_workspace_size(n_components: int, n_units: int) -> int:
+    return int(lib().score_and_allocate_workspace_size(n_components, n_units))
+
+
+def score_and_allocate(ctx: Context, sigma, seg_offset, cost, budget: int, ranks, mode: int = KF_KEY_HALF_SIGMA2,
+                       fixed_rank=None, cut=None, used=None, workspace=None, stream=None):
+    """Global sort-and-truncate allocation over concatenated spectra (all device tensors)."""
+    n_units = int(cost.numel())
+    n = int(sigma.numel()) if sigma is not None else 0
+    ws, wsb = _ws(score_and_allocate_workspace_size(n, n_units), workspace, ranks.device)
+    _check(lib().score_and_allocate(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
+                                    int(budget), int(mode), _ptr(fixed_rank), _ptr(ranks), _ptr(cut),
+                                    _ptr(used), _ptr(ws), wsb, _stream(stream)))
+
+
+def unwhiten_workspace_size(m: int, n: int, r: int) -> int:
+    return int(lib().unwhiten_workspace_size(m, n, r))
+
+
+def unwhiten(ctx: Context, W, Sx, Sg, Sinv, sigma, vecs, r: int, U, V, workspace=None, stream=None):
+    """Rank-r factors U (m x r), V (r x n) with W ~= U V in the original space."""
+    m, n = W.shape
+    ws, wsb = _ws(unwhiten_workspace_size(m, n, r), workspace, W.device)
+    _check(lib().unwhiten(ctx.handle, _ptr(W), _dtype_code(W), _ld(W), m, n, _ptr(Sx), _ld(Sx), _ptr(Sg),
+                          _ld(Sg), _ptr(Sinv), _ld(Sinv), _ptr(sigma), _ptr(vecs), _ld(vecs), int(r), _ptr(U),
+                          _ld(U) if r > 0 else max(r, 1), _ptr(V), _ld(V), _ptr(ws), wsb, _stream(stream)))
