@@ -218,6 +218,23 @@ KF_API kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64
                              int32_t* ranks, float* cut, int64_t* used, void* workspace,
                              size_t workspace_bytes, kf_stream_t stream);
 
+/* score_and_allocate_noalloc - score_and_allocate for callers that cannot allocate device
+ * memory: for example a host framework that has already handed all device memory to its own
+ * pool, or a caller that must not trigger a device allocation (which may synchronise the
+ * device) in the middle of a job.  It takes no workspace and allocates nothing: its scratch
+ * is a 25 MiB array placed in device memory when the library is loaded, held on every GPU
+ * that loads the library until the process exits.  The papers have no counterpart; this is
+ * a packaging variant of (5a) with identical results.
+ * Limit: n_components <= 1048576 (2^20); larger calls return KF_ERR_UNSUPPORTED before any
+ * launch.  The first call on a device looks up the array's device address (once per
+ * device); make that first call before any stream capture.  Every call reuses the same
+ * array (the parts that must start at zero are cleared by each call): calls that overlap on
+ * the GPU, on any stream or context of the same device, race and must be serialised. */
+KF_API kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset,
+                                            const int64_t* cost, int32_t n_units, int64_t n_components,
+                                            int64_t budget, kf_alloc_mode mode, const int32_t* fixed_rank,
+                                            int32_t* ranks, float* cut, int64_t* used, kf_stream_t stream);
+
 /* ------------------------------------------------------------------------------------
  * (5b) unwhiten - rank-r factors in the original space.
  * LASER Methodology 1: the low-rank factors of W~ are mapped back to the original space.

@@ -10,6 +10,8 @@
 //          the walk stops at the first overflow); ranks = kept count per unit.
 #include "kf_internal.cuh"
 
+#include <mutex>
+
 namespace kf {
 namespace {
 
@@ -339,4 +341,75 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   return check_cuda(cudaGetLastError(), "allocation launch");
 }
 
+// ------------------------------------------------------------------------------------
+// Allocation-free variant of score_and_allocate.  Its scratch (sort keys, digit
+// histograms, prefix sums) lives in one file-scope device array instead of a caller
+// workspace, so neither the library nor the caller allocates device memory for the call.
+// The array is sized for NOALLOC_MAX_COMPONENTS components and stays resident on every
+// GPU that loads the library until the process exits.
+namespace {
+constexpr int64_t NOALLOC_MAX_COMPONENTS = int64_t(1) << 20;
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(25) << 20;  // >= alloc_workspace(1 << 20)
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
+}  // namespace
+
 }  // namespace kf
+
+// Scratch of score_and_allocate_noalloc (file scope, internal linkage).
+static __device__ __align__(256) unsigned char g_alloc_scratch[kf::NOALLOC_SCRATCH_BYTES];
+
+namespace kf {
+
+// Device address of g_alloc_scratch on `device`, looked up once per device with that device
+// current (host code only sees a host-side stand-in for the symbol).
+static kf_status noalloc_scratch(int device, void** out) {
+  if (device < 0 || device >= NOALLOC_MAX_DEVICES) return fail(KF_ERR_UNSUPPORTED, "score_and_allocate_noalloc: device index");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[device]) {
+    if (alloc_workspace(NOALLOC_MAX_COMPONENTS) > NOALLOC_SCRATCH_BYTES)
+      return fail(KF_ERR_UNSUPPORTED, "score_and_allocate_noalloc: static scratch smaller than its stated maximum");
+    int prev = 0;
+    KF_CUDA(cudaGetDevice(&prev));
+    if (prev != device) KF_CUDA(cudaSetDevice(device));
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_alloc_scratch);
+    if (prev != device) cudaSetDevice(prev);
+    if (e != cudaSuccess || !p) return check_cuda(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[device] = p;
+  }
+  *out = g_noalloc_ptr[device];
+  return KF_OK;
+}
+
+}  // namespace kf
+
+extern "C" kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset,
+                                                const int64_t* cost, int32_t n_units, int64_t n_components,
+                                                int64_t budget, kf_alloc_mode mode, const int32_t* fixed_rank,
+                                                int32_t* ranks, float* cut, int64_t* used, kf_stream_t stream) {
+  using namespace kf;
+  if (!ctx) return fail(KF_ERR_INVALID, "score_and_allocate_noalloc: null context");
+  if (n_units <= 0 || n_components < 0) return fail(KF_ERR_INVALID, "score_and_allocate_noalloc: sizes");
+  if (n_components > NOALLOC_MAX_COMPONENTS)
+    return fail(KF_ERR_UNSUPPORTED, "score_and_allocate_noalloc: at most 1048576 components (static scratch limit); "
+                                    "use score_and_allocate with a workspace for more");
+  if (!seg_offset || !cost || !ranks) return fail(KF_ERR_INVALID, "score_and_allocate_noalloc: null pointer");
+  if (mode != KF_KEY_HALF_SIGMA2 && mode != KF_KEY_PER_PARAM && mode != KF_FIXED_RANK)
+    return fail(KF_ERR_INVALID, "score_and_allocate_noalloc: mode");
+  if (mode == KF_FIXED_RANK && !fixed_rank) return fail(KF_ERR_INVALID, "score_and_allocate_noalloc: fixed_rank is null");
+  if (mode != KF_FIXED_RANK && !sigma && n_components > 0)
+    return fail(KF_ERR_INVALID, "score_and_allocate_noalloc: sigma is null");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (mode != KF_FIXED_RANK && n_components == 0) {
+    KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
+    if (used) KF_CUDA(cudaMemsetAsync(used, 0, sizeof(int64_t), st));
+    if (cut) KF_CUDA(cudaMemsetAsync(cut, 0xFF, 2 * sizeof(float), st));
+    return KF_OK;
+  }
+  void* scratch = nullptr;
+  KF_TRY(noalloc_scratch(ctx->device, &scratch));
+  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, ranks, cut, used,
+                   scratch, NOALLOC_SCRATCH_BYTES, st);
+}

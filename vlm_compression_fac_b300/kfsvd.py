@@ -31,7 +31,7 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "kfac_accumulate_workspace_size", "kfac_accumulate", "kf_finalize_covariance",
             "whiten_workspace_size", "whiten", "kf_svd_profile_enable", "kf_svd_profile_read",
             "whitened_svd_workspace_size", "whitened_svd",
-            "score_and_allocate_workspace_size", "score_and_allocate",
+            "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_noalloc",
             "unwhiten_workspace_size", "unwhiten"]
 
 
@@ -74,6 +74,7 @@ _SIGS = {
     "whitened_svd": (_I32, [_P, _I32, ctypes.POINTER(SvdProblem), _F, _I32, _P, _SZ, _P]),
     "score_and_allocate_workspace_size": (_SZ, [_I64, _I32]),
     "score_and_allocate": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "score_and_allocate_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "unwhiten_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "unwhiten": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _I64,
                         _I32, _P, _I64, _P, _I64, _P, _SZ, _P]),
@@ -251,6 +252,17 @@ def score_and_allocate(ctx: Context, sigma, seg_offset, cost, budget: int, ranks
     _check(lib().score_and_allocate(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
                                     int(budget), int(mode), _ptr(fixed_rank), _ptr(ranks), _ptr(cut),
                                     _ptr(used), _ptr(ws), wsb, _stream(stream)))
+
+
+def score_and_allocate_noalloc(ctx: Context, sigma, seg_offset, cost, budget: int, ranks,
+                               mode: int = KF_KEY_HALF_SIGMA2, fixed_rank=None, cut=None, used=None, stream=None):
+    """score_and_allocate without a workspace: for callers that cannot allocate device memory
+    (its scratch is a fixed array inside the library; at most 2**20 components)."""
+    n_units = int(cost.numel())
+    n = int(sigma.numel()) if sigma is not None else 0
+    _check(lib().score_and_allocate_noalloc(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
+                                            int(budget), int(mode), _ptr(fixed_rank), _ptr(ranks), _ptr(cut),
+                                            _ptr(used), _stream(stream)))
 
 
 def unwhiten_workspace_size(m: int, n: int, r: int) -> int:
