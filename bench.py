@@ -41,6 +41,9 @@ def parse():
     ap.add_argument("--impl", default="kfsvd", choices=["kfsvd", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="calibration tokens per site (default: the workload's 131072); a smaller N "
+                         "keeps every matrix shape and is meant for profiler captures")
     return ap.parse_args()
 
 
@@ -126,7 +129,7 @@ def run_kfsvd(args):
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    wl = recipes.llama7b_block()
+    wl = recipes.llama7b_block() if args.tokens is None else recipes.llama7b_block(n_tokens=args.tokens)
     ctx = K.Context(local)
     K.kf_svd_profile_enable(ctx, True)
     units = [pipeline.UnitSpec(u.name, u.m, u.n, u.x_site, u.g_site) for u in wl.units]
