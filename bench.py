@@ -281,6 +281,7 @@ def run_kfsvd(args):
         "kfac_tokens_per_s": round(tokens / ((phases["kfac"]) / K_ / 1e3), 1),
         "phases_ms": {k: round(v / K_, 3) for k, v in phases.items()},
         "svd_profile": svd_prof, "ranks": [int(x) for x in res.ranks.cpu().tolist()],
+        "jacobi_sweeps": [int(u.sweeps) for u in res.units],
         "roofline": roof, "kernels": kern, "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
         "cpu_baseline": cpu,
     }

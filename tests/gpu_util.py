@@ -24,18 +24,21 @@ def bf16_dev(x, torch):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).cuda()
 
 
-def rank_parity(ranks_gpu, alloc_oracle, sig_oracle, tie_rel):
-    """Ranks equal except where every differing component has an oracle score within
-    tie_rel (relative) of the oracle's cut score.  Returns (ok, n_components_moved)."""
-    moved = 0
+def moved_components(ranks_gpu, alloc_oracle, sig_oracle):
+    """Components on which the GPU's and the oracle's ranks disagree, as
+    (unit, component index, relative distance of its oracle score from the oracle's cut)."""
     cut = alloc_oracle.cut_score if np.isfinite(alloc_oracle.cut_score) else alloc_oracle.next_score
+    out = []
     for u, (rg, ro) in enumerate(zip(ranks_gpu, alloc_oracle.ranks)):
         rg, ro = int(rg), int(ro)
-        if rg == ro:
-            continue
-        lo, hi = min(rg, ro), max(rg, ro)
-        sc = 0.5 * np.asarray(sig_oracle[u][lo:hi], dtype=np.float64) ** 2
-        if np.any(np.abs(sc - cut) > tie_rel * abs(cut)):
-            return False, hi - lo
-        moved += hi - lo
-    return True, moved
+        for i in range(min(rg, ro), max(rg, ro)):
+            sc = 0.5 * float(sig_oracle[u][i]) ** 2
+            out.append((u, i, abs(sc - cut) / abs(cut)))
+    return out
+
+
+def rank_parity(ranks_gpu, alloc_oracle, sig_oracle, tie_rel):
+    """Ranks equal except where every differing component has an oracle score within
+    tie_rel (relative) of the oracle's cut score.  Returns (ok, moved components)."""
+    mv = moved_components(ranks_gpu, alloc_oracle, sig_oracle)
+    return all(d <= tie_rel for _, _, d in mv), mv

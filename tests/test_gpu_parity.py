@@ -326,7 +326,7 @@ def test_end_to_end(ctx, which):
         assert np.max(np.abs(s_g - o.sigma)) <= 1e-3 * o.sigma[0], g.name
     ranks = res.ranks.cpu().numpy()
     ok, moved = rank_parity(ranks, ref["alloc"], sig_o, 1e-6)
-    assert ok, (ranks, ref["alloc"].ranks)
+    assert ok, (ranks, ref["alloc"].ranks, moved)
     for g, o in zip(res.units, ref["units"]):
         r = g.rank
         e = O.whitened_error(recipes.gen_weight(wl, wl.units[[u.name for u in wl.units].index(g.name)]),

@@ -23,6 +23,21 @@ using namespace kf;
 namespace {
 
 constexpr int64_t ACC_CHUNK = 8192;  // tokens per preprocessing chunk (float32 / QAW input)
+// Tokens accumulated inside the tensor cores before the partial sum is added to the float32
+// covariance in global memory.  The tensor cores' float32 accumulation loses accuracy on
+// long sums of positive terms: the error of a diagonal entry grows about linearly with the
+// number of tokens summed in one pass (about 6e-4 relative after 131072 tokens, 1e-5 after
+// 4096); 2048-token partials keep it near 5e-6.
+#ifndef KF_SYRK_KCHUNK
+#define KF_SYRK_KCHUNK 2048
+#endif
+constexpr int64_t SYRK_KCHUNK = KF_SYRK_KCHUNK;
+// The same bound for the whitening / unwhitening products (mixed-sign sums of up to 28672
+// terms per pass, several passes per output).
+#ifndef KF_PRODUCT_KCHUNK
+#define KF_PRODUCT_KCHUNK 1024
+#endif
+constexpr int64_t PRODUCT_KCHUNK = KF_PRODUCT_KCHUNK;
 constexpr int FINAL_SLOTS = 1024;
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -127,6 +142,7 @@ kf_status kfac_accumulate(kf_ctx* ctx, const void* act, kf_dtype dtype, int64_t 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   TcGemm g{};
   g.M = d; g.N = d; g.D = cov_sum; g.ldd = ldc; g.accumulate = true; g.sched = TC_LOWER; g.krange = KR_FULL;
+  g.kchunk = SYRK_KCHUNK;
   if (dtype == KF_BF16 && quant == KF_QUANT_NONE) {
     KF_TRY(need((reinterpret_cast<uintptr_t>(act) & 15) == 0 && (ld * 2) % 16 == 0,
                 "kfac_accumulate: bf16 rows need a 16-byte aligned base and ld a multiple of 8"));
@@ -173,11 +189,105 @@ kf_status kf_finalize_covariance(kf_ctx* ctx, float* cov, int64_t ldc, int64_t d
 
 // --------------------------------------------------------------------- (2)+(3)
 namespace {
-size_t whiten_carve(Carve& cv, int64_t m, int64_t n, float** dinv, float** T, float** tt) {
+
+// A matrix operand for the tensor-core engine: bfloat16 planes whose sum is the value
+// (one plane for bfloat16 data; two (hi + lo, 16 significant bits) or three (the full 24-bit
+// float32 significand) for float32 data), 16-byte aligned rows.
+struct Planes {
+  const __nv_bfloat16* p[3];
+  int64_t ld;
+  int n;  // 1, 2 or 3
+};
+
+// Room for the planes of a rows x cols operand.
+struct PlaneBuf {
+  __nv_bfloat16* p[3] = {nullptr, nullptr, nullptr};
+  int64_t ld = 0;
+  int n = 0;
+};
+PlaneBuf take_planes(Carve& cv, int64_t rows, int64_t cols, int nplanes) {
+  PlaneBuf b;
+  b.ld = round_up(cols, 8);
+  b.n = nplanes;
+  for (int i = 0; i < nplanes; ++i) b.p[i] = cv.take<__nv_bfloat16>(size_t(rows) * b.ld);
+  return b;
+}
+
+// float32 rows x cols (ld) -> the buffer's planes (two or three).
+kf_status split_f32(const float* in, int64_t ld, int64_t rows, int64_t cols, const PlaneBuf& b, Planes* out,
+                    cudaStream_t st) {
+  if (b.n == 3) {
+    KF_TRY(launch_split3_bf16(in, rows, cols, ld, b.p[0], b.p[1], b.p[2], b.ld, st));
+  } else {
+    KF_TRY(launch_split_bf16(in, rows, cols, ld, b.p[0], b.p[1], b.ld, st));
+  }
+  *out = Planes{{b.p[0], b.p[1], b.n == 3 ? b.p[2] : nullptr}, b.ld, b.n};
+  return KF_OK;
+}
+
+// A caller matrix (bfloat16 or float32) as planes: bfloat16 rows that are already aligned
+// are used in place; other bfloat16 rows are copied to an aligned plane; float32 is split.
+kf_status as_planes(const void* in, kf_dtype dt, int64_t ld, int64_t rows, int64_t cols, const PlaneBuf& b,
+                    Planes* out, cudaStream_t st) {
+  if (dt == KF_F32) return split_f32(static_cast<const float*>(in), ld, rows, cols, b, out, st);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(in);
+  if ((reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ld % 8) == 0) {
+    *out = Planes{{x, nullptr, nullptr}, ld, 1};
+    return KF_OK;
+  }
+  KF_TRY(launch_copy_bf16(x, rows, cols, ld, b.p[0], b.ld, st));
+  *out = Planes{{b.p[0], nullptr, nullptr}, b.ld, 1};
+  return KF_OK;
+}
+
+// D (M x N float32, ldd) = A B on the tensor cores, A and B given as planes: every cross
+// term A_i B_j with i + j < max(A.n, B.n) (0-based), i.e. all terms down to the last plane's
+// weight; the omitted terms are below the rounding of the planes themselves.  Up to three
+// terms run in one launch, further terms accumulate in a second one.
+// a_mn / b_mn: the operand is stored MN-major (A as K x M rows, B as K x N rows).
+kf_status tc_product(kf_ctx* ctx, int64_t M, int64_t N, int64_t K, const Planes& A, bool a_mn, const Planes& B,
+                     bool b_mn, int krange, float* D, int64_t ldd, cudaStream_t st) {
+  const int L = A.n > B.n ? A.n : B.n;
+  TcOperand ta[9], tb[9];
+  int nt = 0;
+  for (int i = 0; i < A.n; ++i)
+    for (int j = 0; j < B.n; ++j)
+      if (i + j < L) {
+        ta[nt] = TcOperand{A.p[i], A.ld, a_mn};
+        tb[nt] = TcOperand{B.p[j], B.ld, b_mn};
+        ++nt;
+      }
+  for (int t0 = 0; t0 < nt; t0 += 3) {
+    TcGemm g{};
+    g.M = M; g.N = N; g.K = K;
+    g.D = D; g.ldd = ldd; g.accumulate = t0 > 0; g.sched = TC_FULL; g.krange = krange;
+    g.kchunk = PRODUCT_KCHUNK;
+    g.npass = nt - t0 < 3 ? nt - t0 : 3;
+    for (int p = 0; p < g.npass; ++p) {
+      g.a[p] = ta[t0 + p];
+      g.b[p] = tb[t0 + p];
+    }
+    KF_TRY(tc_gemm(ctx, g, st));
+  }
+  return KF_OK;
+}
+
+struct WhitenBufs {
+  float *dinv, *T, *tt;
+  PlaneBuf w, sg, t, sx;
+  int64_t ldT;
+};
+
+size_t whiten_carve(Carve& cv, int64_t m, int64_t n, bool w_f32, WhitenBufs& b) {
   const int64_t mx = m > n ? m : n;
-  *dinv = cv.take<float>(size_t(round_up(mx, CHOL_NB)) * CHOL_NB);
-  *T = cv.take<float>(size_t(m) * n);
-  *tt = cv.take<float>(trtri_tmp_floats(mx));
+  b.dinv = cv.take<float>(size_t(round_up(mx, CHOL_NB)) * CHOL_NB);
+  b.ldT = round_up(n, 8);
+  b.T = cv.take<float>(size_t(m) * b.ldT);
+  b.tt = cv.take<float>(trtri_tmp_floats(mx));
+  b.w = take_planes(cv, m, n, w_f32 ? 3 : 1);
+  b.sg = take_planes(cv, n, n, 3);
+  b.t = take_planes(cv, m, n, 3);
+  b.sx = take_planes(cv, m, m, 3);
   return cv.off;
 }
 }  // namespace
@@ -185,8 +295,8 @@ size_t whiten_carve(Carve& cv, int64_t m, int64_t n, float** dinv, float** T, fl
 size_t whiten_workspace_size(int64_t m, int64_t n) {
   if (m <= 0 || n <= 0) return 0;
   Carve cv(nullptr, 0, true);
-  float *a, *b, *c;
-  return whiten_carve(cv, m, n, &a, &b, &c) + 256;
+  WhitenBufs b;
+  return whiten_carve(cv, m, n, true, b) + 256;
 }
 
 kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const float* G, int64_t ldg, int64_t n,
@@ -202,42 +312,39 @@ kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const floa
   const int64_t s = side == KF_SIDE_RIGHT ? n : m;
   KF_TRY(need(ldsi >= s, "whiten: ldsi"));
   Carve cv(workspace, workspace_bytes, false);
-  float *dinv, *T, *tt;
-  whiten_carve(cv, m, n, &dinv, &T, &tt);
+  WhitenBufs b;
+  whiten_carve(cv, m, n, true, b);
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "whiten: workspace too small");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
   // S_x = chol_lower(X)^T  (and S_x^-1 for the left Gram side)
   if (!(flags & KF_REUSE_SX)) {
     KF_TRY(launch_copy(X, ldx, Sx, ldsx, m, m, false, st));
-    KF_TRY(cholesky_lower(ctx, Sx, ldsx, m, dinv, st));
+    KF_TRY(cholesky_lower(ctx, Sx, ldsx, m, b.dinv, st));
     if (side == KF_SIDE_LEFT && !(flags & KF_REUSE_SINV)) {
-      KF_TRY(trtri_lower(ctx, Sx, ldsx, m, dinv, Sinv, ldsi, tt, st));   // L_x^-1
-      KF_TRY(launch_transpose_inplace(Sinv, ldsi, m, st));               // S_x^-1 = L_x^-T
+      KF_TRY(trtri_lower(ctx, Sx, ldsx, m, b.dinv, Sinv, ldsi, b.tt, st));   // L_x^-1
+      KF_TRY(launch_transpose_inplace(Sinv, ldsi, m, st));                   // S_x^-1 = L_x^-T
     }
-    KF_TRY(launch_transpose_inplace(Sx, ldsx, m, st));                   // S_x = L_x^T
+    KF_TRY(launch_transpose_inplace(Sx, ldsx, m, st));                       // S_x = L_x^T
   }
   // S_g = chol_lower(G)  (and S_g^-1 for the right Gram side)
   if (!(flags & KF_REUSE_SG)) {
     KF_TRY(launch_copy(G, ldg, Sg, ldsg, n, n, false, st));
-    KF_TRY(cholesky_lower(ctx, Sg, ldsg, n, dinv, st));
+    KF_TRY(cholesky_lower(ctx, Sg, ldsg, n, b.dinv, st));
     if (side == KF_SIDE_RIGHT && !(flags & KF_REUSE_SINV)) {
-      KF_TRY(trtri_lower(ctx, Sg, ldsg, n, dinv, Sinv, ldsi, tt, st));
+      KF_TRY(trtri_lower(ctx, Sg, ldsg, n, b.dinv, Sinv, ldsi, b.tt, st));
     }
   }
-  // T = W S_g  (S_g lower: column j needs k >= j), then W~ = S_x T (S_x upper: k >= i).
-  GemmDesc g{};
-  g.M = m; g.N = n; g.K = n; g.batch = 1;
-  g.A = W; g.lda = ldw; g.a_bf16 = w_dtype == KF_BF16;
-  g.B = Sg; g.ldb = ldsg;
-  g.C = T; g.ldc = n; g.alpha = 1.f; g.beta = 0.f; g.krange = KR_GE_COL;
-  KF_TRY(simt_gemm(g, st));
-  GemmDesc h{};
-  h.M = m; h.N = n; h.K = m; h.batch = 1;
-  h.A = Sx; h.lda = ldsx;
-  h.B = T; h.ldb = n;
-  h.C = Wt; h.ldc = ldwt; h.alpha = 1.f; h.beta = 0.f; h.krange = KR_GE_ROW;
-  return simt_gemm(h, st);
+  // Tensor cores, float32 operands as three bfloat16 planes (float32-accurate products):
+  // T = W S_g (S_g lower, so output column j needs k >= j), then W~ = S_x T (S_x upper,
+  // output row i needs k >= i).
+  Planes pw, psg, pt, psx;
+  KF_TRY(as_planes(W, w_dtype, ldw, m, n, b.w, &pw, st));
+  KF_TRY(split_f32(Sg, ldsg, n, n, b.sg, &psg, st));
+  KF_TRY(tc_product(ctx, m, n, n, pw, false, psg, true, KR_GE_COL, b.T, b.ldT, st));
+  KF_TRY(split_f32(b.T, b.ldT, m, n, b.t, &pt, st));
+  KF_TRY(split_f32(Sx, ldsx, m, m, b.sx, &psx, st));
+  return tc_product(ctx, m, n, m, psx, false, pt, true, KR_GE_ROW, Wt, ldwt, st);
 }
 
 // ------------------------------------------------------------------------ (4)
@@ -315,16 +422,27 @@ kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64_t* seg
 
 // ----------------------------------------------------------------------- (5b)
 namespace {
-size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, float** q0, float** q1, float** gm, float** li,
-                      float** dinv, float** tt, float** P) {
+struct UnwhitenBufs {
+  float *q0, *q1, *gm, *li, *dinv, *tt, *P;
+  int64_t ldP;
+  PlaneBuf c, w, sg, si, p;
+};
+
+size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, UnwhitenBufs& b) {
   const int64_t s = m < n ? m : n, mx = m > n ? m : n;
-  *q0 = cv.take<float>(size_t(s) * r);
-  *q1 = cv.take<float>(size_t(s) * r);
-  *gm = cv.take<float>(size_t(r) * r);
-  *li = cv.take<float>(size_t(r) * r);
-  *dinv = cv.take<float>(size_t(round_up(r, CHOL_NB)) * CHOL_NB);
-  *tt = cv.take<float>(trtri_tmp_floats(r));
-  *P = cv.take<float>(size_t(mx) * r);
+  b.q0 = cv.take<float>(size_t(s) * r);
+  b.q1 = cv.take<float>(size_t(s) * r);
+  b.gm = cv.take<float>(size_t(r) * r);
+  b.li = cv.take<float>(size_t(r) * r);
+  b.dinv = cv.take<float>(size_t(round_up(r, CHOL_NB)) * CHOL_NB);
+  b.tt = cv.take<float>(trtri_tmp_floats(r));
+  b.ldP = round_up(mx, 8);
+  b.P = cv.take<float>(size_t(mx) * b.ldP);   // n x r (right side) or r x m (left side)
+  b.c = take_planes(cv, s, r, 2);
+  b.w = take_planes(cv, m, n, 2);
+  b.sg = take_planes(cv, mx, mx, 2);          // S_g (right) or S_x (left)
+  b.si = take_planes(cv, s, s, 2);            // the Gram-side inverse
+  b.p = take_planes(cv, mx, mx, 2);           // P as an operand (n x r or r x m)
   return cv.off;
 }
 }  // namespace
@@ -332,8 +450,8 @@ size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, float** q0, fl
 size_t unwhiten_workspace_size(int64_t m, int64_t n, int32_t r) {
   if (m <= 0 || n <= 0 || r <= 0) return 0;
   Carve cv(nullptr, 0, true);
-  float *a, *b, *c, *d, *e, *f, *g;
-  return unwhiten_carve(cv, m, n, r, &a, &b, &c, &d, &e, &f, &g) + 256;
+  UnwhitenBufs b;
+  return unwhiten_carve(cv, m, n, r, b) + 256;
 }
 
 kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m, int64_t n, const float* Sx,
@@ -348,75 +466,56 @@ kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, in
   KF_TRY(need(W && Sx && Sg && Sinv && sigma && vecs && U && V, "unwhiten: null pointer"));
   KF_TRY(need(ldw >= n && ldsx >= m && ldsg >= n && ldsi >= s && ldv >= s && ldu >= r && ldvo >= n,
               "unwhiten: leading dimension"));
+  KF_TRY(need(w_dtype == KF_BF16 || w_dtype == KF_F32, "unwhiten: dtype"));
   Carve cv(workspace, workspace_bytes, false);
-  float *q0, *q1, *gm, *li, *dinv, *tt, *P;
-  unwhiten_carve(cv, m, n, r, &q0, &q1, &gm, &li, &dinv, &tt, &P);
+  UnwhitenBufs b;
+  unwhiten_carve(cv, m, n, r, b);
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "unwhiten: workspace too small");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  // CholeskyQR2 of the r leading Gram-side vectors: twice Q <- Q R^-1 with R^T R = Q^T Q.
-  KF_TRY(launch_copy(vecs, ldv, q0, r, s, r, false, st));
-  float* cur = q0;
-  float* nxt = q1;
+  // CholeskyQR2 of the r leading Gram-side vectors: twice Q <- Q R^-1 with R^T R = Q^T Q
+  // (float32 SIMT: the Gram of nearly orthonormal columns needs float32 accuracy).
+  KF_TRY(launch_copy(vecs, ldv, b.q0, r, s, r, false, st));
+  float* cur = b.q0;
+  float* nxt = b.q1;
   for (int it = 0; it < 2; ++it) {
     GemmDesc g{};
     g.M = r; g.N = r; g.K = s; g.batch = 1;
     g.A = cur; g.lda = r; g.trans_a = true;
     g.B = cur; g.ldb = r;
-    g.C = gm; g.ldc = r; g.alpha = 1.f; g.beta = 0.f; g.out_mask = OUT_LOWER;
+    g.C = b.gm; g.ldc = r; g.alpha = 1.f; g.beta = 0.f; g.out_mask = OUT_LOWER;
     KF_TRY(simt_gemm(g, st));
-    KF_TRY(cholesky_lower(ctx, gm, r, r, dinv, st));
-    KF_TRY(trtri_lower(ctx, gm, r, r, dinv, li, r, tt, st));
+    KF_TRY(cholesky_lower(ctx, b.gm, r, r, b.dinv, st));
+    KF_TRY(trtri_lower(ctx, b.gm, r, r, b.dinv, b.li, r, b.tt, st));
     GemmDesc h{};
     h.M = s; h.N = r; h.K = r; h.batch = 1;
     h.A = cur; h.lda = r;
-    h.B = li; h.ldb = r; h.trans_b = true; h.krange = KR_LE_COL;  // (L^-1)^T is upper
+    h.B = b.li; h.ldb = r; h.trans_b = true; h.krange = KR_LE_COL;  // (L^-1)^T is upper
     h.C = nxt; h.ldc = r; h.alpha = 1.f; h.beta = 0.f;
     KF_TRY(simt_gemm(h, st));
     float* tmp = cur; cur = nxt; nxt = tmp;
   }
-  const bool wbf = w_dtype == KF_BF16;
+  // The remaining products run on the tensor cores with float32 operands split hi + lo.
+  Planes pc, pw, pf, pi, pp;
+  KF_TRY(split_f32(cur, r, s, r, b.c, &pc, st));
+  KF_TRY(as_planes(W, w_dtype, ldw, m, n, b.w, &pw, st));
   if (kf_gram_side(m, n) == KF_SIDE_RIGHT) {
     // P = S_g V~_r (S_g lower: row i needs k <= i);  U = W P;  V = V~_r^T S_g^-1.
-    GemmDesc a{};
-    a.M = n; a.N = r; a.K = n; a.batch = 1;
-    a.A = Sg; a.lda = ldsg; a.krange = KR_LE_ROW;
-    a.B = cur; a.ldb = r;
-    a.C = P; a.ldc = r; a.alpha = 1.f; a.beta = 0.f;
-    KF_TRY(simt_gemm(a, st));
-    GemmDesc b{};
-    b.M = m; b.N = r; b.K = n; b.batch = 1;
-    b.A = W; b.lda = ldw; b.a_bf16 = wbf;
-    b.B = P; b.ldb = r;
-    b.C = U; b.ldc = ldu; b.alpha = 1.f; b.beta = 0.f;
-    KF_TRY(simt_gemm(b, st));
-    GemmDesc c{};
-    c.M = r; c.N = n; c.K = n; c.batch = 1;
-    c.A = cur; c.lda = r; c.trans_a = true;
-    c.B = Sinv; c.ldb = ldsi; c.krange = KR_GE_COL;  // S_g^-1 lower
-    c.C = V; c.ldc = ldvo; c.alpha = 1.f; c.beta = 0.f;
-    return simt_gemm(c, st);
+    KF_TRY(split_f32(Sg, ldsg, n, n, b.sg, &pf, st));
+    KF_TRY(tc_product(ctx, n, r, n, pf, false, pc, true, KR_LE_ROW, b.P, b.ldP, st));
+    KF_TRY(split_f32(b.P, b.ldP, n, r, b.p, &pp, st));
+    KF_TRY(tc_product(ctx, m, r, n, pw, false, pp, true, KR_FULL, U, ldu, st));
+    KF_TRY(split_f32(Sinv, ldsi, n, n, b.si, &pi, st));
+    return tc_product(ctx, r, n, n, pc, true, pi, true, KR_GE_COL, V, ldvo, st);  // S_g^-1 lower
   }
   // Left side: U = S_x^-1 U~_r Sigma_r;  V = Sigma_r^-1 (U~_r^T S_x) W.
-  GemmDesc a{};
-  a.M = m; a.N = r; a.K = m; a.batch = 1;
-  a.A = Sinv; a.lda = ldsi; a.krange = KR_GE_ROW;  // S_x^-1 upper
-  a.B = cur; a.ldb = r;
-  a.C = U; a.ldc = ldu; a.alpha = 1.f; a.beta = 0.f;
-  KF_TRY(simt_gemm(a, st));
+  KF_TRY(split_f32(Sinv, ldsi, m, m, b.si, &pi, st));
+  KF_TRY(tc_product(ctx, m, r, m, pi, false, pc, true, KR_GE_ROW, U, ldu, st));  // S_x^-1 upper
   KF_TRY(launch_scale_cols(U, ldu, m, r, sigma, false, st));
-  GemmDesc b{};
-  b.M = r; b.N = m; b.K = m; b.batch = 1;
-  b.A = cur; b.lda = r; b.trans_a = true;
-  b.B = Sx; b.ldb = ldsx; b.krange = KR_LE_COL;  // S_x upper: B[k][j] needs k <= j
-  b.C = P; b.ldc = m; b.alpha = 1.f; b.beta = 0.f;
-  KF_TRY(simt_gemm(b, st));
-  GemmDesc c{};
-  c.M = r; c.N = n; c.K = m; c.batch = 1;
-  c.A = P; c.lda = m;
-  c.B = W; c.ldb = ldw; c.b_bf16 = wbf;
-  c.C = V; c.ldc = ldvo; c.alpha = 1.f; c.beta = 0.f;
-  KF_TRY(simt_gemm(c, st));
+  KF_TRY(split_f32(Sx, ldsx, m, m, b.sg, &pf, st));
+  KF_TRY(tc_product(ctx, r, m, m, pc, true, pf, true, KR_LE_COL, b.P, b.ldP, st));  // S_x upper: k <= j
+  KF_TRY(split_f32(b.P, b.ldP, r, m, b.p, &pp, st));
+  KF_TRY(tc_product(ctx, r, n, m, pp, false, pw, true, KR_FULL, V, ldvo, st));
   return launch_scale_rows(V, ldvo, r, n, sigma, true, st);
 }
 

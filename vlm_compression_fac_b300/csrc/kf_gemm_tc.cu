@@ -1,9 +1,14 @@
 // Tensor-core GEMM / SYRK engine for sm_103a: tcgen05.mma (kind::f16, bfloat16 operands,
 // float32 accumulation in tensor memory), operands staged by TMA (cp.async.bulk.tensor,
 // 128-byte swizzle) through a 4-stage mbarrier pipeline, accumulators read back with
-// tcgen05.ld.  One 128 x 256 output tile per CTA of 4 warps:
+// tcgen05.ld.  One 128 x 256 output tile per CTA of 10 warps:
 //   warp 0 lane 0  TMA producer           warp 1 lane 0  MMA issuer (single thread)
-//   warp 0         TMEM alloc / dealloc    warps 0-3      epilogue (TMEM lanes 32w..32w+31)
+//   warp 0         TMEM alloc / dealloc    warps 2-9      epilogue (TMEM lanes 32(w%4)..+31,
+//                                                         128 of the 256 columns each)
+// The K range is cut into chunks (at most `kcb` k-blocks of 64 each): a chunk accumulates
+// in one of two TMEM accumulators while the epilogue warps add the previous chunk into a
+// float32 running sum held in registers (IEEE adds).  Bounding the length of each in-tensor-
+// core accumulation keeps long sums (a covariance over 10^5 tokens) float32-accurate.
 // Several "passes" (A_p, B_p) accumulate into the same tile, which is how float32 operands
 // enter as bfloat16 hi/lo splits.  TC_LOWER visits only the tiles that touch the lower
 // triangle (the covariance SYRK X += A^T A) and writes only i >= j.
@@ -22,7 +27,7 @@ constexpr int TBM = 128, TBN = 256, TBK = 64, STAGES = 4;
 constexpr uint32_t A_BYTES = TBM * TBK * 2;  // 16 KB
 constexpr uint32_t B_BYTES = TBN * TBK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;  // stages + alignment + barriers
 constexpr uint32_t TMEM_COLS = 256;
 constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s
 constexpr int SUPER_M = 8, SUPER_N = 4;
@@ -38,6 +43,7 @@ struct TcArgs {
   float* D;
   int64_t ldd;
   int accumulate, sched, krange;
+  int64_t kcb;   // k-blocks per accumulation chunk (0: the whole K range)
   int64_t ntm, ntn;
   int* status;
 };
@@ -153,13 +159,16 @@ __device__ bool decode_tile(int64_t idx, const TcArgs& g, int64_t& tm, int64_t& 
 }
 
 template <bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
+__global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__ TcMaps maps,
                                                          const TcArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES), done = smem_u32(bars + 2 * STAGES);
+  // bars: full[STAGES] | empty[STAGES] | acc_full[2] | acc_empty[2] | done ; then the TMEM slot
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
+  const uint32_t accf0 = smem_u32(bars + 2 * STAGES), acce0 = smem_u32(bars + 2 * STAGES + 2);
+  const uint32_t done = smem_u32(bars + 2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int64_t tm, tn;
@@ -172,20 +181,26 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   else if (g.krange == KR_GE_COL) klo = n0;
   else if (g.krange == KR_LE_COL) khi = min(g.K, n0 + TBN);
   const int64_t nkb = khi > klo ? (khi - klo + TBK - 1) / TBK : 0;
-  const int64_t iters = nkb * g.npass;
+  const int64_t kcb = (g.kcb > 0 && g.kcb < nkb) ? g.kcb : (nkb > 0 ? nkb : 1);
+  const int64_t nchunks = nkb > 0 ? (nkb + kcb - 1) / kcb : 1;
+  const uint32_t tmem_cols = nchunks > 1 ? 2 * TMEM_COLS : TMEM_COLS;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
+    mbar_init(accf0, 1);
+    mbar_init(accf0 + 8, 1);
+    mbar_init(acce0, 8);
+    mbar_init(acce0 + 8, 8);
     mbar_init(done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(TMEM_COLS)
+                 "r"(tmem_cols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -198,128 +213,183 @@ __global__ void __launch_bounds__(128, 1) tc_gemm_kernel(const __grid_constant__
   if (threadIdx.x == 0) abort_flag = 0;
   __syncthreads();
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    int64_t issued = 0;
-    for (int64_t it = 0; it < iters; ++it) {
-      const int s = int(it % STAGES);
-      const uint32_t ph = uint32_t((it / STAGES) & 1);
-      if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
-        raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_EMPTY);
-        atomicExch(&abort_flag, 1);
-        break;
-      }
-      if (*(volatile int*)&abort_flag) break;
-      const int p = int(it / nkb);
-      const int32_t k0 = int32_t(klo + (it % nkb) * TBK);
-      const uint32_t sa = smem_u32(smem + s * STAGE_BYTES), sb = sa + A_BYTES;
-      const uint32_t fb = full0 + 8 * s;
-      mbar_expect_tx(fb, STAGE_BYTES);
-      if (A_MN) {
-        tma_load_2d(sa, &maps.a[p], int32_t(m0), k0, fb);
-        tma_load_2d(sa + 8192, &maps.a[p], int32_t(m0 + 64), k0, fb);
-      } else {
-        tma_load_2d(sa, &maps.a[p], k0, int32_t(m0), fb);
-      }
-      if (B_MN) {
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: k-blocks of every chunk, every pass
+      int64_t issued = 0, it = 0;
+      for (int64_t c = 0; c < nchunks && nkb > 0; ++c) {
+        const int64_t kb0 = c * kcb, kb1 = min(nkb, kb0 + kcb);
+        for (int p = 0; p < g.npass; ++p) {
+          for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = int(it % STAGES);
+            const uint32_t ph = uint32_t((it / STAGES) & 1);
+            if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
+              raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_EMPTY);
+              atomicExch(&abort_flag, 1);
+            }
+            if (*(volatile int*)&abort_flag) goto producer_done;
+            const int32_t k0 = int32_t(klo + kb * TBK);
+            const uint32_t sa = smem_u32(smem + s * STAGE_BYTES), sb = sa + A_BYTES;
+            const uint32_t fb = full0 + 8 * s;
+            mbar_expect_tx(fb, STAGE_BYTES);
+            if (A_MN) {
+              tma_load_2d(sa, &maps.a[p], int32_t(m0), k0, fb);
+              tma_load_2d(sa + 8192, &maps.a[p], int32_t(m0 + 64), k0, fb);
+            } else {
+              tma_load_2d(sa, &maps.a[p], k0, int32_t(m0), fb);
+            }
+            if (B_MN) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) tma_load_2d(sb + 8192 * h, &maps.b[p], int32_t(n0 + 64 * h), k0, fb);
-      } else {
-        tma_load_2d(sb, &maps.b[p], k0, int32_t(n0), fb);
+              for (int h = 0; h < 4; ++h) tma_load_2d(sb + 8192 * h, &maps.b[p], int32_t(n0 + 64 * h), k0, fb);
+            } else {
+              tma_load_2d(sb, &maps.b[p], k0, int32_t(n0), fb);
+            }
+            issued = it + 1;
+          }
+        }
       }
-      issued = it + 1;
-    }
-    // Drain: every issued stage must have landed before the CTA may exit.
-    for (int64_t it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it) {
-      const int s = int(it % STAGES);
-      const uint32_t ph = uint32_t((it / STAGES) & 1);
+    producer_done:
+      // After an abort, every issued stage must still land before the CTA may exit.
       if (*(volatile int*)&abort_flag) {
-        if (!mbar_wait(full0 + 8 * s, ph)) raise_status(g.status, KF_ERR_TIMEOUT, WAIT_DRAIN);
+        for (int64_t j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
+          if (!mbar_wait(full0 + 8 * int(j % STAGES), uint32_t((j / STAGES) & 1)))
+            raise_status(g.status, KF_ERR_TIMEOUT, WAIT_DRAIN);
+        }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = make_idesc(A_MN, B_MN);
-    for (int64_t it = 0; it < iters; ++it) {
-      const int s = int(it % STAGES);
-      const uint32_t ph = uint32_t((it / STAGES) & 1);
-      if (!mbar_wait(full0 + 8 * s, ph)) {
-        raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_FULL);
-        atomicExch(&abort_flag, 1);
-        break;
-      }
-      if (*(volatile int*)&abort_flag) break;
-      tc_fence_after();
-      const uint32_t sa = smem_u32(smem + s * STAGE_BYTES), sb = sa + A_BYTES;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer (one thread)
+      constexpr uint32_t idesc = make_idesc(A_MN, B_MN);
+      int64_t it = 0;
+      for (int64_t c = 0; c < nchunks; ++c) {
+        const int b = int(c & 1);
+        if (c >= 2 && !*(volatile int*)&abort_flag) {
+          if (!mbar_wait(acce0 + 8 * b, uint32_t(((c >> 1) - 1) & 1))) {
+            raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
+            atomicExch(&abort_flag, 1);
+          }
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + uint32_t(b * TMEM_COLS);
+        const int64_t kb0 = c * kcb, kb1 = nkb > 0 ? min(nkb, kb0 + kcb) : 0;
+        int64_t first = 1;
+        for (int p = 0; p < g.npass && !*(volatile int*)&abort_flag; ++p) {
+          for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = int(it % STAGES);
+            const uint32_t ph = uint32_t((it / STAGES) & 1);
+            if (!mbar_wait(full0 + 8 * s, ph)) {
+              raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_FULL);
+              atomicExch(&abort_flag, 1);
+            }
+            if (*(volatile int*)&abort_flag) break;
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + s * STAGE_BYTES), sb = sa + A_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < TBK / 16; ++kk) {
-        // A: K-major SW128 (rows of 128 B, 8-row groups 1024 B apart, k-step 32 B) or
-        //    MN-major SW128 (64-wide MN chunks 8 KB apart, 8-row k groups 1024 B apart).
-        const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
-        const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, 8192, 1024) : smem_desc(sb + kk * 32, 16, 1024);
-        tc_mma(tmem, ad, bd, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < TBK / 16; ++kk) {
+              // A: K-major SW128 (rows of 128 B, 8-row groups 1024 B apart, k-step 32 B) or
+              //    MN-major SW128 (64-wide MN chunks 8 KB apart, 8-row k groups 1024 B apart).
+              const uint64_t ad = A_MN ? smem_desc(sa + kk * 2048, 8192, 1024) : smem_desc(sa + kk * 32, 16, 1024);
+              const uint64_t bd = B_MN ? smem_desc(sb + kk * 2048, 8192, 1024) : smem_desc(sb + kk * 32, 16, 1024);
+              tc_mma(acc, ad, bd, idesc, (first && kk == 0) ? 0u : 1u);
+            }
+            first = 0;
+            tc_commit(empty0 + 8 * s);
+          }
+        }
+        tc_commit(accf0 + 8 * b);
       }
-      tc_commit(empty0 + 8 * s);
+      tc_commit(done);
     }
-    tc_commit(done);
+  } else {
+    // ---------------- epilogue warps 2..9: warp w reads TMEM lanes 32 (w % 4) .. + 31 (one
+    // output row per thread) and 128 of the 256 columns ((w - 2) / 4 selects the half).  The
+    // chunk partials are summed in registers with IEEE float32 adds; global memory is touched
+    // once per tile, after the last chunk.
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int64_t row = m0 + quarter * 32 + lane;
+    const int64_t col0 = n0 + half * 128;
+    float acc[128];
+#pragma unroll
+    for (int j = 0; j < 128; ++j) acc[j] = 0.f;
+    bool all_ok = true;
+    for (int64_t c = 0; c < nchunks; ++c) {
+      const int b = int(c & 1);
+      bool ok = mbar_wait(accf0 + 8 * b, uint32_t((c >> 1) & 1));
+      if (!ok) {
+        raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
+        atomicExch(&abort_flag, 1);
+      }
+      if (*(volatile int*)&abort_flag) ok = false;
+      all_ok = all_ok && ok;
+      tc_fence_after();
+      if (ok && nkb > 0) {
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t v[32];
+          const uint32_t taddr =
+              tmem + (uint32_t(quarter * 32) << 16) + uint32_t(b * TMEM_COLS + half * 128 + cc * 32);
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+              : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+              : "r"(taddr));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[cc * 32 + j] += __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8 * b) : "memory");
+    }
+    // Write the tile: D = acc (or D += acc), rows < M, columns < N, lower triangle for TC_LOWER.
+    if (all_ok && row < g.M) {
+      const bool vec_ok = (g.ldd % 4) == 0;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int64_t c0 = col0 + cc * 32;
+        if (c0 >= g.N || (g.sched == TC_LOWER && c0 > row)) continue;
+        float* dst = g.D + row * g.ldd + c0;
+        const bool full = vec_ok && c0 + 32 <= g.N && (g.sched != TC_LOWER || c0 + 31 <= row);
+        if (full) {
+          float4 old[8];
+          if (g.accumulate) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) old[j] = reinterpret_cast<const float4*>(dst)[j];
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4 o = make_float4(acc[cc * 32 + 4 * j], acc[cc * 32 + 4 * j + 1], acc[cc * 32 + 4 * j + 2],
+                                   acc[cc * 32 + 4 * j + 3]);
+            if (g.accumulate) {
+              o.x += old[j].x; o.y += old[j].y; o.z += old[j].z; o.w += old[j].w;
+            }
+            reinterpret_cast<float4*>(dst)[j] = o;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t col = c0 + j;
+            if (col >= g.N || (g.sched == TC_LOWER && col > row)) continue;
+            dst[j] = g.accumulate ? dst[j] + acc[cc * 32 + j] : acc[cc * 32 + j];
+          }
+        }
+      }
+    }
   }
   __syncwarp();
-
-  // ---------------- epilogue: TMEM -> registers -> global (float32, optional accumulate)
-  bool ok = true;
-  if (!mbar_wait(done, 0)) {
-    raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
-    ok = false;
-  }
-  if (*(volatile int*)&abort_flag) ok = false;
-  tc_fence_after();
-  const int64_t row = m0 + warp * 32 + lane;
-  const bool vec_ok = (g.ldd % 4) == 0;
-#pragma unroll 1
-  for (int c = 0; c < TBN / 32; ++c) {
-    uint32_t v[32];
-    const uint32_t taddr = tmem + (uint32_t(warp * 32) << 16) + uint32_t(c * 32);
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
-          "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
-          "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-    if (!ok || row >= g.M) continue;
-    const int64_t c0 = n0 + c * 32;
-    if (c0 >= g.N) continue;
-    float* dst = g.D + row * g.ldd + c0;
-    const bool full = c0 + 32 <= g.N && (g.sched != TC_LOWER || c0 + 31 <= row);
-    if (full && vec_ok && iters > 0) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        float4 o = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                               __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-        if (g.accumulate) {
-          const float4 old = *reinterpret_cast<const float4*>(dst + j);
-          o.x += old.x; o.y += old.y; o.z += old.z; o.w += old.w;
-        }
-        *reinterpret_cast<float4*>(dst + j) = o;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int64_t col = c0 + j;
-        if (col >= g.N || (g.sched == TC_LOWER && col > row)) continue;
-        const float val = iters > 0 ? __uint_as_float(v[j]) : 0.f;
-        dst[j] = g.accumulate ? dst[j] + val : val;
-      }
-    }
-  }
+  // Every MMA must have completed before the tensor memory is released.
+  if (!mbar_wait(done, 0)) raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
   }
 }
 
@@ -364,7 +434,7 @@ kf_status launch_tc(const TcMaps& maps, const TcArgs& a, int64_t ntiles, cudaStr
                                  int(SMEM_BYTES)));
     attr_set = true;
   }
-  tc_gemm_kernel<AM, BM_><<<unsigned(ntiles), 128, SMEM_BYTES, st>>>(maps, a); note_launch();
+  tc_gemm_kernel<AM, BM_><<<unsigned(ntiles), 320, SMEM_BYTES, st>>>(maps, a); note_launch();
   return check_cuda(cudaGetLastError(), "tc_gemm launch");
 }
 
@@ -386,6 +456,7 @@ kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st) {
   a.M = g.M; a.N = g.N; a.K = g.K; a.npass = g.npass;
   a.D = g.D; a.ldd = g.ldd;
   a.accumulate = g.accumulate ? 1 : 0; a.sched = g.sched; a.krange = g.krange;
+  a.kcb = g.kchunk > 0 ? (g.kchunk + TBK - 1) / TBK : 0;
   a.ntm = (g.M + TBM - 1) / TBM; a.ntn = (g.N + TBN - 1) / TBN;
   a.status = ctx->d_status;
   const int64_t ntiles = count_tiles(g, a.ntm, a.ntn);

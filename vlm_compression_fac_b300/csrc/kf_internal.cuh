@@ -109,6 +109,8 @@ struct TcGemm {
   bool accumulate;   // D += result (else D = result)
   int sched;         // TC_LOWER: only tiles touching i >= j, only i >= j written
   int krange;        // KR_FULL / KR_GE_ROW / KR_LE_ROW / KR_GE_COL / KR_LE_COL
+  int64_t kchunk;    // longest K range accumulated inside the tensor cores (0: unbounded);
+                     // each chunk's partial result is added to D in float32
 };
 kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st);
 
@@ -117,6 +119,10 @@ kf_status launch_fake_quant(const void* in, kf_dtype dt, int64_t rows, int64_t d
                             __nv_bfloat16* out, cudaStream_t st);
 kf_status launch_split_bf16(const float* in, int64_t rows, int64_t d, int64_t ld,
                             __nv_bfloat16* hi, __nv_bfloat16* lo, int64_t ldo, cudaStream_t st);
+kf_status launch_split3_bf16(const float* in, int64_t rows, int64_t d, int64_t ld, __nv_bfloat16* p1,
+                             __nv_bfloat16* p2, __nv_bfloat16* p3, int64_t ldo, cudaStream_t st);
+kf_status launch_copy_bf16(const __nv_bfloat16* in, int64_t rows, int64_t d, int64_t ld,
+                           __nv_bfloat16* out, int64_t ldo, cudaStream_t st);
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
                           float* scratch, cudaStream_t st);
 kf_status launch_copy(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,

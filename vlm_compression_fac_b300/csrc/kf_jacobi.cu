@@ -8,7 +8,9 @@
 //     shared memory and diagonalises it by threshold cyclic Jacobi (32 disjoint rotations per
 //     round), accumulating the 64 x 64 orthogonal V_p;
 //   * jac_apply: C <- P^T C P and Q <- Q P for the block-diagonal P = diag(V_p), as 64 x 64
-//     tile products (only tiles with p <= q of C, mirrored);
+//     tile products (only tiles with p <= q of C, mirrored; since C stays symmetric the
+//     transposed operand is read from the mirrored tile).  Q is stored transposed (one
+//     eigenvector per row), so Q P becomes P^T Qt, again without any transposition;
 //   * a sweep in which no pair had |c_pq| > tol * sqrt(c_pp c_qq) (entries below a float32
 //     rounding floor count as zero) ends the iteration for that problem.
 // The singular values are then the Rayleigh quotients sigma_i = ||W~ q_i|| / ||q_i||,
@@ -22,7 +24,7 @@
 namespace kf {
 namespace {
 
-constexpr int JB = 32, JP = 64, TS = 68;  // block, pair problem, smem row stride (floats)
+constexpr int JB = 32, JP = 64;  // block width, pair problem size
 
 __device__ __forceinline__ int rr_pos(int pos, int round, int n) {  // circle method
   return pos == 0 ? 0 : 1 + (pos - 1 + round) % (n - 1);
@@ -33,7 +35,7 @@ __device__ __forceinline__ int64_t gidx(int r, int b0, int b1) {  // pair-local 
 }
 
 // ----------------------------------------------------------------------- prepare
-// Mirror the Gram's lower triangle, zero the padding, set Q = I.
+// Mirror the Gram's lower triangle, zero the padding, set Q = I (Q is kept transposed).
 __global__ void jac_prepare_kernel(float* __restrict__ Call, float* __restrict__ Qall, int64_t s,
                                    int64_t sp) {
   const int64_t u = blockIdx.y;
@@ -150,35 +152,41 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
       }
       if (!__syncthreads_or(act)) continue;
       rotated = 1;
-      // Columns: A <- A J, V <- V J.
-      for (int e = t; e < 2 * 32 * JP; e += 256) {
-        const int mat = e >> 11, rem = e & 2047, j = rem >> 6, i = rem & 63;
-        if (!ract[j]) continue;
-        const int p = rp[j], q = rq[j];
-        const float c = rc[j], s = rs[j];
-        float (*M)[JP + 1] = mat ? V : A;
-        const float x = M[i][p], y = M[i][q];
-        M[i][p] = c * x - s * y;
-        M[i][q] = s * x + c * y;
+      // One pass over the 32 x 32 grid of 2 x 2 blocks that this round's pairing cuts A
+      // into: block (j, k) becomes R_j^T A_jk R_k (R = [[c, s], [-s, c]] on (p, q); an
+      // inactive rotation is the identity), the rotated diagonal blocks are set exactly.
+      // Every entry of A belongs to exactly one block, so the pass needs no ordering.
+      for (int e = t; e < 32 * 32; e += 256) {
+        const int j = e >> 5, k = e & 31;
+        const int pj = rp[j], qj = rq[j], pk = rp[k], qk = rq[k];
+        if (j == k) {
+          if (ract[j]) {
+            A[pj][pj] = rap[j];
+            A[qj][qj] = raq[j];
+            A[pj][qj] = 0.f;
+            A[qj][pj] = 0.f;
+          }
+          continue;
+        }
+        if (!ract[j] && !ract[k]) continue;
+        const float cj = rc[j], sj = rs[j], ck = rc[k], sk = rs[k];
+        const float a = A[pj][pk], b = A[pj][qk], c = A[qj][pk], d = A[qj][qk];
+        const float a1 = a * ck - b * sk, b1 = a * sk + b * ck;
+        const float c1 = c * ck - d * sk, d1 = c * sk + d * ck;
+        A[pj][pk] = cj * a1 - sj * c1;
+        A[pj][qk] = cj * b1 - sj * d1;
+        A[qj][pk] = sj * a1 + cj * c1;
+        A[qj][qk] = sj * b1 + cj * d1;
       }
-      __syncthreads();
-      // Rows: A <- J^T A, with the rotated 2 x 2 block set exactly.
+      // V <- V J (columns p_j, q_j of every row).
       for (int e = t; e < 32 * JP; e += 256) {
         const int j = e >> 6, i = e & 63;
         if (!ract[j]) continue;
         const int p = rp[j], q = rq[j];
-        if (i == p) {
-          A[p][p] = rap[j];
-          A[q][p] = 0.f;
-        } else if (i == q) {
-          A[p][q] = 0.f;
-          A[q][q] = raq[j];
-        } else {
-          const float c = rc[j], s = rs[j];
-          const float x = A[p][i], y = A[q][i];
-          A[p][i] = c * x - s * y;
-          A[q][i] = s * x + c * y;
-        }
+        const float c = rc[j], s = rs[j];
+        const float x = V[i][p], y = V[i][q];
+        V[i][p] = c * x - s * y;
+        V[i][q] = s * x + c * y;
       }
       __syncthreads();
     }
@@ -216,17 +224,18 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
 }
 
 // ------------------------------------------------------------------------- apply
-// 64 x 64 x 64 product out = X^T-stored-as-rows * Y: out[i][j] = sum_k Xt[k][i] * Y[k][j].
-__device__ __forceinline__ void mm64(const float (*Xt)[TS], const float (*Y)[TS], float acc[4][4], int tx,
-                                     int ty) {
+// 64 x 64 x 64 product out[i][j] = sum_k X[k][i] * Y[k][j] with X, Y dense row-major
+// 64 x 64 in shared memory; thread (tx, ty) owns rows ty*4..+3, columns tx*4..+3.
+__device__ __forceinline__ void mm64(const float* __restrict__ X, const float* __restrict__ Y, float acc[4][4],
+                                     int tx, int ty) {
 #pragma unroll
   for (int a = 0; a < 4; ++a)
 #pragma unroll
     for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
 #pragma unroll 8
   for (int k = 0; k < JP; ++k) {
-    const float4 x = *reinterpret_cast<const float4*>(&Xt[k][ty * 4]);
-    const float4 y = *reinterpret_cast<const float4*>(&Y[k][tx * 4]);
+    const float4 x = *reinterpret_cast<const float4*>(X + k * JP + ty * 4);
+    const float4 y = *reinterpret_cast<const float4*>(Y + k * JP + tx * 4);
     const float xa[4] = {x.x, x.y, x.z, x.w}, yb[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
     for (int a = 0; a < 4; ++a)
@@ -235,100 +244,166 @@ __device__ __forceinline__ void mm64(const float (*Xt)[TS], const float (*Y)[TS]
   }
 }
 
-__global__ void __launch_bounds__(256) jac_apply_kernel(float* __restrict__ Call, float* __restrict__ Qall,
-                                                        int64_t sp, int nblk, int step,
-                                                        const float* __restrict__ Vall,
-                                                        const int* __restrict__ skipall,
-                                                        const int* __restrict__ conv, int ntile_c,
-                                                        unsigned long long* __restrict__ flops) {
-  extern __shared__ __align__(16) float sm[];
-  float (*Xt)[TS] = reinterpret_cast<float (*)[TS]>(sm);
-  float (*Va)[TS] = reinterpret_cast<float (*)[TS]>(sm + JP * TS);
-  float (*Vb)[TS] = reinterpret_cast<float (*)[TS]>(sm + 2 * JP * TS);
-  float (*Ub)[TS] = reinterpret_cast<float (*)[TS]>(sm + 3 * JP * TS);
+__device__ __forceinline__ void cp_async16(float* smem_dst, const float* gsrc) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-  const int u = blockIdx.y, t = threadIdx.x, tx = t & 15, ty = t >> 4;
-  if (conv[u]) return;
-  const int npairs = nblk / 2;
-  const int* skip = skipall + int64_t(u) * npairs;
-  const float* Vu = Vall + int64_t(u) * npairs * (JP * JP);
-  float* C = Call + int64_t(u) * sp * sp;
-  float* Q = Qall + int64_t(u) * sp * sp;
-  int task = blockIdx.x;
+// One task of a Jacobi step: a tile of C (pair p rows x pair q columns, p <= q) or a
+// 64-column panel cb of the transposed eigenvector matrix for pair q.
+struct ApplyTask {
+  int u, kind, p, q, cb, wp, wq;  // kind 0: C tile, 1: Qt panel; wp/wq: V_p, V_q are applied
+};
 
+__device__ __forceinline__ bool decode_apply(int g, int per_u, int ntile_c, int npairs, const int* __restrict__ skipall,
+                                             const int* __restrict__ conv, ApplyTask& t) {
+  t.u = g / per_u;
+  int task = g - t.u * per_u;
+  if (conv[t.u]) return false;
+  const int* skip = skipall + int64_t(t.u) * npairs;
   if (task < ntile_c) {
     int p = 0;
     while (task >= npairs - p) { task -= npairs - p; ++p; }
-    const int q = p + task;
-    const int sp_ = skip[p], sq = skip[q];
-    if (sp_ && sq) return;
-    if (flops && t == 0) atomicAdd(flops, (unsigned long long)((sp_ ? 0 : 1) + (sq ? 0 : 1)) * 2ull * JP * JP * JP);
-    const int p0 = rr_pos(p, step, nblk), p1 = rr_pos(nblk - 1 - p, step, nblk);
-    const int q0 = rr_pos(q, step, nblk), q1 = rr_pos(nblk - 1 - q, step, nblk);
-    // Xt = T^T where T = C[rows of pair p, cols of pair q].
-    for (int e = t; e < JP * JP; e += 256) {
-      const int i = e >> 6, c = e & 63;
-      Xt[c][i] = C[gidx(i, p0, p1) * sp + gidx(c, q0, q1)];
-      if (!sq) Vb[i][c] = Vu[int64_t(q) * JP * JP + e];
-      if (!sp_) Va[i][c] = Vu[int64_t(p) * JP * JP + e];
+    t.kind = 0; t.p = p; t.q = p + task; t.cb = 0;
+    t.wp = !skip[t.p]; t.wq = !skip[t.q];
+    return t.wp || t.wq;
+  }
+  task -= ntile_c;
+  t.kind = 1; t.cb = task / npairs; t.q = task - t.cb * npairs; t.p = t.q;
+  t.wp = 0; t.wq = !skip[t.q];
+  return t.wq != 0;
+}
+
+// Stage layout (floats): X (64 x 64) | Vp (64 x 64) | Vq (64 x 64).
+constexpr int STAGE_F = 3 * JP * JP;
+
+__device__ __forceinline__ void issue_apply_loads(const ApplyTask& t, float* stage, const float* __restrict__ Call,
+                                                  const float* __restrict__ Qtall, const float* __restrict__ Vall,
+                                                  int64_t sp, int nblk, int step, int npairs, int tid) {
+  const float* C = Call + int64_t(t.u) * sp * sp;
+  const float* Qt = Qtall + int64_t(t.u) * sp * sp;
+  const float* Vu = Vall + int64_t(t.u) * npairs * (JP * JP);
+  const int q0 = rr_pos(t.q, step, nblk), q1 = rr_pos(nblk - 1 - t.q, step, nblk);
+  if (t.kind == 0) {
+    const int p0 = rr_pos(t.p, step, nblk), p1 = rr_pos(nblk - 1 - t.p, step, nblk);
+    // C stays symmetric, so X[k][i] = C[q_k][p_i] is the transpose of T = C[rows p][cols q].
+    for (int e = tid; e < JP * JP / 4; e += 256) {
+      const int k = e >> 4, c = (e & 15) * 4;
+      cp_async16(stage + k * JP + c, C + gidx(k, q0, q1) * sp + gidx(c, p0, p1));
+      if (t.wp) cp_async16(stage + JP * JP + 4 * e, Vu + int64_t(t.p) * JP * JP + 4 * e);
+      if (t.wq) cp_async16(stage + 2 * JP * JP + 4 * e, Vu + int64_t(t.q) * JP * JP + 4 * e);
+    }
+  } else {
+    for (int e = tid; e < JP * JP / 4; e += 256) {
+      const int k = e >> 4, c = (e & 15) * 4;
+      cp_async16(stage + k * JP + c, Qt + gidx(k, q0, q1) * sp + int64_t(t.cb) * JP + c);
+      cp_async16(stage + 2 * JP * JP + 4 * e, Vu + int64_t(t.q) * JP * JP + 4 * e);
+    }
+  }
+}
+
+// Persistent: each CTA walks the tasks of every problem (stride gridDim.x), prefetching the
+// next task's three 16 KB operands with cp.async while it computes the current one.
+__global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ Call, float* __restrict__ Qtall,
+                                                           int64_t sp, int nblk, int step,
+                                                           const float* __restrict__ Vall,
+                                                           const int* __restrict__ skipall,
+                                                           const int* __restrict__ conv, int ntile_c, int per_u,
+                                                           int total, unsigned long long* __restrict__ flops) {
+  extern __shared__ __align__(16) float sm[];
+  float* stages[2] = {sm, sm + STAGE_F};
+  float* Ub = sm + 2 * STAGE_F;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int npairs = nblk / 2;
+
+  ApplyTask cur, nxt;
+  int g = blockIdx.x;
+  while (g < total && !decode_apply(g, per_u, ntile_c, npairs, skipall, conv, cur)) g += gridDim.x;
+  if (g >= total) return;
+  issue_apply_loads(cur, stages[0], Call, Qtall, Vall, sp, nblk, step, npairs, tid);
+  cp_async_commit();
+  int s = 0;
+  unsigned long long done_flops = 0;
+  while (true) {
+    int gn = g + gridDim.x;
+    while (gn < total && !decode_apply(gn, per_u, ntile_c, npairs, skipall, conv, nxt)) gn += gridDim.x;
+    const bool more = gn < total;
+    if (more) {
+      issue_apply_loads(nxt, stages[s ^ 1], Call, Qtall, Vall, sp, nblk, step, npairs, tid);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
+    const float* X = stages[s];
+    const float* Vp = stages[s] + JP * JP;
+    const float* Vq = stages[s] + 2 * JP * JP;
     float acc[4][4];
-    if (!sq) {
-      mm64(Xt, Vb, acc, tx, ty);  // U = T Vq
+    const int q0 = rr_pos(cur.q, step, nblk), q1 = rr_pos(nblk - 1 - cur.q, step, nblk);
+    if (cur.kind == 0) {
+      float* C = Call + int64_t(cur.u) * sp * sp;
+      const int p0 = rr_pos(cur.p, step, nblk), p1 = rr_pos(nblk - 1 - cur.p, step, nblk);
+      if (cur.wq) {
+        mm64(X, Vq, acc, tx, ty);  // U = T Vq
+      } else {
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) acc[a][b] = X[(tx * 4 + b) * JP + ty * 4 + a];
+      }
+      if (cur.wp) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          *reinterpret_cast<float4*>(Ub + (ty * 4 + a) * JP + tx * 4) =
+              make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        __syncthreads();
+        mm64(Vp, Ub, acc, tx, ty);  // T' = Vp^T U
+      }
+      done_flops += (unsigned long long)(cur.wp + cur.wq) * 2ull * JP * JP * JP;
+      // T' (rows ty*4+a, cols tx*4+b) -> C[rows p][cols q]; the mirrored tile gets T'^T,
+      // which this thread holds as four contiguous runs of 4 (rows tx*4+b, cols ty*4..+3).
+      if (cur.p != cur.q) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+          *reinterpret_cast<float4*>(C + gidx(ty * 4 + a, p0, p1) * sp + gidx(tx * 4, q0, q1)) =
+              make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          *reinterpret_cast<float4*>(C + gidx(tx * 4 + b, q0, q1) * sp + gidx(ty * 4, p0, p1)) =
+              make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
+      } else {
+        // Diagonal tile: keep it exactly symmetric by writing entries i <= j to (i, j) and (j, i).
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int i = ty * 4 + a, j = tx * 4 + b;
+            if (i <= j) {
+              C[gidx(i, p0, p1) * sp + gidx(j, p0, p1)] = acc[a][b];
+              C[gidx(j, p0, p1) * sp + gidx(i, p0, p1)] = acc[a][b];
+            }
+          }
+      }
     } else {
+      float* Qt = Qtall + int64_t(cur.u) * sp * sp;
+      mm64(Vq, X, acc, tx, ty);  // Qt[rows q][panel] <- Vq^T Qt[rows q][panel]
+      done_flops += 2ull * JP * JP * JP;
 #pragma unroll
       for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) acc[a][b] = Xt[tx * 4 + b][ty * 4 + a];
+        *reinterpret_cast<float4*>(Qt + gidx(ty * 4 + a, q0, q1) * sp + int64_t(cur.cb) * JP + tx * 4) =
+            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
     }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-      *reinterpret_cast<float4*>(&Ub[ty * 4 + a][tx * 4]) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-    __syncthreads();
-    if (!sp_) {
-      mm64(Va, Ub, acc, tx, ty);  // T' = Vp^T U
-    }
-    // acc holds T' (rows ty*4+a, cols tx*4+b); stage it for the mirrored write.
-    __syncthreads();
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const int i = ty * 4 + a;
-      const int64_t gr = gidx(i, p0, p1);
-      const int64_t gc = gidx(tx * 4, q0, q1);
-      *reinterpret_cast<float4*>(&C[gr * sp + gc]) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-      *reinterpret_cast<float4*>(&Xt[i][tx * 4]) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-    }
-    if (p != q) {
-      __syncthreads();
-      for (int e = t; e < JP * JP; e += 256) {
-        const int a = e >> 6, b = e & 63;  // mirrored tile row a (pair q), col b (pair p)
-        C[gidx(a, q0, q1) * sp + gidx(b, p0, p1)] = Xt[b][a];
-      }
-    }
-    return;
+    __syncthreads();  // the stage and Ub are rewritten by the next iteration's loads
+    if (!more) break;
+    cur = nxt;
+    g = gn;
+    s ^= 1;
   }
-
-  // Q panel: rows rp*64..+63, columns of pair q.
-  task -= ntile_c;
-  const int rp = task / npairs, q = task - (task / npairs) * npairs;
-  if (skip[q]) return;
-  if (flops && t == 0) atomicAdd(flops, 2ull * JP * JP * JP);
-  const int q0 = rr_pos(q, step, nblk), q1 = rr_pos(nblk - 1 - q, step, nblk);
-  for (int e = t; e < JP * JP; e += 256) {
-    const int i = e >> 6, c = e & 63;
-    Xt[c][i] = Q[(int64_t(rp) * JP + i) * sp + gidx(c, q0, q1)];
-    Vb[i][c] = Vu[int64_t(q) * JP * JP + e];
-  }
-  __syncthreads();
-  float acc[4][4];
-  mm64(Xt, Vb, acc, tx, ty);
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const int64_t gr = int64_t(rp) * JP + ty * 4 + a;
-    const int64_t gc = gidx(tx * 4, q0, q1);
-    *reinterpret_cast<float4*>(&Q[gr * sp + gc]) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-  }
+  if (flops && tid == 0 && done_flops) atomicAdd(flops, done_flops);
 }
 
 __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* __restrict__ off, float tol,
@@ -347,23 +422,37 @@ __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* 
 }
 
 // ------------------------------------------------------------- Rayleigh + sort
-// sig2[j] = sum_i Y[i][j]^2 / sum_i Q[i][j]^2 (float64 sums), per column.
-__global__ void col_norms_kernel(const float* __restrict__ Y, int64_t ldy, int64_t rows_y,
-                                 const float* __restrict__ Q, int64_t ldq, int64_t rows_q, int64_t s,
-                                 float* __restrict__ sigma, float* __restrict__ qinv) {
-  const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (j >= s) return;
+// sigma_j^2 = ||y_j||^2 / ||q_j||^2 with y_j = W~ q_j (right side) or W~^T q_j (left side):
+// one CTA per vector j, float64 sums over row j of Yt and of Qt (both contiguous).
+__global__ void __launch_bounds__(256) rayleigh_norms_kernel(const float* __restrict__ Yt, int64_t ldy,
+                                                             int64_t len_y, const float* __restrict__ Qt,
+                                                             int64_t ldq, int64_t len_q,
+                                                             float* __restrict__ sigma, float* __restrict__ qinv) {
+  __shared__ double ra[8], rb[8];
+  const int64_t j = blockIdx.x;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   double a = 0.0, b = 0.0;
-  for (int64_t i = 0; i < rows_y; ++i) {
-    const double v = Y[i * ldy + j];
+  for (int64_t i = threadIdx.x; i < len_y; i += blockDim.x) {
+    const double v = Yt[j * ldy + i];
     a += v * v;
   }
-  for (int64_t i = 0; i < rows_q; ++i) {
-    const double v = Q[i * ldq + j];
+  for (int64_t i = threadIdx.x; i < len_q; i += blockDim.x) {
+    const double v = Qt[j * ldq + i];
     b += v * v;
   }
-  sigma[j] = b > 0.0 ? float(sqrt(a / b)) : 0.f;
-  qinv[j] = b > 0.0 ? float(1.0 / sqrt(b)) : 0.f;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    a += __shfl_xor_sync(0xffffffffu, a, o);
+    b += __shfl_xor_sync(0xffffffffu, b, o);
+  }
+  if (lane == 0) { ra[w] = a; rb[w] = b; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double aa = 0.0, bb = 0.0;
+    for (int x = 0; x < 8; ++x) { aa += ra[x]; bb += rb[x]; }
+    sigma[j] = bb > 0.0 ? float(sqrt(aa / bb)) : 0.f;
+    qinv[j] = bb > 0.0 ? float(1.0 / sqrt(bb)) : 0.f;
+  }
 }
 
 // One CTA per problem: bitonic sort of (sigma, index) by sigma descending, index ascending.
@@ -401,15 +490,28 @@ __global__ void __launch_bounds__(1024) sort_desc_kernel(const float* __restrict
   for (int i = threadIdx.x; i < s; i += blockDim.x) perm_out[u * perm_stride + i] = idx[i];
 }
 
-__global__ void gather_kernel(const float* __restrict__ Q, int64_t ldq, int64_t s, const int* __restrict__ perm,
+// vecs[r][i] = Qt[perm[i]][r] * qinv[perm[i]] (column i of vecs = i-th sorted vector), as
+// 32 x 32 tiles transposed through shared memory so that reads and writes are coalesced.
+__global__ void gather_kernel(const float* __restrict__ Qt, int64_t ldq, int64_t s, const int* __restrict__ perm,
                               const float* __restrict__ sig, const float* __restrict__ qinv,
                               float* __restrict__ vecs, int64_t ldv, float* __restrict__ sigma_out) {
-  const int64_t n = s * s;
-  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < n; e += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = e / s, i = e - r * s;
-    const int j = perm[i];
-    vecs[r * ldv + i] = Q[r * ldq + j] * qinv[j];
-    if (r == 0) sigma_out[i] = sig[j];
+  __shared__ float tile[32][33];
+  const int64_t i0 = int64_t(blockIdx.x) * 32, r0 = int64_t(blockIdx.y) * 32;
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int64_t i = i0 + k, r = r0 + threadIdx.x;
+    if (i < s && r < s) {
+      const int j = perm[i];
+      tile[k][threadIdx.x] = Qt[int64_t(j) * ldq + r] * qinv[j];
+    }
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += 8) {
+    const int64_t r = r0 + k, i = i0 + threadIdx.x;
+    if (r < s && i < s) vecs[r * ldv + i] = tile[threadIdx.x][k];
+  }
+  if (blockIdx.y == 0 && threadIdx.y == 0) {
+    const int64_t i = i0 + threadIdx.x;
+    if (i < s) sigma_out[i] = sig[perm[i]];
   }
 }
 
@@ -512,7 +614,11 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
 
   const int ntile_c = pl.npairs * (pl.npairs + 1) / 2;
   const int ntile_q = int(pl.sp / JP) * pl.npairs;
-  const size_t apply_smem = size_t(4) * JP * TS * sizeof(float);
+  const size_t apply_smem = size_t(2 * STAGE_F + JP * JP) * sizeof(float);
+  const int per_u = ntile_c + ntile_q;
+  const int64_t total_tasks = int64_t(per_u) * nu;
+  if (total_tasks > 0x7fffffff) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: too many Jacobi tasks");
+  const int apply_grid = int(total_tasks < int64_t(ctx->sm_count) * 2 ? total_tasks : int64_t(ctx->sm_count) * 2);
   static bool attr = false;
   if (!attr) {
     KF_CUDA(cudaFuncSetAttribute(jac_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(apply_smem)));
@@ -525,8 +631,8 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
       jac_solve_kernel<<<dim3(pl.npairs, nu), 256, 0, st>>>(C, pl.sp, pl.nblk, step, V, skip, conv, off, flo, tol,
                                                            max_inner); note_launch();
       KF_CUDA(cudaGetLastError());
-      jac_apply_kernel<<<dim3(ntile_c + ntile_q, nu), 256, apply_smem, st>>>(C, Q, pl.sp, pl.nblk, step, V, skip,
-                                                                             conv, ntile_c, flops); note_launch();
+      jac_apply_kernel<<<apply_grid, 256, apply_smem, st>>>(C, Q, pl.sp, pl.nblk, step, V, skip, conv, ntile_c,
+                                                            per_u, int(total_tasks), flops); note_launch();
       KF_CUDA(cudaGetLastError());
     }
     jac_check_kernel<<<1, 256, 0, st>>>(nu, conv, off, tol, sw, max_sweeps, sweeps_dev, ctx->d_status); note_launch();
@@ -548,18 +654,19 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   }
   for (int i = 0; i < nu; ++i) {
     const kf_svd_problem& p = pr[i];
-    const float* Qi = Q + int64_t(i) * pl.sp * pl.sp;
+    const float* Qti = Q + int64_t(i) * pl.sp * pl.sp;  // eigenvectors as rows
     const bool right = kf_gram_side(p.m, p.n) == KF_SIDE_RIGHT;
-    const int64_t rows_y = right ? p.m : p.n;
+    const int64_t len_y = right ? p.m : p.n;
+    // Yt = Qt W~^T (right side, y_j = W~ q_j) or Qt W~ (left side, y_j = W~^T q_j)
     GemmDesc g{};
-    g.M = rows_y; g.N = s; g.K = s; g.batch = 1;
-    g.A = p.Wt; g.lda = p.ldw; g.trans_a = !right;   // W~ (m x n) or W~^T
-    g.B = Qi; g.ldb = pl.sp;
-    g.C = Y; g.ldc = s;
+    g.M = s; g.N = len_y; g.K = s; g.batch = 1;
+    g.A = Qti; g.lda = pl.sp;
+    g.B = p.Wt; g.ldb = p.ldw; g.trans_b = right;
+    g.C = Y; g.ldc = len_y;
     g.alpha = 1.f; g.beta = 0.f;
     KF_TRY(simt_gemm(g, st));
-    col_norms_kernel<<<unsigned((s + 127) / 128), 128, 0, st>>>(Y, s, rows_y, Qi, pl.sp, s, s, sig + int64_t(i) * s,
-                                                                qinv + int64_t(i) * s); note_launch();
+    rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(Y, len_y, len_y, Qti, pl.sp, s, sig + int64_t(i) * s,
+                                                      qinv + int64_t(i) * s); note_launch();
     KF_CUDA(cudaGetLastError());
   }
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[3], st));
@@ -567,11 +674,10 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   KF_CUDA(cudaGetLastError());
   for (int i = 0; i < nu; ++i) {
     const kf_svd_problem& p = pr[i];
-    int64_t n = s * s, blocks = (n + 255) / 256;
-    if (blocks > 148 * 16) blocks = 148 * 16;
-    gather_kernel<<<unsigned(blocks), 256, 0, st>>>(Q + int64_t(i) * pl.sp * pl.sp, pl.sp, s, perm + int64_t(i) * s,
-                                                    sig + int64_t(i) * s, qinv + int64_t(i) * s, p.vecs, p.ldv,
-                                                    p.sigma); note_launch();
+    dim3 grid(unsigned((s + 31) / 32), unsigned((s + 31) / 32));
+    gather_kernel<<<grid, dim3(32, 8), 0, st>>>(Q + int64_t(i) * pl.sp * pl.sp, pl.sp, s, perm + int64_t(i) * s,
+                                                sig + int64_t(i) * s, qinv + int64_t(i) * s, p.vecs, p.ldv, p.sigma);
+    note_launch();
     KF_CUDA(cudaGetLastError());
   }
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[4], st));

@@ -89,6 +89,36 @@ __global__ void split_kernel(const float* __restrict__ in, int64_t rows, int64_t
   }
 }
 
+// x = x1 + x2 + x3 with each term a bfloat16 (8 significant bits): together they hold the
+// full 24-bit float32 significand.
+__global__ void split3_kernel(const float* __restrict__ in, int64_t rows, int64_t d, int64_t ld,
+                              __nv_bfloat16* __restrict__ p1, __nv_bfloat16* __restrict__ p2,
+                              __nv_bfloat16* __restrict__ p3, int64_t ldo) {
+  const int64_t n = rows * d;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / d, c = i - r * d;
+    const float v = in[r * ld + c];
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(h1);
+    const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(h2);
+    p1[r * ldo + c] = h1;
+    p2[r * ldo + c] = h2;
+    p3[r * ldo + c] = __float2bfloat16_rn(r2);
+  }
+}
+
+__global__ void copy_bf16_kernel(const __nv_bfloat16* __restrict__ in, int64_t rows, int64_t d, int64_t ld,
+                                 __nv_bfloat16* __restrict__ out, int64_t ldo) {
+  const int64_t n = rows * d;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / d, c = i - r * d;
+    out[r * ldo + c] = in[r * ld + c];
+  }
+}
+
 // Sum of the diagonal in float64, fixed order (one CTA).
 __global__ void diag_mean_kernel(const float* __restrict__ C, int64_t ldc, int64_t d,
                                  int64_t n_tokens, float lambda, float* __restrict__ out) {
@@ -201,6 +231,20 @@ kf_status launch_split_bf16(const float* in, int64_t rows, int64_t d, int64_t ld
   if (rows <= 0 || d <= 0) return KF_OK;
   split_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, hi, lo, ldo); note_launch();
   return check_cuda(cudaGetLastError(), "split launch");
+}
+
+kf_status launch_split3_bf16(const float* in, int64_t rows, int64_t d, int64_t ld, __nv_bfloat16* p1,
+                             __nv_bfloat16* p2, __nv_bfloat16* p3, int64_t ldo, cudaStream_t st) {
+  if (rows <= 0 || d <= 0) return KF_OK;
+  split3_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, p1, p2, p3, ldo); note_launch();
+  return check_cuda(cudaGetLastError(), "split3 launch");
+}
+
+kf_status launch_copy_bf16(const __nv_bfloat16* in, int64_t rows, int64_t d, int64_t ld,
+                           __nv_bfloat16* out, int64_t ldo, cudaStream_t st) {
+  if (rows <= 0 || d <= 0) return KF_OK;
+  copy_bf16_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, out, ldo); note_launch();
+  return check_cuda(cudaGetLastError(), "copy_bf16 launch");
 }
 
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
