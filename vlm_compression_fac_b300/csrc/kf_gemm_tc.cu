@@ -355,7 +355,11 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
         const int64_t c0 = col0 + cc * 32;
         if (c0 >= g.N || (g.sched == TC_LOWER && c0 > row)) continue;
         float* dst = g.D + row * g.ldd + c0;
-        const bool full = vec_ok && c0 + 32 <= g.N && (g.sched != TC_LOWER || c0 + 31 <= row);
+        bool full = vec_ok && c0 + 32 <= g.N && (g.sched != TC_LOWER || c0 + 31 <= row);
+        if (full && (reinterpret_cast<uintptr_t>(dst) & 15) != 0) {  // alignment self-check
+          raise_status(g.status, KF_ERR_INVALID, 131);
+          full = false;
+        }
         if (full) {
           float4 old[8];
           if (g.accumulate) {

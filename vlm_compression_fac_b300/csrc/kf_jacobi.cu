@@ -26,6 +26,14 @@ namespace {
 
 constexpr int JB = 32, JP = 64;  // block width, pair problem size
 
+// Alignment self-check for vector accesses: a misaligned address is recorded in the status
+// word (KF_ERR_INVALID, info = site) and the access is skipped instead of faulting.
+__device__ __forceinline__ bool aligned16(const void* p, int* st, int site) {
+  if ((reinterpret_cast<uintptr_t>(p) & 15) == 0) return true;
+  raise_status(st, KF_ERR_INVALID, site);
+  return false;
+}
+
 __device__ __forceinline__ int rr_pos(int pos, int round, int n) {  // circle method
   return pos == 0 ? 0 : 1 + (pos - 1 + round) % (n - 1);
 }
@@ -282,7 +290,7 @@ constexpr int STAGE_F = 3 * JP * JP;
 
 __device__ __forceinline__ void issue_apply_loads(const ApplyTask& t, float* stage, const float* __restrict__ Call,
                                                   const float* __restrict__ Qtall, const float* __restrict__ Vall,
-                                                  int64_t sp, int nblk, int step, int npairs, int tid) {
+                                                  int64_t sp, int nblk, int step, int npairs, int tid, int* st) {
   const float* C = Call + int64_t(t.u) * sp * sp;
   const float* Qt = Qtall + int64_t(t.u) * sp * sp;
   const float* Vu = Vall + int64_t(t.u) * npairs * (JP * JP);
@@ -292,15 +300,20 @@ __device__ __forceinline__ void issue_apply_loads(const ApplyTask& t, float* sta
     // C stays symmetric, so X[k][i] = C[q_k][p_i] is the transpose of T = C[rows p][cols q].
     for (int e = tid; e < JP * JP / 4; e += 256) {
       const int k = e >> 4, c = (e & 15) * 4;
-      cp_async16(stage + k * JP + c, C + gidx(k, q0, q1) * sp + gidx(c, p0, p1));
-      if (t.wp) cp_async16(stage + JP * JP + 4 * e, Vu + int64_t(t.p) * JP * JP + 4 * e);
-      if (t.wq) cp_async16(stage + 2 * JP * JP + 4 * e, Vu + int64_t(t.q) * JP * JP + 4 * e);
+      const float* a = C + gidx(k, q0, q1) * sp + gidx(c, p0, p1);
+      if (aligned16(a, st, 101)) cp_async16(stage + k * JP + c, a);
+      const float* vp = Vu + int64_t(t.p) * JP * JP + 4 * e;
+      const float* vq = Vu + int64_t(t.q) * JP * JP + 4 * e;
+      if (t.wp && aligned16(vp, st, 102)) cp_async16(stage + JP * JP + 4 * e, vp);
+      if (t.wq && aligned16(vq, st, 103)) cp_async16(stage + 2 * JP * JP + 4 * e, vq);
     }
   } else {
     for (int e = tid; e < JP * JP / 4; e += 256) {
       const int k = e >> 4, c = (e & 15) * 4;
-      cp_async16(stage + k * JP + c, Qt + gidx(k, q0, q1) * sp + int64_t(t.cb) * JP + c);
-      cp_async16(stage + 2 * JP * JP + 4 * e, Vu + int64_t(t.q) * JP * JP + 4 * e);
+      const float* a = Qt + gidx(k, q0, q1) * sp + int64_t(t.cb) * JP + c;
+      const float* vq = Vu + int64_t(t.q) * JP * JP + 4 * e;
+      if (aligned16(a, st, 104)) cp_async16(stage + k * JP + c, a);
+      if (aligned16(vq, st, 105)) cp_async16(stage + 2 * JP * JP + 4 * e, vq);
     }
   }
 }
@@ -312,7 +325,8 @@ __global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ C
                                                            const float* __restrict__ Vall,
                                                            const int* __restrict__ skipall,
                                                            const int* __restrict__ conv, int ntile_c, int per_u,
-                                                           int total, unsigned long long* __restrict__ flops) {
+                                                           int total, unsigned long long* __restrict__ flops,
+                                                           int* status) {
   extern __shared__ __align__(16) float sm[];
   float* stages[2] = {sm, sm + STAGE_F};
   float* Ub = sm + 2 * STAGE_F;
@@ -323,7 +337,7 @@ __global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ C
   int g = blockIdx.x;
   while (g < total && !decode_apply(g, per_u, ntile_c, npairs, skipall, conv, cur)) g += gridDim.x;
   if (g >= total) return;
-  issue_apply_loads(cur, stages[0], Call, Qtall, Vall, sp, nblk, step, npairs, tid);
+  issue_apply_loads(cur, stages[0], Call, Qtall, Vall, sp, nblk, step, npairs, tid, status);
   cp_async_commit();
   int s = 0;
   unsigned long long done_flops = 0;
@@ -332,7 +346,7 @@ __global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ C
     while (gn < total && !decode_apply(gn, per_u, ntile_c, npairs, skipall, conv, nxt)) gn += gridDim.x;
     const bool more = gn < total;
     if (more) {
-      issue_apply_loads(nxt, stages[s ^ 1], Call, Qtall, Vall, sp, nblk, step, npairs, tid);
+      issue_apply_loads(nxt, stages[s ^ 1], Call, Qtall, Vall, sp, nblk, step, npairs, tid, status);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -368,13 +382,15 @@ __global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ C
       // which this thread holds as four contiguous runs of 4 (rows tx*4+b, cols ty*4..+3).
       if (cur.p != cur.q) {
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-          *reinterpret_cast<float4*>(C + gidx(ty * 4 + a, p0, p1) * sp + gidx(tx * 4, q0, q1)) =
-              make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        for (int a = 0; a < 4; ++a) {
+          float* d = C + gidx(ty * 4 + a, p0, p1) * sp + gidx(tx * 4, q0, q1);
+          if (aligned16(d, status, 106)) *reinterpret_cast<float4*>(d) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        }
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          *reinterpret_cast<float4*>(C + gidx(tx * 4 + b, q0, q1) * sp + gidx(ty * 4, p0, p1)) =
-              make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
+        for (int b = 0; b < 4; ++b) {
+          float* d = C + gidx(tx * 4 + b, q0, q1) * sp + gidx(ty * 4, p0, p1);
+          if (aligned16(d, status, 107)) *reinterpret_cast<float4*>(d) = make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
+        }
       } else {
         // Diagonal tile: keep it exactly symmetric by writing entries i <= j to (i, j) and (j, i).
 #pragma unroll
@@ -393,9 +409,10 @@ __global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ C
       mm64(Vq, X, acc, tx, ty);  // Qt[rows q][panel] <- Vq^T Qt[rows q][panel]
       done_flops += 2ull * JP * JP * JP;
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-        *reinterpret_cast<float4*>(Qt + gidx(ty * 4 + a, q0, q1) * sp + int64_t(cur.cb) * JP + tx * 4) =
-            make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+      for (int a = 0; a < 4; ++a) {
+        float* d = Qt + gidx(ty * 4 + a, q0, q1) * sp + int64_t(cur.cb) * JP + tx * 4;
+        if (aligned16(d, status, 108)) *reinterpret_cast<float4*>(d) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+      }
     }
     __syncthreads();  // the stage and Ub are rewritten by the next iteration's loads
     if (!more) break;
@@ -427,7 +444,8 @@ __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* 
 __global__ void __launch_bounds__(256) rayleigh_norms_kernel(const float* __restrict__ Yt, int64_t ldy,
                                                              int64_t len_y, const float* __restrict__ Qt,
                                                              int64_t ldq, int64_t len_q,
-                                                             float* __restrict__ sigma, float* __restrict__ qinv) {
+                                                             float* __restrict__ sigma, float* __restrict__ qinv,
+                                                             int* status) {
   __shared__ double ra[8], rb[8];
   const int64_t j = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -452,6 +470,7 @@ __global__ void __launch_bounds__(256) rayleigh_norms_kernel(const float* __rest
     for (int x = 0; x < 8; ++x) { aa += ra[x]; bb += rb[x]; }
     sigma[j] = bb > 0.0 ? float(sqrt(aa / bb)) : 0.f;
     qinv[j] = bb > 0.0 ? float(1.0 / sqrt(bb)) : 0.f;
+    if (!isfinite(aa) || !isfinite(bb)) raise_status(status, KF_ERR_INVALID, 141);
   }
 }
 
@@ -464,8 +483,9 @@ __global__ void __launch_bounds__(1024) sort_desc_kernel(const float* __restrict
   const int64_t u = blockIdx.x;
   const float* sig = sig_in + u * s;
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    key[i] = i < s ? sig[i] : -INFINITY;
-    idx[i] = i;
+    const float v = i < s ? sig[i] : -INFINITY;
+    key[i] = isnan(v) ? -INFINITY : v;  // padding and non-numbers sort last
+    idx[i] = i < s ? i : P + i;         // padding after every real index on ties
   }
   __syncthreads();
   for (int kk = 2; kk <= P; kk <<= 1) {
@@ -487,7 +507,7 @@ __global__ void __launch_bounds__(1024) sort_desc_kernel(const float* __restrict
       __syncthreads();
     }
   }
-  for (int i = threadIdx.x; i < s; i += blockDim.x) perm_out[u * perm_stride + i] = idx[i];
+  for (int i = threadIdx.x; i < s; i += blockDim.x) perm_out[u * perm_stride + i] = idx[i] < s ? idx[i] : 0;
 }
 
 // vecs[r][i] = Qt[perm[i]][r] * qinv[perm[i]] (column i of vecs = i-th sorted vector), as
@@ -515,6 +535,265 @@ __global__ void gather_kernel(const float* __restrict__ Qt, int64_t ldq, int64_t
   }
 }
 
+// ------------------------------------------------------ windowed Rayleigh-Ritz refinement
+// The rounding of thousands of block rotations applied as 64-term products leaves the
+// accumulated eigenvectors with couplings of order 1e-5 ||C|| to their neighbours in the
+// spectrum, which the Rayleigh quotient turns into relative errors of order 1e-4 on the
+// smaller kept singular values.  The refinement removes them: with the vectors sorted by
+// Rayleigh value, every window of RW consecutive vectors gets the exact Gram of its images,
+// B = Y_w Y_w^T (y_i = W~ q_i, float32 products summed in float64), which is diagonalised in
+// shared memory; the window's q and y rows are rotated by the eigenvectors.  Two passes with
+// windows offset by RW/2 leave every vector in the interior of one window; couplings to
+// vectors outside the window only enter at second order, divided by large gaps.
+constexpr int RW = 128;
+
+// Dst[r][c] = Src[perm[r]][c] for r < s, zero rows for s <= r < rows; one CTA per row.
+__global__ void gather_rows_kernel(const float* __restrict__ Src, int64_t lds, int64_t prob_src,
+                                   const int* __restrict__ perm, int64_t s, float* __restrict__ Dst, int64_t ldd,
+                                   int64_t prob_dst, int64_t cols) {
+  const int64_t r = blockIdx.x, u = blockIdx.y;
+  float* d = Dst + u * prob_dst + r * ldd;
+  if (r >= s) {
+    for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) d[c] = 0.f;
+    return;
+  }
+  const float* src = Src + u * prob_src + int64_t(perm[u * s + r]) * lds;
+  for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) d[c] = src[c];
+}
+
+// B_w = Y_w Y_w^T for the RW rows of window w of problem u (rows start at off + w * RW):
+// float32 products over k-blocks of 32 columns, block partial sums added in float64.
+__global__ void __launch_bounds__(256) win_gram_kernel(const float* __restrict__ Ys, int64_t ldy, int64_t prob_y,
+                                                       int64_t cols, int64_t off, float* __restrict__ B,
+                                                       int nwin, int* status) {
+  __shared__ __align__(16) float T[32][RW + 4];  // T[k][i] = Y[row i][k0 + k]
+  const int w = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
+  const int tx = t & 15, ty = t >> 4;             // output rows ty*8.., columns tx*8..
+  const float* Y = Ys + int64_t(u) * prob_y + (off + int64_t(w) * RW) * ldy;
+  float part[8][8];
+  double tot[8][8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) tot[a][b] = 0.0;
+  for (int64_t k0 = 0; k0 < cols; k0 += 32) {
+    // 128 rows x 32 columns: lane-consecutive rows, so the transposed shared stores do not conflict
+    for (int e = t; e < RW * 8; e += 256) {
+      const int i = e & (RW - 1), kc = e >> 7;  // kc: 4-column chunk 0..7
+      const int64_t k = k0 + kc * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (k + 3 < cols) {
+        const float* a = Y + int64_t(i) * ldy + k;
+        if (aligned16(a, status, 111)) v = *reinterpret_cast<const float4*>(a);
+      } else {
+        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q = 0; q < 4; ++q)
+          if (k + q < cols) tmp[q] = Y[int64_t(i) * ldy + k + q];
+        v = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
+      }
+      T[kc * 4 + 0][i] = v.x;
+      T[kc * 4 + 1][i] = v.y;
+      T[kc * 4 + 2][i] = v.z;
+      T[kc * 4 + 3][i] = v.w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) part[a][b] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) {
+      const float4 x0 = *reinterpret_cast<const float4*>(&T[k][ty * 8]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&T[k][ty * 8 + 4]);
+      const float4 y0 = *reinterpret_cast<const float4*>(&T[k][tx * 8]);
+      const float4 y1 = *reinterpret_cast<const float4*>(&T[k][tx * 8 + 4]);
+      const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const float yb[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) part[a][b] = fmaf(xa[a], yb[b], part[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) tot[a][b] += double(part[a][b]);
+    __syncthreads();
+  }
+  float* Bw = B + (int64_t(u) * nwin + w) * RW * RW;
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) Bw[(ty * 8 + a) * RW + tx * 8 + b] = float(tot[a][b]);
+}
+
+// Diagonalises B_w (RW x RW, symmetric) in shared memory by threshold cyclic Jacobi (RW/2
+// disjoint rotations per round, one pass over the 2 x 2 blocks of the round's pairing) and
+// writes its eigenvectors as columns of V_w, ordered by eigenvalue, largest first.
+__global__ void __launch_bounds__(256) win_eig_kernel(const float* __restrict__ B, float* __restrict__ Vout,
+                                                      float tol, int max_sweeps, int* status) {
+  extern __shared__ __align__(16) float smw[];
+  float (*A)[RW + 1] = reinterpret_cast<float (*)[RW + 1]>(smw);
+  float (*V)[RW + 1] = reinterpret_cast<float (*)[RW + 1]>(smw + RW * (RW + 1));
+  __shared__ float rc[RW / 2], rs[RW / 2], rap[RW / 2], raq[RW / 2];
+  __shared__ int rp[RW / 2], rq[RW / 2], ract[RW / 2];
+  __shared__ int order[RW];
+  __shared__ float dmax;
+  const int t = threadIdx.x;
+  const int64_t wid = blockIdx.x;
+  const float* Bw = B + wid * RW * RW;
+  for (int e = t; e < RW * RW; e += 256) {
+    const int i = e / RW, j = e % RW;
+    A[i][j] = 0.5f * (Bw[i * RW + j] + Bw[j * RW + i]);
+    V[i][j] = i == j ? 1.f : 0.f;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float m = 0.f;
+    for (int i = 0; i < RW; ++i) m = fmaxf(m, A[i][i]);
+    dmax = m;
+  }
+  __syncthreads();
+  const float flo = 2.f * FLT_EPSILON * dmax;  // couplings below the window's float32 noise count as zero
+  for (int sweep = 0; sweep < max_sweeps; ++sweep) {
+    int rotated = 0;
+    for (int r = 0; r < RW - 1; ++r) {
+      int act = 0;
+      if (t < RW / 2) {
+        const int p = rr_pos(t, r, RW), q = rr_pos(RW - 1 - t, r, RW);
+        const float a = A[p][p], b = A[q][q], d = A[p][q];
+        float c = 1.f, sn = 0.f, td = 0.f;
+        if (fabsf(d) > flo && fabsf(d) > tol * sqrtf(fmaxf(a * b, 0.f))) {
+          const float tau = __fdiv_rn(b - a, 2.f * d);
+          const float tt = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f)));
+          c = 1.0f / sqrtf(fmaf(tt, tt, 1.f));
+          sn = tt * c;
+          td = tt * d;
+          act = 1;
+        }
+        rc[t] = c; rs[t] = sn; rp[t] = p; rq[t] = q; ract[t] = act;
+        rap[t] = a - td; raq[t] = b + td;
+      }
+      if (!__syncthreads_or(act)) continue;
+      rotated = 1;
+      for (int e = t; e < (RW / 2) * (RW / 2); e += 256) {
+        const int j = e / (RW / 2), k = e % (RW / 2);
+        const int pj = rp[j], qj = rq[j], pk = rp[k], qk = rq[k];
+        if (j == k) {
+          if (ract[j]) {
+            A[pj][pj] = rap[j];
+            A[qj][qj] = raq[j];
+            A[pj][qj] = 0.f;
+            A[qj][pj] = 0.f;
+          }
+          continue;
+        }
+        if (!ract[j] && !ract[k]) continue;
+        const float cj = rc[j], sj = rs[j], ck = rc[k], sk = rs[k];
+        const float a = A[pj][pk], b = A[pj][qk], c = A[qj][pk], d = A[qj][qk];
+        const float a1 = a * ck - b * sk, b1 = a * sk + b * ck;
+        const float c1 = c * ck - d * sk, d1 = c * sk + d * ck;
+        A[pj][pk] = cj * a1 - sj * c1;
+        A[pj][qk] = cj * b1 - sj * d1;
+        A[qj][pk] = sj * a1 + cj * c1;
+        A[qj][qk] = sj * b1 + cj * d1;
+      }
+      for (int e = t; e < (RW / 2) * RW; e += 256) {
+        const int j = e / RW, i = e % RW;
+        if (!ract[j]) continue;
+        const int p = rp[j], q = rq[j];
+        const float c = rc[j], sn = rs[j];
+        const float x = V[i][p], y = V[i][q];
+        V[i][p] = c * x - sn * y;
+        V[i][q] = sn * x + c * y;
+      }
+      __syncthreads();
+    }
+    if (!rotated) break;
+  }
+  // Order by eigenvalue, descending (ties: lower index first; a value that is not a number
+  // sorts last), so that `order` is always a permutation of 0..RW-1.
+  if (t < RW) {
+    const float di = isnan(A[t][t]) ? -INFINITY : A[t][t];
+    if (isnan(A[t][t])) raise_status(status, KF_ERR_INVALID, 123);
+    int rank = 0;
+    for (int j = 0; j < RW; ++j) {
+      const float dj = isnan(A[j][j]) ? -INFINITY : A[j][j];
+      rank += (dj > di) || (dj == di && j < t);
+    }
+    order[rank] = t;
+  }
+  __syncthreads();
+  float* Vw = Vout + wid * RW * RW;
+  for (int e = t; e < RW * RW; e += 256) {
+    const int i = e / RW, c = e % RW;
+    int oc = order[c];
+    if (oc < 0 || oc >= RW) {  // bounds self-check
+      raise_status(status, KF_ERR_INVALID, 124);
+      oc = c;
+    }
+    Vw[i * RW + c] = V[i][oc];
+  }
+}
+
+// X_w <- V_w^T X_w in place for the RW rows of every window (rows start at off + w * RW)
+// and one 64-column block per CTA: out[i][j] = sum_k V[k][i] X[k][j].
+__global__ void __launch_bounds__(256) win_rotate_kernel(float* __restrict__ Xs, int64_t ldx, int64_t prob_x,
+                                                         int64_t cols, int64_t off, const float* __restrict__ Vw_all,
+                                                         int nwin, int* status) {
+  extern __shared__ __align__(16) float smr[];
+  float* Vs = smr;              // RW x RW
+  float* Xb = smr + RW * RW;    // RW x 64
+  const int cb = blockIdx.x, w = blockIdx.y % nwin, u = blockIdx.y / nwin, t = threadIdx.x;
+  const float* Vw = Vw_all + (int64_t(u) * nwin + w) * RW * RW;
+  float* X = Xs + int64_t(u) * prob_x + (off + int64_t(w) * RW) * ldx + int64_t(cb) * 64;
+  const int64_t c0 = int64_t(cb) * 64;
+  for (int e = t; e < RW * RW / 4; e += 256)
+    if (aligned16(Vw + 4 * e, status, 121)) reinterpret_cast<float4*>(Vs)[e] = reinterpret_cast<const float4*>(Vw)[e];
+  for (int e = t; e < RW * 16; e += 256) {
+    const int i = e >> 4, c = (e & 15) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c0 + c + 3 < cols) {
+      const float* a = X + int64_t(i) * ldx + c;
+      if (aligned16(a, status, 122)) v = *reinterpret_cast<const float4*>(a);
+    } else {
+      float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < 4; ++q)
+        if (c0 + c + q < cols) tmp[q] = X[int64_t(i) * ldx + c + q];
+      v = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
+    }
+    *reinterpret_cast<float4*>(Xb + i * 64 + c) = v;
+  }
+  __syncthreads();
+  const int tx = t & 15, ty = t >> 4;  // rows ty*8..+7, columns tx*4..+3
+  float acc[8][4];
+#pragma unroll
+  for (int a = 0; a < 8; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < RW; ++k) {
+    const float4 v0 = *reinterpret_cast<const float4*>(Vs + k * RW + ty * 8);
+    const float4 v1 = *reinterpret_cast<const float4*>(Vs + k * RW + ty * 8 + 4);
+    const float4 x = *reinterpret_cast<const float4*>(Xb + k * 64 + tx * 4);
+    const float va[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const float xb[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(va[a], xb[b], acc[a][b]);
+  }
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    const int i = ty * 8 + a;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int64_t c = c0 + tx * 4 + b;
+      if (c < cols) X[int64_t(i) * ldx + tx * 4 + b] = acc[a][b];
+    }
+  }
+}
+
 }  // namespace
 
 struct JacPlan {
@@ -531,30 +810,42 @@ static JacPlan jac_plan(int64_t s) {
   return p;
 }
 
-static size_t svd_carve(Carve& cv, int nu, int64_t m_max, int64_t n_max, int64_t s, float** C, float** Q,
-                        float** V, int** skip, int** conv, unsigned** off, float** flo, float** Y,
-                        float** sig, float** qinv, int** perm) {
+struct SvdBufs {
+  float *C, *Q, *V, *flo, *Y, *sig, *qinv, *Qs, *Ys, *Bw, *Vw;
+  int *skip, *conv, *perm;
+  unsigned* off;
+  int64_t R, lyM;
+  int nwin;
+};
+
+static size_t svd_carve(Carve& cv, int nu, int64_t m_max, int64_t n_max, int64_t s, SvdBufs& b) {
   const JacPlan pl = jac_plan(s);
-  *C = cv.take<float>(size_t(nu) * pl.sp * pl.sp);
-  *Q = cv.take<float>(size_t(nu) * pl.sp * pl.sp);
-  *V = cv.take<float>(size_t(nu) * pl.npairs * JP * JP);
-  *skip = cv.take<int>(size_t(nu) * pl.npairs);
-  *conv = cv.take<int>(nu);
-  *off = cv.take<unsigned>(nu);
-  *flo = cv.take<float>(nu);
-  *Y = cv.take<float>(size_t(m_max > n_max ? m_max : n_max) * s);
-  *sig = cv.take<float>(size_t(nu) * s);
-  *qinv = cv.take<float>(size_t(nu) * s);
-  *perm = cv.take<int>(size_t(nu) * s);
+  // image rows of every problem padded to one length that keeps float4 rows aligned
+  b.lyM = ((m_max > n_max ? m_max : n_max) + 3) / 4 * 4;
+  b.nwin = int((s + RW - 1) / RW);
+  b.R = int64_t(b.nwin) * RW + RW / 2;
+  b.C = cv.take<float>(size_t(nu) * pl.sp * pl.sp);
+  b.Q = cv.take<float>(size_t(nu) * pl.sp * pl.sp);
+  b.V = cv.take<float>(size_t(nu) * pl.npairs * JP * JP);
+  b.skip = cv.take<int>(size_t(nu) * pl.npairs);
+  b.conv = cv.take<int>(nu);
+  b.off = cv.take<unsigned>(nu);
+  b.flo = cv.take<float>(nu);
+  b.Y = cv.take<float>(size_t(nu) * s * b.lyM);
+  b.sig = cv.take<float>(size_t(nu) * s);
+  b.qinv = cv.take<float>(size_t(nu) * s);
+  b.perm = cv.take<int>(size_t(nu) * s);
+  b.Qs = cv.take<float>(size_t(nu) * b.R * pl.sp);
+  b.Ys = cv.take<float>(size_t(nu) * b.R * b.lyM);
+  b.Bw = cv.take<float>(size_t(nu) * b.nwin * RW * RW);
+  b.Vw = cv.take<float>(size_t(nu) * b.nwin * RW * RW);
   return cv.off;
 }
 
 size_t svd_workspace(int32_t nu, int64_t m_max, int64_t n_max, int64_t s) {
   Carve cv(nullptr, 0, true);
-  float *C, *Q, *V, *flo, *Y, *sig, *qinv;
-  int *skip, *conv, *perm;
-  unsigned* off;
-  return svd_carve(cv, nu, m_max, n_max, s, &C, &Q, &V, &skip, &conv, &off, &flo, &Y, &sig, &qinv, &perm) + 256;
+  SvdBufs b;
+  return svd_carve(cv, nu, m_max, n_max, s, b) + 256;
 }
 
 kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, int32_t max_sweeps, void* ws,
@@ -566,11 +857,12 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   }
   const JacPlan pl = jac_plan(s);
   Carve cv(ws, ws_bytes, false);
-  float *C, *Q, *V, *flo, *Y, *sig, *qinv;
-  int *skip, *conv, *perm;
-  unsigned* off;
-  svd_carve(cv, nu, m_max, n_max, s, &C, &Q, &V, &skip, &conv, &off, &flo, &Y, &sig, &qinv, &perm);
+  SvdBufs bf;
+  svd_carve(cv, nu, m_max, n_max, s, bf);
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "whitened_svd: workspace too small");
+  float *C = bf.C, *Q = bf.Q, *V = bf.V, *flo = bf.flo, *sig = bf.sig, *qinv = bf.qinv;
+  int *skip = bf.skip, *conv = bf.conv, *perm = bf.perm;
+  unsigned* off = bf.off;
 
   const bool prof = ctx->prof_enabled;
   unsigned long long* flops = prof ? ctx->prof_flops() : nullptr;
@@ -603,10 +895,10 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   {
     dim3 grid(unsigned((pl.sp * pl.sp + 255) / 256 > 4096 ? 4096 : (pl.sp * pl.sp + 255) / 256), unsigned(nu));
     jac_prepare_kernel<<<grid, 256, 0, st>>>(C, Q, s, pl.sp); note_launch();
-    KF_CUDA(cudaGetLastError());
+    KF_TRY(check_cuda(cudaGetLastError(), "jac_prepare_kernel"));
     int* sweeps_tmp = nullptr;
     jac_floor_kernel<<<nu, 256, 0, st>>>(C, pl.sp, flo, 8.0f, conv, off, sweeps_tmp); note_launch();
-    KF_CUDA(cudaGetLastError());
+    KF_TRY(check_cuda(cudaGetLastError(), "jac_floor_kernel"));
   }
   // Per-problem sweep counters (copied to the callers' pointers after the sweeps).
   int* sweeps_dev = perm;  // reuse: perm is rewritten by the sort afterwards
@@ -630,55 +922,93 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     for (int step = 0; step < pl.nblk - 1; ++step) {
       jac_solve_kernel<<<dim3(pl.npairs, nu), 256, 0, st>>>(C, pl.sp, pl.nblk, step, V, skip, conv, off, flo, tol,
                                                            max_inner); note_launch();
-      KF_CUDA(cudaGetLastError());
+      KF_TRY(check_cuda(cudaGetLastError(), "jac_solve_kernel"));
       jac_apply_kernel<<<apply_grid, 256, apply_smem, st>>>(C, Q, pl.sp, pl.nblk, step, V, skip, conv, ntile_c,
-                                                            per_u, int(total_tasks), flops); note_launch();
-      KF_CUDA(cudaGetLastError());
+                                                            per_u, int(total_tasks), flops, ctx->d_status); note_launch();
+      KF_TRY(check_cuda(cudaGetLastError(), "jac_apply_kernel"));
     }
     jac_check_kernel<<<1, 256, 0, st>>>(nu, conv, off, tol, sw, max_sweeps, sweeps_dev, ctx->d_status); note_launch();
-    KF_CUDA(cudaGetLastError());
+    KF_TRY(check_cuda(cudaGetLastError(), "jac_check_kernel"));
   }
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[2], st));
   for (int i = 0; i < nu; ++i)
     if (pr[i].sweeps) KF_CUDA(cudaMemcpyAsync(pr[i].sweeps, sweeps_dev + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
 
-  // Rayleigh quotients on W~ itself, then sort and gather.
+  // Rayleigh quotients on W~ itself, sort, windowed Rayleigh-Ritz refinement, final sort.
   int P = 1;
   while (P < s) P <<= 1;
   const size_t sort_smem = size_t(P) * 8;
   if (sort_smem > 227 * 1024) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: s too large for the in-CTA sort");
+  const size_t eig_smem = size_t(2) * RW * (RW + 1) * sizeof(float);
+  const size_t rot_smem = size_t(RW * RW + RW * 64) * sizeof(float);
   static bool sattr = false;
   if (!sattr) {
     KF_CUDA(cudaFuncSetAttribute(sort_desc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
+    KF_CUDA(cudaFuncSetAttribute(win_eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(eig_smem)));
+    KF_CUDA(cudaFuncSetAttribute(win_rotate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(rot_smem)));
     sattr = true;
   }
+  const int64_t lyM = bf.lyM, R = bf.R;
+  const int nwin = bf.nwin;
+  KF_CUDA(cudaMemsetAsync(bf.Y, 0, sizeof(float) * size_t(nu) * s * lyM, st));
   for (int i = 0; i < nu; ++i) {
     const kf_svd_problem& p = pr[i];
     const float* Qti = Q + int64_t(i) * pl.sp * pl.sp;  // eigenvectors as rows
     const bool right = kf_gram_side(p.m, p.n) == KF_SIDE_RIGHT;
     const int64_t len_y = right ? p.m : p.n;
+    float* Yi = bf.Y + int64_t(i) * s * lyM;
     // Yt = Qt W~^T (right side, y_j = W~ q_j) or Qt W~ (left side, y_j = W~^T q_j)
     GemmDesc g{};
     g.M = s; g.N = len_y; g.K = s; g.batch = 1;
     g.A = Qti; g.lda = pl.sp;
     g.B = p.Wt; g.ldb = p.ldw; g.trans_b = right;
-    g.C = Y; g.ldc = len_y;
+    g.C = Yi; g.ldc = lyM;
     g.alpha = 1.f; g.beta = 0.f;
     KF_TRY(simt_gemm(g, st));
-    rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(Y, len_y, len_y, Qti, pl.sp, s, sig + int64_t(i) * s,
-                                                      qinv + int64_t(i) * s); note_launch();
-    KF_CUDA(cudaGetLastError());
+    rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(Yi, lyM, len_y, Qti, pl.sp, s, sig + int64_t(i) * s,
+                                                      qinv + int64_t(i) * s, ctx->d_status); note_launch();
+    KF_TRY(check_cuda(cudaGetLastError(), "rayleigh_norms_kernel"));
   }
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[3], st));
   sort_desc_kernel<<<unsigned(nu), 1024, sort_smem, st>>>(sig, s, P, perm, s); note_launch();
-  KF_CUDA(cudaGetLastError());
+  KF_TRY(check_cuda(cudaGetLastError(), "sort_desc_kernel"));
+  // vectors and their images in sorted order, zero rows up to R
+  gather_rows_kernel<<<dim3(unsigned(R), unsigned(nu)), 256, 0, st>>>(Q, pl.sp, pl.sp * pl.sp, perm, s, bf.Qs, pl.sp,
+                                                                      R * pl.sp, pl.sp); note_launch();
+  KF_TRY(check_cuda(cudaGetLastError(), "gather_rows_kernel"));
+  gather_rows_kernel<<<dim3(unsigned(R), unsigned(nu)), 256, 0, st>>>(bf.Y, lyM, s * lyM, perm, s, bf.Ys, lyM,
+                                                                      R * lyM, lyM); note_launch();
+  KF_TRY(check_cuda(cudaGetLastError(), "gather_rows_kernel"));
+  if (int64_t(nu) * nwin > 65535) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: too many refinement windows");
+  for (int pass = 0; pass < 2; ++pass) {
+    const int64_t offr = pass * (RW / 2);
+    win_gram_kernel<<<dim3(unsigned(nwin), unsigned(nu)), 256, 0, st>>>(bf.Ys, lyM, R * lyM, lyM, offr, bf.Bw, nwin, ctx->d_status);
+    note_launch();
+    KF_TRY(check_cuda(cudaGetLastError(), "win_gram_kernel"));
+    win_eig_kernel<<<unsigned(nu * nwin), 256, eig_smem, st>>>(bf.Bw, bf.Vw, 1e-6f, 12, ctx->d_status); note_launch();
+    KF_TRY(check_cuda(cudaGetLastError(), "win_eig_kernel"));
+    win_rotate_kernel<<<dim3(unsigned(pl.sp / 64), unsigned(nu * nwin)), 256, rot_smem, st>>>(
+        bf.Qs, pl.sp, R * pl.sp, pl.sp, offr, bf.Vw, nwin, ctx->d_status); note_launch();
+    KF_TRY(check_cuda(cudaGetLastError(), "win_rotate_kernel"));
+    win_rotate_kernel<<<dim3(unsigned((lyM + 63) / 64), unsigned(nu * nwin)), 256, rot_smem, st>>>(
+        bf.Ys, lyM, R * lyM, lyM, offr, bf.Vw, nwin, ctx->d_status); note_launch();
+    KF_TRY(check_cuda(cudaGetLastError(), "win_rotate_kernel"));
+  }
+  for (int i = 0; i < nu; ++i) {
+    rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(bf.Ys + int64_t(i) * R * lyM, lyM, lyM,
+                                                      bf.Qs + int64_t(i) * R * pl.sp, pl.sp, s, sig + int64_t(i) * s,
+                                                      qinv + int64_t(i) * s, ctx->d_status); note_launch();
+    KF_TRY(check_cuda(cudaGetLastError(), "rayleigh_norms_kernel"));
+  }
+  sort_desc_kernel<<<unsigned(nu), 1024, sort_smem, st>>>(sig, s, P, perm, s); note_launch();
+  KF_TRY(check_cuda(cudaGetLastError(), "sort_desc_kernel"));
   for (int i = 0; i < nu; ++i) {
     const kf_svd_problem& p = pr[i];
     dim3 grid(unsigned((s + 31) / 32), unsigned((s + 31) / 32));
-    gather_kernel<<<grid, dim3(32, 8), 0, st>>>(Q + int64_t(i) * pl.sp * pl.sp, pl.sp, s, perm + int64_t(i) * s,
+    gather_kernel<<<grid, dim3(32, 8), 0, st>>>(bf.Qs + int64_t(i) * R * pl.sp, pl.sp, s, perm + int64_t(i) * s,
                                                 sig + int64_t(i) * s, qinv + int64_t(i) * s, p.vecs, p.ldv, p.sigma);
     note_launch();
-    KF_CUDA(cudaGetLastError());
+    KF_TRY(check_cuda(cudaGetLastError(), "gather_kernel"));
   }
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[4], st));
   return KF_OK;
@@ -694,7 +1024,7 @@ kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out) {
   out->gram_ms = t[0];
   out->jacobi_ms = t[1];
   out->rayleigh_ms = t[2];
-  out->sort_ms = t[3];
+  out->refine_ms = t[3];
   out->jacobi_steps = ctx->prof_steps;
   out->jacobi_apply_flops = double(f);
   return KF_OK;

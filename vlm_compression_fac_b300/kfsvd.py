@@ -49,7 +49,7 @@ class SvdProblem(ctypes.Structure):
 
 class SvdProfile(ctypes.Structure):
     _fields_ = [("gram_ms", ctypes.c_float), ("jacobi_ms", ctypes.c_float), ("rayleigh_ms", ctypes.c_float),
-                ("sort_ms", ctypes.c_float), ("jacobi_steps", ctypes.c_int64),
+                ("refine_ms", ctypes.c_float), ("jacobi_steps", ctypes.c_int64),
                 ("jacobi_apply_flops", ctypes.c_double)]
 
 
