@@ -252,7 +252,9 @@ KF_API kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma, con
  *                            V = V~_r^T S_g^-1.
  * KF_SIDE_LEFT  (vecs = U~): U = S_x^-1 U~_r Sigma_r,
  *                            V = Sigma_r^-1 (U~_r^T S_x) W   (= V~_r^T S_g^-1).
- * Sx, Sg, Sinv as written by whiten(); sigma, vecs as written by whitened_svd().
+ * Sx, Sg, Sinv as written by whiten(); sigma, vecs as written by whitened_svd().  Only the
+ * Gram-side factor is read (Sg for KF_SIDE_RIGHT, Sx for KF_SIDE_LEFT); the other one may be
+ * NULL (its leading dimension is then ignored), so a caller can free it after whiten().
  * U: m x r float32 out (ldu); V: r x n float32 out (ldvo).  0 <= r <= min(m, n).
  * ---------------------------------------------------------------------------------- */
 KF_API size_t unwhiten_workspace_size(int64_t m, int64_t n, int32_t r);

@@ -19,12 +19,15 @@ in float64 (numpy/LAPACK routines serve as textbook steps).  Sources:
             Compression", section 2A (closed form W_k = W V_k V_k^T; incremental
             covariance aggregation; one eigendecomposition of the aggregated covariance).
 
-Readings where the pages are silent (all listed in DESIGN.md): W is d_in x d_out (y = x W);
+Readings where the pages are silent: W is d_in x d_out (y = x W);
 X = A^T A / N and G = Gr^T Gr / N uncentred, each damped by lam * mean(diag); the
 Cholesky factors are S_x = chol_lower(X)^T and S_g = chol_lower(G), which is the choice
 that makes ||S_x dW S_g||_F^2 equal the K-FAC form with column-major vec; the score of a
 component is half its squared whitened singular value; the greedy cut keeps the longest
-prefix of the sorted list whose cumulative cost stays within the budget.
+prefix of the sorted list whose cumulative cost stays within the budget; an attention head
+is a unit of its own (LASER 2 allocates across heads): q, k and v heads are column blocks of
+their weight with the head's diagonal block of G, o heads are row blocks with the head's
+diagonal block of X, each block taken from the factor after damping.
 
 Parity status: every function here is pinned by tests/test_oracle_pins.py against
 closed forms, the pages' identities, brute force or hand-worked values; none is
@@ -260,7 +263,9 @@ def compress_workload(wl, units: Optional[List[int]] = None) -> Dict:
     res: List[UnitResult] = []
     for i in idx:
         u = wl.units[i]
-        X, G = cov(u.x_site), cov(u.g_site)
+        # an attention-head unit uses the diagonal blocks of its (already damped) factors
+        X = cov(u.x_site)[u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m]
+        G = cov(u.g_site)[u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n]
         Sx, Sg = cholesky_factors(X, G)
         W = recipes.gen_weight(wl, u).astype(np.float64)
         Wt = whiten(W, Sx, Sg)

@@ -46,9 +46,27 @@ def stream_on_device(wl: recipes.Workload, site: recipes.Site, t0: int, t1: int,
 
 
 def weight_on_device(wl: recipes.Workload, unit: recipes.Unit, torch, device="cuda"):
+    """The whole weight the unit belongs to (for an attention head: the full matrix)."""
     dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-    out = torch.empty((unit.m, unit.n), dtype=dt, device=device)
-    fill(out.data_ptr(), wl.dtype, unit.m, unit.n, unit.n, 0, unit.n, 0,
+    wm, wn = unit.weight_shape
+    out = torch.empty((wm, wn), dtype=dt, device=device)
+    fill(out.data_ptr(), wl.dtype, wm, wn, wn, 0, wn, 0,
          recipes.weight_seed(wl, unit), 0, float(recipes.weight_std(wl)),
          torch.cuda.current_stream().cuda_stream)
     return out
+
+
+def weights_on_device(wl: recipes.Workload, torch, device="cuda"):
+    """Every weight of a workload, keyed by weight name (heads share their matrix)."""
+    out = {}
+    for u in wl.units:
+        if u.weight not in out:
+            out[u.weight] = weight_on_device(wl, u, torch, device)
+    return out
+
+
+def rows_fn(wl: recipes.Workload, torch, device="cuda"):
+    """A callable (site, t0, t1) -> device rows, generating calibration chunks on demand."""
+    def rows(name, t0, t1):
+        return stream_on_device(wl, wl.sites[name], t0, t1, torch, device)
+    return rows

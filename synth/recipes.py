@@ -63,6 +63,25 @@ class Unit:
     x_site: str
     g_site: str
     block: int = 0
+    # A unit may be a block of a larger weight (an attention head): rows [row0, row0 + m)
+    # and columns [col0, col0 + n) of the weight `w_name` (w_m x w_n); it then uses the
+    # diagonal blocks [x_off, x_off + m) of its input factor and [g_off, g_off + n) of its
+    # output factor.  An empty w_name means the unit is the whole weight `name`.
+    w_name: str = ""
+    w_m: int = 0
+    w_n: int = 0
+    row0: int = 0
+    col0: int = 0
+    x_off: int = 0
+    g_off: int = 0
+
+    @property
+    def weight(self) -> str:
+        return self.w_name or self.name
+
+    @property
+    def weight_shape(self):
+        return (self.w_m, self.w_n) if self.w_name else (self.m, self.n)
 
 
 @dataclass
@@ -128,7 +147,7 @@ def stream_seed(wl: Workload, site: Site) -> int:
 
 
 def weight_seed(wl: Workload, unit: Unit) -> int:
-    return tensor_seed(wl.seed, unit.block, "weight", unit.name)
+    return tensor_seed(wl.seed, unit.block, "weight", unit.weight)
 
 
 # ----------------------------------------------------------------- generation
@@ -151,11 +170,19 @@ def gen_stream(wl: Workload, site: Site, t0: int, t1: int, cols=None) -> np.ndar
     return _finish(z * std[cols][None, :], wl.dtype)
 
 
-def gen_weight(wl: Workload, unit: Unit) -> np.ndarray:
-    i = np.arange(unit.m, dtype=np.uint64)[:, None]
-    j = np.arange(unit.n, dtype=np.uint64)[None, :]
-    z = philox.standard_normal(i * np.uint64(unit.n) + j, weight_seed(wl, unit))
+def gen_full_weight(wl: Workload, unit: Unit) -> np.ndarray:
+    """The whole weight a unit belongs to (w_m x w_n, or m x n for a whole-matrix unit)."""
+    wm, wn = unit.weight_shape
+    i = np.arange(wm, dtype=np.uint64)[:, None]
+    j = np.arange(wn, dtype=np.uint64)[None, :]
+    z = philox.standard_normal(i * np.uint64(wn) + j, weight_seed(wl, unit))
     return _finish(z * weight_std(wl), wl.dtype)
+
+
+def gen_weight(wl: Workload, unit: Unit) -> np.ndarray:
+    """The unit's own block of its weight (m x n)."""
+    w = gen_full_weight(wl, unit)
+    return np.ascontiguousarray(w[unit.row0:unit.row0 + unit.m, unit.col0:unit.col0 + unit.n])
 
 
 # ------------------------------------------------------------------ workloads
@@ -199,6 +226,61 @@ def llama7b_model(n_tokens: int = 65536, n_blocks: int = 32) -> Workload:
 def llama70b_block(n_tokens: int = 262144) -> Workload:
     """One 70B-shaped block (GQA k/v 8192x1024), N = 262144 tokens, 30% kept."""
     return decoder_blocks(1, 8192, 28672, 1024, n_tokens, 0.3, 1004, "llama70b_block")
+
+
+def _attn_heads(units: List[Unit], sites: Dict[str, Site], p: str, b: int, d: int, kv: int,
+                head: int, x_attn: str, x_o: str) -> None:
+    """Per-head units of one attention layer: q, k, v heads are column blocks (full input
+    factor, the head's diagonal block of the output factor); o heads are row blocks (the
+    head's diagonal block of the input factor, full output factor)."""
+    for nm, n_out in (("q", d), ("k", kv), ("v", kv)):
+        g = p + nm + "_out"
+        sites[g] = Site(g, n_out, "grad", b)
+        for h in range(n_out // head):
+            units.append(Unit("%s%s.h%d" % (p, nm, h), d, head, x_attn, g, b, w_name=p + nm, w_m=d, w_n=n_out,
+                              col0=h * head, g_off=h * head))
+    g = p + "o_out"
+    sites[g] = Site(g, d, "grad", b)
+    for h in range(d // head):
+        units.append(Unit("%so.h%d" % (p, h), head, d, x_o, g, b, w_name=p + "o", w_m=d, w_n=d,
+                          row0=h * head, x_off=h * head))
+
+
+def vlm(n_tokens: int = 147456, vit_blocks: int = 24, vit_d: int = 1024, vit_ffn: int = 4096,
+        lm_blocks: int = 28, lm_d: int = 3584, lm_ffn: int = 18944, lm_kv: int = 512, head: int = 128,
+        rho: float = 0.5, seed: int = 1003, quant: str = "int8_token", name: str = "vlm") -> Workload:
+    """A ViT-L-shaped vision tower (whole-matrix units) and a decoder LM with 128-dim attention
+    heads as units (GQA k/v), one global allocation pool, INT8 per-token fake-quantised
+    activations (quantisation-aware whitening)."""
+    sites: Dict[str, Site] = {}
+    units: List[Unit] = []
+    for b in range(vit_blocks):
+        p = "vit.b%d." % b
+        for s_, dd in (("attn_in", vit_d), ("o_in", vit_d), ("mlp_in", vit_d), ("fc2_in", vit_ffn)):
+            sites[p + s_] = Site(p + s_, dd, "act", b)
+        for nm, m, n, xs in (("q", vit_d, vit_d, "attn_in"), ("k", vit_d, vit_d, "attn_in"),
+                             ("v", vit_d, vit_d, "attn_in"), ("o", vit_d, vit_d, "o_in"),
+                             ("fc1", vit_d, vit_ffn, "mlp_in"), ("fc2", vit_ffn, vit_d, "fc2_in")):
+            sites[p + nm + "_out"] = Site(p + nm + "_out", n, "grad", b)
+            units.append(Unit(p + nm, m, n, p + xs, p + nm + "_out", b))
+    for b in range(lm_blocks):
+        bb = vit_blocks + b
+        p = "lm.b%d." % b
+        for s_, dd in (("attn_in", lm_d), ("o_in", lm_d), ("mlp_in", lm_d), ("down_in", lm_ffn)):
+            sites[p + s_] = Site(p + s_, dd, "act", bb)
+        _attn_heads(units, sites, p, bb, lm_d, lm_kv, head, p + "attn_in", p + "o_in")
+        for nm, m, n, xs in (("gate", lm_d, lm_ffn, "mlp_in"), ("up", lm_d, lm_ffn, "mlp_in"),
+                             ("down", lm_ffn, lm_d, "down_in")):
+            sites[p + nm + "_out"] = Site(p + nm + "_out", n, "grad", bb)
+            units.append(Unit(p + nm, m, n, p + xs, p + nm + "_out", bb))
+    return Workload(name, n_tokens, "bf16", units, sites, seed, rho=rho, quant=quant)
+
+
+def mini_vlm(n_tokens: int = 600, seed: int = 79) -> Workload:
+    """A scaled-down VLM (one ViT block, one LM block with two q heads and one k/v head) with
+    ragged FFN widths, for parity tests of the per-head path."""
+    return vlm(n_tokens=n_tokens, vit_blocks=1, vit_d=192, vit_ffn=320, lm_blocks=1, lm_d=256, lm_ffn=328,
+               lm_kv=128, head=128, rho=0.5, seed=seed, name="mini_vlm")
 
 
 def mini_block(n_tokens: int = 1000, d: int = 320, ffn: int = 704, kv: int = 192,

@@ -295,28 +295,43 @@ def test_unwhiten(ctx, m, n, r):
 
 
 # ---------------------------------------------------------------- end to end
-def _run_pipeline(ctx, wl):
+def _run_pipeline(ctx, wl, streamed=False, chunk=256):
     from synth import device
     from vlm_compression_fac_b300 import pipeline
-    units = [pipeline.UnitSpec(u.name, u.m, u.n, u.x_site, u.g_site) for u in wl.units]
-    acts = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
-    grads = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
-    weights = {u.name: device.weight_on_device(wl, u, torch) for u in wl.units}
-    res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
-                            fixed_rank=wl.fixed_rank, quant=wl.quant == "int8_token")
+    units = pipeline.unit_specs(wl)
+    weights = device.weights_on_device(wl, torch)
+    quant = wl.quant == "int8_token"
+    if not streamed:
+        acts = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
+        grads = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
+        res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                                fixed_rank=wl.fixed_rank, quant=quant)
+    else:
+        blocks = sorted({u.block for u in wl.units})
+        groups = [[i for i, u in enumerate(wl.units) if u.block == b] for b in blocks]
+        res = pipeline.compress(ctx, units, weights, device.rows_fn(wl, torch), None, wl.n_tokens, lam=wl.lam,
+                                budget=wl.budget, fixed_rank=wl.fixed_rank, quant=quant,
+                                site_dims={n: s.d for n, s in wl.sites.items()},
+                                act_sites=[n for n, s in wl.sites.items() if s.kind == "act"],
+                                groups=groups, chunk_tokens=chunk)
     ctx.sync_status()
     return res
 
 
-@pytest.mark.parametrize("which", ["single_linear", "mini_block", "mini_block_qaw"])
+E2E = {
+    "single_linear": (lambda: recipes.single_linear(), False),
+    "mini_block": (lambda: recipes.mini_block(n_tokens=1200), False),
+    "mini_block_qaw": (lambda: recipes.mini_block(n_tokens=1200, quant="int8_token", seed=91), False),
+    "mini_model_streamed": (lambda: recipes.decoder_blocks(2, 256, 328, 128, 900, 0.4, 93, "mini_model"), True),
+    "mini_vlm_heads_qaw_streamed": (lambda: recipes.mini_vlm(n_tokens=700), True),
+}
+
+
+@pytest.mark.parametrize("which", list(E2E))
 def test_end_to_end(ctx, which):
-    if which == "single_linear":
-        wl = recipes.single_linear()
-    elif which == "mini_block":
-        wl = recipes.mini_block(n_tokens=1200)
-    else:
-        wl = recipes.mini_block(n_tokens=1200, quant="int8_token", seed=91)
-    res = _run_pipeline(ctx, wl)
+    make, streamed = E2E[which]
+    wl = make()
+    res = _run_pipeline(ctx, wl, streamed=streamed)
     ref = O.compress_workload(wl)
     for name, cov in res.covs.items():
         assert rel_fro(cov.cpu().numpy(), ref["covs"][name]) <= 1e-4, name
@@ -327,10 +342,9 @@ def test_end_to_end(ctx, which):
     ranks = res.ranks.cpu().numpy()
     ok, moved = rank_parity(ranks, ref["alloc"], sig_o, 1e-6)
     assert ok, (ranks, ref["alloc"].ranks, moved)
-    for g, o in zip(res.units, ref["units"]):
+    for g, o, u in zip(res.units, ref["units"], wl.units):
         r = g.rank
-        e = O.whitened_error(recipes.gen_weight(wl, wl.units[[u.name for u in wl.units].index(g.name)]),
-                             g.U.cpu().numpy(), g.V.cpu().numpy(), o.Sx, o.Sg)
+        e = O.whitened_error(recipes.gen_weight(wl, u), g.U.cpu().numpy(), g.V.cpu().numpy(), o.Sx, o.Sg)
         e_opt = float(np.sum(o.sigma[r:] ** 2))
         total = float(np.sum(o.sigma ** 2))
         if e_opt <= 1e-12 * total:

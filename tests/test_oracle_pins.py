@@ -269,3 +269,44 @@ def test_fake_quant_properties():
     for row, sc in zip(Q, s):
         lv = np.unique(np.round(row / sc))
         assert lv.min() >= -127 and lv.max() <= 127
+
+
+def test_head_units_use_the_diagonal_factor_blocks():
+    """A perturbation confined to one attention head's column block (q/k/v) or row block (o)
+    changes the K-FAC form only through the head's diagonal block of G (resp. X), so the
+    head unit's whitened error with that block equals the full Kronecker form: LASER 2
+    allocates across heads, and this is what makes a head a unit of its own."""
+    r = np.random.default_rng(5)
+    m, n, hd = 6, 8, 4  # two heads of width 4 on the output side
+    A = r.standard_normal((60, m))
+    Gr = r.standard_normal((60, n)) @ r.standard_normal((n, n))   # correlated across heads
+    X = O.finalize_covariance(O.covariance_sum(A), 60, 1e-2)
+    G = O.finalize_covariance(O.covariance_sum(Gr), 60, 1e-2)
+    for h in range(2):
+        dW = np.zeros((m, n))
+        dW[:, h * hd:(h + 1) * hd] = r.standard_normal((m, hd))
+        full = O.kfac_quadratic(dW, X, G)
+        Sx, Sg = O.cholesky_factors(X, G[h * hd:(h + 1) * hd, h * hd:(h + 1) * hd])
+        head = 0.5 * O.whitened_error(dW[:, h * hd:(h + 1) * hd], np.zeros((m, 1)), np.zeros((1, hd)), Sx, Sg)
+        assert abs(full - head) <= 1e-12 * abs(full)
+        # the o-side: a row block of W with the head's block of X and the full G
+        dW = np.zeros((n, m))
+        dW[h * hd:(h + 1) * hd, :] = r.standard_normal((hd, m))
+        Xo = G  # any SPD factor on the input side
+        full = O.kfac_quadratic(dW, Xo, X)
+        Sx, Sg = O.cholesky_factors(Xo[h * hd:(h + 1) * hd, h * hd:(h + 1) * hd], X)
+        head = 0.5 * O.whitened_error(dW[h * hd:(h + 1) * hd, :], np.zeros((hd, 1)), np.zeros((1, m)), Sx, Sg)
+        assert abs(full - head) <= 1e-12 * abs(full)
+    # the oracle's whole-workload run takes exactly those blocks for head units
+    from synth import recipes
+    wl = recipes.mini_vlm(n_tokens=64)
+    ids = [i for i, u in enumerate(wl.units) if u.name in ("lm.b0.q.h1", "lm.b0.o.h1")]
+    res = O.compress_workload(wl, units=ids)
+    for ur, i in zip(res["units"], ids):
+        u = wl.units[i]
+        Xf = res["covs"][u.x_site]
+        Gf = res["covs"][u.g_site]
+        np.testing.assert_array_equal(ur.X, Xf[u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m])
+        np.testing.assert_array_equal(ur.G, Gf[u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n])
+        np.testing.assert_array_equal(ur.Wt, O.whiten(recipes.gen_full_weight(wl, u)[
+            u.row0:u.row0 + u.m, u.col0:u.col0 + u.n], ur.Sx, ur.Sg))

@@ -463,8 +463,11 @@ kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, in
   const int64_t s = m < n ? m : n;
   KF_TRY(need(r >= 0 && r <= s, "unwhiten: r must be in [0, min(m, n)]"));
   if (r == 0) return KF_OK;
-  KF_TRY(need(W && Sx && Sg && Sinv && sigma && vecs && U && V, "unwhiten: null pointer"));
-  KF_TRY(need(ldw >= n && ldsx >= m && ldsg >= n && ldsi >= s && ldv >= s && ldu >= r && ldvo >= n,
+  // Only the Gram-side factor is read (S_g for KF_SIDE_RIGHT, S_x for KF_SIDE_LEFT).
+  const bool right_side = kf_gram_side(m, n) == KF_SIDE_RIGHT;
+  KF_TRY(need(W && Sinv && sigma && vecs && U && V && (right_side ? Sg != nullptr : Sx != nullptr),
+              "unwhiten: null pointer"));
+  KF_TRY(need(ldw >= n && (right_side ? ldsg >= n : ldsx >= m) && ldsi >= s && ldv >= s && ldu >= r && ldvo >= n,
               "unwhiten: leading dimension"));
   KF_TRY(need(w_dtype == KF_BF16 || w_dtype == KF_F32, "unwhiten: dtype"));
   Carve cv(workspace, workspace_bytes, false);

@@ -25,6 +25,9 @@ namespace kf {
 namespace {
 
 constexpr int JB = 32, JP = 64;  // block width, pair problem size
+#ifndef KF_JAC_MAX_INNER
+#define KF_JAC_MAX_INNER 12  // inner sweeps of a pair problem
+#endif
 
 // Alignment self-check for vector accesses: a misaligned address is recorded in the status
 // word (KF_ERR_INVALID, info = site) and the access is skipped instead of faulting.
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
     const int r = e >> 5, c = JB + (e & 31);
     const float v = fabsf(A[r][c]);
     if (v > flo) {
-      const float den = fmaxf(sqrtf(A[r][r] * A[c][c]), flo);
+      const float den = fmaxf(sqrtf(fmaxf(A[r][r] * A[c][c], 0.f)), flo);
       m = fmaxf(m, v / den);
     }
   }
@@ -200,6 +203,21 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
     }
     if (!rotated) break;
   }
+#ifdef KF_JAC_SORT_PAIRS
+  // Order the pair's eigenvectors by eigenvalue, largest first, so that the first block of
+  // the pair receives the larger half of the pair's spectrum.
+  __shared__ int pord[JP];
+  if (t < JP) {
+    const float di = A[t][t];
+    int rank = 0;
+    for (int j = 0; j < JP; ++j) {
+      const float dj = A[j][j];
+      rank += (dj > di) || (dj == di && j < t);
+    }
+    pord[rank] = t;
+  }
+  __syncthreads();
+#endif
   // One Newton-Schulz step V <- V (3I - V^T V) / 2 removes the orthogonality drift that the
   // rounding of many plane rotations leaves in V (A is free now: the apply step rebuilds C).
   for (int e = t; e < JP * JP; e += 256) {
@@ -227,7 +245,14 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   }
   __syncthreads();
   float* Vo = Vall + (int64_t(u) * npairs + k) * (JP * JP);
+#ifdef KF_JAC_SORT_PAIRS
+  for (int e = t; e < JP * JP; e += 256) {
+    const int oc = pord[e & 63];
+    Vo[e] = V[e >> 6][oc >= 0 && oc < JP ? oc : (e & 63)];
+  }
+#else
   for (int e = t; e < JP * JP; e += 256) Vo[e] = V[e >> 6][e & 63];
+#endif
   if (t == 0) skip[k] = 0;
 }
 
@@ -916,7 +941,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     KF_CUDA(cudaFuncSetAttribute(jac_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(apply_smem)));
     attr = true;
   }
-  const int max_inner = 12;
+  const int max_inner = KF_JAC_MAX_INNER;
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[1], st));
   for (int sw = 0; sw < max_sweeps; ++sw) {
     for (int step = 0; step < pl.nblk - 1; ++step) {

@@ -270,9 +270,11 @@ def unwhiten_workspace_size(m: int, n: int, r: int) -> int:
 
 
 def unwhiten(ctx: Context, W, Sx, Sg, Sinv, sigma, vecs, r: int, U, V, workspace=None, stream=None):
-    """Rank-r factors U (m x r), V (r x n) with W ~= U V in the original space."""
+    """Rank-r factors U (m x r), V (r x n) with W ~= U V in the original space.  Only the
+    Gram-side factor is read (Sg when n <= m, else Sx); the other may be None."""
     m, n = W.shape
     ws, wsb = _ws(unwhiten_workspace_size(m, n, r), workspace, W.device)
-    _check(lib().unwhiten(ctx.handle, _ptr(W), _dtype_code(W), _ld(W), m, n, _ptr(Sx), _ld(Sx), _ptr(Sg),
-                          _ld(Sg), _ptr(Sinv), _ld(Sinv), _ptr(sigma), _ptr(vecs), _ld(vecs), int(r), _ptr(U),
+    _check(lib().unwhiten(ctx.handle, _ptr(W), _dtype_code(W), _ld(W), m, n, _ptr(Sx),
+                          0 if Sx is None else _ld(Sx), _ptr(Sg), 0 if Sg is None else _ld(Sg),
+                          _ptr(Sinv), _ld(Sinv), _ptr(sigma), _ptr(vecs), _ld(vecs), int(r), _ptr(U),
                           _ld(U) if r > 0 else max(r, 1), _ptr(V), _ld(V), _ptr(ws), wsb, _stream(stream)))

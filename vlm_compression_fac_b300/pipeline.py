@@ -1,16 +1,27 @@
 """Whole-workload driver over the C ABI: the call a user makes to compress a set of layers.
 
 For every calibration site it streams the rows into a K-FAC factor (kfac_accumulate) and
-finalises it (kf_finalize_covariance); for every unit it whitens W (whiten, sharing the
-input factor S_x between the units that read the same site); it takes the spectra of all
-units in batches of equal min(m, n) (whitened_svd); it allocates ranks globally
-(score_and_allocate) and maps the kept factors back (unwhiten).  The only host round trip
-is reading the per-unit ranks after the allocation, to size U and V.
+finalises it (kf_finalize_covariance); for every unit it whitens W (whiten, sharing a factor
+between the units that read the same site); it takes the spectra of the units in batches of
+equal min(m, n) (whitened_svd); it allocates ranks globally (score_and_allocate) and maps the
+kept factors back (unwhiten).  The only host round trip is reading the per-unit ranks after
+the allocation, to size U and V.
+
+A unit may be a block of a larger weight (an attention head): it then reads the rows/columns
+of its weight and the diagonal blocks of its factors given by its spec (LASER allocates
+across heads; q/k/v heads are column blocks with the head's block of G, o heads row blocks
+with the head's block of X).
+
+Calibration rows are either resident device tensors (one per site) or produced on demand by
+a callable ``rows(site, t0, t1)``; with ``groups`` the units are processed group by group
+(e.g. one transformer block at a time): a group's covariances are built, its units whitened
+and their spectra taken, then the covariances and every factor that the unwhitening does not
+need are released, so that workloads far larger than device memory stream through.
 """
 from __future__ import annotations
 
 from dataclasses import dataclass, field
-from typing import Callable, Dict, List, Optional, Sequence
+from typing import Callable, Dict, List, Optional, Sequence, Union
 
 import torch
 
@@ -24,6 +35,15 @@ class UnitSpec:
     n: int
     x_site: str
     g_site: str
+    w_name: str = ""      # weight this unit is a block of (empty: the weight `name` itself)
+    row0: int = 0
+    col0: int = 0
+    x_off: int = 0        # diagonal block [x_off, x_off + m) of the input factor
+    g_off: int = 0        # diagonal block [g_off, g_off + n) of the output factor
+
+    @property
+    def weight(self) -> str:
+        return self.w_name or self.name
 
 
 @dataclass
@@ -32,10 +52,10 @@ class UnitOut:
     m: int
     n: int
     side: int
-    Sx: torch.Tensor
-    Sg: torch.Tensor
+    Sx: Optional[torch.Tensor]
+    Sg: Optional[torch.Tensor]
     Sinv: torch.Tensor
-    Wt: torch.Tensor
+    Wt: Optional[torch.Tensor]
     sigma: Optional[torch.Tensor] = None
     vecs: Optional[torch.Tensor] = None
     sweeps: int = 0
@@ -54,75 +74,141 @@ class Result:
     timings: Dict[str, float] = field(default_factory=dict)
 
 
+RowsFn = Callable[[str, int, int], torch.Tensor]
+
+
+def unit_specs(wl) -> List[UnitSpec]:
+    """The pipeline's unit specs of a synthetic workload (synth.recipes.Workload)."""
+    return [UnitSpec(u.name, u.m, u.n, u.x_site, u.g_site, u.w_name, u.row0, u.col0, u.x_off, u.g_off)
+            for u in wl.units]
+
+
 def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch.Tensor],
-             acts: Dict[str, torch.Tensor], grads: Dict[str, torch.Tensor], n_tokens: int, lam: float = 1e-2,
-             budget: Optional[int] = None, fixed_rank: Optional[int] = None, mode: int = K.KF_KEY_HALF_SIGMA2,
-             quant: bool = False, tol: float = 1e-6, max_sweeps: int = 30, stream=None,
-             sync_timer: Optional[Callable[[str], None]] = None) -> Result:
-    """Runs the five steps on device-resident calibration rows and weights.
+             acts: Union[Dict[str, torch.Tensor], RowsFn], grads: Union[Dict[str, torch.Tensor], RowsFn, None],
+             n_tokens: int, lam: float = 1e-2, budget: Optional[int] = None, fixed_rank: Optional[int] = None,
+             mode: int = K.KF_KEY_HALF_SIGMA2, quant: bool = False, tol: float = 1e-6, max_sweeps: int = 30,
+             stream=None, sync_timer: Optional[Callable[[str], None]] = None,
+             site_dims: Optional[Dict[str, int]] = None, act_sites: Optional[Sequence[str]] = None,
+             groups: Optional[Sequence[Sequence[int]]] = None, chunk_tokens: int = 16384,
+             keep_covs: Union[bool, Sequence[str]] = True, keep_whitened: bool = True) -> Result:
+    """Runs the five steps.
 
+    ``acts``/``grads``: dicts of resident (n_tokens x d) device tensors, or ``acts`` a callable
+    ``rows(site, t0, t1)`` returning device rows of any site (``grads`` is then ignored), with
+    ``site_dims`` giving every site's width and ``act_sites`` naming the activation sites (the
+    ones fake-quantised when ``quant``).
+    ``groups``: lists of unit indices processed one after the other (default: one group).
+    ``keep_covs``: keep every finished covariance in the result (True), none (False) or the
+    named sites only; ``keep_whitened=False`` releases W~ after its spectrum and, per unit,
+    the factor that the unwhitening does not read.
     ``sync_timer(tag)`` (optional) is called at phase boundaries ("kfac", "whiten", "svd",
-    "allocate", "unwhiten") and around every kfac_accumulate call ("syrk<", "syrk>"), so a
-    caller can record CUDA events there."""
-    dev = next(iter(weights.values())).device
+    "allocate", "unwhiten"; per group for the first three) and around every kfac_accumulate
+    call ("syrk<", "syrk>"), so a caller can record CUDA events there.
+    """
     mark = sync_timer or (lambda _name: None)
+    dev = next(iter(weights.values())).device
+    if callable(acts):
+        rows_fn = acts
+        dims = dict(site_dims or {})
+        quant_sites = set(act_sites or [])
+    else:
+        resident = dict(acts)
+        resident.update(grads or {})
+        rows_fn = lambda name, t0, t1: resident[name][t0:t1]
+        dims = {k: v.shape[1] for k, v in resident.items()}
+        quant_sites = set(acts.keys())
+        chunk_tokens = max(n_tokens, 1)   # resident rows: one call per site
+    groups = [list(range(len(units)))] if groups is None else [list(g) for g in groups]
 
-    covs: Dict[str, torch.Tensor] = {}
-    for name, rows in list(acts.items()) + list(grads.items()):
-        d = rows.shape[1]
-        cov = torch.zeros((d, d), dtype=torch.float32, device=rows.device)
-        q = K.KF_QUANT_INT8_TOKEN if (quant and name in acts) else K.KF_QUANT_NONE
-        mark("syrk<")
-        K.kfac_accumulate(ctx, rows, cov, quant=q, stream=stream)
-        mark("syrk>")
-        K.kf_finalize_covariance(ctx, cov, n_tokens, lam, stream=stream)
-        covs[name] = cov
-    mark("kfac")
+    outs: List[Optional[UnitOut]] = [None] * len(units)
+    sweeps_dev = torch.zeros(len(units), dtype=torch.int32, device=dev)
+    all_covs: Dict[str, torch.Tensor] = {}
+    for grp in groups:
+        # ---- step 1: the group's calibration sites
+        needed: List[str] = []
+        for i in grp:
+            for sname in (units[i].x_site, units[i].g_site):
+                if sname not in needed:
+                    needed.append(sname)
+        covs: Dict[str, torch.Tensor] = {}
+        for sname in needed:
+            d = dims[sname]
+            cov = torch.zeros((d, d), dtype=torch.float32, device=dev)
+            q = K.KF_QUANT_INT8_TOKEN if (quant and sname in quant_sites) else K.KF_QUANT_NONE
+            for t0 in range(0, n_tokens, chunk_tokens):
+                rows = rows_fn(sname, t0, min(n_tokens, t0 + chunk_tokens))
+                mark("syrk<")
+                K.kfac_accumulate(ctx, rows, cov, quant=q, stream=stream)
+                mark("syrk>")
+                del rows
+            K.kf_finalize_covariance(ctx, cov, n_tokens, lam, stream=stream)
+            covs[sname] = cov
+        mark("kfac")
 
-    outs: List[UnitOut] = []
-    sx_done: Dict[str, torch.Tensor] = {}
-    sxinv_done: Dict[str, torch.Tensor] = {}
-    for u in units:
-        side = K.kf_gram_side(u.m, u.n)
-        s = min(u.m, u.n)
-        flags = 0
-        if u.x_site in sx_done:
-            Sx = sx_done[u.x_site]
-            flags |= K.KF_REUSE_SX
-        else:
-            Sx = torch.empty((u.m, u.m), dtype=torch.float32, device=dev)
-            sx_done[u.x_site] = Sx
-        if side == K.KF_SIDE_LEFT:
-            if u.x_site in sxinv_done:
-                Sinv = sxinv_done[u.x_site]
+        # ---- steps 2 and 3: factors and whitened weights (a factor is shared by the units
+        # that use the same block of the same site)
+        fx: Dict[tuple, torch.Tensor] = {}
+        fg: Dict[tuple, torch.Tensor] = {}
+        inv_x: Dict[tuple, torch.Tensor] = {}
+        inv_g: Dict[tuple, torch.Tensor] = {}
+        for i in grp:
+            u = units[i]
+            side = K.kf_gram_side(u.m, u.n)
+            s = min(u.m, u.n)
+            kx, kg = (u.x_site, u.x_off, u.m), (u.g_site, u.g_off, u.n)
+            flags = 0
+            if kx in fx:
+                Sx = fx[kx]
+                flags |= K.KF_REUSE_SX
+            else:
+                Sx = fx[kx] = torch.empty((u.m, u.m), dtype=torch.float32, device=dev)
+            if kg in fg:
+                Sg = fg[kg]
+                flags |= K.KF_REUSE_SG
+            else:
+                Sg = fg[kg] = torch.empty((u.n, u.n), dtype=torch.float32, device=dev)
+            invs, key = (inv_x, kx) if side == K.KF_SIDE_LEFT else (inv_g, kg)
+            if key in invs:
+                Sinv = invs[key]
                 flags |= K.KF_REUSE_SINV
             else:
-                Sinv = torch.empty((s, s), dtype=torch.float32, device=dev)
-                sxinv_done[u.x_site] = Sinv
-                flags &= ~K.KF_REUSE_SX  # the left inverse is computed together with S_x
-        else:
-            Sinv = torch.empty((s, s), dtype=torch.float32, device=dev)
-        Sg = torch.empty((u.n, u.n), dtype=torch.float32, device=dev)
-        Wt = torch.empty((u.m, u.n), dtype=torch.float32, device=dev)
-        K.whiten(ctx, covs[u.x_site], covs[u.g_site], weights[u.name], Sx, Sg, Sinv, Wt, flags=flags,
-                 stream=stream)
-        outs.append(UnitOut(u.name, u.m, u.n, side, Sx, Sg, Sinv, Wt))
-    mark("whiten")
+                Sinv = invs[key] = torch.empty((s, s), dtype=torch.float32, device=dev)
+                # the Gram-side inverse is produced together with its factor
+                flags &= ~(K.KF_REUSE_SX if side == K.KF_SIDE_LEFT else K.KF_REUSE_SG)
+            X = covs[u.x_site][u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m]
+            G = covs[u.g_site][u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n]
+            W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
+            Wt = torch.empty((u.m, u.n), dtype=torch.float32, device=dev)
+            K.whiten(ctx, X, G, W, Sx, Sg, Sinv, Wt, flags=flags, stream=stream)
+            keep_x = keep_whitened or side == K.KF_SIDE_LEFT
+            keep_g = keep_whitened or side == K.KF_SIDE_RIGHT
+            outs[i] = UnitOut(u.name, u.m, u.n, side, Sx if keep_x else None, Sg if keep_g else None, Sinv, Wt)
+        del fx, fg, inv_x, inv_g
+        if keep_covs is True:
+            all_covs.update(covs)
+        elif keep_covs:
+            all_covs.update({k: v for k, v in covs.items() if k in set(keep_covs)})
+        del covs
+        mark("whiten")
 
-    groups: Dict[int, List[int]] = {}
-    for i, o in enumerate(outs):
-        groups.setdefault(min(o.m, o.n), []).append(i)
-    sweeps_all = torch.zeros(len(outs), dtype=torch.int32, device=dev)
-    for s, idx in groups.items():
-        for i in idx:
-            outs[i].sigma = torch.empty(s, dtype=torch.float32, device=dev)
-            outs[i].vecs = torch.empty((s, s), dtype=torch.float32, device=dev)
-        sw = torch.zeros(len(idx), dtype=torch.int32, device=dev)
-        K.whitened_svd(ctx, [outs[i].Wt for i in idx], [outs[i].sigma for i in idx], [outs[i].vecs for i in idx],
-                       sweeps=sw, tol=tol, max_sweeps=max_sweeps, stream=stream)
-        sweeps_all[torch.tensor(idx, device=dev)] = sw
-    mark("svd")
+        # ---- step 4: spectra, batched by min(m, n)
+        by_s: Dict[int, List[int]] = {}
+        for i in grp:
+            by_s.setdefault(min(units[i].m, units[i].n), []).append(i)
+        for s, idx in by_s.items():
+            for i in idx:
+                outs[i].sigma = torch.empty(s, dtype=torch.float32, device=dev)
+                outs[i].vecs = torch.empty((s, s), dtype=torch.float32, device=dev)
+            sw = torch.zeros(len(idx), dtype=torch.int32, device=dev)
+            K.whitened_svd(ctx, [outs[i].Wt for i in idx], [outs[i].sigma for i in idx],
+                           [outs[i].vecs for i in idx], sweeps=sw, tol=tol, max_sweeps=max_sweeps, stream=stream)
+            sweeps_dev[torch.tensor(idx, device=dev)] = sw
+            if not keep_whitened:
+                for i in idx:
+                    outs[i].Wt = None
+        mark("svd")
 
+    # ---- step 5a: global allocation
     sig = torch.cat([o.sigma for o in outs])
     lens = [min(o.m, o.n) for o in outs]
     off = torch.tensor([0] + list(_cumsum(lens)), dtype=torch.int64, device=dev)
@@ -138,18 +224,20 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
         K.score_and_allocate(ctx, sig, off, cost, int(budget), ranks, mode=mode, cut=cut, used=used,
                              stream=stream)
     ranks_h = ranks.cpu().tolist()
-    sweeps_h = sweeps_all.cpu().tolist()
+    sweeps_h = sweeps_dev.cpu().tolist()
     mark("allocate")
 
-    for o, r, sw in zip(outs, ranks_h, sweeps_h):
+    # ---- step 5b: factors in the original space
+    for o, u, r, sw in zip(outs, units, ranks_h, sweeps_h):
         o.rank = int(r)
         o.sweeps = int(sw)
         o.U = torch.empty((o.m, max(o.rank, 1)), dtype=torch.float32, device=dev)[:, :o.rank]
         o.V = torch.empty((max(o.rank, 1), o.n), dtype=torch.float32, device=dev)[:o.rank]
         if o.rank > 0:
-            K.unwhiten(ctx, weights[o.name], o.Sx, o.Sg, o.Sinv, o.sigma, o.vecs, o.rank, o.U, o.V, stream=stream)
+            W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
+            K.unwhiten(ctx, W, o.Sx, o.Sg, o.Sinv, o.sigma, o.vecs, o.rank, o.U, o.V, stream=stream)
     mark("unwhiten")
-    return Result(outs, covs, ranks, cut, used)
+    return Result(outs, all_covs, ranks, cut, used)
 
 
 def _cumsum(xs):
