@@ -96,8 +96,6 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
                                                         int max_inner) {
   __shared__ float A[JP][JP + 1];
   __shared__ float V[JP][JP + 1];
-  __shared__ float rc[32], rs[32], rap[32], raq[32];
-  __shared__ int rp[32], rq[32], ract[32];
   __shared__ float red[8];
 
   const int k = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
@@ -142,67 +140,71 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   for (int e = t; e < JP * JP; e += 256) V[e >> 6][e & 63] = ((e >> 6) == (e & 63)) ? 1.f : 0.f;
   __syncthreads();
 
+  // Threshold cyclic Jacobi on the 64 x 64 pair problem, 32 disjoint rotations per round.
+  // Every warp computes all 32 rotations of a round (lane l: pair l) from the same entries,
+  // so the parameters reach the threads that need them by warp shuffles rather than
+  // through shared memory; thread (warp w, lane k) then updates the 2 x 2 blocks (j, k),
+  // j = w, w + 8, w + 16, w + 24, and rows w, w + 8, ... of the columns p_k, q_k of V.
+  const int lane = t & 31, warp = t >> 5;
   for (int sweep = 0; sweep < max_inner; ++sweep) {
     int rotated = 0;
     for (int r = 0; r < JP - 1; ++r) {
+      const int p = rr_pos(lane, r, JP), q = rr_pos(JP - 1 - lane, r, JP);
+      const float a = A[p][p], b = A[q][q], d = A[p][q];
+      float c = 1.f, sn = 0.f, td = 0.f;
       int act = 0;
-      if (t < 32) {
-        const int p = rr_pos(t, r, JP), q = rr_pos(JP - 1 - t, r, JP);
-        const float a = A[p][p], b = A[q][q], d = A[p][q];
-        float c = 1.f, s = 0.f, td = 0.f;
-        if (fabsf(d) > flo && fabsf(d) > tol * sqrtf(fmaxf(a * b, 0.f))) {
-          const float tau = __fdiv_rn(b - a, 2.f * d);
-          const float tt = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f)));
-          c = 1.0f / sqrtf(fmaf(tt, tt, 1.f));
-          s = tt * c;
-          td = tt * d;
-          act = 1;
-        }
-        rc[t] = c; rs[t] = s; rp[t] = p; rq[t] = q; ract[t] = act;
-        rap[t] = a - td; raq[t] = b + td;
+      if (fabsf(d) > flo && fabsf(d) > tol * sqrtf(fmaxf(a * b, 0.f))) {
+        const float tau = __fdiv_rn(b - a, 2.f * d);
+        const float tt = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f)));
+        c = 1.0f / sqrtf(fmaf(tt, tt, 1.f));
+        sn = tt * c;
+        td = tt * d;
+        act = 1;
       }
-      if (!__syncthreads_or(act)) continue;
+      // identical in every warp (same inputs), so the branch is uniform over the CTA
+      if (!__any_sync(0xffffffffu, act)) continue;
       rotated = 1;
-      // One pass over the 32 x 32 grid of 2 x 2 blocks that this round's pairing cuts A
-      // into: block (j, k) becomes R_j^T A_jk R_k (R = [[c, s], [-s, c]] on (p, q); an
-      // inactive rotation is the identity), the rotated diagonal blocks are set exactly.
-      // Every entry of A belongs to exactly one block, so the pass needs no ordering.
-      for (int e = t; e < 32 * 32; e += 256) {
-        const int j = e >> 5, k = e & 31;
-        const int pj = rp[j], qj = rq[j], pk = rp[k], qk = rq[k];
-        if (j == k) {
-          if (ract[j]) {
-            A[pj][pj] = rap[j];
-            A[qj][qj] = raq[j];
-            A[pj][qj] = 0.f;
-            A[qj][pj] = 0.f;
+      __syncthreads();  // every warp has read the entries this round rewrites
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const int j = warp + 8 * x;
+        const int pj = __shfl_sync(0xffffffffu, p, j), qj = __shfl_sync(0xffffffffu, q, j);
+        const float cj = __shfl_sync(0xffffffffu, c, j), sj = __shfl_sync(0xffffffffu, sn, j);
+        const int actj = __shfl_sync(0xffffffffu, act, j);
+        if (j == lane) {
+          if (act) {
+            A[p][p] = a - td;
+            A[q][q] = b + td;
+            A[p][q] = 0.f;
+            A[q][p] = 0.f;
           }
           continue;
         }
-        if (!ract[j] && !ract[k]) continue;
-        const float cj = rc[j], sj = rs[j], ck = rc[k], sk = rs[k];
-        const float a = A[pj][pk], b = A[pj][qk], c = A[qj][pk], d = A[qj][qk];
-        const float a1 = a * ck - b * sk, b1 = a * sk + b * ck;
-        const float c1 = c * ck - d * sk, d1 = c * sk + d * ck;
-        A[pj][pk] = cj * a1 - sj * c1;
-        A[pj][qk] = cj * b1 - sj * d1;
-        A[qj][pk] = sj * a1 + cj * c1;
-        A[qj][qk] = sj * b1 + cj * d1;
+        if (!actj && !act) continue;
+        const float e00 = A[pj][p], e01 = A[pj][q], e10 = A[qj][p], e11 = A[qj][q];
+        const float a1 = e00 * c - e01 * sn, b1 = e00 * sn + e01 * c;
+        const float c1 = e10 * c - e11 * sn, d1 = e10 * sn + e11 * c;
+        A[pj][p] = cj * a1 - sj * c1;
+        A[pj][q] = cj * b1 - sj * d1;
+        A[qj][p] = sj * a1 + cj * c1;
+        A[qj][q] = sj * b1 + cj * d1;
       }
-      // V <- V J (columns p_j, q_j of every row).
-      for (int e = t; e < 32 * JP; e += 256) {
-        const int j = e >> 6, i = e & 63;
-        if (!ract[j]) continue;
-        const int p = rp[j], q = rq[j];
-        const float c = rc[j], s = rs[j];
-        const float x = V[i][p], y = V[i][q];
-        V[i][p] = c * x - s * y;
-        V[i][q] = s * x + c * y;
+      if (act) {
+#pragma unroll
+        for (int y = 0; y < JP / 8; ++y) {
+          const int i = warp + 8 * y;
+          const float x0 = V[i][p], y0 = V[i][q];
+          V[i][p] = c * x0 - sn * y0;
+          V[i][q] = sn * x0 + c * y0;
+        }
       }
       __syncthreads();
     }
     if (!rotated) break;
   }
+  // Rounds without an active rotation have no barrier: every warp must have finished reading
+  // A before it is reused as scratch below.
+  __syncthreads();
 #ifdef KF_JAC_SORT_PAIRS
   // Order the pair's eigenvectors by eigenvalue, largest first, so that the first block of
   // the pair receives the larger half of the pair's spectrum.
