@@ -29,7 +29,7 @@
  *    the first one wins.  kf_sync_status() synchronises the stream and returns it.
  *  - Scratch memory is passed in by the caller as `workspace` / `workspace_bytes`; each
  *    call has a *_workspace_size() query.  The library allocates nothing per call; the
- *    context owns a few bytes of device status only.
+ *    context owns a few bytes of device status and one pinned host word.
  *  - A context may be used by one host thread at a time.
  */
 #ifndef KFSVD_H
@@ -155,6 +155,9 @@ KF_API kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, con
  * the aggregated output instead of repeated SVDs).
  *
  * Batched: all problems of one call must have the same s = min(m, n) (s <= 16384).
+ * Unlike the other calls, whitened_svd waits on the stream once per Jacobi sweep (from the
+ * third on): it reads a 4-byte convergence flag and launches no further sweep once every
+ * problem of the call has converged.
  * For each problem: C = W~^T W~ (KF_SIDE_RIGHT) or W~ W~^T (KF_SIDE_LEFT) in float32;
  * C = Q Lambda Q^T by blocked parallel cyclic Jacobi (32-wide blocks, round-robin pairing,
  * every 64 x 64 pair problem diagonalised in shared memory) until every block pair has
@@ -186,6 +189,9 @@ typedef struct {
   float gram_ms, jacobi_ms, rayleigh_ms, refine_ms;  /* refine: windowed refinement + final sort */
   int64_t jacobi_steps;          /* solve + apply launch pairs issued */
   double jacobi_apply_flops;     /* executed multiply-add flops of the rotation products */
+  float jacobi_solve_ms;         /* summed device time of the pair-solve launches */
+  float jacobi_apply_ms;         /* summed device time of the rotation-apply launches */
+  int64_t jacobi_apply_launches; /* number of rotation-apply launches timed */
 } kf_svd_profile;
 
 /* Enables (1) or disables (0) recording of the profile by later whitened_svd calls. */

@@ -84,6 +84,11 @@ kf_status kf_create(int device, kf_ctx** out) {
     return fail(KF_ERR_CUDA, "kf_create: cudaMalloc of the status word failed");
   }
   cudaMemset(c->d_status, 0, bytes);
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->h_flag), sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+    cudaFree(c->d_status);
+    delete c;
+    return fail(KF_ERR_CUDA, "kf_create: cudaHostAlloc of the poll flag failed");
+  }
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
@@ -101,7 +106,9 @@ void kf_destroy(kf_ctx* ctx) {
   if (!ctx) return;
   for (int e = 0; e < 5; ++e)
     if (ctx->prof_ev[e]) cudaEventDestroy(ctx->prof_ev[e]);
+  for (cudaEvent_t e : ctx->prof_kev) cudaEventDestroy(e);
   if (ctx->d_status) cudaFree(ctx->d_status);
+  if (ctx->h_flag) cudaFreeHost(ctx->h_flag);
   delete ctx;
 }
 

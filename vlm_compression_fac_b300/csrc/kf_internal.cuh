@@ -8,6 +8,7 @@
 #include <stddef.h>
 
 #include <string>
+#include <vector>
 
 #include "../../include/kfsvd.h"
 
@@ -34,13 +35,17 @@ struct kf_ctx {
   int device = 0;
   int sm_count = 148;
   int cc_major = 0, cc_minor = 0;
-  int* d_status = nullptr;          // int32[4] on the device
+  int* d_status = nullptr;          // int32[4] on the device: code, info, Jacobi flag, spare
+  int* h_flag = nullptr;            // pinned host int: the Jacobi convergence poll
   kf::PFN_encodeTiled encode = nullptr;
   // whitened_svd profile (events on the caller's stream; flop counter at d_status + 4)
   bool prof_enabled = false;
   bool prof_valid = false;
   cudaEvent_t prof_ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
   int64_t prof_steps = 0;
+  // per-step events of the profiled Jacobi (solve start, apply start, apply end per step)
+  std::vector<cudaEvent_t> prof_kev;
+  int64_t prof_kev_used = 0;
   unsigned long long* prof_flops() { return reinterpret_cast<unsigned long long*>(d_status + 4); }
 };
 

@@ -94,7 +94,9 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
                                                         unsigned* __restrict__ offmax,
                                                         const float* __restrict__ floorv, float tol,
                                                         int max_inner) {
-  __shared__ float A[JP][JP + 1];
+  // Row stride JP + 2: the 32 couplings A[p][q] that one rotation round reads lie on an
+  // anti-diagonal (p + q constant), which a stride of JP + 1 would put in a single bank.
+  __shared__ float A[JP][JP + 2];
   __shared__ float V[JP][JP + 1];
   __shared__ float red[8];
 
@@ -451,7 +453,9 @@ __global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ C
 }
 
 __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* __restrict__ off, float tol,
-                                 int sweep, int max_sweeps, int* __restrict__ sweeps, int* status) {
+                                 int sweep, int max_sweeps, int* __restrict__ sweeps, int* status,
+                                 int* __restrict__ all_conv) {
+  int mine = 1;
   for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
     if (conv[u]) continue;
     const float o = __uint_as_float(off[u]);
@@ -459,10 +463,13 @@ __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* 
     if (sweeps) sweeps[u] = sweep + 1;
     if (o <= tol) {
       conv[u] = 1;
-    } else if (sweep + 1 == max_sweeps) {
-      raise_status(status, KF_ERR_NO_CONVERGENCE, u);
+    } else {
+      mine = 0;
+      if (sweep + 1 == max_sweeps) raise_status(status, KF_ERR_NO_CONVERGENCE, u);
     }
   }
+  const int all = __syncthreads_and(mine);
+  if (threadIdx.x == 0) *all_conv = all;
 }
 
 // ------------------------------------------------------------- Rayleigh + sort
@@ -898,6 +905,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
       if (!ctx->prof_ev[e]) KF_CUDA(cudaEventCreate(&ctx->prof_ev[e]));
     KF_CUDA(cudaMemsetAsync(flops, 0, sizeof(unsigned long long), st));
     KF_CUDA(cudaEventRecord(ctx->prof_ev[0], st));
+    ctx->prof_kev_used = 0;
     ctx->prof_steps = int64_t(max_sweeps) * (pl.nblk - 1);
     ctx->prof_valid = true;
   }
@@ -944,19 +952,42 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     attr = true;
   }
   const int max_inner = KF_JAC_MAX_INNER;
+  int sweeps_run = 0;
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[1], st));
   for (int sw = 0; sw < max_sweeps; ++sw) {
     for (int step = 0; step < pl.nblk - 1; ++step) {
+      cudaEvent_t* kev = nullptr;
+      if (prof) {
+        while (int64_t(ctx->prof_kev.size()) < ctx->prof_kev_used + 3) {
+          cudaEvent_t e;
+          KF_CUDA(cudaEventCreate(&e));
+          ctx->prof_kev.push_back(e);
+        }
+        kev = ctx->prof_kev.data() + ctx->prof_kev_used;
+        ctx->prof_kev_used += 3;
+        KF_CUDA(cudaEventRecord(kev[0], st));
+      }
       jac_solve_kernel<<<dim3(pl.npairs, nu), 256, 0, st>>>(C, pl.sp, pl.nblk, step, V, skip, conv, off, flo, tol,
                                                            max_inner); note_launch();
       KF_TRY(check_cuda(cudaGetLastError(), "jac_solve_kernel"));
+      if (prof) KF_CUDA(cudaEventRecord(kev[1], st));
       jac_apply_kernel<<<apply_grid, 256, apply_smem, st>>>(C, Q, pl.sp, pl.nblk, step, V, skip, conv, ntile_c,
                                                             per_u, int(total_tasks), flops, ctx->d_status); note_launch();
       KF_TRY(check_cuda(cudaGetLastError(), "jac_apply_kernel"));
+      if (prof) KF_CUDA(cudaEventRecord(kev[2], st));
     }
-    jac_check_kernel<<<1, 256, 0, st>>>(nu, conv, off, tol, sw, max_sweeps, sweeps_dev, ctx->d_status); note_launch();
+    jac_check_kernel<<<1, 256, 0, st>>>(nu, conv, off, tol, sw, max_sweeps, sweeps_dev, ctx->d_status,
+                                        ctx->d_status + 2); note_launch();
     KF_TRY(check_cuda(cudaGetLastError(), "jac_check_kernel"));
+    ++sweeps_run;
+    // Convergence poll: once every problem has converged no further sweep is launched.
+    if (sw >= 2 && sw + 1 < max_sweeps) {
+      KF_CUDA(cudaMemcpyAsync(ctx->h_flag, ctx->d_status + 2, sizeof(int), cudaMemcpyDeviceToHost, st));
+      KF_CUDA(cudaStreamSynchronize(st));
+      if (*ctx->h_flag) break;
+    }
   }
+  if (prof) ctx->prof_steps = int64_t(sweeps_run) * (pl.nblk - 1);
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[2], st));
   for (int i = 0; i < nu; ++i)
     if (pr[i].sweeps) KF_CUDA(cudaMemcpyAsync(pr[i].sweeps, sweeps_dev + i, sizeof(int), cudaMemcpyDeviceToDevice, st));
@@ -1053,6 +1084,17 @@ kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out) {
   out->rayleigh_ms = t[2];
   out->refine_ms = t[3];
   out->jacobi_steps = ctx->prof_steps;
+  double ts = 0.0, ta = 0.0;
+  for (int64_t i = 0; i + 3 <= ctx->prof_kev_used; i += 3) {
+    float a = 0.f, b = 0.f;
+    KF_CUDA(cudaEventElapsedTime(&a, ctx->prof_kev[i], ctx->prof_kev[i + 1]));
+    KF_CUDA(cudaEventElapsedTime(&b, ctx->prof_kev[i + 1], ctx->prof_kev[i + 2]));
+    ts += a;
+    ta += b;
+  }
+  out->jacobi_solve_ms = float(ts);
+  out->jacobi_apply_ms = float(ta);
+  out->jacobi_apply_launches = ctx->prof_kev_used / 3;
   out->jacobi_apply_flops = double(f);
   return KF_OK;
 }
