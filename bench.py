@@ -292,7 +292,7 @@ def run_kfsvd(args):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K_,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Philox; see DESIGN.md)",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded Philox4x32-10 streams and weights generated on the device",
         "config": {"workload": WORKLOAD, "global_batch": wl.n_tokens * world, "seq_len": wl.n_tokens,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs (%.1f GB) larger than L2; no flush" % (in_bytes / 1e9)},

@@ -7,7 +7,7 @@ covariance G of exactly one unit.  Values are drawn by ``synth.philox`` and are 
 function of (workload seed, block, site, element index), so any row or column range of
 any stream can be regenerated independently on the host or on the device.
 
-Distributions (the readings are listed in the design doc):
+Distributions:
   * single 256x512 layer: activations N(0, 1/i) on channel i (1-based), gradients
     N(0, i^-1/2), weights N(0, 0.02^2), all float32;
   * transformer blocks: activations unit Gaussian with round(0.01 d) outlier channels at
