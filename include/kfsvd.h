@@ -63,7 +63,12 @@ typedef enum {
 
 typedef enum { KF_BF16 = 0, KF_F32 = 1 } kf_dtype;
 typedef enum { KF_QUANT_NONE = 0, KF_QUANT_INT8_TOKEN = 1 } kf_quant;
-typedef enum { KF_KEY_HALF_SIGMA2 = 0, KF_KEY_PER_PARAM = 1, KF_FIXED_RANK = 2 } kf_alloc_mode;
+typedef enum {
+  KF_KEY_HALF_SIGMA2 = 0,   /* 1/2 sigma^2: the K-FAC estimate of the loss increase */
+  KF_KEY_PER_PARAM = 1,     /* 1/2 sigma^2 / (m + n): score per parameter cost */
+  KF_FIXED_RANK = 2,        /* a given rank per unit, no sort */
+  KF_KEY_ENERGY_RATIO = 3   /* sigma_i^2 / sum_j sigma_j^2 of the unit (UniRank's local significance) */
+} kf_alloc_mode;
 typedef enum { KF_SIDE_RIGHT = 0, KF_SIDE_LEFT = 1 } kf_side;
 
 /* whiten() flags: reuse factors that an earlier whiten() call already wrote into the
@@ -215,6 +220,7 @@ KF_API kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_prob
  * seg_offset: device int64[n_units + 1]; cost: device int64[n_units] (m_u + n_u).
  * mode:       KF_KEY_HALF_SIGMA2: key 0.5f * (sigma * sigma);
  *             KF_KEY_PER_PARAM:  that divided by (float)cost[u];
+ *             KF_KEY_ENERGY_RATIO: (sigma * sigma) / (sum of the unit's sigma^2);
  *             KF_FIXED_RANK:     ranks[u] = min(fixed_rank[u], length of unit u).
  * The keys are sorted descending (ties: lower unit, then lower component index first) by
  * a device LSD radix sort on 64-bit (~key_bits << 32 | component id) words; the prefix
@@ -231,6 +237,21 @@ KF_API kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64
                              int64_t budget, kf_alloc_mode mode, const int32_t* fixed_rank,
                              int32_t* ranks, float* cut, int64_t* used, void* workspace,
                              size_t workspace_bytes, kf_stream_t stream);
+
+/* score_and_allocate_weighted - the same allocation with every key multiplied by a per-unit
+ * weight: UniRank 2.1's aggregated score s_{l,i} = I_l sigma_{l,i}^2 / ||Sigma_l||_F^2 is
+ * KF_KEY_ENERGY_RATIO with unit_weight = I_l (the layer's functional importance, computed by
+ * the caller from forward passes); any other scoring mode may be weighted the same way.
+ * unit_weight: device float[n_units], finite and >= 0 (a negative or NaN weight counts as 0);
+ * NULL means 1 for every unit.  KF_FIXED_RANK is rejected.  The energy of a unit is the float64
+ * sum of its sigma^2 rounded to float32; every key is then formed in float32 with one rounding
+ * per operation (square, divide, multiply by the weight).  Workspace as for
+ * score_and_allocate (score_and_allocate_workspace_size covers every mode). */
+KF_API kf_status score_and_allocate_weighted(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset,
+                                             const int64_t* cost, int32_t n_units, int64_t n_components,
+                                             int64_t budget, kf_alloc_mode mode, const float* unit_weight,
+                                             int32_t* ranks, float* cut, int64_t* used, void* workspace,
+                                             size_t workspace_bytes, kf_stream_t stream);
 
 /* score_and_allocate_noalloc - score_and_allocate for callers that cannot allocate device
  * memory: for example a host framework that has already handed all device memory to its own

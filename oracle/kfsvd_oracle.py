@@ -43,6 +43,7 @@ import scipy.linalg as sla
 
 KEY_HALF_SIGMA2 = "half_sigma2"
 KEY_PER_PARAM = "per_param"
+KEY_ENERGY_RATIO = "energy_ratio"
 FIXED_RANK = "fixed_rank"
 
 
@@ -118,25 +119,43 @@ def gram_eigenvalues(Wt: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------- step 5: allocation
-def component_scores(sigma: np.ndarray, cost: int, mode: str, precision: str):
+def component_scores(sigma: np.ndarray, cost: int, mode: str, precision: str, weight: Optional[float] = None):
     """Score of each component: half its squared whitened singular value (the K-FAC
     estimate of the loss increase when it is dropped, [LASER] 1), or that divided by the
-    m+n parameters the pair costs ([LASER] 2, "score per parameter cost").
+    m+n parameters the pair costs ([LASER] 2, "score per parameter cost"), or [UniRank] 2.1's
+    local structural significance, the energy ratio sigma_i^2 / ||Sigma||_F^2 of the unit.
+    A unit weight (UniRank's functional importance I_l) multiplies every key of the unit;
+    a weight that is not positive gives 0.
 
-    ``precision="f32"`` evaluates 0.5 * (sigma * sigma) [/ cost] in float32 with one
-    rounding per operation, the order the GPU uses, so that both sides rank identical
-    float32 sigma identically.
+    ``precision="f32"`` evaluates the key in float32 with one rounding per operation, the
+    order the GPU uses (square, divide, multiply by the weight; the energy is the float64 sum
+    of the squares rounded to float32), so that both sides rank identical float32 sigma
+    identically.
     """
     if precision == "f32":
         s = np.asarray(sigma, dtype=np.float32)
-        sc = (np.float32(0.5) * (s * s)).astype(np.float32)
-        if mode == KEY_PER_PARAM:
-            sc = (sc / np.float32(cost)).astype(np.float32)
+        q = (s * s).astype(np.float32)
+        if mode == KEY_ENERGY_RATIO:
+            e = np.float32(np.sum(np.asarray(s, dtype=np.float64) ** 2))
+            sc = (q / e).astype(np.float32) if e > 0 else np.zeros_like(q)
+        else:
+            sc = (np.float32(0.5) * q).astype(np.float32)
+            if mode == KEY_PER_PARAM:
+                sc = (sc / np.float32(cost)).astype(np.float32)
+        if weight is not None:
+            w = np.float32(weight)
+            sc = (w * sc).astype(np.float32) if w > 0 else np.zeros_like(sc)
         return sc
     s = np.asarray(sigma, dtype=np.float64)
-    sc = 0.5 * s * s
-    if mode == KEY_PER_PARAM:
-        sc = sc / float(cost)
+    if mode == KEY_ENERGY_RATIO:
+        e = float(np.sum(s * s))
+        sc = s * s / e if e > 0 else np.zeros_like(s)
+    else:
+        sc = 0.5 * s * s
+        if mode == KEY_PER_PARAM:
+            sc = sc / float(cost)
+    if weight is not None:
+        sc = sc * float(weight) if weight > 0 else np.zeros_like(sc)
     return sc
 
 
@@ -153,7 +172,7 @@ class Allocation:
 
 def allocate(sigmas: Sequence[np.ndarray], costs: Sequence[int], budget: int,
              mode: str = KEY_HALF_SIGMA2, fixed_ranks: Optional[Sequence[int]] = None,
-             precision: str = "f64") -> Allocation:
+             precision: str = "f64", weights: Optional[Sequence[float]] = None) -> Allocation:
     """Global sort-and-truncate rank allocation.
 
     [UniRank] 2.1 and [LASER] 2: pool the scores of every component of every unit, sort
@@ -170,7 +189,7 @@ def allocate(sigmas: Sequence[np.ndarray], costs: Sequence[int], budget: int,
         return Allocation(ranks, float("nan"), float("nan"), used, e, e, np.zeros(0))
     units, comps, scores = [], [], []
     for u, s in enumerate(sigmas):
-        sc = component_scores(s, costs[u], mode, precision)
+        sc = component_scores(s, costs[u], mode, precision, None if weights is None else weights[u])
         units.append(np.full(len(sc), u, dtype=np.int64))
         comps.append(np.arange(len(sc), dtype=np.int64))
         scores.append(sc.astype(np.float64))

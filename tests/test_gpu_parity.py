@@ -264,6 +264,38 @@ def test_allocation_bit_identical(ctx, case):
         assert (np.isnan(g) and np.isnan(w)) or np.float32(g) == np.float32(w)
 
 
+@pytest.mark.parametrize("mode", ["energy_ratio", "half_sigma2", "per_param"])
+def test_weighted_allocation_bit_identical(ctx, mode):
+    """UniRank's aggregated key I_l sigma^2 / ||Sigma_l||^2 (and weighted forms of the other
+    keys) through score_and_allocate_weighted: bit-identical ranks, cut and used."""
+    r = np.random.default_rng({"energy_ratio": 1, "half_sigma2": 2, "per_param": 3}[mode])
+    sig, costs = [], []
+    for u in range(40):
+        m, n = int(r.integers(8, 600)), int(r.integers(8, 600))
+        sig.append(np.sort(r.gamma(1.0, 1.0, size=min(m, n)))[::-1].astype(np.float32))
+        costs.append(m + n)
+    w = r.uniform(0.0, 2.0, len(sig)).astype(np.float32)
+    w[3] = 0.0
+    budget = int(0.35 * sum(len(s) * c for s, c in zip(sig, costs)))
+    kmode = {"energy_ratio": K().KF_KEY_ENERGY_RATIO, "half_sigma2": K().KF_KEY_HALF_SIGMA2,
+             "per_param": K().KF_KEY_PER_PARAM}[mode]
+    sd = torch.from_numpy(np.concatenate(sig)).cuda()
+    off = torch.tensor([0] + list(np.cumsum([len(s) for s in sig])), dtype=torch.int64, device="cuda")
+    cost = torch.tensor(costs, dtype=torch.int64, device="cuda")
+    ranks = torch.empty(len(sig), dtype=torch.int32, device="cuda")
+    cut = torch.empty(2, dtype=torch.float32, device="cuda")
+    used = torch.zeros(1, dtype=torch.int64, device="cuda")
+    K().score_and_allocate_weighted(ctx, sd, off, cost, budget, ranks, mode=kmode, unit_weight=torch.from_numpy(w).cuda(),
+                                    cut=cut, used=used)
+    ctx.sync_status()
+    al = O.allocate(sig, costs, budget, mode, precision="f32", weights=list(w))
+    np.testing.assert_array_equal(ranks.cpu().numpy(), al.ranks)
+    assert int(used.item()) == al.used
+    c = cut.cpu().numpy()
+    assert np.float32(c[0]) == np.float32(al.cut_score) and np.float32(c[1]) == np.float32(al.next_score)
+    assert int(ranks[3].item()) == 0
+
+
 def test_allocation_fixed_rank(ctx):
     ranks, cut, used = _gpu_alloc(ctx, [np.ones(5, np.float32), np.ones(3, np.float32)], [10, 20], 0,
                                   K().KF_FIXED_RANK, fixed=[4, 4])

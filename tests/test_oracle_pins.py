@@ -310,3 +310,40 @@ def test_head_units_use_the_diagonal_factor_blocks():
         np.testing.assert_array_equal(ur.G, Gf[u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n])
         np.testing.assert_array_equal(ur.Wt, O.whiten(recipes.gen_full_weight(wl, u)[
             u.row0:u.row0 + u.m, u.col0:u.col0 + u.n], ur.Sx, ur.Sg))
+
+
+def test_energy_ratio_key_unirank():
+    """UniRank 2.1: s_{l,i} = I_l sigma_{l,i}^2 / ||Sigma_l||_F^2, sorted and truncated under the
+    m + n cost of each kept pair."""
+    # hand case: unit 0 sigma (2, 1) -> energy 5 -> keys 0.8, 0.2; unit 1 sigma (1, 1) ->
+    # keys 0.5, 0.5; costs 10 each.  Sorted: 0.8 (u0), 0.5 (u1), 0.5 (u1), 0.2 (u0).
+    sig = [np.array([2.0, 1.0]), np.array([1.0, 1.0])]
+    al = O.allocate(sig, [10, 10], 30, O.KEY_ENERGY_RATIO)
+    assert list(al.ranks) == [1, 2] and al.used == 30 and abs(al.cut_score - 0.5) < 1e-15
+    # weights I = (1, 2): unit 1's keys become 1.0, 1.0, ahead of 0.8; budget 20 keeps only them
+    al = O.allocate(sig, [10, 10], 20, O.KEY_ENERGY_RATIO, weights=[1.0, 2.0])
+    assert list(al.ranks) == [0, 2] and abs(al.cut_score - 1.0) < 1e-15 and abs(al.next_score - 0.8) < 1e-15
+    # a zero weight removes a unit from the competition
+    al = O.allocate(sig, [10, 10], 40, O.KEY_ENERGY_RATIO, weights=[0.0, 1.0])
+    assert list(al.ranks) == [2, 2] and al.order_unit[-1] == 0
+    r = np.random.default_rng(11)
+    sigs = [np.sort(r.gamma(1.0, 1.0, k))[::-1] for k in (9, 14, 6)]
+    costs = [30, 25, 17]
+    budget = 300
+    # one unit alone: a positive multiple of sigma^2, so the same ranks as 1/2 sigma^2
+    for s_ in sigs:
+        assert list(O.allocate([s_], [20], 100, O.KEY_ENERGY_RATIO).ranks) == \
+            list(O.allocate([s_], [20], 100, O.KEY_HALF_SIGMA2).ranks)
+    # invariant to rescaling a unit's spectrum (1/2 sigma^2 is not)
+    base = O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO).ranks
+    scaled = [sigs[0] * 10.0] + sigs[1:]
+    assert list(O.allocate(scaled, costs, budget, O.KEY_ENERGY_RATIO).ranks) == list(base)
+    assert list(O.allocate(scaled, costs, budget, O.KEY_HALF_SIGMA2).ranks) != \
+        list(O.allocate(sigs, costs, budget, O.KEY_HALF_SIGMA2).ranks)
+    # weights multiply: w = 1 everywhere changes nothing, a common factor changes nothing
+    assert list(O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO, weights=[1, 1, 1]).ranks) == list(base)
+    assert list(O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO, weights=[3, 3, 3]).ranks) == list(base)
+    # the float32 evaluation ranks like the float64 one away from ties
+    assert list(O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO, precision="f32",
+                           weights=[0.5, 2.0, 1.0]).ranks) == \
+        list(O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO, weights=[0.5, 2.0, 1.0]).ranks)

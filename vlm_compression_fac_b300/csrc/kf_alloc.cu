@@ -1,5 +1,7 @@
 // Global sort-and-truncate rank allocation (UniRank 2.1; LASER Methodology 2).
-//   keys:  k = (~bits(score) << 32) | component id, score = 0.5f * (sigma * sigma) [/ cost];
+//   keys:  k = (~bits(score) << 32) | component id, score = 0.5f * (sigma * sigma) [/ cost],
+//          or UniRank's energy ratio sigma^2 / sum_unit sigma^2, optionally times a per-unit
+//          weight (UniRank's layer importance I_l);
 //          ascending k is score descending, then lower unit, then lower component index
 //          (ids are assigned in unit order), which makes the order total and deterministic;
 //   sort:  LSD radix sort, 8 passes of 8 bits; each pass = per-tile digit histogram,
@@ -29,16 +31,54 @@ __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_un
   return lo;
 }
 
+// Key of every component: base score per mode (KF_KEY_HALF_SIGMA2: 0.5 sigma^2;
+// KF_KEY_PER_PARAM: that divided by the unit's m + n; KF_KEY_ENERGY_RATIO: sigma^2 divided
+// by the unit's energy sum sigma^2), times the unit's weight when weights are given (a
+// weight that is negative or not a number counts as 0).  float32, one rounding per operation.
 __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off,
                                   const int64_t* __restrict__ cost, int n_units, int64_t n, int mode,
+                                  const float* __restrict__ weight, const float* __restrict__ energy,
                                   unsigned long long* __restrict__ keys) {
   for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += int64_t(gridDim.x) * blockDim.x) {
     const int u = unit_of(off, n_units, g);
     const float s = sigma[g];
-    float sc = 0.5f * __fmul_rn(s, s);
-    if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
+    const float q = __fmul_rn(s, s);
+    float sc;
+    if (mode == KF_KEY_ENERGY_RATIO) {
+      const float e = energy[u];
+      sc = e > 0.f ? __fdiv_rn(q, e) : 0.f;
+    } else {
+      sc = 0.5f * q;
+      if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
+    }
+    if (weight) {
+      const float w = weight[u];
+      sc = (w > 0.f) ? __fmul_rn(w, sc) : 0.f;  // also maps a NaN weight to 0
+    }
     const unsigned bits = ~__float_as_uint(sc);
     keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(uint32_t(g));
+  }
+}
+
+// energy[u] = sum of sigma^2 over unit u's segment (float64 sum of exact squares, rounded).
+__global__ void __launch_bounds__(256) unit_energy_kernel(const float* __restrict__ sigma,
+                                                          const int64_t* __restrict__ off,
+                                                          float* __restrict__ energy) {
+  __shared__ double red[8];
+  const int u = blockIdx.x;
+  double acc = 0.0;
+  for (int64_t g = off[u] + threadIdx.x; g < off[u + 1]; g += blockDim.x) {
+    const double v = sigma[g];
+    acc += v * v;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    energy[u] = float(t);
   }
 }
 
@@ -274,9 +314,11 @@ struct AllocBufs {
   unsigned long long *ka, *kb, *kcount;
   unsigned* hist;
   long long *bsum, *prefix;
+  float* energy;
 };
 
-size_t alloc_carve(Carve& cv, int64_t n, AllocBufs& b) {
+// n_energy: units whose energy is needed (KF_KEY_ENERGY_RATIO), else 0.
+size_t alloc_carve(Carve& cv, int64_t n, int64_t n_energy, AllocBufs& b) {
   const int64_t ntiles = (n + TILE - 1) / TILE;
   const int64_t nb = (n + SCAN_T - 1) / SCAN_T;
   b.ka = cv.take<unsigned long long>(n > 0 ? n : 1);
@@ -285,20 +327,21 @@ size_t alloc_carve(Carve& cv, int64_t n, AllocBufs& b) {
   b.bsum = cv.take<long long>(nb > 0 ? nb : 1);
   b.prefix = cv.take<long long>(n > 0 ? n : 1);
   b.kcount = cv.take<unsigned long long>(1);
+  b.energy = n_energy > 0 ? cv.take<float>(n_energy) : nullptr;
   return cv.off;
 }
 
 }  // namespace
 
-size_t alloc_workspace(int64_t n) {
+size_t alloc_workspace(int64_t n, int64_t n_energy) {
   Carve cv(nullptr, 0, true);
   AllocBufs b;
-  return alloc_carve(cv, n, b) + 256;
+  return alloc_carve(cv, n, n_energy, b) + 256;
 }
 
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
-                    int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, int32_t* ranks, float* cut,
-                    int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st) {
+                    int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
+                    int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st) {
   (void)ctx;
   KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
   if (mode == KF_FIXED_RANK) {
@@ -307,10 +350,15 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   }
   Carve cv(ws, ws_bytes, false);
   AllocBufs b;
-  alloc_carve(cv, n, b);
+  alloc_carve(cv, n, mode == KF_KEY_ENERGY_RATIO ? n_units : 0, b);
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "score_and_allocate: workspace too small");
   const int ntiles = int((n + TILE - 1) / TILE);
-  build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), b.ka); note_launch();
+  if (mode == KF_KEY_ENERGY_RATIO) {
+    unit_energy_kernel<<<unsigned(n_units), 256, 0, st>>>(sigma, off, b.energy); note_launch();
+    KF_CUDA(cudaGetLastError());
+  }
+  build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), weight, b.energy,
+                                                      b.ka); note_launch();
   KF_CUDA(cudaGetLastError());
   unsigned long long* src = b.ka;
   unsigned long long* dst = b.kb;
@@ -349,7 +397,7 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
 // GPU that loads the library until the process exits.
 namespace {
 constexpr int64_t NOALLOC_MAX_COMPONENTS = int64_t(1) << 20;
-constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(25) << 20;  // >= alloc_workspace(1 << 20)
+constexpr size_t NOALLOC_SCRATCH_BYTES = size_t(25) << 20;  // >= alloc_workspace(1 << 20, 0)
 constexpr int NOALLOC_MAX_DEVICES = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {};
@@ -368,7 +416,7 @@ static kf_status noalloc_scratch(int device, void** out) {
   if (device < 0 || device >= NOALLOC_MAX_DEVICES) return fail(KF_ERR_UNSUPPORTED, "score_and_allocate_noalloc: device index");
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[device]) {
-    if (alloc_workspace(NOALLOC_MAX_COMPONENTS) > NOALLOC_SCRATCH_BYTES)
+    if (alloc_workspace(NOALLOC_MAX_COMPONENTS, 0) > NOALLOC_SCRATCH_BYTES)
       return fail(KF_ERR_UNSUPPORTED, "score_and_allocate_noalloc: static scratch smaller than its stated maximum");
     int prev = 0;
     KF_CUDA(cudaGetDevice(&prev));
@@ -410,6 +458,6 @@ extern "C" kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma,
   }
   void* scratch = nullptr;
   KF_TRY(noalloc_scratch(ctx->device, &scratch));
-  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, ranks, cut, used,
-                   scratch, NOALLOC_SCRATCH_BYTES, st);
+  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, nullptr, ranks, cut,
+                   used, scratch, NOALLOC_SCRATCH_BYTES, st);
 }

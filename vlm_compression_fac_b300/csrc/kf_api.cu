@@ -12,10 +12,10 @@ size_t svd_workspace(int32_t nu, int64_t m_max, int64_t n_max, int64_t s);
 kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, int32_t max_sweeps, void* ws,
                   size_t ws_bytes, cudaStream_t st);
 kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out);
-size_t alloc_workspace(int64_t n);
+size_t alloc_workspace(int64_t n, int64_t n_energy);
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
-                    int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, int32_t* ranks, float* cut,
-                    int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st);
+                    int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
+                    int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st);
 }  // namespace kf
 
 using namespace kf;
@@ -398,24 +398,28 @@ kf_status kf_svd_profile_read(kf_ctx* ctx, kf_svd_profile* out) {
 
 // ----------------------------------------------------------------------- (5a)
 size_t score_and_allocate_workspace_size(int64_t n_components, int32_t n_units) {
-  (void)n_units;
-  return alloc_workspace(n_components > 0 ? n_components : 1);
+  // room for the per-unit energies too, so one size serves every mode
+  return alloc_workspace(n_components > 0 ? n_components : 1, n_units > 0 ? n_units : 0);
 }
 
-kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset, const int64_t* cost,
-                             int32_t n_units, int64_t n_components, int64_t budget, kf_alloc_mode mode,
-                             const int32_t* fixed_rank, int32_t* ranks, float* cut, int64_t* used, void* workspace,
-                             size_t workspace_bytes, kf_stream_t stream) {
-  KF_TRY(need(ctx != nullptr, "score_and_allocate: null context"));
-  KF_TRY(need(n_units > 0 && n_components >= 0, "score_and_allocate: sizes"));
-  KF_TRY(need(n_components < (int64_t(1) << 32), "score_and_allocate: at most 2^32 - 1 components"));
-  KF_TRY(need(seg_offset && cost && ranks, "score_and_allocate: null pointer"));
-  KF_TRY(need(mode == KF_KEY_HALF_SIGMA2 || mode == KF_KEY_PER_PARAM || mode == KF_FIXED_RANK,
-              "score_and_allocate: mode"));
-  if (mode == KF_FIXED_RANK) KF_TRY(need(fixed_rank != nullptr, "score_and_allocate: fixed_rank is null"));
-  else KF_TRY(need(sigma != nullptr || n_components == 0, "score_and_allocate: sigma is null"));
-  if (mode != KF_FIXED_RANK && workspace_bytes < alloc_workspace(n_components > 0 ? n_components : 1))
-    return fail(KF_ERR_WORKSPACE, "score_and_allocate: workspace too small");
+namespace {
+kf_status allocate_common(kf_ctx* ctx, const char* who, const float* sigma, const int64_t* seg_offset,
+                          const int64_t* cost, int32_t n_units, int64_t n_components, int64_t budget,
+                          kf_alloc_mode mode, const int32_t* fixed_rank, const float* weight, int32_t* ranks,
+                          float* cut, int64_t* used, void* workspace, size_t workspace_bytes, kf_stream_t stream) {
+  const std::string w(who);
+  KF_TRY(need(ctx != nullptr, (w + ": null context").c_str()));
+  KF_TRY(need(n_units > 0 && n_components >= 0, (w + ": sizes").c_str()));
+  KF_TRY(need(n_components < (int64_t(1) << 32), (w + ": at most 2^32 - 1 components").c_str()));
+  KF_TRY(need(seg_offset && cost && ranks, (w + ": null pointer").c_str()));
+  KF_TRY(need(mode == KF_KEY_HALF_SIGMA2 || mode == KF_KEY_PER_PARAM || mode == KF_FIXED_RANK ||
+                  mode == KF_KEY_ENERGY_RATIO,
+              (w + ": mode").c_str()));
+  if (mode == KF_FIXED_RANK) KF_TRY(need(fixed_rank != nullptr, (w + ": fixed_rank is null").c_str()));
+  else KF_TRY(need(sigma != nullptr || n_components == 0, (w + ": sigma is null").c_str()));
+  const int64_t n_energy = mode == KF_KEY_ENERGY_RATIO ? n_units : 0;
+  if (mode != KF_FIXED_RANK && workspace_bytes < alloc_workspace(n_components > 0 ? n_components : 1, n_energy))
+    return fail(KF_ERR_WORKSPACE, w + ": workspace too small");
   if (mode != KF_FIXED_RANK && n_components == 0) {
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
@@ -423,8 +427,26 @@ kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64_t* seg
     if (cut) KF_CUDA(cudaMemsetAsync(cut, 0xFF, 2 * sizeof(float), st));  // NaN
     return KF_OK;
   }
-  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, ranks, cut, used,
-                   workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, weight, ranks, cut,
+                   used, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+kf_status score_and_allocate(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset, const int64_t* cost,
+                             int32_t n_units, int64_t n_components, int64_t budget, kf_alloc_mode mode,
+                             const int32_t* fixed_rank, int32_t* ranks, float* cut, int64_t* used, void* workspace,
+                             size_t workspace_bytes, kf_stream_t stream) {
+  return allocate_common(ctx, "score_and_allocate", sigma, seg_offset, cost, n_units, n_components, budget, mode,
+                         fixed_rank, nullptr, ranks, cut, used, workspace, workspace_bytes, stream);
+}
+
+kf_status score_and_allocate_weighted(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset,
+                                      const int64_t* cost, int32_t n_units, int64_t n_components, int64_t budget,
+                                      kf_alloc_mode mode, const float* unit_weight, int32_t* ranks, float* cut,
+                                      int64_t* used, void* workspace, size_t workspace_bytes, kf_stream_t stream) {
+  if (mode == KF_FIXED_RANK) return fail(KF_ERR_INVALID, "score_and_allocate_weighted: KF_FIXED_RANK has no scores");
+  return allocate_common(ctx, "score_and_allocate_weighted", sigma, seg_offset, cost, n_units, n_components, budget,
+                         mode, nullptr, unit_weight, ranks, cut, used, workspace, workspace_bytes, stream);
 }
 
 // ----------------------------------------------------------------------- (5b)

@@ -19,7 +19,7 @@ KF_OK, KF_ERR_INVALID, KF_ERR_WORKSPACE, KF_ERR_CUDA = 0, 1, 2, 3
 KF_ERR_NOT_SPD, KF_ERR_NO_CONVERGENCE, KF_ERR_TIMEOUT, KF_ERR_UNSUPPORTED = 4, 5, 6, 7
 KF_BF16, KF_F32 = 0, 1
 KF_QUANT_NONE, KF_QUANT_INT8_TOKEN = 0, 1
-KF_KEY_HALF_SIGMA2, KF_KEY_PER_PARAM, KF_FIXED_RANK = 0, 1, 2
+KF_KEY_HALF_SIGMA2, KF_KEY_PER_PARAM, KF_FIXED_RANK, KF_KEY_ENERGY_RATIO = 0, 1, 2, 3
 KF_SIDE_RIGHT, KF_SIDE_LEFT = 0, 1
 KF_REUSE_SX, KF_REUSE_SG, KF_REUSE_SINV = 1, 2, 4
 
@@ -31,7 +31,8 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "kfac_accumulate_workspace_size", "kfac_accumulate", "kf_finalize_covariance",
             "whiten_workspace_size", "whiten", "kf_svd_profile_enable", "kf_svd_profile_read",
             "whitened_svd_workspace_size", "whitened_svd",
-            "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_noalloc",
+            "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_weighted",
+            "score_and_allocate_noalloc",
             "unwhiten_workspace_size", "unwhiten"]
 
 
@@ -75,6 +76,7 @@ _SIGS = {
     "whitened_svd": (_I32, [_P, _I32, ctypes.POINTER(SvdProblem), _F, _I32, _P, _SZ, _P]),
     "score_and_allocate_workspace_size": (_SZ, [_I64, _I32]),
     "score_and_allocate": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "score_and_allocate_weighted": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
     "unwhiten_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "unwhiten": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _I64,
@@ -253,6 +255,18 @@ def score_and_allocate(ctx: Context, sigma, seg_offset, cost, budget: int, ranks
     _check(lib().score_and_allocate(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
                                     int(budget), int(mode), _ptr(fixed_rank), _ptr(ranks), _ptr(cut),
                                     _ptr(used), _ptr(ws), wsb, _stream(stream)))
+
+
+def score_and_allocate_weighted(ctx: Context, sigma, seg_offset, cost, budget: int, ranks,
+                                mode: int = KF_KEY_ENERGY_RATIO, unit_weight=None, cut=None, used=None,
+                                workspace=None, stream=None):
+    """Allocation with per-unit weighted keys (UniRank: KF_KEY_ENERGY_RATIO, weight I_l)."""
+    n_units = int(cost.numel())
+    n = int(sigma.numel()) if sigma is not None else 0
+    ws, wsb = _ws(score_and_allocate_workspace_size(n, n_units), workspace, ranks.device)
+    _check(lib().score_and_allocate_weighted(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
+                                             int(budget), int(mode), _ptr(unit_weight), _ptr(ranks), _ptr(cut),
+                                             _ptr(used), _ptr(ws), wsb, _stream(stream)))
 
 
 def score_and_allocate_noalloc(ctx: Context, sigma, seg_offset, cost, budget: int, ranks,
