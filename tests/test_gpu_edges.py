@@ -93,7 +93,9 @@ def test_vector_shaped_layers(ctx, m, n):
     V = torch.empty((1, n), device="cuda")
     K().unwhiten(ctx, to_dev(W, torch), Sx, Sg, Si, sig, vec, 1, U, V)
     ctx.sync_status()
-    np.testing.assert_allclose(U.cpu().numpy() @ V.cpu().numpy(), W, rtol=0, atol=1e-5 * np.abs(W).max())
+    # full rank: U V reproduces W up to the unwhitening's operand split (hi + lo bfloat16
+    # planes, 16 significant bits, about 1.5e-5 relative per operand and product)
+    np.testing.assert_allclose(U.cpu().numpy() @ V.cpu().numpy(), W, rtol=0, atol=1e-4 * np.abs(W).max())
 
 
 def test_allocation_empty_pool_and_extreme_budgets(ctx):
