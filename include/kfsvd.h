@@ -253,6 +253,20 @@ KF_API kf_status score_and_allocate_weighted(kf_ctx* ctx, const float* sigma, co
                                              int32_t* ranks, float* cut, int64_t* used, void* workspace,
                                              size_t workspace_bytes, kf_stream_t stream);
 
+/* score_and_allocate_keys - sort-and-truncate over per-component keys computed elsewhere
+ * (UniRank 2.1's procedure with any score, e.g. LASER Methodology 2's empirical-Fisher scores
+ * from empirical_fisher_accumulate).  keys: device float[n_components] laid out like sigma
+ * (unit u owns keys[seg_offset[u] .. seg_offset[u+1])), >= 0 (a negative or NaN key counts as
+ * 0), in any order within a unit.  Ties: lower unit, then lower component index first.
+ * ranks: kept components per unit; keep: device uint8[n_components] out (may be NULL), 1 for
+ * every kept component (the kept set of a unit need not be a prefix of its spectrum);
+ * cut / used as for score_and_allocate.  Workspace: score_and_allocate_workspace_size. */
+KF_API kf_status score_and_allocate_keys(kf_ctx* ctx, const float* keys, const int64_t* seg_offset,
+                                         const int64_t* cost, int32_t n_units, int64_t n_components,
+                                         int64_t budget, int32_t* ranks, uint8_t* keep, float* cut,
+                                         int64_t* used, void* workspace, size_t workspace_bytes,
+                                         kf_stream_t stream);
+
 /* score_and_allocate_noalloc - score_and_allocate for callers that cannot allocate device
  * memory: for example a host framework that has already handed all device memory to its own
  * pool, or a caller that must not trigger a device allocation (which may synchronise the
@@ -290,6 +304,26 @@ KF_API kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t 
                    const float* Sinv, int64_t ldsi, const float* sigma, const float* vecs,
                    int64_t ldv, int32_t r, float* U, int64_t ldu, float* V, int64_t ldvo,
                    void* workspace, size_t workspace_bytes, kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * empirical_fisher_accumulate - LASER Methodology 2's component importance: the
+ * contribution of each singular pair to the empirical-Fisher quadratic loss, evaluated with
+ * the calibration gradients in the original space.  For the factors U (m x r, column i =
+ * u_i) and V (r x n, row i = v_i) of all the components to be scored (unwhiten with r =
+ * min(m, n) gives every component):
+ *   score_sum[i] += sum_t (a_t . u_i)^2 (g_t . v_i)^2      (float64)
+ * over the n_tokens rows of act (n_tokens x m, lda) and grad (n_tokens x n, ldg), bfloat16 or
+ * float32.  The score is score_sum / (2 N) after the last chunk.  The projections run on the
+ * tensor cores with U and V split into hi + lo bfloat16 planes (about 3e-5 relative per
+ * projection); the squares and sums are float64, in a fixed order (deterministic).
+ * ---------------------------------------------------------------------------------- */
+KF_API size_t empirical_fisher_workspace_size(int64_t m, int64_t n, int32_t r);
+KF_API kf_status empirical_fisher_accumulate(kf_ctx* ctx, const void* act, kf_dtype act_dtype, int64_t lda,
+                                             const void* grad, kf_dtype grad_dtype, int64_t ldg,
+                                             int64_t n_tokens, int64_t m, int64_t n, const float* U,
+                                             int64_t ldu, const float* V, int64_t ldv, int32_t r,
+                                             double* score_sum, void* workspace, size_t workspace_bytes,
+                                             kf_stream_t stream);
 
 #ifdef __cplusplus
 }

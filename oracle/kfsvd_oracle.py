@@ -219,6 +219,45 @@ def unwhiten(Sx: np.ndarray, Sg: np.ndarray, Ut: np.ndarray, sigma: np.ndarray,
     return U, V
 
 
+# ------------------------------------------------ empirical-Fisher component scores
+def empirical_fisher_scores(A: np.ndarray, Gr: np.ndarray, U: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """[LASER] 2: the importance of component i is its contribution to the empirical-Fisher
+    quadratic loss, evaluated with the calibration gradients in the original space:
+    score_i = 1/2 (1/N) sum_t (a_t . u_i)^2 (g_t . v_i)^2, with u_i the i-th column of U
+    (d_in x r) and v_i the i-th row of V (r x d_out).  This is 1/2 vec(dW)^T F vec(dW) for the
+    rank-one dW = u_i v_i and F = (1/N) sum_t vec(a_t^T g_t) vec(a_t^T g_t)^T."""
+    A = np.asarray(A, dtype=np.float64)
+    Gr = np.asarray(Gr, dtype=np.float64)
+    P = A @ np.asarray(U, dtype=np.float64)            # N x r: a_t . u_i
+    Q = Gr @ np.asarray(V, dtype=np.float64).T         # N x r: g_t . v_i
+    return 0.5 * np.mean(P * P * Q * Q, axis=0)
+
+
+def allocate_keys(keys: Sequence[np.ndarray], costs: Sequence[int], budget: int) -> Allocation:
+    """Sort-and-truncate over arbitrary non-negative per-component keys ([UniRank] 2.1's
+    procedure with any score, e.g. [LASER] 2's empirical-Fisher scores, which are not
+    monotone along a unit's spectrum): ties by unit, then component index; the kept set of a
+    unit is then any subset, returned as order_unit/order_comp of the first `ranks.sum()`
+    entries and by the per-unit counts."""
+    units, comps, scores = [], [], []
+    for u, k in enumerate(keys):
+        k = np.asarray(k, dtype=np.float64)
+        units.append(np.full(len(k), u, dtype=np.int64))
+        comps.append(np.arange(len(k), dtype=np.int64))
+        scores.append(k)
+    units = np.concatenate(units)
+    comps = np.concatenate(comps)
+    scores = np.concatenate(scores)
+    order = np.lexsort((comps, units, -scores))
+    prefix = np.cumsum(np.asarray(costs, dtype=np.int64)[units[order]])
+    n_keep = int(np.searchsorted(prefix, budget, side="right"))
+    ranks = np.bincount(units[order[:n_keep]], minlength=len(keys)).astype(np.int64)
+    cut = float(scores[order[n_keep - 1]]) if n_keep > 0 else float("nan")
+    nxt = float(scores[order[n_keep]]) if n_keep < len(order) else float("nan")
+    used = int(prefix[n_keep - 1]) if n_keep > 0 else 0
+    return Allocation(ranks, cut, nxt, used, units[order], comps[order], scores[order])
+
+
 # --------------------------------------------------------------- the objective
 def kfac_quadratic(dW: np.ndarray, X: np.ndarray, G: np.ndarray) -> float:
     """[LASER] 1, K-FAC surrogate: 1/2 vec(dW)^T (G kron X) vec(dW), built explicitly

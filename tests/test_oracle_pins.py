@@ -347,3 +347,48 @@ def test_energy_ratio_key_unirank():
     assert list(O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO, precision="f32",
                            weights=[0.5, 2.0, 1.0]).ranks) == \
         list(O.allocate(sigs, costs, budget, O.KEY_ENERGY_RATIO, weights=[0.5, 2.0, 1.0]).ranks)
+
+
+def test_empirical_fisher_score_is_the_rank_one_fisher_form():
+    """LASER 2: the empirical-Fisher score of component i is 1/2 vec(dW)^T F vec(dW) for
+    dW = u_i v_i, with F the explicit empirical Fisher (1/N) sum_t g_t g_t^T over the
+    per-token weight gradients g_t = vec(a_t^T gr_t) (column-major vec, d_in x d_out)."""
+    r = np.random.default_rng(21)
+    N, m, n, k = 40, 4, 5, 3
+    A = r.standard_normal((N, m))
+    Gr = r.standard_normal((N, n))
+    U = r.standard_normal((m, k))
+    V = r.standard_normal((k, n))
+    F = np.zeros((m * n, m * n))
+    for t in range(N):
+        g = np.outer(A[t], Gr[t]).reshape(-1, order="F")
+        F += np.outer(g, g) / N
+    sc = O.empirical_fisher_scores(A, Gr, U, V)
+    for i in range(k):
+        dw = np.outer(U[:, i], V[i]).reshape(-1, order="F")
+        assert abs(sc[i] - 0.5 * dw @ F @ dw) <= 1e-12 * abs(sc[i])
+    # when the gradients are a fixed direction times a scalar independent of the activation
+    # amplitudes... the K-FAC factorisation is exact, F = G kron X, and the score is
+    # 1/2 (u^T X u)(v G v^T); with the whitened factors this is 1/2 sigma^2
+    c = r.standard_normal(N)
+    d = r.standard_normal(n)
+    Gr1 = np.outer(np.ones(N), d)             # g_t = d for every token: G = d d^T
+    X = A.T @ A / N
+    Gm = np.outer(d, d)
+    sc = O.empirical_fisher_scores(A, Gr1, U, V)
+    for i in range(k):
+        assert abs(sc[i] - 0.5 * (U[:, i] @ X @ U[:, i]) * (V[i] @ Gm @ V[i])) <= 1e-10 * abs(sc[i])
+
+
+def test_allocate_keys_matches_monotone_allocation_and_selects_subsets():
+    r = np.random.default_rng(22)
+    sigs = [np.sort(r.gamma(1.0, 1.0, k))[::-1] for k in (8, 11, 5)]
+    costs = [13, 21, 9]
+    for budget in (0, 50, 150, 10 ** 6):
+        a = O.allocate(sigs, costs, budget)
+        b = O.allocate_keys([0.5 * s * s for s in sigs], costs, budget)
+        assert list(a.ranks) == list(b.ranks) and a.used == b.used
+    keys = [np.array([0.1, 0.9, 0.5]), np.array([0.7, 0.2])]
+    al = O.allocate_keys(keys, [10, 10], 30)      # keeps 0.9 (u0 c1), 0.7 (u1 c0), 0.5 (u0 c2)
+    assert list(al.ranks) == [2, 1]
+    assert sorted(zip(al.order_unit[:3], al.order_comp[:3])) == [(0, 1), (0, 2), (1, 0)]

@@ -35,6 +35,8 @@ __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_un
 // KF_KEY_PER_PARAM: that divided by the unit's m + n; KF_KEY_ENERGY_RATIO: sigma^2 divided
 // by the unit's energy sum sigma^2), times the unit's weight when weights are given (a
 // weight that is negative or not a number counts as 0).  float32, one rounding per operation.
+constexpr int MODE_GIVEN_KEYS = 100;  // internal: the caller's keys, as given
+
 __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off,
                                   const int64_t* __restrict__ cost, int n_units, int64_t n, int mode,
                                   const float* __restrict__ weight, const float* __restrict__ energy,
@@ -44,7 +46,9 @@ __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t
     const float s = sigma[g];
     const float q = __fmul_rn(s, s);
     float sc;
-    if (mode == KF_KEY_ENERGY_RATIO) {
+    if (mode == MODE_GIVEN_KEYS) {
+      sc = s > 0.f ? s : 0.f;  // a negative or not-a-number key counts as 0
+    } else if (mode == KF_KEY_ENERGY_RATIO) {
       const float e = energy[u];
       sc = e > 0.f ? __fdiv_rn(q, e) : 0.f;
     } else {
@@ -267,6 +271,14 @@ __global__ void ranks_kernel(const unsigned long long* __restrict__ keys, const 
     atomicAdd(&ranks[unit_of(off, n_units, int64_t(uint32_t(keys[i])))], 1);
 }
 
+// keep[id] = 1 for the components of the kept prefix (the mask was cleared before).
+__global__ void keep_mask_kernel(const unsigned long long* __restrict__ keys,
+                                 const unsigned long long* __restrict__ kcount, unsigned char* __restrict__ keep) {
+  const int64_t k = int64_t(*kcount);
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x)
+    keep[uint32_t(keys[i])] = 1;
+}
+
 __device__ __forceinline__ float key_score(unsigned long long k) { return __uint_as_float(~unsigned(k >> 32)); }
 
 __global__ void finish_kernel(const unsigned long long* __restrict__ keys, const long long* __restrict__ prefix,
@@ -333,6 +345,8 @@ size_t alloc_carve(Carve& cv, int64_t n, int64_t n_energy, AllocBufs& b) {
 
 }  // namespace
 
+int alloc_mode_given_keys() { return MODE_GIVEN_KEYS; }
+
 size_t alloc_workspace(int64_t n, int64_t n_energy) {
   Carve cv(nullptr, 0, true);
   AllocBufs b;
@@ -341,7 +355,8 @@ size_t alloc_workspace(int64_t n, int64_t n_energy) {
 
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
                     int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
-                    int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st) {
+                    int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st,
+                    unsigned char* keep) {
   (void)ctx;
   KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
   if (mode == KF_FIXED_RANK) {
@@ -385,6 +400,11 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   KF_CUDA(cudaGetLastError());
   ranks_kernel<<<grid_cap(n, 256), 256, 0, st>>>(src, off, n_units, b.kcount, ranks); note_launch();
   KF_CUDA(cudaGetLastError());
+  if (keep) {
+    KF_CUDA(cudaMemsetAsync(keep, 0, size_t(n), st));
+    keep_mask_kernel<<<grid_cap(n, 256), 256, 0, st>>>(src, b.kcount, keep); note_launch();
+    KF_CUDA(cudaGetLastError());
+  }
   finish_kernel<<<1, 1, 0, st>>>(src, b.prefix, n, b.kcount, cut, (long long*)used); note_launch();
   return check_cuda(cudaGetLastError(), "allocation launch");
 }
@@ -459,5 +479,5 @@ extern "C" kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma,
   void* scratch = nullptr;
   KF_TRY(noalloc_scratch(ctx->device, &scratch));
   return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, nullptr, ranks, cut,
-                   used, scratch, NOALLOC_SCRATCH_BYTES, st);
+                   used, scratch, NOALLOC_SCRATCH_BYTES, st, nullptr);
 }

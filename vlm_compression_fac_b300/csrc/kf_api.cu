@@ -15,7 +15,9 @@ kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out);
 size_t alloc_workspace(int64_t n, int64_t n_energy);
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
                     int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
-                    int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st);
+                    int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st,
+                    unsigned char* keep);
+int alloc_mode_given_keys();
 }  // namespace kf
 
 using namespace kf;
@@ -428,7 +430,7 @@ kf_status allocate_common(kf_ctx* ctx, const char* who, const float* sigma, cons
     return KF_OK;
   }
   return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, weight, ranks, cut,
-                   used, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                   used, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 }  // namespace
 
@@ -447,6 +449,29 @@ kf_status score_and_allocate_weighted(kf_ctx* ctx, const float* sigma, const int
   if (mode == KF_FIXED_RANK) return fail(KF_ERR_INVALID, "score_and_allocate_weighted: KF_FIXED_RANK has no scores");
   return allocate_common(ctx, "score_and_allocate_weighted", sigma, seg_offset, cost, n_units, n_components, budget,
                          mode, nullptr, unit_weight, ranks, cut, used, workspace, workspace_bytes, stream);
+}
+
+kf_status score_and_allocate_keys(kf_ctx* ctx, const float* keys, const int64_t* seg_offset, const int64_t* cost,
+                                  int32_t n_units, int64_t n_components, int64_t budget, int32_t* ranks,
+                                  uint8_t* keep, float* cut, int64_t* used, void* workspace, size_t workspace_bytes,
+                                  kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "score_and_allocate_keys: null context"));
+  KF_TRY(need(n_units > 0 && n_components >= 0, "score_and_allocate_keys: sizes"));
+  KF_TRY(need(n_components < (int64_t(1) << 32), "score_and_allocate_keys: at most 2^32 - 1 components"));
+  KF_TRY(need(seg_offset && cost && ranks && (keys != nullptr || n_components == 0),
+              "score_and_allocate_keys: null pointer"));
+  if (workspace_bytes < alloc_workspace(n_components > 0 ? n_components : 1, 0))
+    return fail(KF_ERR_WORKSPACE, "score_and_allocate_keys: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n_components == 0) {
+    KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
+    if (used) KF_CUDA(cudaMemsetAsync(used, 0, sizeof(int64_t), st));
+    if (cut) KF_CUDA(cudaMemsetAsync(cut, 0xFF, 2 * sizeof(float), st));
+    return KF_OK;
+  }
+  return alloc_run(ctx, keys, seg_offset, cost, n_units, n_components, budget,
+                   static_cast<kf_alloc_mode>(alloc_mode_given_keys()), nullptr, nullptr, ranks, cut, used, workspace,
+                   workspace_bytes, st, keep);
 }
 
 // ----------------------------------------------------------------------- (5b)
@@ -549,6 +574,70 @@ kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, in
   KF_TRY(split_f32(b.P, b.ldP, r, m, b.p, &pp, st));
   KF_TRY(tc_product(ctx, r, n, m, pp, false, pw, true, KR_FULL, V, ldvo, st));
   return launch_scale_rows(V, ldvo, r, n, sigma, true, st);
+}
+
+// ------------------------------------------------------- empirical-Fisher scores
+namespace {
+constexpr int64_t FISHER_CHUNK = 4096;  // tokens per projection chunk
+
+struct FisherBufs {
+  PlaneBuf a, g, u, v;
+  float *P, *Q;
+  int64_t ldPQ;
+};
+
+size_t fisher_carve(Carve& cv, int64_t m, int64_t n, int64_t r, FisherBufs& b) {
+  b.a = take_planes(cv, FISHER_CHUNK, m, 2);
+  b.g = take_planes(cv, FISHER_CHUNK, n, 2);
+  b.u = take_planes(cv, m, r, 2);
+  b.v = take_planes(cv, r, n, 2);
+  b.ldPQ = round_up(r, 4);
+  b.P = cv.take<float>(size_t(FISHER_CHUNK) * b.ldPQ);
+  b.Q = cv.take<float>(size_t(FISHER_CHUNK) * b.ldPQ);
+  return cv.off;
+}
+}  // namespace
+
+size_t empirical_fisher_workspace_size(int64_t m, int64_t n, int32_t r) {
+  if (m <= 0 || n <= 0 || r <= 0) return 0;
+  Carve cv(nullptr, 0, true);
+  FisherBufs b;
+  return fisher_carve(cv, m, n, r, b) + 256;
+}
+
+kf_status empirical_fisher_accumulate(kf_ctx* ctx, const void* act, kf_dtype act_dtype, int64_t lda,
+                                      const void* grad, kf_dtype grad_dtype, int64_t ldg, int64_t n_tokens,
+                                      int64_t m, int64_t n, const float* U, int64_t ldu, const float* V,
+                                      int64_t ldv, int32_t r, double* score_sum, void* workspace,
+                                      size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "empirical_fisher_accumulate: null context"));
+  KF_TRY(need(n_tokens >= 0 && m > 0 && n > 0 && r >= 0, "empirical_fisher_accumulate: sizes"));
+  if (n_tokens == 0 || r == 0) return KF_OK;
+  KF_TRY(need(act && grad && U && V && score_sum, "empirical_fisher_accumulate: null pointer"));
+  KF_TRY(need(lda >= m && ldg >= n && ldu >= r && ldv >= n, "empirical_fisher_accumulate: leading dimension"));
+  KF_TRY(need((act_dtype == KF_BF16 || act_dtype == KF_F32) && (grad_dtype == KF_BF16 || grad_dtype == KF_F32),
+              "empirical_fisher_accumulate: dtype"));
+  Carve cv(workspace, workspace_bytes, false);
+  FisherBufs b;
+  fisher_carve(cv, m, n, r, b);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "empirical_fisher_accumulate: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Planes pu, pv, pa, pg;
+  KF_TRY(split_f32(U, ldu, m, r, b.u, &pu, st));
+  KF_TRY(split_f32(V, ldv, r, n, b.v, &pv, st));
+  const size_t ea = act_dtype == KF_BF16 ? 2 : 4, eg = grad_dtype == KF_BF16 ? 2 : 4;
+  for (int64_t t0 = 0; t0 < n_tokens; t0 += FISHER_CHUNK) {
+    const int64_t rows = n_tokens - t0 < FISHER_CHUNK ? n_tokens - t0 : FISHER_CHUNK;
+    const void* ac = static_cast<const char*>(act) + size_t(t0) * lda * ea;
+    const void* gc = static_cast<const char*>(grad) + size_t(t0) * ldg * eg;
+    KF_TRY(as_planes(ac, act_dtype, lda, rows, m, b.a, &pa, st));
+    KF_TRY(as_planes(gc, grad_dtype, ldg, rows, n, b.g, &pg, st));
+    // P = A_c U (a_t . u_i), Q = Gr_c V^T (g_t . v_i); V is r x n, i.e. V^T stored K-major
+    KF_TRY(tc_product(ctx, rows, r, m, pa, false, pu, true, KR_FULL, b.P, b.ldPQ, st));
+    KF_TRY(tc_product(ctx, rows, r, n, pg, false, pv, false, KR_FULL, b.Q, b.ldPQ, st));
+    KF_TRY(launch_fisher_reduce(b.P, b.ldPQ, b.Q, b.ldPQ, rows, r, score_sum, st));
+  }
+  return KF_OK;
 }
 
 }  // extern "C"

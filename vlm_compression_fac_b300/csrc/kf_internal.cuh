@@ -128,6 +128,8 @@ kf_status launch_split3_bf16(const float* in, int64_t rows, int64_t d, int64_t l
                              __nv_bfloat16* p2, __nv_bfloat16* p3, int64_t ldo, cudaStream_t st);
 kf_status launch_copy_bf16(const __nv_bfloat16* in, int64_t rows, int64_t d, int64_t ld,
                            __nv_bfloat16* out, int64_t ldo, cudaStream_t st);
+kf_status launch_fisher_reduce(const float* P, int64_t ldp, const float* Q, int64_t ldq, int64_t rows, int64_t cols,
+                               double* acc, cudaStream_t st);
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
                           float* scratch, cudaStream_t st);
 kf_status launch_copy(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,

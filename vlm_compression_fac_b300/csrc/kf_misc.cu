@@ -119,6 +119,31 @@ __global__ void copy_bf16_kernel(const __nv_bfloat16* __restrict__ in, int64_t r
   }
 }
 
+// acc[j] += sum over rows t of P[t][j]^2 Q[t][j]^2 in float64.  A CTA owns 32 columns; its 8
+// warps take every 8th row (a warp reads 32 consecutive floats of a row), and the 8 partial
+// sums of a column are added in a fixed order, so the result is deterministic.
+__global__ void __launch_bounds__(256) fisher_reduce_kernel(const float* __restrict__ P, int64_t ldp,
+                                                            const float* __restrict__ Q, int64_t ldq,
+                                                            int64_t rows, int64_t cols, double* __restrict__ acc) {
+  __shared__ double part[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t j = int64_t(blockIdx.x) * 32 + lane;
+  double s = 0.0;
+  if (j < cols) {
+    for (int64_t t = w; t < rows; t += 8) {
+      const double p = P[t * ldp + j], q = Q[t * ldq + j];
+      s += (p * p) * (q * q);
+    }
+  }
+  part[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && j < cols) {
+    double tot = 0.0;
+    for (int x = 0; x < 8; ++x) tot += part[x][lane];
+    acc[j] += tot;
+  }
+}
+
 // Sum of the diagonal in float64, fixed order (one CTA).
 __global__ void diag_mean_kernel(const float* __restrict__ C, int64_t ldc, int64_t d,
                                  int64_t n_tokens, float lambda, float* __restrict__ out) {
@@ -245,6 +270,13 @@ kf_status launch_copy_bf16(const __nv_bfloat16* in, int64_t rows, int64_t d, int
   if (rows <= 0 || d <= 0) return KF_OK;
   copy_bf16_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, out, ldo); note_launch();
   return check_cuda(cudaGetLastError(), "copy_bf16 launch");
+}
+
+kf_status launch_fisher_reduce(const float* P, int64_t ldp, const float* Q, int64_t ldq, int64_t rows, int64_t cols,
+                               double* acc, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  fisher_reduce_kernel<<<unsigned((cols + 31) / 32), 256, 0, st>>>(P, ldp, Q, ldq, rows, cols, acc); note_launch();
+  return check_cuda(cudaGetLastError(), "fisher_reduce launch");
 }
 
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,

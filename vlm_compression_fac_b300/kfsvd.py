@@ -32,7 +32,8 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "whiten_workspace_size", "whiten", "kf_svd_profile_enable", "kf_svd_profile_read",
             "whitened_svd_workspace_size", "whitened_svd",
             "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_weighted",
-            "score_and_allocate_noalloc",
+            "score_and_allocate_keys", "score_and_allocate_noalloc",
+            "empirical_fisher_workspace_size", "empirical_fisher_accumulate",
             "unwhiten_workspace_size", "unwhiten"]
 
 
@@ -77,7 +78,11 @@ _SIGS = {
     "score_and_allocate_workspace_size": (_SZ, [_I64, _I32]),
     "score_and_allocate": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_weighted": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
+    "score_and_allocate_keys": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
+    "empirical_fisher_workspace_size": (_SZ, [_I64, _I64, _I32]),
+    "empirical_fisher_accumulate": (_I32, [_P, _P, _I32, _I64, _P, _I32, _I64, _I64, _I64, _I64, _P, _I64, _P,
+                                           _I64, _I32, _P, _P, _SZ, _P]),
     "unwhiten_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "unwhiten": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _I64,
                         _I32, _P, _I64, _P, _I64, _P, _SZ, _P]),
@@ -267,6 +272,33 @@ def score_and_allocate_weighted(ctx: Context, sigma, seg_offset, cost, budget: i
     _check(lib().score_and_allocate_weighted(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
                                              int(budget), int(mode), _ptr(unit_weight), _ptr(ranks), _ptr(cut),
                                              _ptr(used), _ptr(ws), wsb, _stream(stream)))
+
+
+def score_and_allocate_keys(ctx: Context, keys, seg_offset, cost, budget: int, ranks, keep=None, cut=None, used=None,
+                            workspace=None, stream=None):
+    """Sort-and-truncate over given per-component keys; ``keep`` (uint8 device tensor) marks the
+    kept components."""
+    n_units = int(cost.numel())
+    n = int(keys.numel()) if keys is not None else 0
+    ws, wsb = _ws(score_and_allocate_workspace_size(n, n_units), workspace, ranks.device)
+    _check(lib().score_and_allocate_keys(ctx.handle, _ptr(keys), _ptr(seg_offset), _ptr(cost), n_units, n, int(budget),
+                                         _ptr(ranks), _ptr(keep), _ptr(cut), _ptr(used), _ptr(ws), wsb,
+                                         _stream(stream)))
+
+
+def empirical_fisher_workspace_size(m: int, n: int, r: int) -> int:
+    return int(lib().empirical_fisher_workspace_size(m, n, r))
+
+
+def empirical_fisher_accumulate(ctx: Context, act, grad, U, V, score_sum, workspace=None, stream=None):
+    """score_sum (float64, r) += sum_t (a_t . u_i)^2 (g_t . v_i)^2 over the rows of act, grad."""
+    n_tok, m = act.shape
+    n = grad.shape[1]
+    r = U.shape[1]
+    ws, wsb = _ws(empirical_fisher_workspace_size(m, n, r), workspace, act.device)
+    _check(lib().empirical_fisher_accumulate(ctx.handle, _ptr(act), _dtype_code(act), _ld(act), _ptr(grad),
+                                             _dtype_code(grad), _ld(grad), n_tok, m, n, _ptr(U), _ld(U), _ptr(V),
+                                             _ld(V), r, _ptr(score_sum), _ptr(ws), wsb, _stream(stream)))
 
 
 def score_and_allocate_noalloc(ctx: Context, sigma, seg_offset, cost, budget: int, ranks,

@@ -62,6 +62,8 @@ class UnitOut:
     rank: int = 0
     U: Optional[torch.Tensor] = None
     V: Optional[torch.Tensor] = None
+    kept: Optional[torch.Tensor] = None     # empirical-Fisher allocation: kept component indices
+    scores: Optional[torch.Tensor] = None   # empirical-Fisher allocation: the component scores
 
 
 @dataclass
@@ -90,7 +92,8 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
              stream=None, sync_timer: Optional[Callable[[str], None]] = None,
              site_dims: Optional[Dict[str, int]] = None, act_sites: Optional[Sequence[str]] = None,
              groups: Optional[Sequence[Sequence[int]]] = None, chunk_tokens: int = 16384,
-             keep_covs: Union[bool, Sequence[str]] = True, keep_whitened: bool = True) -> Result:
+             keep_covs: Union[bool, Sequence[str]] = True, keep_whitened: bool = True,
+             score: Optional[str] = None, unit_weights: Optional[Sequence[float]] = None) -> Result:
     """Runs the five steps.
 
     ``acts``/``grads``: dicts of resident (n_tokens x d) device tensors, or ``acts`` a callable
@@ -101,6 +104,12 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     ``keep_covs``: keep every finished covariance in the result (True), none (False) or the
     named sites only; ``keep_whitened=False`` releases W~ after its spectrum and, per unit,
     the factor that the unwhitening does not read.
+    ``score``: "half_sigma2" (default; ``mode`` may also select the per-parameter key),
+    "energy_ratio" (UniRank: sigma^2 / ||Sigma||^2 of the unit, times ``unit_weights``, its
+    layer importance) or "empirical_fisher" (LASER: each component's contribution to the
+    empirical-Fisher loss, 1/2 mean_t (a_t . u_i)^2 (g_t . v_i)^2, from a second pass over the
+    calibration rows with every component mapped back; the kept set of a unit is then any
+    subset, and its factors are the kept columns of U and rows of V).
     ``sync_timer(tag)`` (optional) is called at phase boundaries ("kfac", "whiten", "svd",
     "allocate", "unwhiten"; per group for the first three) and around every kfac_accumulate
     call ("syrk<", "syrk>"), so a caller can record CUDA events there.
@@ -216,6 +225,14 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     ranks = torch.empty(len(outs), dtype=torch.int32, device=dev)
     cut = torch.empty(2, dtype=torch.float32, device=dev)
     used = torch.zeros(1, dtype=torch.int64, device=dev)
+    if score == "empirical_fisher":
+        return _fisher_allocation(ctx, units, outs, weights, rows_fn, n_tokens, chunk_tokens, int(budget), off, cost,
+                                  ranks, cut, used, sweeps_dev, all_covs, stream, mark)
+    if score == "energy_ratio":
+        w = None if unit_weights is None else torch.tensor(list(unit_weights), dtype=torch.float32, device=dev)
+        K.score_and_allocate_weighted(ctx, sig, off, cost, int(budget), ranks, mode=K.KF_KEY_ENERGY_RATIO,
+                                      unit_weight=w, cut=cut, used=used, stream=stream)
+        return _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, stream, mark)
     if fixed_rank is not None:
         fr = torch.full((len(outs),), int(fixed_rank), dtype=torch.int32, device=dev)
         K.score_and_allocate(ctx, sig, off, cost, 0, ranks, mode=K.KF_FIXED_RANK, fixed_rank=fr, cut=cut,
@@ -223,6 +240,11 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     else:
         K.score_and_allocate(ctx, sig, off, cost, int(budget), ranks, mode=mode, cut=cut, used=used,
                              stream=stream)
+    return _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, stream, mark)
+
+
+def _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, stream, mark) -> Result:
+    dev = ranks.device
     ranks_h = ranks.cpu().tolist()
     sweeps_h = sweeps_dev.cpu().tolist()
     mark("allocate")
@@ -236,6 +258,46 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
         if o.rank > 0:
             W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
             K.unwhiten(ctx, W, o.Sx, o.Sg, o.Sinv, o.sigma, o.vecs, o.rank, o.U, o.V, stream=stream)
+    mark("unwhiten")
+    return Result(outs, all_covs, ranks, cut, used)
+
+
+def _fisher_allocation(ctx, units, outs, weights, rows_fn, n_tokens, chunk_tokens, budget, off, cost, ranks, cut,
+                       used, sweeps_dev, all_covs, stream, mark) -> Result:
+    """LASER's empirical-Fisher allocation: every component mapped back (U_all, V_all), its
+    score accumulated over the calibration rows, then sort-and-truncate on the scores."""
+    dev = ranks.device
+    keys = []
+    full = []
+    for o, u in zip(outs, units):
+        s = min(o.m, o.n)
+        W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
+        Ua = torch.empty((o.m, s), dtype=torch.float32, device=dev)
+        Va = torch.empty((s, o.n), dtype=torch.float32, device=dev)
+        K.unwhiten(ctx, W, o.Sx, o.Sg, o.Sinv, o.sigma, o.vecs, s, Ua, Va, stream=stream)
+        acc = torch.zeros(s, dtype=torch.float64, device=dev)
+        for t0 in range(0, n_tokens, chunk_tokens):
+            t1 = min(n_tokens, t0 + chunk_tokens)
+            a = rows_fn(u.x_site, t0, t1)[:, u.x_off:u.x_off + u.m]
+            g = rows_fn(u.g_site, t0, t1)[:, u.g_off:u.g_off + u.n]
+            K.empirical_fisher_accumulate(ctx, a, g, Ua, Va, acc, stream=stream)
+        keys.append((acc / (2.0 * n_tokens)).to(torch.float32))
+        full.append((Ua, Va))
+    keys_t = torch.cat(keys)
+    keep = torch.empty(keys_t.numel(), dtype=torch.uint8, device=dev)
+    K.score_and_allocate_keys(ctx, keys_t, off, cost, budget, ranks, keep=keep, cut=cut, used=used, stream=stream)
+    ranks_h = ranks.cpu().tolist()
+    sweeps_h = sweeps_dev.cpu().tolist()
+    mark("allocate")
+    offs = off.cpu().tolist()
+    for i, (o, (Ua, Va), r, sw) in enumerate(zip(outs, full, ranks_h, sweeps_h)):
+        o.rank = int(r)
+        o.sweeps = int(sw)
+        sel = torch.nonzero(keep[offs[i]:offs[i + 1]]).flatten()
+        o.U = Ua.index_select(1, sel)
+        o.V = Va.index_select(0, sel)
+        o.kept = sel
+        o.scores = keys[i]
     mark("unwhiten")
     return Result(outs, all_covs, ranks, cut, used)
 
