@@ -274,6 +274,67 @@ def whitened_error(W: np.ndarray, U: np.ndarray, V: np.ndarray, Sx: np.ndarray,
     return float(np.sum(D * D))
 
 
+# ------------------------------------------------ Swift-SVD activation-only route
+def output_covariance(A: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """[Swift] 2A: the covariance of the layer output aggregated over the calibration tokens,
+    C = (1/N) sum_t y_t^T y_t with y_t = a_t W (row t of Y = A W)."""
+    Y = np.asarray(A, dtype=np.float64) @ np.asarray(W, dtype=np.float64)
+    return Y.T @ Y / A.shape[0]
+
+
+def output_eig(C: np.ndarray):
+    """[Swift] 2A: one eigendecomposition of C.  Returns sigma = sqrt(max(lambda, 0)) in
+    descending order (the singular values of Y / sqrt(N)) and the eigenvectors as columns."""
+    lam, V = np.linalg.eigh(np.asarray(C, dtype=np.float64))
+    order = np.argsort(-lam, kind="stable")
+    return np.sqrt(np.maximum(lam[order], 0.0)), V[:, order]
+
+
+def activation_factors(W: np.ndarray, V: np.ndarray, k: int):
+    """[Swift] 2A closed form W_k = W V_k V_k^T, as the factors U = W V_k (d_in x k) and
+    V_k^T (k x d_out)."""
+    Vk = np.asarray(V, dtype=np.float64)[:, :k]
+    return np.asarray(W, dtype=np.float64) @ Vk, Vk.T.copy()
+
+
+def activation_loss(A: np.ndarray, W: np.ndarray, U: np.ndarray, V: np.ndarray) -> float:
+    """(1/N) ||A W - A U V||_F^2: the activation-aware reconstruction loss [Swift] 2A
+    minimises."""
+    A = np.asarray(A, dtype=np.float64)
+    D = A @ (np.asarray(W, np.float64) - np.asarray(U, np.float64) @ np.asarray(V, np.float64))
+    return float(np.sum(D * D)) / A.shape[0]
+
+
+def compress_workload_activation_only(wl, units: Optional[List[int]] = None, chunk: int = 8192) -> Dict:
+    """The activation-only route on a synthetic workload: per unit the output covariance of
+    its calibration rows (fake-quantised first under quantisation-aware whitening; a head
+    unit reads its block of the input channels), one eigendecomposition, the global
+    sort-and-truncate on 1/2 sigma^2 over the first min(m, n) components of every unit
+    (rank(Y) <= min(m, n)), and the factors W V_k, V_k^T."""
+    from synth import recipes
+    idx = list(range(len(wl.units))) if units is None else list(units)
+    out = []
+    for i in idx:
+        u = wl.units[i]
+        site = wl.sites[u.x_site]
+        W = recipes.gen_weight(wl, u).astype(np.float64)
+        C = np.zeros((u.n, u.n))
+        for t0 in range(0, wl.n_tokens, chunk):
+            A = recipes.gen_stream(wl, site, t0, min(wl.n_tokens, t0 + chunk))
+            if wl.quant == "int8_token":
+                A = fake_quant_int8_token(A)
+            C += output_covariance(A[:, u.x_off:u.x_off + u.m], W) * A.shape[0]
+        C /= wl.n_tokens
+        sig, V = output_eig(C)
+        out.append({"name": u.name, "m": u.m, "n": u.n, "C": C, "sigma": sig, "V": V, "W": W})
+    sigs = [o["sigma"][:min(o["m"], o["n"])] for o in out]
+    alloc = allocate(sigs, [o["m"] + o["n"] for o in out], wl.budget)
+    for o, k in zip(out, alloc.ranks):
+        o["rank"] = int(k)
+        o["U"], o["Vt"] = activation_factors(o["W"], o["V"], int(k))
+    return {"units": out, "alloc": alloc}
+
+
 # ------------------------------------------------------------ whole workloads
 @dataclass
 class UnitResult:

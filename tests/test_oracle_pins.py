@@ -392,3 +392,71 @@ def test_allocate_keys_matches_monotone_allocation_and_selects_subsets():
     al = O.allocate_keys(keys, [10, 10], 30)      # keeps 0.9 (u0 c1), 0.7 (u1 c0), 0.5 (u0 c2)
     assert list(al.ranks) == [2, 1]
     assert sorted(zip(al.order_unit[:3], al.order_comp[:3])) == [(0, 1), (0, 2), (1, 0)]
+
+
+def test_swift_closed_form_hand_case():
+    """Swift-SVD 2A on a hand case: A = [[2, 0], [0, 1]], W = I: C = diag(2, 0.5), sigma =
+    (sqrt 2, sqrt 0.5), W_1 = diag(1, 0), loss (1/N)||A (W - W_1)||^2 = 0.5 = lambda_2."""
+    A = np.array([[2.0, 0.0], [0.0, 1.0]])
+    W = np.eye(2)
+    C = O.output_covariance(A, W)
+    np.testing.assert_array_equal(C, np.diag([2.0, 0.5]))
+    sig, V = O.output_eig(C)
+    np.testing.assert_allclose(sig, [np.sqrt(2.0), np.sqrt(0.5)], rtol=1e-15)
+    U, Vt = O.activation_factors(W, V, 1)
+    np.testing.assert_allclose(np.abs(U @ Vt), np.diag([1.0, 0.0]), atol=1e-15)
+    assert abs(O.activation_loss(A, W, U, Vt) - 0.5) < 1e-15
+
+
+@pytest.mark.parametrize("shape", [(60, 6, 5), (60, 4, 7), (3, 5, 6)])
+def test_swift_closed_form_is_the_activation_aware_optimum(shape):
+    """Swift-SVD 2A: W V_k V_k^T minimises ||A W - A W_k||; its loss is the sum of the dropped
+    eigenvalues of C, equals the Eckart-Young optimum of Y = A W (library SVD of Y, not the
+    eigendecomposition), and no random rank-k candidate does better.  The last shape has
+    N < m (rank-deficient activations, where a Cholesky of X would fail)."""
+    N, m, n = shape
+    r = np.random.default_rng(N * 100 + m * 10 + n)
+    A = r.standard_normal((N, m)) * np.linspace(3.0, 0.2, m)[None, :]
+    W = r.standard_normal((m, n))
+    sig, V = O.output_eig(O.output_covariance(A, W))
+    y_sv = np.linalg.svd(A @ W, compute_uv=False)
+    for k in range(0, min(m, n) + 1):
+        U, Vt = O.activation_factors(W, V, k)
+        loss = O.activation_loss(A, W, U, Vt)
+        assert abs(loss - np.sum(sig[k:] ** 2)) <= 1e-10 * max(1.0, np.sum(sig ** 2))
+        assert abs(loss - np.sum(y_sv[k:] ** 2) / N) <= 1e-10 * max(1.0, np.sum(sig ** 2))
+        for _ in range(50):
+            Ur = r.standard_normal((m, k))
+            Vr = r.standard_normal((k, n))
+            assert O.activation_loss(A, W, Ur, Vr) >= loss - 1e-9
+            P = np.linalg.qr(r.standard_normal((n, n)))[0][:, :k]
+            assert O.activation_loss(A, W, W @ P, P.T) >= loss - 1e-9
+
+
+def test_swift_route_is_the_whitened_path_with_identity_gradient_factor():
+    """With G = I and no damping the whitened path computes the same thing: S_x^T S_x = X
+    gives W~^T W~ = W^T X W = C, so the whitened singular values equal Swift's sigma and
+    the unwhitened rank-k product S_x^-1 U~_k Sigma_k V~_k^T equals W V_k V_k^T."""
+    r = np.random.default_rng(31)
+    N, m, n = 80, 7, 5
+    A = r.standard_normal((N, m))
+    W = r.standard_normal((m, n))
+    X = O.finalize_covariance(O.covariance_sum(A), N, 0.0)
+    np.testing.assert_allclose(W.T @ X @ W, O.output_covariance(A, W), rtol=1e-12, atol=1e-12)
+    Sx, Sg = O.cholesky_factors(X, np.eye(n))
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    sig, V = O.output_eig(O.output_covariance(A, W))
+    np.testing.assert_allclose(s, sig[:len(s)], rtol=1e-10)
+    for k in range(0, n + 1):
+        U1, V1 = O.unwhiten(Sx, Sg, Ut, s, Vt, k)
+        U2, V2 = O.activation_factors(W, V, k)
+        np.testing.assert_allclose(U1 @ V1, U2 @ V2, atol=1e-10)
+
+
+def test_swift_output_covariance_aggregates_by_chunks():
+    """Swift-SVD 2A's incremental aggregation: token chunks summed give the whole covariance."""
+    r = np.random.default_rng(32)
+    A = r.standard_normal((37, 6))
+    W = r.standard_normal((6, 4))
+    parts = sum(O.output_covariance(A[t:t + 10], W) * len(A[t:t + 10]) for t in range(0, 37, 10)) / 37
+    np.testing.assert_allclose(parts, O.output_covariance(A, W), rtol=1e-13, atol=1e-13)
