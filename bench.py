@@ -7,6 +7,7 @@ the 7 weights, their spectra (Gram + blocked Jacobi), global sort-and-truncate a
 and the rank-r factors U, V.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kfsvd|reference]
+                    [--score half_sigma2|energy_ratio|empirical_fisher] [--route whitened|activation_only]
 
 Prints one JSON line.  `value` is calibration tokens per second through the whole step with
 inputs resident in HBM (17.2 GB of synthetic bf16 rows, larger than L2, so no L2 flush is
@@ -14,6 +15,10 @@ needed between steps); `e2e` is the same metric when every step also copies its 
 from pinned host memory and reads the factors back.  --impl reference times the fp64 CPU
 oracle on a bounded sample of the same workload.  Under torchrun each rank runs its own
 replica of the workload (the path has no data exchange): scaling is weak, value sums ranks.
+--score picks the allocation key (LASER's empirical-Fisher score adds a second pass over the
+rows, timed as its own kernel entry); --route activation_only times Swift-SVD's route over
+the same block (activation rows only: output covariance, one eigendecomposition per matrix,
+W V_k V_k^T).  The default line is the whitened path with 1/2 sigma^2.
 """
 from __future__ import annotations
 
@@ -41,6 +46,12 @@ def parse():
     ap.add_argument("--impl", default="kfsvd", choices=["kfsvd", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--score", default="half_sigma2", choices=["half_sigma2", "energy_ratio", "empirical_fisher"],
+                    help="allocation key: 1/2 sigma^2 (default), UniRank's energy ratio, or LASER's "
+                         "empirical-Fisher score (adds a second pass over the calibration rows)")
+    ap.add_argument("--route", default="whitened", choices=["whitened", "activation_only"],
+                    help="whitened: the K-FAC path (default); activation_only: Swift-SVD's route "
+                         "(output covariance W^T X W, one eigendecomposition, W V_k V_k^T)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="calibration tokens per site (default: the workload's 131072); a smaller N "
                          "keeps every matrix shape and is meant for profiler captures")
@@ -141,7 +152,8 @@ def run_kfsvd(args):
     K.kf_svd_profile_enable(ctx, True)
     units = [pipeline.UnitSpec(u.name, u.m, u.n, u.x_site, u.g_site) for u in wl.units]
     acts = {n: sdev.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
-    grads = {n: sdev.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
+    grads = {} if args.route == "activation_only" else \
+        {n: sdev.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
     weights = {u.name: sdev.weight_on_device(wl, u, torch) for u in wl.units}
     torch.cuda.synchronize()
     in_bytes = sum(t.numel() * t.element_size() for t in list(acts.values()) + list(grads.values()))
@@ -155,9 +167,16 @@ def run_kfsvd(args):
         e.record(stream)
         rec.append((tag, e))
 
+    swift = args.route == "activation_only"
+
+    def run(a, g, w, timer=None):
+        if swift:
+            return pipeline.compress_activation_only(ctx, units, w, a, wl.n_tokens, wl.budget, sync_timer=timer)
+        return pipeline.compress(ctx, units, w, a, g, wl.n_tokens, lam=wl.lam, budget=wl.budget, sync_timer=timer,
+                                 score=args.score)
+
     def one_step(a, g, w):
-        return pipeline.compress(ctx, units, w, a, g, wl.n_tokens, lam=wl.lam, budget=wl.budget,
-                                 sync_timer=mark)
+        return run(a, g, w, mark)
 
     for _ in range(args.warmup):
         rec.clear()
@@ -166,8 +185,10 @@ def run_kfsvd(args):
     torch.cuda.synchronize()
 
     # ---------------- timed region (device-resident inputs)
-    phases = {k: 0.0 for k in ("kfac", "whiten", "svd", "allocate", "unwhiten")}
+    phases = {k: 0.0 for k in (("kfac", "cov", "eig", "allocate", "factors") if swift else
+                               ("kfac", "whiten", "svd", "score", "allocate", "unwhiten"))}
     syrk_ms, jac_ms, jac_flops, svd_prof = 0.0, 0.0, 0.0, None
+    fisher_ms, n_fisher = 0.0, 0
     apply_ms, solve_ms, apply_launches = 0.0, 0.0, 0
     n_syrk = 0
     clocks = ClockSampler(local)
@@ -204,7 +225,7 @@ def run_kfsvd(args):
         total_ms = float(tt.item())
     for marks in per_step_marks:
         prev = marks[0][1]
-        open_syrk = None
+        open_syrk = open_fisher = None
         for tag, e in marks[1:]:
             if tag == "syrk<":
                 open_syrk = e
@@ -212,6 +233,13 @@ def run_kfsvd(args):
             if tag == "syrk>":
                 syrk_ms += open_syrk.elapsed_time(e)
                 n_syrk += 1
+                continue
+            if tag == "fisher<":
+                open_fisher = e
+                continue
+            if tag == "fisher>":
+                fisher_ms += open_fisher.elapsed_time(e)
+                n_fisher += 1
                 continue
             phases[tag] += prev.elapsed_time(e)
             prev = e
@@ -238,7 +266,7 @@ def run_kfsvd(args):
             a = {k: v.to("cuda", non_blocking=True) for k, v in h_acts.items()}
             g = {k: v.to("cuda", non_blocking=True) for k, v in h_grads.items()}
             w = {k: v.to("cuda", non_blocking=True) for k, v in h_w.items()}
-            r = pipeline.compress(ctx, units, w, a, g, wl.n_tokens, lam=wl.lam, budget=wl.budget)
+            r = run(a, g, w)
             outs = [u.U.cpu() for u in r.units] + [u.V.cpu() for u in r.units] + [r.ranks.cpu()]
             out_bytes = sum(o.numel() * o.element_size() for o in outs)
             del a, g, w, r
@@ -278,6 +306,15 @@ def run_kfsvd(args):
             "bound": "latency", "ms_per_step": round(solve_ms / K_, 3),
             "launches_per_step": apply_launches // K_},
     }
+    if n_fisher:
+        # projections P = A U, Q = Gr V^T over every component: one bf16 activation plane times
+        # the hi and lo planes of U (and of V), 2 x 2 N s (m + n) flop per unit
+        f_flops = sum(4.0 * wl.n_tokens * min(u.m, u.n) * (u.m + u.n) for u in wl.units) * K_
+        f_tf = f_flops / (fisher_ms / 1e3) / 1e12
+        kern["empirical-Fisher pass (tc_gemm_kernel projections + fisher_reduce_kernel)"] = {
+            "bound": "tensor", "achieved": round(f_tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+            "frac": round(f_tf / bf16_peak, 4), "ms_per_step": round(fisher_ms / K_, 3),
+            "calls_per_step": n_fisher // K_, "peak_kind": "bf16 dense, sustained, of measured"}
     dom = max(("tc_gemm_kernel (covariance SYRK)", syrk_ms), ("jac_apply_kernel (Jacobi rotations)", apply_ms),
               key=lambda kv: kv[1])[0]
     roof = {k: v for k, v in kern[dom].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
@@ -286,17 +323,19 @@ def run_kfsvd(args):
 
     # ---------------- CPU baseline (oracle on a bounded sample), rank 0 only at N=1
     cpu = None
-    if not args.no_cpu_baseline and rank == 0 and world == 1:
+    if not args.no_cpu_baseline and rank == 0 and world == 1 and not swift:
         cpu = oracle_sample(wl, sample_tokens=1024)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K_,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic: seeded Philox4x32-10 streams and weights generated on the device",
-        "config": {"workload": WORKLOAD, "global_batch": wl.n_tokens * world, "seq_len": wl.n_tokens,
+        "config": {"workload": WORKLOAD, "route": args.route, "score": None if swift else args.score,
+                   "global_batch": wl.n_tokens * world, "seq_len": wl.n_tokens,
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs (%.1f GB) larger than L2; no flush" % (in_bytes / 1e9)},
-        "layers_per_s": round(len(units) * world / ((phases["whiten"] + phases["svd"]) / K_ / 1e3), 3),
+        "layers_per_s": round(len(units) * world / ((phases["cov"] + phases["eig"]) if swift else
+                                                     (phases["whiten"] + phases["svd"])) * K_ * 1e3, 3),
         "kfac_tokens_per_s": round(tokens / ((phases["kfac"]) / K_ / 1e3), 1),
         "phases_ms": {k: round(v / K_, 3) for k, v in phases.items()},
         "svd_profile": svd_prof, "ranks": [int(x) for x in res.ranks.cpu().tolist()],

@@ -124,6 +124,15 @@ KF_API kf_status kfac_accumulate(kf_ctx* ctx, const void* act, kf_dtype dtype, i
                           int64_t d, int64_t ld, kf_quant quant, float* cov_sum, int64_t ldc,
                           void* workspace, size_t workspace_bytes, kf_stream_t stream);
 
+/* Step 1a on its own: the per-token INT8 fake quantisation that kfac_accumulate applies with
+ * KF_QUANT_INT8_TOKEN (LASER Methodology 1, quantisation-aware whitening), for callers that
+ * need the quantised rows themselves (the empirical-Fisher pass reads the same quantised
+ * activations the covariance was built from).  in: n_tokens x d rows (KF_BF16 or KF_F32,
+ * leading dimension ld); out: n_tokens x d bfloat16, leading dimension d, caller-owned.  Every
+ * row is quantised over its full width d (the scale is max|row| / 127). */
+KF_API kf_status fake_quant_rows(kf_ctx* ctx, const void* in, kf_dtype dtype, int64_t n_tokens, int64_t d,
+                                 int64_t ld, void* out, kf_stream_t stream);
+
 /* Step 1, tail: turns a finished sum into the damped factor, in place:
  * C = sum / n_tokens (lower triangle mirrored to the full matrix), then
  * C += lambda * mean(diag(C)) * I.  Call once per site after its last kfac_accumulate. */
@@ -324,6 +333,48 @@ KF_API kf_status empirical_fisher_accumulate(kf_ctx* ctx, const void* act, kf_dt
                                              int64_t ldu, const float* V, int64_t ldv, int32_t r,
                                              double* score_sum, void* workspace, size_t workspace_bytes,
                                              kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * Swift-SVD activation-only route (Swift-SVD 2A): the rank-k W_k minimising
+ * ||A W - A W_k||_F is W V_k V_k^T, with V_k the top-k eigenvectors of the covariance of the
+ * layer output C = (1/N) sum_t y_t^T y_t, y_t = a_t W; no gradient factor, no Cholesky.
+ *
+ * activation_covariance: C (n x n float32, ldc, full matrix) = W^T X W for the activation
+ *   second moment X (m x m float32, ldx, full symmetric, e.g. kfac_accumulate's sum
+ *   finalised with lambda = 0) and W (m x n, KF_BF16 or KF_F32).  Since
+ *   sum_t (a_t W)^T (a_t W) = W^T (sum_t a_t^T a_t) W this is the output covariance, with the
+ *   token stream read once per activation site (shared by every matrix reading that site).
+ *   Tensor cores, float32 operands as three bfloat16 planes (float32-level accuracy).
+ * activation_eig: eigenpairs of every C_i by the blocked Jacobi solver of whitened_svd
+ *   applied to C itself (Rayleigh quotients q.Cq / q.q, windowed Rayleigh-Ritz refinement
+ *   on C); sigma = sqrt(max(lambda, 0)) descending (the singular values of Y / sqrt(N)),
+ *   vecs column i = the unit-norm eigenvector of sigma[i].  Same-n problems per call
+ *   (n <= 16384); waits on the stream once per sweep like whitened_svd.
+ * activation_factors: U = W V_r (m x r, tensor cores, W and V_r as hi + lo bfloat16 planes)
+ *   and V = V_r^T (r x n), V_r the first r columns of vecs; U V = W V_r V_r^T.
+ * The ranks come from score_and_allocate on the concatenated sigma (1/2 sigma^2 is half the
+ * activation-aware loss increase per dropped component, m + n parameters per kept pair).
+ * ---------------------------------------------------------------------------------- */
+typedef struct {
+  const float* C;    /* n x n, ldc (lower triangle read) */
+  int64_t n, ldc;
+  float* sigma;      /* n */
+  float* vecs;       /* n x n, ldv */
+  int64_t ldv;
+  int32_t* sweeps;   /* device, may be NULL */
+} kf_sym_problem;
+
+KF_API size_t activation_covariance_workspace_size(int64_t m, int64_t n);
+KF_API kf_status activation_covariance(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const void* W,
+                                       kf_dtype w_dtype, int64_t ldw, int64_t n, float* C, int64_t ldc,
+                                       void* workspace, size_t workspace_bytes, kf_stream_t stream);
+KF_API size_t activation_eig_workspace_size(int32_t n_problems, int64_t n);
+KF_API kf_status activation_eig(kf_ctx* ctx, int32_t n_problems, const kf_sym_problem* problems, float tol,
+                                int32_t max_sweeps, void* workspace, size_t workspace_bytes, kf_stream_t stream);
+KF_API size_t activation_factors_workspace_size(int64_t m, int64_t n, int32_t r);
+KF_API kf_status activation_factors(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m, int64_t n,
+                                    const float* vecs, int64_t ldv, int32_t r, float* U, int64_t ldu, float* V,
+                                    int64_t ldvo, void* workspace, size_t workspace_bytes, kf_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -85,16 +85,18 @@ def test_allocation_over_given_keys(ctx):
     np.testing.assert_array_equal(keep.cpu().numpy(), want)
 
 
-def test_end_to_end_empirical_fisher(ctx):
+@pytest.mark.parametrize("name", ["mini_block", "mini_vlm_heads_qaw"])
+def test_end_to_end_empirical_fisher(ctx, name):
     from synth import device
     from vlm_compression_fac_b300 import pipeline
-    wl = recipes.mini_block(n_tokens=1100, seed=95)
+    wl = recipes.mini_block(n_tokens=1100, seed=95) if name == "mini_block" else recipes.mini_vlm(n_tokens=700)
+    quant = wl.quant == "int8_token"
     units = pipeline.unit_specs(wl)
     weights = device.weights_on_device(wl, torch)
     acts = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
     grads = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
     res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
-                            score="empirical_fisher")
+                            quant=quant, score="empirical_fisher")
     ctx.sync_status()
     ref = O.compress_workload(wl)
     keys = [g.scores.cpu().numpy() for g in res.units]
@@ -112,7 +114,10 @@ def test_end_to_end_empirical_fisher(ctx):
         U, V = g.U.cpu().numpy(), g.V.cpu().numpy()
         # the keys of the kept components are LASER's scores of the GPU's own factors
         A = recipes.gen_stream(wl, wl.sites[u.x_site], 0, wl.n_tokens)
-        Gr = recipes.gen_stream(wl, wl.sites[u.g_site], 0, wl.n_tokens)
+        if quant:
+            A = O.fake_quant_int8_token(A)        # over the full width, as for the covariance
+        A = A[:, u.x_off:u.x_off + u.m]
+        Gr = recipes.gen_stream(wl, wl.sites[u.g_site], 0, wl.n_tokens)[:, u.g_off:u.g_off + u.n]
         if len(kept):
             ko = O.empirical_fisher_scores(A, Gr, U, V)
             kg = g.scores.cpu().numpy().astype(np.float64)[kept]
@@ -144,3 +149,20 @@ def test_end_to_end_energy_ratio_with_layer_weights(ctx):
     assert int(res.used.item()) == al.used <= wl.budget
     for g in res.units:
         assert g.U.shape[1] == g.rank and g.V.shape[0] == g.rank
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_fake_quant_rows_bit_exact(ctx, dtype):
+    rng = np.random.default_rng(12)
+    A = (rng.standard_normal((257, 136)) * rng.gamma(1.0, 1.0, (257, 1))).astype(np.float32)
+    A[3] = 0.0
+    A[7, 5] = -40.0
+    if dtype == "bf16":
+        A = recipes.philox.bf16_bits_to_f32(recipes.philox.f32_to_bf16_bits(A))
+        Ad = bf16_dev(A, torch)
+    else:
+        Ad = to_dev(A, torch)
+    out = torch.empty(A.shape, dtype=torch.bfloat16, device="cuda")
+    K().fake_quant_rows(ctx, Ad, out)
+    ctx.sync_status()
+    np.testing.assert_array_equal(out.float().cpu().numpy(), O.fake_quant_int8_token(A))

@@ -4,13 +4,14 @@
 
 #include <cstring>
 #include <string>
+#include <vector>
 
 namespace kf {
 const char* last_error_cstr();
 unsigned long long launch_count();
 size_t svd_workspace(int32_t nu, int64_t m_max, int64_t n_max, int64_t s);
 kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, int32_t max_sweeps, void* ws,
-                  size_t ws_bytes, cudaStream_t st);
+                  size_t ws_bytes, cudaStream_t st, bool sym);
 kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out);
 size_t alloc_workspace(int64_t n, int64_t n_energy);
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
@@ -185,6 +186,18 @@ kf_status kfac_accumulate(kf_ctx* ctx, const void* act, kf_dtype dtype, int64_t 
     KF_TRY(tc_gemm(ctx, g, st));
   }
   return KF_OK;
+}
+
+kf_status fake_quant_rows(kf_ctx* ctx, const void* in, kf_dtype dtype, int64_t n_tokens, int64_t d, int64_t ld,
+                          void* out, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "fake_quant_rows: null context"));
+  KF_TRY(need(dtype == KF_BF16 || dtype == KF_F32, "fake_quant_rows: dtype"));
+  KF_TRY(need(n_tokens >= 0 && d > 0 && ld >= d, "fake_quant_rows: sizes"));
+  KF_TRY(need(n_tokens <= 0x7fffffff, "fake_quant_rows: at most 2^31 - 1 rows per call"));
+  if (n_tokens == 0) return KF_OK;
+  KF_TRY(need(in && out, "fake_quant_rows: null pointer"));
+  return launch_fake_quant(in, dtype, n_tokens, d, ld, static_cast<__nv_bfloat16*>(out),
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 kf_status kf_finalize_covariance(kf_ctx* ctx, float* cov, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
@@ -384,7 +397,121 @@ kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_problem* pr
   if (workspace_bytes < svd_workspace(n_problems, m_max, n_max, s0))
     return fail(KF_ERR_WORKSPACE, "whitened_svd: workspace too small");
   return svd_run(ctx, n_problems, problems, tol, max_sweeps, workspace, workspace_bytes,
-                 reinterpret_cast<cudaStream_t>(stream));
+                 reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+// ------------------------------------------------- Swift-SVD activation-only route
+namespace {
+struct ActCovBufs {
+  float* T;
+  int64_t ldT;
+  PlaneBuf x, w, t;
+};
+size_t actcov_carve(Carve& cv, int64_t m, int64_t n, ActCovBufs& b) {
+  b.ldT = round_up(n, 8);
+  b.T = cv.take<float>(size_t(m) * b.ldT);
+  b.x = take_planes(cv, m, m, 3);
+  b.w = take_planes(cv, m, n, 3);
+  b.t = take_planes(cv, m, n, 3);
+  return cv.off;
+}
+}  // namespace
+
+size_t activation_covariance_workspace_size(int64_t m, int64_t n) {
+  if (m <= 0 || n <= 0) return 0;
+  Carve cv(nullptr, 0, true);
+  ActCovBufs b;
+  return actcov_carve(cv, m, n, b) + 256;
+}
+
+kf_status activation_covariance(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const void* W, kf_dtype w_dtype,
+                                int64_t ldw, int64_t n, float* C, int64_t ldc, void* workspace,
+                                size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "activation_covariance: null context"));
+  KF_TRY(need(m > 0 && n > 0, "activation_covariance: sizes"));
+  KF_TRY(need(X && W && C, "activation_covariance: null pointer"));
+  KF_TRY(need(ldx >= m && ldw >= n && ldc >= n, "activation_covariance: leading dimension"));
+  KF_TRY(need(w_dtype == KF_BF16 || w_dtype == KF_F32, "activation_covariance: dtype"));
+  Carve cv(workspace, workspace_bytes, false);
+  ActCovBufs b;
+  actcov_carve(cv, m, n, b);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "activation_covariance: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // T = X W, then C = W^T T; float32 operands as three bfloat16 planes, W^T read MN-major
+  Planes px, pw, pt;
+  KF_TRY(split_f32(X, ldx, m, m, b.x, &px, st));
+  KF_TRY(as_planes(W, w_dtype, ldw, m, n, b.w, &pw, st));
+  KF_TRY(tc_product(ctx, m, n, m, px, false, pw, true, KR_FULL, b.T, b.ldT, st));
+  KF_TRY(split_f32(b.T, b.ldT, m, n, b.t, &pt, st));
+  return tc_product(ctx, n, n, m, pw, true, pt, true, KR_FULL, C, ldc, st);
+}
+
+size_t activation_eig_workspace_size(int32_t n_problems, int64_t n) {
+  if (n_problems <= 0 || n <= 0) return 0;
+  return svd_workspace(n_problems, n, n, n);
+}
+
+kf_status activation_eig(kf_ctx* ctx, int32_t n_problems, const kf_sym_problem* problems, float tol,
+                         int32_t max_sweeps, void* workspace, size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "activation_eig: null context"));
+  if (n_problems == 0) return KF_OK;
+  KF_TRY(need(n_problems > 0 && problems, "activation_eig: problems"));
+  KF_TRY(need(n_problems <= 65535, "activation_eig: at most 65535 problems per call"));
+  KF_TRY(need(tol > 0.f && max_sweeps > 0, "activation_eig: tol and max_sweeps must be positive"));
+  std::vector<kf_svd_problem> pr(static_cast<size_t>(n_problems));
+  const int64_t n0 = problems[0].n;
+  for (int i = 0; i < n_problems; ++i) {
+    const kf_sym_problem& p = problems[i];
+    KF_TRY(need(p.C && p.sigma && p.vecs && p.n > 0 && p.ldc >= p.n && p.ldv >= p.n,
+                "activation_eig: problem fields"));
+    KF_TRY(need(p.n == n0, "activation_eig: all problems of a call need the same n"));
+    pr[size_t(i)] = kf_svd_problem{p.C, p.n, p.n, p.ldc, p.sigma, p.vecs, p.ldv, p.sweeps};
+  }
+  if (n0 > 16384) return fail(KF_ERR_UNSUPPORTED, "activation_eig: n > 16384");
+  if (workspace_bytes < svd_workspace(n_problems, n0, n0, n0))
+    return fail(KF_ERR_WORKSPACE, "activation_eig: workspace too small");
+  return svd_run(ctx, n_problems, pr.data(), tol, max_sweeps, workspace, workspace_bytes,
+                 reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+namespace {
+struct ActFacBufs {
+  PlaneBuf w, v;
+};
+size_t actfac_carve(Carve& cv, int64_t m, int64_t n, int32_t r, ActFacBufs& b) {
+  b.w = take_planes(cv, m, n, 2);
+  b.v = take_planes(cv, n, r, 2);
+  return cv.off;
+}
+}  // namespace
+
+size_t activation_factors_workspace_size(int64_t m, int64_t n, int32_t r) {
+  if (m <= 0 || n <= 0 || r <= 0) return 0;
+  Carve cv(nullptr, 0, true);
+  ActFacBufs b;
+  return actfac_carve(cv, m, n, r, b) + 256;
+}
+
+kf_status activation_factors(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m, int64_t n,
+                             const float* vecs, int64_t ldv, int32_t r, float* U, int64_t ldu, float* V,
+                             int64_t ldvo, void* workspace, size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "activation_factors: null context"));
+  KF_TRY(need(m > 0 && n > 0 && r >= 0 && r <= n, "activation_factors: sizes"));
+  if (r == 0) return KF_OK;
+  KF_TRY(need(W && vecs && U && V, "activation_factors: null pointer"));
+  KF_TRY(need(ldw >= n && ldv >= n && ldu >= r && ldvo >= n, "activation_factors: leading dimension"));
+  KF_TRY(need(w_dtype == KF_BF16 || w_dtype == KF_F32, "activation_factors: dtype"));
+  Carve cv(workspace, workspace_bytes, false);
+  ActFacBufs b;
+  actfac_carve(cv, m, n, r, b);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "activation_factors: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // U = W V_r (V_r: the first r columns of vecs, n x r, read MN-major), V = V_r^T
+  Planes pw, pv;
+  KF_TRY(as_planes(W, w_dtype, ldw, m, n, b.w, &pw, st));
+  KF_TRY(split_f32(vecs, ldv, n, r, b.v, &pv, st));
+  KF_TRY(tc_product(ctx, m, r, n, pw, false, pv, true, KR_FULL, U, ldu, st));
+  return launch_copy(vecs, ldv, V, ldvo, r, n, true, st);
 }
 
 kf_status kf_svd_profile_enable(kf_ctx* ctx, int enable) {

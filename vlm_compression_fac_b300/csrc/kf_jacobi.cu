@@ -16,6 +16,8 @@
 // The singular values are then the Rayleigh quotients sigma_i = ||W~ q_i|| / ||q_i||,
 // evaluated on W~ rather than on C so that the Gram's rounding errors enter only at second
 // order, sorted descending with their vectors.
+// The same solver serves a symmetric matrix given directly (Swift-SVD 2A's covariance of
+// the layer output): the values are then the Rayleigh quotients q.Cq / q.q.
 #include "kf_internal.cuh"
 
 #include <cfloat>
@@ -475,18 +477,24 @@ __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* 
 // ------------------------------------------------------------- Rayleigh + sort
 // sigma_j^2 = ||y_j||^2 / ||q_j||^2 with y_j = W~ q_j (right side) or W~^T q_j (left side):
 // one CTA per vector j, float64 sums over row j of Yt and of Qt (both contiguous).
+// dot != 0 (a symmetric matrix C given directly, y_j = C q_j): the Rayleigh quotient
+// lambda_j = (q_j . y_j) / ||q_j||^2 instead (the first len_q entries of both rows).
 __global__ void __launch_bounds__(256) rayleigh_norms_kernel(const float* __restrict__ Yt, int64_t ldy,
                                                              int64_t len_y, const float* __restrict__ Qt,
                                                              int64_t ldq, int64_t len_q,
                                                              float* __restrict__ sigma, float* __restrict__ qinv,
-                                                             int* status) {
+                                                             int* status, int dot) {
   __shared__ double ra[8], rb[8];
   const int64_t j = blockIdx.x;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   double a = 0.0, b = 0.0;
-  for (int64_t i = threadIdx.x; i < len_y; i += blockDim.x) {
-    const double v = Yt[j * ldy + i];
-    a += v * v;
+  if (dot) {
+    for (int64_t i = threadIdx.x; i < len_q; i += blockDim.x) a += double(Yt[j * ldy + i]) * double(Qt[j * ldq + i]);
+  } else {
+    for (int64_t i = threadIdx.x; i < len_y; i += blockDim.x) {
+      const double v = Yt[j * ldy + i];
+      a += v * v;
+    }
   }
   for (int64_t i = threadIdx.x; i < len_q; i += blockDim.x) {
     const double v = Qt[j * ldq + i];
@@ -502,7 +510,7 @@ __global__ void __launch_bounds__(256) rayleigh_norms_kernel(const float* __rest
   if (threadIdx.x == 0) {
     double aa = 0.0, bb = 0.0;
     for (int x = 0; x < 8; ++x) { aa += ra[x]; bb += rb[x]; }
-    sigma[j] = bb > 0.0 ? float(sqrt(aa / bb)) : 0.f;
+    sigma[j] = bb > 0.0 ? float(dot ? aa / bb : sqrt(aa / bb)) : 0.f;
     qinv[j] = bb > 0.0 ? float(1.0 / sqrt(bb)) : 0.f;
     if (!isfinite(aa) || !isfinite(bb)) raise_status(status, KF_ERR_INVALID, 141);
   }
@@ -546,9 +554,10 @@ __global__ void __launch_bounds__(1024) sort_desc_kernel(const float* __restrict
 
 // vecs[r][i] = Qt[perm[i]][r] * qinv[perm[i]] (column i of vecs = i-th sorted vector), as
 // 32 x 32 tiles transposed through shared memory so that reads and writes are coalesced.
+// sqrt_out: the sorted values are eigenvalues of a symmetric C; sigma_out gets sqrt(max(., 0)).
 __global__ void gather_kernel(const float* __restrict__ Qt, int64_t ldq, int64_t s, const int* __restrict__ perm,
                               const float* __restrict__ sig, const float* __restrict__ qinv,
-                              float* __restrict__ vecs, int64_t ldv, float* __restrict__ sigma_out) {
+                              float* __restrict__ vecs, int64_t ldv, float* __restrict__ sigma_out, int sqrt_out) {
   __shared__ float tile[32][33];
   const int64_t i0 = int64_t(blockIdx.x) * 32, r0 = int64_t(blockIdx.y) * 32;
   for (int k = threadIdx.y; k < 32; k += 8) {
@@ -565,7 +574,10 @@ __global__ void gather_kernel(const float* __restrict__ Qt, int64_t ldq, int64_t
   }
   if (blockIdx.y == 0 && threadIdx.y == 0) {
     const int64_t i = i0 + threadIdx.x;
-    if (i < s) sigma_out[i] = sig[perm[i]];
+    if (i < s) {
+      const float v = sig[perm[i]];
+      sigma_out[i] = sqrt_out ? sqrtf(fmaxf(v, 0.f)) : v;
+    }
   }
 }
 
@@ -595,15 +607,46 @@ __global__ void gather_rows_kernel(const float* __restrict__ Src, int64_t lds, i
   for (int64_t c = threadIdx.x; c < cols; c += blockDim.x) d[c] = src[c];
 }
 
+// Loads rows [0, RW) x columns [k0, k0 + 32) of Y (ldy) transposed into T[k][i].
+__device__ __forceinline__ void win_load_t(float (*T)[RW + 4], const float* __restrict__ Y, int64_t ldy,
+                                           int64_t k0, int64_t cols, int t, int* status) {
+  // 128 rows x 32 columns: lane-consecutive rows, so the transposed shared stores do not conflict
+  for (int e = t; e < RW * 8; e += 256) {
+    const int i = e & (RW - 1), kc = e >> 7;  // kc: 4-column chunk 0..7
+    const int64_t k = k0 + kc * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (k + 3 < cols) {
+      const float* a = Y + int64_t(i) * ldy + k;
+      if (aligned16(a, status, 111)) v = *reinterpret_cast<const float4*>(a);
+    } else {
+      float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < 4; ++q)
+        if (k + q < cols) tmp[q] = Y[int64_t(i) * ldy + k + q];
+      v = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
+    }
+    T[kc * 4 + 0][i] = v.x;
+    T[kc * 4 + 1][i] = v.y;
+    T[kc * 4 + 2][i] = v.z;
+    T[kc * 4 + 3][i] = v.w;
+  }
+}
+
 // B_w = Y_w Y_w^T for the RW rows of window w of problem u (rows start at off + w * RW):
 // float32 products over k-blocks of 32 columns, block partial sums added in float64.
+// With Xs != nullptr the cross product B_w = X_w Y_w^T instead (X_w the same rows of Xs):
+// for a symmetric C given directly, X = the vectors and Y = their images C q, so B_w is the
+// window's Rayleigh-Ritz matrix (symmetrised by the window eigensolver).
 __global__ void __launch_bounds__(256) win_gram_kernel(const float* __restrict__ Ys, int64_t ldy, int64_t prob_y,
                                                        int64_t cols, int64_t off, float* __restrict__ B,
-                                                       int nwin, int* status) {
-  __shared__ __align__(16) float T[32][RW + 4];  // T[k][i] = Y[row i][k0 + k]
+                                                       int nwin, int* status, const float* __restrict__ Xs,
+                                                       int64_t ldx, int64_t prob_x) {
+  __shared__ __align__(16) float T[32][RW + 4];   // T[k][i] = Y[row i][k0 + k]
+  __shared__ __align__(16) float T2[32][RW + 4];  // the same for X (cross product only)
   const int w = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
   const int tx = t & 15, ty = t >> 4;             // output rows ty*8.., columns tx*8..
   const float* Y = Ys + int64_t(u) * prob_y + (off + int64_t(w) * RW) * ldy;
+  const float* X = Xs ? Xs + int64_t(u) * prob_x + (off + int64_t(w) * RW) * ldx : nullptr;
+  float (*TX)[RW + 4] = X ? T2 : T;
   float part[8][8];
   double tot[8][8];
 #pragma unroll
@@ -611,25 +654,8 @@ __global__ void __launch_bounds__(256) win_gram_kernel(const float* __restrict__
 #pragma unroll
     for (int b = 0; b < 8; ++b) tot[a][b] = 0.0;
   for (int64_t k0 = 0; k0 < cols; k0 += 32) {
-    // 128 rows x 32 columns: lane-consecutive rows, so the transposed shared stores do not conflict
-    for (int e = t; e < RW * 8; e += 256) {
-      const int i = e & (RW - 1), kc = e >> 7;  // kc: 4-column chunk 0..7
-      const int64_t k = k0 + kc * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (k + 3 < cols) {
-        const float* a = Y + int64_t(i) * ldy + k;
-        if (aligned16(a, status, 111)) v = *reinterpret_cast<const float4*>(a);
-      } else {
-        float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int q = 0; q < 4; ++q)
-          if (k + q < cols) tmp[q] = Y[int64_t(i) * ldy + k + q];
-        v = make_float4(tmp[0], tmp[1], tmp[2], tmp[3]);
-      }
-      T[kc * 4 + 0][i] = v.x;
-      T[kc * 4 + 1][i] = v.y;
-      T[kc * 4 + 2][i] = v.z;
-      T[kc * 4 + 3][i] = v.w;
-    }
+    win_load_t(T, Y, ldy, k0, cols, t, status);
+    if (X) win_load_t(T2, X, ldx, k0, cols, t, status);
     __syncthreads();
 #pragma unroll
     for (int a = 0; a < 8; ++a)
@@ -637,8 +663,8 @@ __global__ void __launch_bounds__(256) win_gram_kernel(const float* __restrict__
       for (int b = 0; b < 8; ++b) part[a][b] = 0.f;
 #pragma unroll 4
     for (int k = 0; k < 32; ++k) {
-      const float4 x0 = *reinterpret_cast<const float4*>(&T[k][ty * 8]);
-      const float4 x1 = *reinterpret_cast<const float4*>(&T[k][ty * 8 + 4]);
+      const float4 x0 = *reinterpret_cast<const float4*>(&TX[k][ty * 8]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&TX[k][ty * 8 + 4]);
       const float4 y0 = *reinterpret_cast<const float4*>(&T[k][tx * 8]);
       const float4 y1 = *reinterpret_cast<const float4*>(&T[k][tx * 8 + 4]);
       const float xa[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
@@ -882,8 +908,11 @@ size_t svd_workspace(int32_t nu, int64_t m_max, int64_t n_max, int64_t s) {
   return svd_carve(cv, nu, m_max, n_max, s, b) + 256;
 }
 
+// sym: every problem's Wt is a symmetric s x s matrix C whose eigenpairs are wanted (its lower
+// triangle is read); the images are y = C q, the values Rayleigh quotients q.Cq / q.q, the
+// refinement uses the windows' Rayleigh-Ritz matrices, and sigma = sqrt(max(lambda, 0)).
 kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, int32_t max_sweeps, void* ws,
-                  size_t ws_bytes, cudaStream_t st) {
+                  size_t ws_bytes, cudaStream_t st, bool sym) {
   int64_t s = pr[0].m < pr[0].n ? pr[0].m : pr[0].n, m_max = 0, n_max = 0;
   for (int i = 0; i < nu; ++i) {
     m_max = pr[i].m > m_max ? pr[i].m : m_max;
@@ -912,6 +941,10 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   // Gram of the smaller side, lower triangle, float32 SIMT (accuracy matters here).
   for (int i = 0; i < nu; ++i) {
     const kf_svd_problem& p = pr[i];
+    if (sym) {  // the matrix itself
+      KF_TRY(launch_copy(p.Wt, p.ldw, C + int64_t(i) * pl.sp * pl.sp, pl.sp, s, s, false, st));
+      continue;
+    }
     GemmDesc g{};
     g.M = s; g.N = s; g.batch = 1;
     g.C = C + int64_t(i) * pl.sp * pl.sp; g.ldc = pl.sp;
@@ -1024,7 +1057,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     g.alpha = 1.f; g.beta = 0.f;
     KF_TRY(simt_gemm(g, st));
     rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(Yi, lyM, len_y, Qti, pl.sp, s, sig + int64_t(i) * s,
-                                                      qinv + int64_t(i) * s, ctx->d_status); note_launch();
+                                                      qinv + int64_t(i) * s, ctx->d_status, int(sym)); note_launch();
     KF_TRY(check_cuda(cudaGetLastError(), "rayleigh_norms_kernel"));
   }
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[3], st));
@@ -1040,7 +1073,9 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   if (int64_t(nu) * nwin > 65535) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: too many refinement windows");
   for (int pass = 0; pass < 2; ++pass) {
     const int64_t offr = pass * (RW / 2);
-    win_gram_kernel<<<dim3(unsigned(nwin), unsigned(nu)), 256, 0, st>>>(bf.Ys, lyM, R * lyM, lyM, offr, bf.Bw, nwin, ctx->d_status);
+    win_gram_kernel<<<dim3(unsigned(nwin), unsigned(nu)), 256, 0, st>>>(bf.Ys, lyM, R * lyM, lyM, offr, bf.Bw, nwin,
+                                                                        ctx->d_status, sym ? bf.Qs : nullptr, pl.sp,
+                                                                        R * pl.sp);
     note_launch();
     KF_TRY(check_cuda(cudaGetLastError(), "win_gram_kernel"));
     win_eig_kernel<<<unsigned(nu * nwin), 256, eig_smem, st>>>(bf.Bw, bf.Vw, 1e-6f, 12, ctx->d_status); note_launch();
@@ -1055,7 +1090,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   for (int i = 0; i < nu; ++i) {
     rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(bf.Ys + int64_t(i) * R * lyM, lyM, lyM,
                                                       bf.Qs + int64_t(i) * R * pl.sp, pl.sp, s, sig + int64_t(i) * s,
-                                                      qinv + int64_t(i) * s, ctx->d_status); note_launch();
+                                                      qinv + int64_t(i) * s, ctx->d_status, int(sym)); note_launch();
     KF_TRY(check_cuda(cudaGetLastError(), "rayleigh_norms_kernel"));
   }
   sort_desc_kernel<<<unsigned(nu), 1024, sort_smem, st>>>(sig, s, P, perm, s); note_launch();
@@ -1064,7 +1099,8 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     const kf_svd_problem& p = pr[i];
     dim3 grid(unsigned((s + 31) / 32), unsigned((s + 31) / 32));
     gather_kernel<<<grid, dim3(32, 8), 0, st>>>(bf.Qs + int64_t(i) * R * pl.sp, pl.sp, s, perm + int64_t(i) * s,
-                                                sig + int64_t(i) * s, qinv + int64_t(i) * s, p.vecs, p.ldv, p.sigma);
+                                                sig + int64_t(i) * s, qinv + int64_t(i) * s, p.vecs, p.ldv, p.sigma,
+                                                int(sym));
     note_launch();
     KF_TRY(check_cuda(cudaGetLastError(), "gather_kernel"));
   }

@@ -28,13 +28,15 @@ STATUS_NAMES = {0: "KF_OK", 1: "KF_ERR_INVALID", 2: "KF_ERR_WORKSPACE", 3: "KF_E
                 7: "KF_ERR_UNSUPPORTED"}
 
 EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_sync_status", "kf_gram_side",
-            "kfac_accumulate_workspace_size", "kfac_accumulate", "kf_finalize_covariance",
+            "kfac_accumulate_workspace_size", "kfac_accumulate", "fake_quant_rows", "kf_finalize_covariance",
             "whiten_workspace_size", "whiten", "kf_svd_profile_enable", "kf_svd_profile_read",
             "whitened_svd_workspace_size", "whitened_svd",
             "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_weighted",
             "score_and_allocate_keys", "score_and_allocate_noalloc",
             "empirical_fisher_workspace_size", "empirical_fisher_accumulate",
-            "unwhiten_workspace_size", "unwhiten"]
+            "unwhiten_workspace_size", "unwhiten",
+            "activation_covariance_workspace_size", "activation_covariance", "activation_eig_workspace_size",
+            "activation_eig", "activation_factors_workspace_size", "activation_factors"]
 
 
 class KfsvdError(RuntimeError):
@@ -47,6 +49,12 @@ class SvdProblem(ctypes.Structure):
     _fields_ = [("Wt", ctypes.c_void_p), ("m", ctypes.c_int64), ("n", ctypes.c_int64),
                 ("ldw", ctypes.c_int64), ("sigma", ctypes.c_void_p), ("vecs", ctypes.c_void_p),
                 ("ldv", ctypes.c_int64), ("sweeps", ctypes.c_void_p)]
+
+
+class SymProblem(ctypes.Structure):
+    _fields_ = [("C", ctypes.c_void_p), ("n", ctypes.c_int64), ("ldc", ctypes.c_int64),
+                ("sigma", ctypes.c_void_p), ("vecs", ctypes.c_void_p), ("ldv", ctypes.c_int64),
+                ("sweeps", ctypes.c_void_p)]
 
 
 class SvdProfile(ctypes.Structure):
@@ -67,6 +75,7 @@ _SIGS = {
     "kf_gram_side": (_I32, [_I64, _I64]),
     "kfac_accumulate_workspace_size": (_SZ, [_I32, _I32, _I64]),
     "kfac_accumulate": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _I32, _P, _I64, _P, _SZ, _P]),
+    "fake_quant_rows": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _P]),
     "kf_finalize_covariance": (_I32, [_P, _P, _I64, _I64, _I64, _F, _P]),
     "whiten_workspace_size": (_SZ, [_I64, _I64]),
     "whiten": (_I32, [_P, _P, _I64, _I64, _P, _I64, _I64, _P, _I32, _I64, _U32, _P, _I64, _P, _I64,
@@ -83,6 +92,13 @@ _SIGS = {
     "empirical_fisher_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "empirical_fisher_accumulate": (_I32, [_P, _P, _I32, _I64, _P, _I32, _I64, _I64, _I64, _I64, _P, _I64, _P,
                                            _I64, _I32, _P, _P, _SZ, _P]),
+    "activation_covariance_workspace_size": (_SZ, [_I64, _I64]),
+    "activation_covariance": (_I32, [_P, _P, _I64, _I64, _P, _I32, _I64, _I64, _P, _I64, _P, _SZ, _P]),
+    "activation_eig_workspace_size": (_SZ, [_I32, _I64]),
+    "activation_eig": (_I32, [_P, _I32, ctypes.POINTER(SymProblem), _F, _I32, _P, _SZ, _P]),
+    "activation_factors_workspace_size": (_SZ, [_I64, _I64, _I32]),
+    "activation_factors": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _P, _I64, _P, _SZ,
+                                  _P]),
     "unwhiten_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "unwhiten": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _I64,
                         _I32, _P, _I64, _P, _I64, _P, _SZ, _P]),
@@ -193,6 +209,13 @@ def kfac_accumulate(ctx: Context, act, cov_sum, quant: int = KF_QUANT_NONE, work
     ws, wsb = _ws(kfac_accumulate_workspace_size(dt, quant, d), workspace, act.device)
     _check(lib().kfac_accumulate(ctx.handle, _ptr(act), dt, n, d, _ld(act), quant, _ptr(cov_sum),
                                  _ld(cov_sum), _ptr(ws), wsb, _stream(stream)))
+
+
+def fake_quant_rows(ctx: Context, rows, out, stream=None):
+    """out (n_tokens x d bfloat16, contiguous) = per-token INT8 fake quantisation of rows."""
+    n, d = rows.shape
+    _check(lib().fake_quant_rows(ctx.handle, _ptr(rows), _dtype_code(rows), n, d, _ld(rows), _ptr(out),
+                                 _stream(stream)))
 
 
 def kf_finalize_covariance(ctx: Context, cov, n_tokens: int, lam: float, stream=None):
@@ -325,3 +348,37 @@ def unwhiten(ctx: Context, W, Sx, Sg, Sinv, sigma, vecs, r: int, U, V, workspace
                           0 if Sx is None else _ld(Sx), _ptr(Sg), 0 if Sg is None else _ld(Sg),
                           _ptr(Sinv), _ld(Sinv), _ptr(sigma), _ptr(vecs), _ld(vecs), int(r), _ptr(U),
                           _ld(U) if r > 0 else max(r, 1), _ptr(V), _ld(V), _ptr(ws), wsb, _stream(stream)))
+
+
+# ------------------------------------------------- Swift-SVD activation-only route
+def activation_covariance(ctx: Context, X, W, C, workspace=None, stream=None):
+    """C (n x n) = W^T X W: the covariance of the layer output y = a W from the activation
+    second moment X (m x m, full symmetric)."""
+    m, n = W.shape
+    ws, wsb = _ws(int(lib().activation_covariance_workspace_size(m, n)), workspace, W.device)
+    _check(lib().activation_covariance(ctx.handle, _ptr(X), _ld(X), m, _ptr(W), _dtype_code(W), _ld(W), n,
+                                       _ptr(C), _ld(C), _ptr(ws), wsb, _stream(stream)))
+
+
+def activation_eig(ctx: Context, Cs: Sequence, sigmas: Sequence, vecs: Sequence, sweeps=None,
+                   tol: float = 1e-6, max_sweeps: int = 30, workspace=None, stream=None):
+    """Batched eigenpairs of symmetric C of equal size: sigma = sqrt(max(lambda, 0))
+    descending, vecs the eigenvectors as columns."""
+    k = len(Cs)
+    probs = (SymProblem * k)()
+    for i, (C, sg, V) in enumerate(zip(Cs, sigmas, vecs)):
+        n = C.shape[0]
+        probs[i] = SymProblem(_ptr(C), n, _ld(C), _ptr(sg), _ptr(V), _ld(V),
+                              0 if sweeps is None else int(sweeps.data_ptr()) + 4 * i)
+    n0 = Cs[0].shape[0]
+    ws, wsb = _ws(int(lib().activation_eig_workspace_size(k, n0)), workspace, Cs[0].device)
+    _check(lib().activation_eig(ctx.handle, k, probs, float(tol), int(max_sweeps), _ptr(ws), wsb, _stream(stream)))
+
+
+def activation_factors(ctx: Context, W, vecs, r: int, U, V, workspace=None, stream=None):
+    """U = W V_r (m x r), V = V_r^T (r x n) for the first r eigenvector columns V_r of vecs."""
+    m, n = W.shape
+    ws, wsb = _ws(int(lib().activation_factors_workspace_size(m, n, r)), workspace, W.device)
+    _check(lib().activation_factors(ctx.handle, _ptr(W), _dtype_code(W), _ld(W), m, n, _ptr(vecs), _ld(vecs),
+                                    int(r), _ptr(U), _ld(U) if r > 0 else max(r, 1), _ptr(V), _ld(V), _ptr(ws),
+                                    wsb, _stream(stream)))

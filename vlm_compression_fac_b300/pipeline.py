@@ -111,9 +111,14 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     calibration rows with every component mapped back; the kept set of a unit is then any
     subset, and its factors are the kept columns of U and rows of V).
     ``sync_timer(tag)`` (optional) is called at phase boundaries ("kfac", "whiten", "svd",
-    "allocate", "unwhiten"; per group for the first three) and around every kfac_accumulate
-    call ("syrk<", "syrk>"), so a caller can record CUDA events there.
+    "allocate", "unwhiten"; per group for the first three; "score" after the empirical-Fisher
+    pass) and around every kfac_accumulate and empirical_fisher_accumulate call ("syrk<",
+    "syrk>", "fisher<", "fisher>"), so a caller can record CUDA events there.
     """
+    if score not in (None, "half_sigma2", "energy_ratio", "empirical_fisher"):
+        raise ValueError("compress: unknown score %r" % (score,))
+    if score in ("energy_ratio", "empirical_fisher") and (budget is None or fixed_rank is not None):
+        raise ValueError("compress: score %r needs a budget and no fixed rank" % (score,))
     mark = sync_timer or (lambda _name: None)
     dev = next(iter(weights.values())).device
     if callable(acts):
@@ -226,8 +231,9 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     cut = torch.empty(2, dtype=torch.float32, device=dev)
     used = torch.zeros(1, dtype=torch.int64, device=dev)
     if score == "empirical_fisher":
-        return _fisher_allocation(ctx, units, outs, weights, rows_fn, n_tokens, chunk_tokens, int(budget), off, cost,
-                                  ranks, cut, used, sweeps_dev, all_covs, stream, mark)
+        qsites = quant_sites if quant else set()
+        return _fisher_allocation(ctx, units, outs, weights, rows_fn, qsites, n_tokens, chunk_tokens, int(budget),
+                                  off, cost, ranks, cut, used, sweeps_dev, all_covs, stream, mark)
     if score == "energy_ratio":
         w = None if unit_weights is None else torch.tensor(list(unit_weights), dtype=torch.float32, device=dev)
         K.score_and_allocate_weighted(ctx, sig, off, cost, int(budget), ranks, mode=K.KF_KEY_ENERGY_RATIO,
@@ -262,10 +268,12 @@ def _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, s
     return Result(outs, all_covs, ranks, cut, used)
 
 
-def _fisher_allocation(ctx, units, outs, weights, rows_fn, n_tokens, chunk_tokens, budget, off, cost, ranks, cut,
-                       used, sweeps_dev, all_covs, stream, mark) -> Result:
+def _fisher_allocation(ctx, units, outs, weights, rows_fn, quant_sites, n_tokens, chunk_tokens, budget, off, cost,
+                       ranks, cut, used, sweeps_dev, all_covs, stream, mark) -> Result:
     """LASER's empirical-Fisher allocation: every component mapped back (U_all, V_all), its
-    score accumulated over the calibration rows, then sort-and-truncate on the scores."""
+    score accumulated over the calibration rows, then sort-and-truncate on the scores.  The
+    activations of ``quant_sites`` are fake-quantised over their full width first, as they
+    were for the covariance."""
     dev = ranks.device
     keys = []
     full = []
@@ -278,11 +286,19 @@ def _fisher_allocation(ctx, units, outs, weights, rows_fn, n_tokens, chunk_token
         acc = torch.zeros(s, dtype=torch.float64, device=dev)
         for t0 in range(0, n_tokens, chunk_tokens):
             t1 = min(n_tokens, t0 + chunk_tokens)
-            a = rows_fn(u.x_site, t0, t1)[:, u.x_off:u.x_off + u.m]
+            a = rows_fn(u.x_site, t0, t1)
+            if u.x_site in quant_sites:
+                qa = torch.empty(a.shape, dtype=torch.bfloat16, device=dev)
+                K.fake_quant_rows(ctx, a, qa, stream=stream)
+                a = qa
+            a = a[:, u.x_off:u.x_off + u.m]
             g = rows_fn(u.g_site, t0, t1)[:, u.g_off:u.g_off + u.n]
+            mark("fisher<")
             K.empirical_fisher_accumulate(ctx, a, g, Ua, Va, acc, stream=stream)
+            mark("fisher>")
         keys.append((acc / (2.0 * n_tokens)).to(torch.float32))
         full.append((Ua, Va))
+    mark("score")
     keys_t = torch.cat(keys)
     keep = torch.empty(keys_t.numel(), dtype=torch.uint8, device=dev)
     K.score_and_allocate_keys(ctx, keys_t, off, cost, budget, ranks, keep=keep, cut=cut, used=used, stream=stream)
@@ -300,6 +316,115 @@ def _fisher_allocation(ctx, units, outs, weights, rows_fn, n_tokens, chunk_token
         o.scores = keys[i]
     mark("unwhiten")
     return Result(outs, all_covs, ranks, cut, used)
+
+
+@dataclass
+class ActUnitOut:
+    name: str
+    m: int
+    n: int
+    C: Optional[torch.Tensor]            # n x n output covariance (released unless kept)
+    sigma: Optional[torch.Tensor] = None  # n values, descending (sqrt of C's eigenvalues)
+    vecs: Optional[torch.Tensor] = None   # n x n, eigenvectors as columns
+    sweeps: int = 0
+    rank: int = 0
+    U: Optional[torch.Tensor] = None      # m x rank: W V_k
+    V: Optional[torch.Tensor] = None      # rank x n: V_k^T
+
+
+def compress_activation_only(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch.Tensor],
+                             acts: Union[Dict[str, torch.Tensor], RowsFn], n_tokens: int, budget: int,
+                             quant: bool = False, tol: float = 1e-6, max_sweeps: int = 30, stream=None,
+                             sync_timer: Optional[Callable[[str], None]] = None,
+                             site_dims: Optional[Dict[str, int]] = None,
+                             groups: Optional[Sequence[Sequence[int]]] = None, chunk_tokens: int = 16384,
+                             keep_cov: bool = False) -> Result:
+    """Swift-SVD's activation-only route: W_k = W V_k V_k^T with V_k the top eigenvectors of
+    the covariance of the layer output, C = (1/N) sum_t (a_t W)^T (a_t W); no gradients, no
+    Cholesky.  Per group: the activation second moment of every input site (kfac_accumulate,
+    fake-quantised rows when ``quant``; finalised without damping), C = W^T X W per unit
+    (activation_covariance), the eigenpairs in batches of equal n (activation_eig); then one
+    global sort-and-truncate on 1/2 sigma^2 over the first min(m, n) components of every
+    unit (score_and_allocate) and the factors U = W V_k, V = V_k^T (activation_factors).
+    ``acts`` and ``groups`` as for ``compress``; ``sync_timer`` tags: "kfac", "cov", "eig"
+    per group, "allocate", "factors", and "syrk<"/"syrk>" around every kfac_accumulate."""
+    mark = sync_timer or (lambda _name: None)
+    dev = next(iter(weights.values())).device
+    if callable(acts):
+        rows_fn = acts
+        dims = dict(site_dims or {})
+    else:
+        resident = dict(acts)
+        rows_fn = lambda name, t0, t1: resident[name][t0:t1]
+        dims = {k: v.shape[1] for k, v in resident.items()}
+        chunk_tokens = max(n_tokens, 1)
+    groups = [list(range(len(units)))] if groups is None else [list(g) for g in groups]
+    q = K.KF_QUANT_INT8_TOKEN if quant else K.KF_QUANT_NONE
+    outs: List[Optional[ActUnitOut]] = [None] * len(units)
+    sweeps_dev = torch.zeros(len(units), dtype=torch.int32, device=dev)
+    for grp in groups:
+        covs: Dict[str, torch.Tensor] = {}
+        for i in grp:
+            sname = units[i].x_site
+            if sname in covs:
+                continue
+            d = dims[sname]
+            cov = torch.zeros((d, d), dtype=torch.float32, device=dev)
+            for t0 in range(0, n_tokens, chunk_tokens):
+                rows = rows_fn(sname, t0, min(n_tokens, t0 + chunk_tokens))
+                mark("syrk<")
+                K.kfac_accumulate(ctx, rows, cov, quant=q, stream=stream)
+                mark("syrk>")
+                del rows
+            K.kf_finalize_covariance(ctx, cov, n_tokens, 0.0, stream=stream)
+            covs[sname] = cov
+        mark("kfac")
+        for i in grp:
+            u = units[i]
+            X = covs[u.x_site][u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m]
+            W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
+            C = torch.empty((u.n, u.n), dtype=torch.float32, device=dev)
+            K.activation_covariance(ctx, X, W, C, stream=stream)
+            outs[i] = ActUnitOut(u.name, u.m, u.n, C)
+        del covs
+        mark("cov")
+        by_n: Dict[int, List[int]] = {}
+        for i in grp:
+            by_n.setdefault(units[i].n, []).append(i)
+        for n, idx in by_n.items():
+            for i in idx:
+                outs[i].sigma = torch.empty(n, dtype=torch.float32, device=dev)
+                outs[i].vecs = torch.empty((n, n), dtype=torch.float32, device=dev)
+            sw = torch.zeros(len(idx), dtype=torch.int32, device=dev)
+            K.activation_eig(ctx, [outs[i].C for i in idx], [outs[i].sigma for i in idx],
+                             [outs[i].vecs for i in idx], sweeps=sw, tol=tol, max_sweeps=max_sweeps, stream=stream)
+            sweeps_dev[torch.tensor(idx, device=dev)] = sw
+            if not keep_cov:
+                for i in idx:
+                    outs[i].C = None
+        mark("eig")
+
+    lens = [min(o.m, o.n) for o in outs]
+    sig = torch.cat([o.sigma[:s] for o, s in zip(outs, lens)])
+    off = torch.tensor([0] + list(_cumsum(lens)), dtype=torch.int64, device=dev)
+    cost = torch.tensor([o.m + o.n for o in outs], dtype=torch.int64, device=dev)
+    ranks = torch.empty(len(outs), dtype=torch.int32, device=dev)
+    cut = torch.empty(2, dtype=torch.float32, device=dev)
+    used = torch.zeros(1, dtype=torch.int64, device=dev)
+    K.score_and_allocate(ctx, sig, off, cost, int(budget), ranks, cut=cut, used=used, stream=stream)
+    ranks_h = ranks.cpu().tolist()
+    sweeps_h = sweeps_dev.cpu().tolist()
+    mark("allocate")
+    for o, u, r, swp in zip(outs, units, ranks_h, sweeps_h):
+        o.rank = int(r)
+        o.sweeps = int(swp)
+        o.U = torch.empty((o.m, max(o.rank, 1)), dtype=torch.float32, device=dev)[:, :o.rank]
+        o.V = torch.empty((max(o.rank, 1), o.n), dtype=torch.float32, device=dev)[:o.rank]
+        if o.rank > 0:
+            W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
+            K.activation_factors(ctx, W, o.vecs, o.rank, o.U, o.V, stream=stream)
+    mark("factors")
+    return Result(outs, {}, ranks, cut, used)
 
 
 def _cumsum(xs):
