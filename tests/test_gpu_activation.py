@@ -132,3 +132,68 @@ def test_end_to_end_activation_only(ctx, name):
         opt = float(np.sum(r["sigma"][g.rank:] ** 2))
         tot = float(np.sum(r["sigma"] ** 2))
         assert abs(loss - opt) <= 1e-3 * max(opt, 1e-3 * tot), (g.name, loss, opt)
+
+
+def test_llama7b_block_activation_only_fullsize(ctx):
+    """The route over the Llama-7B-shaped block at full size (N = 131072; q, k, v, o 4096^2,
+    gate/up 4096 x 11008 whose output covariances are 11008^2, down 11008 x 4096), with the
+    checks the oracle can afford: sampled entries of q's C against float64 sums over all
+    tokens; sigma against a float64 eigendecomposition of the GPU's own C (q, down); for the
+    11008^2 problems, eigen-residual bounds |lambda_i - lambda(C)| <= ||C v_i - lambda_i v_i||;
+    the loss of the kept subspace, tr((I - P) C (I - P)), against the optimum; allocation
+    bit-identical on the GPU's spectra."""
+    import time
+    from synth import device
+    from vlm_compression_fac_b300 import pipeline
+    wl = recipes.llama7b_block()
+    units = pipeline.unit_specs(wl)
+    weights = device.weights_on_device(wl, torch)
+    acts = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    res = pipeline.compress_activation_only(ctx, units, weights, acts, wl.n_tokens, wl.budget, keep_cov=True)
+    ctx.sync_status()
+    print("llama7b_block activation-only route: %.2f s, sweeps %s, ranks %s" % (
+        time.perf_counter() - t0, [g.sweeps for g in res.units], res.ranks.cpu().tolist()))
+    sig_g = [g.sigma.cpu().numpy() for g in res.units]
+    costs = [u.m + u.n for u in wl.units]
+    al = O.allocate([s[:min(u.m, u.n)] for s, u in zip(sig_g, wl.units)], costs, wl.budget, precision="f32")
+    np.testing.assert_array_equal(res.ranks.cpu().numpy(), al.ranks)
+    assert int(res.used.item()) == al.used <= wl.budget
+    names = [u.name for u in wl.units]
+
+    # sampled entries of q's output covariance against float64 sums over all tokens
+    iq = names.index("q")
+    Wq = recipes.gen_weight(wl, wl.units[iq]).astype(np.float64)
+    cols = [0, 1, 2000, 4095, 77]
+    Y = np.zeros((0, len(cols)))
+    A_dev = acts[wl.units[iq].x_site]
+    sums = np.zeros((len(cols), len(cols)))
+    for t in range(0, wl.n_tokens, 16384):
+        A = A_dev[t:t + 16384].float().cpu().numpy().astype(np.float64)
+        Y = A @ Wq[:, cols]
+        sums += Y.T @ Y
+    Cq = res.units[iq].C.cpu().numpy().astype(np.float64)
+    for a, b in [(0, 0), (1, 2), (3, 4), (0, 3)]:
+        want = sums[a, b] / wl.n_tokens
+        scale = np.sqrt(sums[a, a] * sums[b, b]) / wl.n_tokens
+        assert abs(Cq[cols[a], cols[b]] - want) <= 1e-4 * scale, (cols[a], cols[b])
+
+    for i, g in enumerate(res.units):
+        C = g.C.cpu().numpy().astype(np.float64)
+        C = 0.5 * (C + C.T)
+        k = int(g.rank)
+        V = g.vecs.cpu().numpy().astype(np.float64)[:, :k]
+        CV = C @ V
+        lam = sig_g[i].astype(np.float64)[:k] ** 2
+        trC = float(np.trace(C))
+        loss = trC - 2.0 * float(np.sum(V * CV)) + float(np.sum((V.T @ V) * (V.T @ CV)))
+        if g.name in ("q", "down"):
+            so = np.sqrt(np.maximum(np.linalg.eigvalsh(C)[::-1], 0.0))
+            assert np.max(np.abs(sig_g[i] - so)) <= 1e-3 * so[0], g.name
+            opt = float(np.sum(so[k:] ** 2))
+        else:
+            resid = np.linalg.norm(CV - V * lam[None, :], axis=0)
+            assert np.all(resid <= 1e-3 * lam[0]), (g.name, float(resid.max() / lam[0]))
+            opt = trC - float(np.sum(lam))
+        assert abs(loss - opt) <= 1e-3 * max(opt, 1e-3 * trC), (g.name, loss, opt)

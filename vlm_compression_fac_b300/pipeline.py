@@ -93,7 +93,8 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
              site_dims: Optional[Dict[str, int]] = None, act_sites: Optional[Sequence[str]] = None,
              groups: Optional[Sequence[Sequence[int]]] = None, chunk_tokens: int = 16384,
              keep_covs: Union[bool, Sequence[str]] = True, keep_whitened: bool = True,
-             score: Optional[str] = None, unit_weights: Optional[Sequence[float]] = None) -> Result:
+             score: Optional[str] = None, unit_weights: Optional[Sequence[float]] = None,
+             defer_allocation: bool = False) -> Result:
     """Runs the five steps.
 
     ``acts``/``grads``: dicts of resident (n_tokens x d) device tensors, or ``acts`` a callable
@@ -110,6 +111,9 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     empirical-Fisher loss, 1/2 mean_t (a_t . u_i)^2 (g_t . v_i)^2, from a second pass over the
     calibration rows with every component mapped back; the kept set of a unit is then any
     subset, and its factors are the kept columns of U and rows of V).
+    ``defer_allocation``: stop after the spectra (steps 1-4) and return the units with their
+    sigma, vecs and the factors the unwhitening reads (ranks, cut and used are None); the
+    sharded driver allocates over every rank's spectra and then maps back with ``_finish``.
     ``sync_timer(tag)`` (optional) is called at phase boundaries ("kfac", "whiten", "svd",
     "allocate", "unwhiten"; per group for the first three; "score" after the empirical-Fisher
     pass) and around every kfac_accumulate and empirical_fisher_accumulate call ("syrk<",
@@ -117,7 +121,8 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     """
     if score not in (None, "half_sigma2", "energy_ratio", "empirical_fisher"):
         raise ValueError("compress: unknown score %r" % (score,))
-    if score in ("energy_ratio", "empirical_fisher") and (budget is None or fixed_rank is not None):
+    if score in ("energy_ratio", "empirical_fisher") and (budget is None or fixed_rank is not None) \
+            and not defer_allocation:
         raise ValueError("compress: score %r needs a budget and no fixed rank" % (score,))
     mark = sync_timer or (lambda _name: None)
     dev = next(iter(weights.values())).device
@@ -221,6 +226,11 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
                 for i in idx:
                     outs[i].Wt = None
         mark("svd")
+
+    if defer_allocation:
+        for o, sw_ in zip(outs, sweeps_dev.cpu().tolist()):
+            o.sweeps = int(sw_)
+        return Result(outs, all_covs, None, None, None)
 
     # ---- step 5a: global allocation
     sig = torch.cat([o.sigma for o in outs])
