@@ -335,6 +335,26 @@ def compress_workload_activation_only(wl, units: Optional[List[int]] = None, chu
     return {"units": out, "alloc": alloc}
 
 
+# ------------------------------------------------ LASER hybrid FFN channel selection
+def channel_errors(W: np.ndarray, U: np.ndarray, V: np.ndarray, X: np.ndarray) -> np.ndarray:
+    """[LASER] hybrid FFN: the reconstruction error of every hidden channel j (column j of a
+    gate or up projection, d_model x d_ffn) under a temporary low-rank approximation U V:
+    e_j = d_j^T X d_j with d_j = (W - U V)[:, j], i.e. the mean squared error of channel j's
+    pre-activation over the calibration inputs when X = A^T A / N."""
+    D = np.asarray(W, np.float64) - np.asarray(U, np.float64) @ np.asarray(V, np.float64)
+    return np.einsum("ij,ik,kj->j", D, np.asarray(X, np.float64), D)
+
+
+def select_svd_channels(errors: Sequence[np.ndarray], n_svd: int) -> np.ndarray:
+    """[LASER] hybrid FFN: the n_svd "SVD-friendly" hidden channels, those with the lowest
+    summed reconstruction error over the projections that share the channel (gate and up);
+    ties go to the lower channel index.  Returned in increasing channel order; the other
+    channels stay dense."""
+    e = np.sum([np.asarray(x, np.float64) for x in errors], axis=0)
+    order = np.lexsort((np.arange(len(e)), e))
+    return np.sort(order[:n_svd])
+
+
 # ------------------------------------------------------------ whole workloads
 @dataclass
 class UnitResult:

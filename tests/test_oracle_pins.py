@@ -460,3 +460,46 @@ def test_swift_output_covariance_aggregates_by_chunks():
     W = r.standard_normal((6, 4))
     parts = sum(O.output_covariance(A[t:t + 10], W) * len(A[t:t + 10]) for t in range(0, 37, 10)) / 37
     np.testing.assert_allclose(parts, O.output_covariance(A, W), rtol=1e-13, atol=1e-13)
+
+
+def test_channel_errors_are_the_per_channel_mean_squared_preactivation_error():
+    """LASER hybrid FFN: with X = A^T A / N the error of channel j is (1/N) sum_t
+    (a_t . (w_j - w^_j))^2, checked token by token; summed over the channels and with
+    X = S_x^T S_x it is ||S_x (W - U V)||_F^2, the whitened error with G = I."""
+    r = np.random.default_rng(51)
+    N, d, f, k = 30, 5, 7, 2
+    A = r.standard_normal((N, d))
+    W = r.standard_normal((d, f))
+    U = r.standard_normal((d, k))
+    V = r.standard_normal((k, f))
+    X = A.T @ A / N
+    e = O.channel_errors(W, U, V, X)
+    D = W - U @ V
+    for j in range(f):
+        want = np.mean([(A[t] @ D[:, j]) ** 2 for t in range(N)])
+        assert abs(e[j] - want) <= 1e-12 * max(1.0, want)
+    Sx, _ = O.cholesky_factors(X, np.eye(f))
+    assert abs(e.sum() - O.whitened_error(W, U, V, Sx, np.eye(f))) <= 1e-10 * e.sum()
+
+
+def test_svd_friendly_channels_hand_case():
+    """Channels inside the span of the temporary factors reconstruct exactly and are chosen;
+    a full-rank temporary SVD makes every error ~0 and the choice falls to the lowest indices."""
+    d = 4
+    u = np.array([[1.0], [0.0], [0.0], [0.0]])
+    W = np.zeros((d, 5))
+    W[:, 1] = 3.0 * u[:, 0]          # in span(u): error 0
+    W[:, 3] = -2.0 * u[:, 0]         # in span(u): error 0
+    W[:, 0] = [0.0, 1.0, 0.0, 0.0]   # orthogonal: error 1 (X = I)
+    W[:, 2] = [0.0, 0.0, 2.0, 0.0]   # error 4
+    W[:, 4] = [0.5, 0.0, 0.0, 0.5]   # error 0.25
+    V = u.T @ W                      # U V = u u^T W: the projection of W onto span(u)
+    e = O.channel_errors(W, u, V, np.eye(d))
+    np.testing.assert_allclose(e, [1.0, 0.0, 4.0, 0.0, 0.25], atol=1e-15)
+    np.testing.assert_array_equal(O.select_svd_channels([e], 2), [1, 3])
+    np.testing.assert_array_equal(O.select_svd_channels([e], 3), [1, 3, 4])
+    # gate and up share the channel: the errors add
+    e_up = np.array([0.0, 5.0, 0.0, 0.0, 0.0])
+    np.testing.assert_array_equal(O.select_svd_channels([e, e_up], 2), [3, 4])
+    # ties at zero: lowest indices first
+    np.testing.assert_array_equal(O.select_svd_channels([np.zeros(5)], 3), [0, 1, 2])
