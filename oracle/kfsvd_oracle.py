@@ -347,12 +347,12 @@ def channel_errors(W: np.ndarray, U: np.ndarray, V: np.ndarray, X: np.ndarray) -
 
 def select_svd_channels(errors: Sequence[np.ndarray], n_svd: int) -> np.ndarray:
     """[LASER] hybrid FFN: the n_svd "SVD-friendly" hidden channels, those with the lowest
-    summed reconstruction error over the projections that share the channel (gate and up);
-    ties go to the lower channel index.  Returned in increasing channel order; the other
-    channels stay dense."""
+    summed reconstruction error over the projections that share the channel (gate and up).
+    Stated the other way round: the len - n_svd channels with the largest error stay dense,
+    ties to the lower channel index.  Returned in increasing channel order."""
     e = np.sum([np.asarray(x, np.float64) for x in errors], axis=0)
-    order = np.lexsort((np.arange(len(e)), e))
-    return np.sort(order[:n_svd])
+    order = np.lexsort((np.arange(len(e)), -e))
+    return np.sort(order[len(e) - n_svd:])
 
 
 # ------------------------------------------------------------ whole workloads

@@ -484,7 +484,7 @@ def test_channel_errors_are_the_per_channel_mean_squared_preactivation_error():
 
 def test_svd_friendly_channels_hand_case():
     """Channels inside the span of the temporary factors reconstruct exactly and are chosen;
-    a full-rank temporary SVD makes every error ~0 and the choice falls to the lowest indices."""
+    equal errors leave the lower channel indices dense."""
     d = 4
     u = np.array([[1.0], [0.0], [0.0], [0.0]])
     W = np.zeros((d, 5))
@@ -501,5 +501,7 @@ def test_svd_friendly_channels_hand_case():
     # gate and up share the channel: the errors add
     e_up = np.array([0.0, 5.0, 0.0, 0.0, 0.0])
     np.testing.assert_array_equal(O.select_svd_channels([e, e_up], 2), [3, 4])
-    # ties at zero: lowest indices first
-    np.testing.assert_array_equal(O.select_svd_channels([np.zeros(5)], 3), [0, 1, 2])
+    # ties: the lower indices stay dense
+    np.testing.assert_array_equal(O.select_svd_channels([np.zeros(5)], 3), [2, 3, 4])
+    np.testing.assert_array_equal(O.select_svd_channels([e], 0), [])
+    np.testing.assert_array_equal(O.select_svd_channels([e], 5), [0, 1, 2, 3, 4])
