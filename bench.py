@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--route", default="whitened", choices=["whitened", "activation_only"],
                     help="whitened: the K-FAC path (default); activation_only: Swift-SVD's route "
                          "(output covariance W^T X W, one eigendecomposition, W V_k V_k^T)")
+    ap.add_argument("--no-alloc-scaled", action="store_true",
+                    help="skip the allocation timed at 2^28 components (its HBM roofline)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="calibration tokens per site (default: the workload's 131072); a smaller N "
                          "keeps every matrix shape and is meant for profiler captures")
@@ -127,9 +129,55 @@ def cost_tail(m, n):
 
 # DRAM bytes (read + written) of one jac_apply_kernel launch that executes every task of a
 # step (7 problems of 4096, early sweep): ncu, dram__bytes_read.sum + dram__bytes_write.sum,
-# 716.0 MB + 882.2 MB.  The algorithmic bytes of such a launch are 7 x 14 B x 4096^2 = 1.64 GB
+# 715.9 MB + 880.8 MB.  The algorithmic bytes of such a launch are 7 x 14 B x 4096^2 = 1.64 GB
 # (half of C read, all of C and Q written, Q read).  Later launches skip converged pairs.
-JAC_APPLY_TRAFFIC = 1.598e9
+JAC_APPLY_TRAFFIC = 1.5967e9
+
+
+# Algorithmic bytes per component of one score_and_allocate call: sigma read (4) and key
+# written (8); four stable radix passes over the score word, each reading and writing the
+# 8-byte key (4 x 16); one read of the sorted keys for the cost prefix and the cut (8).
+ALLOC_BYTES_PER_KEY = 12 + 4 * 16 + 8
+
+
+def alloc_scaled(ctx, torch, K, hbm_peak, log2n=28, unit_len=1 << 17, reps=5):
+    """score_and_allocate over 2^log2n components (units of unit_len descending values, m + n
+    = 2 unit_len each, budget half of everything), timed with CUDA events on the launching
+    stream after two warm-up calls."""
+    n = 1 << log2n
+    n_units = n // unit_len
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    sig = torch.sort(torch.rand((n_units, unit_len), generator=g, device="cuda"), dim=1, descending=True)[0]
+    sig = sig.reshape(-1).contiguous()
+    off = torch.arange(0, n + 1, unit_len, dtype=torch.int64, device="cuda")
+    cost = torch.full((n_units,), 2 * unit_len, dtype=torch.int64, device="cuda")
+    budget = int(n * 2 * unit_len // 2)
+    ranks = torch.empty(n_units, dtype=torch.int32, device="cuda")
+    cut = torch.empty(2, device="cuda")
+    used = torch.zeros(1, dtype=torch.int64, device="cuda")
+    ws = torch.empty(K.score_and_allocate_workspace_size(n, n_units), dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(2):
+        K.score_and_allocate(ctx, sig, off, cost, budget, ranks, cut=cut, used=used, workspace=ws, stream=st)
+    ctx.sync_status()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(reps):
+        K.score_and_allocate(ctx, sig, off, cost, budget, ranks, cut=cut, used=used, workspace=ws, stream=st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    ctx.sync_status()
+    ms = e0.elapsed_time(e1) / reps
+    gbs = ALLOC_BYTES_PER_KEY * n / (ms / 1e3) / 1e9
+    kept = int(ranks.sum().item())
+    del sig, ws
+    torch.cuda.empty_cache()
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(gbs / hbm_peak, 4), "ms": round(ms, 3), "components": n, "units": n_units,
+            "kept": kept, "bytes_per_key": ALLOC_BYTES_PER_KEY, "peak_kind": "HBM copy, of measured"}
 
 
 def syrk_flops(n_tokens, d):
@@ -315,6 +363,8 @@ def run_kfsvd(args):
             "bound": "tensor", "achieved": round(f_tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
             "frac": round(f_tf / bf16_peak, 4), "ms_per_step": round(fisher_ms / K_, 3),
             "calls_per_step": n_fisher // K_, "peak_kind": "bf16 dense, sustained, of measured"}
+    if not args.no_alloc_scaled:
+        kern["score_and_allocate (2^28 components)"] = alloc_scaled(ctx, torch, K, pk.get("hbm_gbs", 6400.0))
     dom = max(("tc_gemm_kernel (covariance SYRK)", syrk_ms), ("jac_apply_kernel (Jacobi rotations)", apply_ms),
               key=lambda kv: kv[1])[0]
     roof = {k: v for k, v in kern[dom].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}

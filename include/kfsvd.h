@@ -376,6 +376,44 @@ KF_API kf_status activation_factors(kf_ctx* ctx, const void* W, kf_dtype w_dtype
                                     const float* vecs, int64_t ldv, int32_t r, float* U, int64_t ldu, float* V,
                                     int64_t ldvo, void* workspace, size_t workspace_bytes, kf_stream_t stream);
 
+/* ------------------------------------------------------------------------------------
+ * Index plumbing for subsets chosen by a keep mask (the empirical-Fisher kept components, the
+ * hybrid FFN's channel split).
+ * gather_rows_cols: dst[i][j] = src[row_idx ? row_idx[i] : i][col_idx ? col_idx[j] : j] for
+ *   i < rows, j < cols; src (src_rows x src_cols, lds) and dst (ldd) of the same dtype
+ *   (KF_BF16 or KF_F32), indices device int64.  An index outside src writes 0 and sets
+ *   KF_ERR_INVALID (info 151) in the status word.
+ * compact_mask: idx[0 .. *count) = the positions p < n whose mask byte is nonzero (want = 1)
+ *   or zero (want = 0), in increasing order; idx has room for n entries; count is device.
+ * ---------------------------------------------------------------------------------- */
+KF_API kf_status gather_rows_cols(kf_ctx* ctx, const void* src, kf_dtype dtype, int64_t lds, int64_t src_rows,
+                                  int64_t src_cols, const int64_t* row_idx, int64_t rows, const int64_t* col_idx,
+                                  int64_t cols, void* dst, int64_t ldd, kf_stream_t stream);
+KF_API kf_status compact_mask(kf_ctx* ctx, const uint8_t* mask, int64_t n, int32_t want, int64_t* idx,
+                              int64_t* count, kf_stream_t stream);
+
+/* ------------------------------------------------------------------------------------
+ * channel_errors - LASER's hybrid FFN channel selection (Hybrid SVD-quantisation for FFNs:
+ * a temporary SVD of the gate and up projections finds the "SVD-friendly" hidden channels,
+ * those it reconstructs with low error; the others stay dense).  For W (m x n, a gate or up
+ * projection, column j = hidden channel j), the temporary factors U (m x r, ldu) and V
+ * (r x n, ldv) and the input factor X (m x m float32, full symmetric):
+ *   err_sum[j] += d_j^T X d_j,  d_j = (W - U V)[:, j]        (float64, deterministic)
+ * the mean squared error of channel j's pre-activation over the calibration inputs.  Call it
+ * for gate and then up with the same err_sum (zeroed first) so that the errors of a channel
+ * add; keys (float[n], may be NULL) receives float(err_sum) after the addition.  Products on
+ * the tensor cores with U, V, X and W - U V as three bfloat16 planes each.  r = 0 scores the
+ * dense weight itself.  The split follows from score_and_allocate_keys on keys with one unit,
+ * cost 1 per channel and budget = the number of dense channels: the kept mask marks the
+ * dense channels (the largest errors; equal errors keep the lower index dense), the rest
+ * are SVD-friendly.
+ * ---------------------------------------------------------------------------------- */
+KF_API size_t channel_errors_workspace_size(int64_t m, int64_t n, int32_t r);
+KF_API kf_status channel_errors(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m, int64_t n,
+                                const float* U, int64_t ldu, const float* V, int64_t ldv, int32_t r,
+                                const float* X, int64_t ldx, double* err_sum, float* keys, void* workspace,
+                                size_t workspace_bytes, kf_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -4,7 +4,8 @@
 //          weight (UniRank's layer importance I_l);
 //          ascending k is score descending, then lower unit, then lower component index
 //          (ids are assigned in unit order), which makes the order total and deterministic;
-//   sort:  LSD radix sort, 8 passes of 8 bits; each pass = per-tile digit histogram,
+//   sort:  LSD radix sort of the score word, 4 passes of 8 bits (equal scores keep their id
+//          order, since the keys start in id order and every pass is stable); each pass = per-tile digit histogram,
 //          one exclusive scan over (digit, tile), stable scatter (warp match + per-warp
 //          digit counters keep the original order inside a tile);
 //   cut:   inclusive prefix sum of the kept pairs' cost m+n in sorted order; the kept
@@ -92,23 +93,54 @@ __global__ void __launch_bounds__(RT) hist_kernel(const unsigned long long* __re
   h[threadIdx.x] = 0;
   __syncthreads();
   const int64_t base = int64_t(blockIdx.x) * TILE;
+  const unsigned lane = threadIdx.x & 31u;
   for (int i = 0; i < RI; ++i) {
     const int64_t g = base + int64_t(i) * RT + threadIdx.x;
-    if (g < n) atomicAdd(&h[(keys[g] >> shift) & 255u], 1u);
+    const unsigned d = g < n ? unsigned((keys[g] >> shift) & 255u) : 256u;
+    // one shared atomic per distinct digit of the warp (the leading bytes of the keys are
+    // often nearly constant, which would serialise per-key atomics on one bin)
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    if (d < 256u && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&h[d], unsigned(__popc(peers)));
   }
   __syncthreads();
   hist[int64_t(threadIdx.x) * ntiles + blockIdx.x] = h[threadIdx.x];
 }
 
-// Exclusive scan of a uint array of length len (one CTA, sequential over chunks).
-__global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__ a, int64_t len) {
+// Multi-CTA exclusive scan of a long uint array in chunks of SCAN_CHUNK: block sums, a scan of
+// the sums, then every chunk rescanned from its base (same result as one sequential scan).
+constexpr int64_t SCAN_CHUNK = 8 * 1024;
+
+__global__ void __launch_bounds__(1024) chunk_sum_u32_kernel(const unsigned* __restrict__ a, int64_t len,
+                                                             unsigned* __restrict__ bsum) {
+  __shared__ unsigned red[32];
+  const int64_t c0 = int64_t(blockIdx.x) * SCAN_CHUNK;
+  unsigned s = 0;
+  for (int64_t i = c0 + threadIdx.x; i < len && i < c0 + SCAN_CHUNK; i += 1024) s += a[i];
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned t = 0;
+    for (int w = 0; w < 32; ++w) t += red[w];
+    bsum[blockIdx.x] = t;
+  }
+}
+
+// Exclusive scan of a uint array: CTA b scans [b * chunk, min(len, (b + 1) * chunk)) in steps
+// of SCAN_T, starting from base[b] (or 0 without base).  One CTA with chunk >= len scans the
+// whole array.
+__global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__ a, int64_t len, int64_t chunk,
+                                                          const unsigned* __restrict__ cbase) {
   __shared__ unsigned ws[32];
   __shared__ unsigned carry;
-  if (threadIdx.x == 0) carry = 0;
+  if (threadIdx.x == 0) carry = cbase ? cbase[blockIdx.x] : 0u;
   __syncthreads();
-  for (int64_t c0 = 0; c0 < len; c0 += SCAN_T) {
+  const int64_t lo = int64_t(blockIdx.x) * chunk;
+  const int64_t hi = lo + chunk < len ? lo + chunk : len;
+  for (int64_t c0 = lo; c0 < hi; c0 += SCAN_T) {
     const int64_t i = c0 + threadIdx.x;
-    const unsigned v = i < len ? a[i] : 0u;
+    const unsigned v = i < hi ? a[i] : 0u;
     unsigned x = v;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
@@ -129,7 +161,7 @@ __global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__
     }
     __syncthreads();
     const unsigned incl = x + (w > 0 ? ws[w - 1] : 0u) + carry;
-    if (i < len) a[i] = incl - v;
+    if (i < hi) a[i] = incl - v;
     __syncthreads();
     if (threadIdx.x == SCAN_T - 1) carry = incl;
     __syncthreads();
@@ -324,7 +356,7 @@ unsigned grid_cap(int64_t n, int per) {
 
 struct AllocBufs {
   unsigned long long *ka, *kb, *kcount;
-  unsigned* hist;
+  unsigned *hist, *hsum;
   long long *bsum, *prefix;
   float* energy;
 };
@@ -336,6 +368,7 @@ size_t alloc_carve(Carve& cv, int64_t n, int64_t n_energy, AllocBufs& b) {
   b.ka = cv.take<unsigned long long>(n > 0 ? n : 1);
   b.kb = cv.take<unsigned long long>(n > 0 ? n : 1);
   b.hist = cv.take<unsigned>(size_t(256) * (ntiles > 0 ? ntiles : 1));
+  b.hsum = cv.take<unsigned>(size_t((256 * (ntiles > 0 ? ntiles : 1) + SCAN_CHUNK - 1) / SCAN_CHUNK));
   b.bsum = cv.take<long long>(nb > 0 ? nb : 1);
   b.prefix = cv.take<long long>(n > 0 ? n : 1);
   b.kcount = cv.take<unsigned long long>(1);
@@ -375,14 +408,28 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), weight, b.energy,
                                                       b.ka); note_launch();
   KF_CUDA(cudaGetLastError());
+  // The keys are built in id order and every pass is stable, so sorting by the score word
+  // alone (the upper 32 bits, four 8-bit passes) leaves equal scores in id order: the same
+  // total order as sorting all 64 bits, at half the passes.
   unsigned long long* src = b.ka;
   unsigned long long* dst = b.kb;
-  for (int pass = 0; pass < 8; ++pass) {
-    const int shift = pass * 8;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 32 + pass * 8;
     hist_kernel<<<ntiles, RT, 0, st>>>(src, n, shift, ntiles, b.hist); note_launch();
     KF_CUDA(cudaGetLastError());
-    scan_u32_kernel<<<1, SCAN_T, 0, st>>>(b.hist, int64_t(256) * ntiles); note_launch();
-    KF_CUDA(cudaGetLastError());
+    const int64_t hlen = int64_t(256) * ntiles;
+    if (hlen <= SCAN_CHUNK) {
+      scan_u32_kernel<<<1, SCAN_T, 0, st>>>(b.hist, hlen, hlen, nullptr); note_launch();
+      KF_CUDA(cudaGetLastError());
+    } else {
+      const int64_t nch = (hlen + SCAN_CHUNK - 1) / SCAN_CHUNK;
+      chunk_sum_u32_kernel<<<unsigned(nch), 1024, 0, st>>>(b.hist, hlen, b.hsum); note_launch();
+      KF_CUDA(cudaGetLastError());
+      scan_u32_kernel<<<1, SCAN_T, 0, st>>>(b.hsum, nch, nch, nullptr); note_launch();
+      KF_CUDA(cudaGetLastError());
+      scan_u32_kernel<<<unsigned(nch), SCAN_T, 0, st>>>(b.hist, hlen, SCAN_CHUNK, b.hsum); note_launch();
+      KF_CUDA(cudaGetLastError());
+    }
     scatter_kernel<<<ntiles, RT, 0, st>>>(src, dst, n, shift, ntiles, b.hist); note_launch();
     KF_CUDA(cudaGetLastError());
     unsigned long long* tmp = src;

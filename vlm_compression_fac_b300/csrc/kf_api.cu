@@ -400,6 +400,89 @@ kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_problem* pr
                  reinterpret_cast<cudaStream_t>(stream), false);
 }
 
+// ------------------------------------------------------- index plumbing
+kf_status gather_rows_cols(kf_ctx* ctx, const void* src, kf_dtype dtype, int64_t lds, int64_t src_rows,
+                           int64_t src_cols, const int64_t* row_idx, int64_t rows, const int64_t* col_idx, int64_t cols,
+                           void* dst, int64_t ldd, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "gather_rows_cols: null context"));
+  KF_TRY(need(dtype == KF_BF16 || dtype == KF_F32, "gather_rows_cols: dtype"));
+  KF_TRY(need(rows >= 0 && cols >= 0 && src_rows >= 0 && src_cols >= 0, "gather_rows_cols: sizes"));
+  if (rows == 0 || cols == 0) return KF_OK;
+  KF_TRY(need(src && dst, "gather_rows_cols: null pointer"));
+  KF_TRY(need(lds >= src_cols && ldd >= cols, "gather_rows_cols: leading dimension"));
+  KF_TRY(need(row_idx || rows <= src_rows, "gather_rows_cols: rows"));
+  KF_TRY(need(col_idx || cols <= src_cols, "gather_rows_cols: cols"));
+  return launch_gather2d(src, dtype, lds, src_rows, src_cols, row_idx, rows, col_idx, cols, dst, ldd, ctx->d_status,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+kf_status compact_mask(kf_ctx* ctx, const uint8_t* mask, int64_t n, int32_t want, int64_t* idx, int64_t* count,
+                       kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "compact_mask: null context"));
+  KF_TRY(need(n >= 0 && count, "compact_mask: sizes"));
+  KF_TRY(need(n == 0 || (mask && idx), "compact_mask: null pointer"));
+  return launch_compact_mask(mask, n, want, idx, count, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------- LASER hybrid FFN channel errors
+namespace {
+struct ChanBufs {
+  float *D, *E;
+  int64_t ld;
+  PlaneBuf u, v, x, d;
+};
+size_t chan_carve(Carve& cv, int64_t m, int64_t n, int32_t r, ChanBufs& b) {
+  b.ld = round_up(n, 8);
+  b.D = cv.take<float>(size_t(m) * b.ld);
+  b.E = cv.take<float>(size_t(m) * b.ld);
+  b.u = take_planes(cv, m, r > 0 ? r : 1, 3);
+  b.v = take_planes(cv, r > 0 ? r : 1, n, 3);
+  b.x = take_planes(cv, m, m, 3);
+  b.d = take_planes(cv, m, n, 3);
+  return cv.off;
+}
+}  // namespace
+
+size_t channel_errors_workspace_size(int64_t m, int64_t n, int32_t r) {
+  if (m <= 0 || n <= 0 || r < 0) return 0;
+  Carve cv(nullptr, 0, true);
+  ChanBufs b;
+  return chan_carve(cv, m, n, r, b) + 256;
+}
+
+kf_status channel_errors(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, int64_t m, int64_t n,
+                         const float* U, int64_t ldu, const float* V, int64_t ldv, int32_t r, const float* X,
+                         int64_t ldx, double* err_sum, float* keys, void* workspace, size_t workspace_bytes,
+                         kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "channel_errors: null context"));
+  KF_TRY(need(m > 0 && n > 0 && r >= 0, "channel_errors: sizes"));
+  KF_TRY(need(W && X && err_sum, "channel_errors: null pointer"));
+  KF_TRY(need(r == 0 || (U && V), "channel_errors: null factor"));
+  KF_TRY(need(ldw >= n && ldx >= m && (r == 0 || (ldu >= r && ldv >= n)), "channel_errors: leading dimension"));
+  KF_TRY(need(w_dtype == KF_BF16 || w_dtype == KF_F32, "channel_errors: dtype"));
+  Carve cv(workspace, workspace_bytes, false);
+  ChanBufs b;
+  chan_carve(cv, m, n, r, b);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "channel_errors: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // D = W - U V (U, V as three bfloat16 planes: float32-level products), E = X D, and the
+  // column dots e_j = d_j . (X d_j) in float64.
+  if (r > 0) {
+    Planes pu, pv;
+    KF_TRY(split_f32(U, ldu, m, r, b.u, &pu, st));
+    KF_TRY(split_f32(V, ldv, r, n, b.v, &pv, st));
+    KF_TRY(tc_product(ctx, m, n, r, pu, false, pv, true, KR_FULL, b.D, b.ld, st));
+  } else {
+    KF_CUDA(cudaMemsetAsync(b.D, 0, sizeof(float) * size_t(m) * b.ld, st));
+  }
+  KF_TRY(launch_sub_from(W, w_dtype, ldw, b.D, b.ld, m, n, st));
+  Planes px, pd;
+  KF_TRY(split_f32(X, ldx, m, m, b.x, &px, st));
+  KF_TRY(split_f32(b.D, b.ld, m, n, b.d, &pd, st));
+  KF_TRY(tc_product(ctx, m, n, m, px, false, pd, true, KR_FULL, b.E, b.ld, st));
+  return launch_coldot(b.D, b.ld, b.E, b.ld, m, n, err_sum, keys, st);
+}
+
 // ------------------------------------------------- Swift-SVD activation-only route
 namespace {
 struct ActCovBufs {

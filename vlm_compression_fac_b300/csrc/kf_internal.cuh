@@ -130,6 +130,15 @@ kf_status launch_copy_bf16(const __nv_bfloat16* in, int64_t rows, int64_t d, int
                            __nv_bfloat16* out, int64_t ldo, cudaStream_t st);
 kf_status launch_fisher_reduce(const float* P, int64_t ldp, const float* Q, int64_t ldq, int64_t rows, int64_t cols,
                                double* acc, cudaStream_t st);
+kf_status launch_coldot(const float* D, int64_t ldd, const float* E, int64_t lde, int64_t rows, int64_t cols,
+                        double* acc, float* keys, cudaStream_t st);
+kf_status launch_sub_from(const void* W, kf_dtype dt, int64_t ldw, float* D, int64_t ldd, int64_t rows, int64_t cols,
+                          cudaStream_t st);
+kf_status launch_gather2d(const void* src, kf_dtype dt, int64_t lds, int64_t src_rows, int64_t src_cols,
+                          const int64_t* ri, int64_t rows, const int64_t* ci, int64_t cols, void* dst, int64_t ldd,
+                          int* status, cudaStream_t st);
+kf_status launch_compact_mask(const unsigned char* mask, int64_t n, int want, int64_t* idx, int64_t* count,
+                              cudaStream_t st);
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
                           float* scratch, cudaStream_t st);
 kf_status launch_copy(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,

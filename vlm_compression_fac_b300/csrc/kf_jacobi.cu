@@ -39,8 +39,14 @@ __device__ __forceinline__ bool aligned16(const void* p, int* st, int site) {
   return false;
 }
 
-__device__ __forceinline__ int rr_pos(int pos, int round, int n) {  // circle method
-  return pos == 0 ? 0 : 1 + (pos - 1 + round) % (n - 1);
+// Circle method: the element at position pos in round `round` of a round-robin over n.
+// Every caller has 0 <= pos < n and 0 <= round < n - 1, so pos - 1 + round < 2 (n - 1) and
+// the reduction modulo n - 1 is one conditional subtraction.
+__device__ __forceinline__ int rr_pos(int pos, int round, int n) {
+  if (pos == 0) return 0;
+  int v = pos - 1 + round;
+  if (v >= n - 1) v -= n - 1;
+  return 1 + v;
 }
 
 __device__ __forceinline__ int64_t gidx(int r, int b0, int b1) {  // pair-local -> global index
@@ -304,8 +310,15 @@ __device__ __forceinline__ bool decode_apply(int g, int per_u, int ntile_c, int 
   if (conv[t.u]) return false;
   const int* skip = skipall + int64_t(t.u) * npairs;
   if (task < ntile_c) {
-    int p = 0;
-    while (task >= npairs - p) { task -= npairs - p; ++p; }
+    // Row p of the upper triangle (p <= q) holds npairs - p tiles; S(p) = p (2 npairs - p + 1) / 2
+    // tiles precede it.  p = the largest row with S(p) <= task: the root of the quadratic,
+    // then an exact integer correction (at most a step or two for npairs <= 256).
+    const int n2 = 2 * npairs + 1;
+    int p = int((float(n2) - sqrtf(float(n2) * float(n2) - 8.f * float(task))) * 0.5f);
+    p = p < 0 ? 0 : (p > npairs - 1 ? npairs - 1 : p);
+    while (p > 0 && p * (n2 - p) / 2 > task) --p;
+    while (p + 1 < npairs && (p + 1) * (n2 - p - 1) / 2 <= task) ++p;
+    task -= p * (n2 - p) / 2;
     t.kind = 0; t.p = p; t.q = p + task; t.cb = 0;
     t.wp = !skip[t.p]; t.wq = !skip[t.q];
     return t.wp || t.wq;

@@ -144,6 +144,98 @@ __global__ void __launch_bounds__(256) fisher_reduce_kernel(const float* __restr
   }
 }
 
+// acc[j] += sum over rows i of D[i][j] E[i][j] in float64 (the same layout and fixed order as
+// fisher_reduce_kernel); keys[j] = float(acc[j]) afterwards when keys is given.
+__global__ void __launch_bounds__(256) coldot_kernel(const float* __restrict__ D, int64_t ldd,
+                                                     const float* __restrict__ E, int64_t lde, int64_t rows,
+                                                     int64_t cols, double* __restrict__ acc,
+                                                     float* __restrict__ keys) {
+  __shared__ double part[8][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t j = int64_t(blockIdx.x) * 32 + lane;
+  double s = 0.0;
+  if (j < cols) {
+    for (int64_t i = w; i < rows; i += 8) s += double(D[i * ldd + j]) * double(E[i * lde + j]);
+  }
+  part[w][lane] = s;
+  __syncthreads();
+  if (w == 0 && j < cols) {
+    double tot = 0.0;
+    for (int x = 0; x < 8; ++x) tot += part[x][lane];
+    const double v = acc[j] + tot;
+    acc[j] = v;
+    if (keys) keys[j] = float(v);
+  }
+}
+
+// D[i][j] <- W[i][j] - D[i][j] (W bfloat16 or float32).
+template <typename T>
+__global__ void sub_from_kernel(const T* __restrict__ W, int64_t ldw, float* __restrict__ D, int64_t ldd,
+                                int64_t rows, int64_t cols) {
+  const int64_t total = rows * cols;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t i = e / cols, j = e - i * cols;
+    D[i * ldd + j] = to_f(W[i * ldw + j]) - D[i * ldd + j];
+  }
+}
+
+// dst[i][j] = src[ri ? ri[i] : i][ci ? ci[j] : j] (float32 or bfloat16 elements); indices are
+// checked against the source extent (an index outside it writes 0 and records the status).
+template <typename T>
+__global__ void gather2d_kernel(const T* __restrict__ src, int64_t lds, int64_t src_rows, int64_t src_cols,
+                                const int64_t* __restrict__ ri, int64_t rows, const int64_t* __restrict__ ci,
+                                int64_t cols, T* __restrict__ dst, int64_t ldd, int* status) {
+  const int64_t total = rows * cols;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t i = e / cols, j = e - i * cols;
+    const int64_t r = ri ? ri[i] : i, c = ci ? ci[j] : j;
+    if (r < 0 || r >= src_rows || c < 0 || c >= src_cols) {
+      raise_status(status, KF_ERR_INVALID, 151);
+      dst[i * ldd + j] = T(0.f);
+      continue;
+    }
+    dst[i * ldd + j] = src[r * lds + c];
+  }
+}
+
+// Ordered compaction: idx[0 .. count) = the positions p < n with (mask[p] != 0) == (want != 0),
+// increasing; one CTA, chunks of 1024 with a block-wide scan.
+__global__ void __launch_bounds__(1024) compact_mask_kernel(const unsigned char* __restrict__ mask, int64_t n,
+                                                             int want, int64_t* __restrict__ idx,
+                                                             int64_t* __restrict__ count) {
+  __shared__ int wsum[32];
+  __shared__ int64_t base;
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  if (t == 0) base = 0;
+  __syncthreads();
+  for (int64_t c0 = 0; c0 < n; c0 += 1024) {
+    const int64_t p = c0 + t;
+    const int f = (p < n && ((mask[p] != 0) == (want != 0))) ? 1 : 0;
+    int x = f;  // inclusive scan within the warp
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int v = wsum[lane];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      wsum[lane] = v;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (w > 0 ? wsum[w - 1] : 0) + x - f;
+    if (f) idx[base + before] = p;
+    __syncthreads();
+    if (t == 0) base += wsum[31];
+    __syncthreads();
+  }
+  if (t == 0) *count = base;
+}
+
 // Sum of the diagonal in float64, fixed order (one CTA).
 __global__ void diag_mean_kernel(const float* __restrict__ C, int64_t ldc, int64_t d,
                                  int64_t n_tokens, float lambda, float* __restrict__ out) {
@@ -277,6 +369,45 @@ kf_status launch_fisher_reduce(const float* P, int64_t ldp, const float* Q, int6
   if (rows <= 0 || cols <= 0) return KF_OK;
   fisher_reduce_kernel<<<unsigned((cols + 31) / 32), 256, 0, st>>>(P, ldp, Q, ldq, rows, cols, acc); note_launch();
   return check_cuda(cudaGetLastError(), "fisher_reduce launch");
+}
+
+kf_status launch_coldot(const float* D, int64_t ldd, const float* E, int64_t lde, int64_t rows, int64_t cols,
+                        double* acc, float* keys, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  coldot_kernel<<<unsigned((cols + 31) / 32), 256, 0, st>>>(D, ldd, E, lde, rows, cols, acc, keys); note_launch();
+  return check_cuda(cudaGetLastError(), "coldot launch");
+}
+
+kf_status launch_sub_from(const void* W, kf_dtype dt, int64_t ldw, float* D, int64_t ldd, int64_t rows, int64_t cols,
+                          cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  if (dt == KF_BF16)
+    sub_from_kernel<__nv_bfloat16><<<grid_for(rows * cols), 256, 0, st>>>((const __nv_bfloat16*)W, ldw, D, ldd, rows,
+                                                                           cols);
+  else
+    sub_from_kernel<float><<<grid_for(rows * cols), 256, 0, st>>>((const float*)W, ldw, D, ldd, rows, cols);
+  note_launch();
+  return check_cuda(cudaGetLastError(), "sub_from launch");
+}
+
+kf_status launch_gather2d(const void* src, kf_dtype dt, int64_t lds, int64_t src_rows, int64_t src_cols,
+                          const int64_t* ri, int64_t rows, const int64_t* ci, int64_t cols, void* dst, int64_t ldd,
+                          int* status, cudaStream_t st) {
+  if (rows <= 0 || cols <= 0) return KF_OK;
+  if (dt == KF_BF16)
+    gather2d_kernel<__nv_bfloat16><<<grid_for(rows * cols), 256, 0, st>>>(
+        (const __nv_bfloat16*)src, lds, src_rows, src_cols, ri, rows, ci, cols, (__nv_bfloat16*)dst, ldd, status);
+  else
+    gather2d_kernel<float><<<grid_for(rows * cols), 256, 0, st>>>((const float*)src, lds, src_rows, src_cols, ri, rows,
+                                                                  ci, cols, (float*)dst, ldd, status);
+  note_launch();
+  return check_cuda(cudaGetLastError(), "gather2d launch");
+}
+
+kf_status launch_compact_mask(const unsigned char* mask, int64_t n, int want, int64_t* idx, int64_t* count,
+                              cudaStream_t st) {
+  compact_mask_kernel<<<1, 1024, 0, st>>>(mask, n, want, idx, count); note_launch();
+  return check_cuda(cudaGetLastError(), "compact_mask launch");
 }
 
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,

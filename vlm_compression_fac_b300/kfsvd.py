@@ -36,7 +36,8 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "empirical_fisher_workspace_size", "empirical_fisher_accumulate",
             "unwhiten_workspace_size", "unwhiten",
             "activation_covariance_workspace_size", "activation_covariance", "activation_eig_workspace_size",
-            "activation_eig", "activation_factors_workspace_size", "activation_factors"]
+            "activation_eig", "activation_factors_workspace_size", "activation_factors",
+            "channel_errors_workspace_size", "channel_errors", "gather_rows_cols", "compact_mask"]
 
 
 class KfsvdError(RuntimeError):
@@ -99,6 +100,11 @@ _SIGS = {
     "activation_factors_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "activation_factors": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _I32, _P, _I64, _P, _I64, _P, _SZ,
                                   _P]),
+    "gather_rows_cols": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P]),
+    "compact_mask": (_I32, [_P, _P, _I64, _I32, _P, _P, _P]),
+    "channel_errors_workspace_size": (_SZ, [_I64, _I64, _I32]),
+    "channel_errors": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _I32, _P, _I64, _P, _P, _P, _SZ,
+                              _P]),
     "unwhiten_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "unwhiten": (_I32, [_P, _P, _I32, _I64, _I64, _I64, _P, _I64, _P, _I64, _P, _I64, _P, _P, _I64,
                         _I32, _P, _I64, _P, _I64, _P, _SZ, _P]),
@@ -382,3 +388,41 @@ def activation_factors(ctx: Context, W, vecs, r: int, U, V, workspace=None, stre
     _check(lib().activation_factors(ctx.handle, _ptr(W), _dtype_code(W), _ld(W), m, n, _ptr(vecs), _ld(vecs),
                                     int(r), _ptr(U), _ld(U) if r > 0 else max(r, 1), _ptr(V), _ld(V), _ptr(ws),
                                     wsb, _stream(stream)))
+
+
+# ------------------------------------------------- LASER hybrid FFN channel selection
+def channel_errors(ctx: Context, W, U, V, X, err_sum, keys=None, workspace=None, stream=None):
+    """err_sum (float64, n) += per-channel errors d_j^T X d_j of W - U V; keys (float32, n) =
+    float(err_sum) afterwards if given.  U (m x r) / V (r x n) may be None for r = 0."""
+    m, n = W.shape
+    r = 0 if U is None else int(U.shape[1])
+    ws, wsb = _ws(int(lib().channel_errors_workspace_size(m, n, r)), workspace, W.device)
+    _check(lib().channel_errors(ctx.handle, _ptr(W), _dtype_code(W), _ld(W), m, n, _ptr(U),
+                                _ld(U) if r > 0 else 1, _ptr(V), _ld(V) if r > 0 else n, r, _ptr(X), _ld(X),
+                                _ptr(err_sum), _ptr(keys), _ptr(ws), wsb, _stream(stream)))
+
+
+# ------------------------------------------------------------- index plumbing
+def gather_rows_cols(ctx: Context, src, row_idx=None, col_idx=None, out=None, stream=None):
+    """out = src[row_idx][:, col_idx] (either index may be None: all rows / columns), by the
+    library's gather kernel; int64 device indices."""
+    import torch
+    R, C = src.shape
+    rows = R if row_idx is None else int(row_idx.numel())
+    cols = C if col_idx is None else int(col_idx.numel())
+    if out is None:
+        out = torch.empty((rows, max(cols, 1)), dtype=src.dtype, device=src.device)[:, :cols]
+    _check(lib().gather_rows_cols(ctx.handle, _ptr(src), _dtype_code(src), _ld(src), R, C, _ptr(row_idx), rows,
+                                  _ptr(col_idx), cols, _ptr(out), _ld(out) if cols > 0 else 1, _stream(stream)))
+    return out
+
+
+def compact_mask(ctx: Context, mask, want: int = 1, stream=None):
+    """Increasing positions where mask (uint8) is nonzero (want=1) or zero (want=0), as an
+    int64 device tensor (one host read of the count)."""
+    import torch
+    n = int(mask.numel())
+    idx = torch.empty(max(n, 1), dtype=torch.int64, device=mask.device)
+    cnt = torch.zeros(1, dtype=torch.int64, device=mask.device)
+    _check(lib().compact_mask(ctx.handle, _ptr(mask), n, int(want), _ptr(idx), _ptr(cnt), _stream(stream)))
+    return idx[:int(cnt.item())]

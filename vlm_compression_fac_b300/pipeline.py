@@ -319,9 +319,9 @@ def _fisher_allocation(ctx, units, outs, weights, rows_fn, quant_sites, n_tokens
     for i, (o, (Ua, Va), r, sw) in enumerate(zip(outs, full, ranks_h, sweeps_h)):
         o.rank = int(r)
         o.sweeps = int(sw)
-        sel = torch.nonzero(keep[offs[i]:offs[i + 1]]).flatten()
-        o.U = Ua.index_select(1, sel)
-        o.V = Va.index_select(0, sel)
+        sel = K.compact_mask(ctx, keep[offs[i]:offs[i + 1]], 1, stream=stream)
+        o.U = K.gather_rows_cols(ctx, Ua, col_idx=sel, stream=stream)
+        o.V = K.gather_rows_cols(ctx, Va, row_idx=sel, stream=stream)
         o.kept = sel
         o.scores = keys[i]
     mark("unwhiten")
@@ -435,6 +435,34 @@ def compress_activation_only(ctx: K.Context, units: Sequence[UnitSpec], weights:
             K.activation_factors(ctx, W, o.vecs, o.rank, o.U, o.V, stream=stream)
     mark("factors")
     return Result(outs, {}, ranks, cut, used)
+
+
+def hybrid_ffn_split(ctx: K.Context, W_gate: torch.Tensor, W_up: torch.Tensor, X: torch.Tensor,
+                     gate_factors, up_factors, n_svd: int, stream=None):
+    """LASER's hybrid FFN channel selection for one FFN: the temporary factors (U, V) of gate
+    and up (e.g. ``unwhiten`` at a temporary rank) score every hidden channel by the error of
+    its pre-activation, d_j^T X d_j with d_j = (W - U V)[:, j], summed over gate and up; the
+    f - n_svd channels with the largest error stay dense (equal errors keep the lower index
+    dense) and the other n_svd are SVD-friendly.  Returns (svd_idx, dense_idx, errors, keys):
+    increasing int64 channel indices, the float64 summed errors and their float32 keys."""
+    dev = W_gate.device
+    f = int(W_gate.shape[1])
+    if not 0 <= n_svd <= f or int(W_up.shape[1]) != f:
+        raise ValueError("hybrid_ffn_split: n_svd must lie in [0, d_ffn] and gate/up must share d_ffn")
+    err = torch.zeros(f, dtype=torch.float64, device=dev)
+    keys = torch.empty(f, dtype=torch.float32, device=dev)
+    Ug, Vg = gate_factors
+    Uu, Vu = up_factors
+    K.channel_errors(ctx, W_gate, Ug, Vg, X, err, stream=stream)
+    K.channel_errors(ctx, W_up, Uu, Vu, X, err, keys=keys, stream=stream)
+    off = torch.tensor([0, f], dtype=torch.int64, device=dev)
+    cost = torch.ones(1, dtype=torch.int64, device=dev)
+    ranks = torch.empty(1, dtype=torch.int32, device=dev)
+    keep = torch.empty(f, dtype=torch.uint8, device=dev)
+    K.score_and_allocate_keys(ctx, keys, off, cost, f - n_svd, ranks, keep=keep, stream=stream)
+    dense = K.compact_mask(ctx, keep, 1, stream=stream)
+    svd = K.compact_mask(ctx, keep, 0, stream=stream)
+    return svd, dense, err, keys
 
 
 def _cumsum(xs):
