@@ -355,6 +355,63 @@ def select_svd_channels(errors: Sequence[np.ndarray], n_svd: int) -> np.ndarray:
     return np.sort(order[len(e) - n_svd:])
 
 
+def compress_hybrid_ffn(wl, r_temp: int, n_svd: int, pairs=None) -> Dict:
+    """[LASER] hybrid FFN over a workload: every other unit as in compress_workload; for each
+    (gate, up) pair, the temporary whitened SVD at rank r_temp scores the hidden channels
+    (channel_errors, summed over gate and up), the n_svd lowest-error channels form the
+    SVD-friendly set S and the rest stay dense.  The SVD branch is gate[:, S] and up[:, S],
+    each whitened with its unit's X and the block G[S, S] of its gradient factor and entered
+    into the global allocation; the dense channels cost d_model parameters each, per
+    projection, taken off the budget first.  ``pairs``: (gate, up) unit-index pairs (default:
+    the units named gate and up of each block)."""
+    from synth import recipes
+    if pairs is None:
+        pairs = []
+        for b in sorted({u.block for u in wl.units}):
+            idx = {u.name.split(".")[-1]: i for i, u in enumerate(wl.units) if u.block == b}
+            pairs.append((idx["gate"], idx["up"]))
+    ref = compress_workload(wl)
+    covs = ref["covs"]
+    units = ref["units"]
+    in_pair = {i for p in pairs for i in p}
+    entries = []          # (kind, unit index, UnitResult-like dict)
+    for i, ur in enumerate(units):
+        if i not in in_pair:
+            entries.append(("unit", i, ur))
+    splits = []
+    dense_cost = 0
+    for gi, ui in pairs:
+        errs = []
+        for i in (gi, ui):
+            ur = units[i]
+            U, V = unwhiten(ur.Sx, ur.Sg, ur.U_t, ur.sigma, ur.V_t, r_temp)
+            errs.append(channel_errors(recipes.gen_weight(wl, wl.units[i]), U, V, ur.X))
+        S = select_svd_channels(errs, n_svd)
+        f = units[gi].n
+        D = np.setdiff1d(np.arange(f), S)
+        splits.append({"gate": gi, "up": ui, "svd": S, "dense": D, "errors": errs[0] + errs[1]})
+        for i in (gi, ui):
+            ur = units[i]
+            dense_cost += ur.m * len(D)
+            if len(S) == 0:
+                continue
+            W = recipes.gen_weight(wl, wl.units[i]).astype(np.float64)[:, S]
+            G = ur.G[np.ix_(S, S)]
+            Sx, Sg = cholesky_factors(ur.X, G)
+            Wt = whiten(W, Sx, Sg)
+            Ut, sg, Vt = whitened_svd(Wt)
+            entries.append(("svd", i, UnitResult(ur.name + ".svd", ur.m, len(S), ur.X, G, Sx, Sg, Wt, Ut, sg, Vt)))
+    costs = [e[2].m + e[2].n for e in entries]
+    budget = wl.budget - dense_cost
+    alloc = allocate([e[2].sigma for e in entries], costs, max(budget, 0))
+    for e, k in zip(entries, alloc.ranks):
+        r = e[2]
+        r.rank = int(k)
+        r.U, r.V = unwhiten(r.Sx, r.Sg, r.U_t, r.sigma, r.V_t, r.rank)
+    return {"entries": entries, "splits": splits, "alloc": alloc, "budget": budget, "dense_cost": dense_cost,
+            "covs": covs}
+
+
 # ------------------------------------------------------------ whole workloads
 @dataclass
 class UnitResult:

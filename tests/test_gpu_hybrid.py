@@ -138,3 +138,50 @@ def test_hybrid_split_on_a_block(ctx):
         Uo, Vo = O.unwhiten(ur.Sx, ur.Sg, ur.U_t, ur.sigma, ur.V_t, r_t)
         own = own + O.channel_errors(recipes.gen_weight(wl, wl.units[names.index(nm)]), Uo, Vo, Xo)
     assert np.max(np.abs(got - own)) <= 1e-3 * own.max()
+
+
+def test_hybrid_flow_end_to_end(ctx):
+    """The whole hybrid FFN flow on a block: the split fed the GPU's keys is the oracle's split
+    of them; every entry's spectrum within 1e-3 sigma_max of the oracle's whitening of the same
+    columns (its G block taken at the GPU's SVD-friendly set); the allocation over the entries,
+    with the dense cost off the budget, bit-identical on the GPU's spectra; every entry's
+    factors at the whitened optimum within 1e-3."""
+    from synth import device
+    from vlm_compression_fac_b300 import pipeline
+    wl = recipes.mini_block(n_tokens=1000, seed=99)
+    units = pipeline.unit_specs(wl)
+    weights = device.weights_on_device(wl, torch)
+    acts = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "act"}
+    grads = {n: device.stream_on_device(wl, s, 0, wl.n_tokens, torch) for n, s in wl.sites.items() if s.kind == "grad"}
+    names = [u.name for u in wl.units]
+    gi, ui = names.index("gate"), names.index("up")
+    res = pipeline.compress_hybrid_ffn(ctx, units, weights, acts, grads, wl.n_tokens, wl.lam, wl.budget,
+                                       r_temp=64, n_svd=400, pairs=[(gi, ui)])
+    ctx.sync_status()
+    sp = res.splits[0]
+    S = sp["svd"].cpu().numpy()
+    np.testing.assert_array_equal(S, O.select_svd_channels([sp["keys"].cpu().numpy()], 400))
+    f = wl.units[gi].n
+    assert res.dense_cost == 2 * wl.units[gi].m * (f - 400) and res.budget == wl.budget - res.dense_cost
+    ref = O.compress_workload(wl)
+    sig = []
+    for e in res.entries:
+        r = ref["units"][e.unit]
+        u = wl.units[e.unit]
+        W = recipes.gen_weight(wl, u).astype(np.float64)
+        if e.kind == "svd":
+            W = W[:, S]
+            Sx, Sg = O.cholesky_factors(r.X, r.G[np.ix_(S, S)])
+        else:
+            Sx, Sg = r.Sx, r.Sg
+        so = np.sqrt(np.maximum(O.gram_eigenvalues(O.whiten(W, Sx, Sg)), 0.0))
+        sg = e.out.sigma.cpu().numpy()
+        assert np.max(np.abs(sg - so)) <= 1e-3 * so[0], (e.kind, u.name)
+        sig.append(sg)
+        k = int(e.out.rank)
+        err = O.whitened_error(W, e.out.U.cpu().numpy(), e.out.V.cpu().numpy(), Sx, Sg)
+        opt = float(np.sum(so[k:] ** 2))
+        assert abs(err - opt) <= 1e-3 * max(opt, 1e-6 * float(np.sum(so ** 2))), (e.kind, u.name, err, opt)
+    al = O.allocate(sig, [e.out.m + e.out.n for e in res.entries], res.budget, precision="f32")
+    np.testing.assert_array_equal(res.ranks.cpu().numpy(), al.ranks)
+    assert int(res.used.item()) == al.used <= res.budget

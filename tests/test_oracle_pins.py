@@ -505,3 +505,32 @@ def test_svd_friendly_channels_hand_case():
     np.testing.assert_array_equal(O.select_svd_channels([np.zeros(5)], 3), [2, 3, 4])
     np.testing.assert_array_equal(O.select_svd_channels([e], 0), [])
     np.testing.assert_array_equal(O.select_svd_channels([e], 5), [0, 1, 2, 3, 4])
+
+
+def test_hybrid_ffn_flow_accounting_and_limits():
+    """LASER hybrid FFN over a small block: the split covers every hidden channel once; the
+    dense channels' cost comes off the budget; with every channel SVD-friendly the SVD branch
+    is the ordinary gate/up whitened SVD (same spectra as the plain path); with none, gate and
+    up are dense and only the other units compete for what is left."""
+    from synth import recipes
+    wl = recipes.mini_block(n_tokens=300, d=64, ffn=96, kv=32, seed=5)
+    f = 96
+    out = O.compress_hybrid_ffn(wl, r_temp=8, n_svd=40)
+    sp = out["splits"][0]
+    assert sorted(np.concatenate([sp["svd"], sp["dense"]]).tolist()) == list(range(f))
+    assert len(sp["svd"]) == 40
+    assert out["dense_cost"] == 2 * 64 * (f - 40)
+    assert out["budget"] == wl.budget - out["dense_cost"]
+    used = sum(e[2].rank * (e[2].m + e[2].n) for e in out["entries"])
+    assert used == out["alloc"].used <= out["budget"]
+    # all channels SVD-friendly: the branch is the plain path's gate and up
+    full = O.compress_hybrid_ffn(wl, r_temp=8, n_svd=f)
+    plain = O.compress_workload(wl)
+    names = [u.name for u in wl.units]
+    for kind, i, r in full["entries"]:
+        if kind == "svd":
+            np.testing.assert_allclose(r.sigma, plain["units"][i].sigma, rtol=1e-10, atol=1e-12)
+    # no channel SVD-friendly: gate and up contribute no entry
+    none = O.compress_hybrid_ffn(wl, r_temp=8, n_svd=0)
+    assert all(kind == "unit" for kind, _, _ in none["entries"])
+    assert {names[i] for _, i, _ in none["entries"]} == set(names) - {"gate", "up"}

@@ -1,0 +1,101 @@
+"""The Python glue of the pipeline drivers, on CPU: every libkfsvd call is replaced for the
+test by a stand-in built from the fp64 oracle (tests/cpu_abi_standin.py), so what is checked
+is the bookkeeping around the calls (unit order, factor sharing, index sets, the budget and
+the dense cost, which factors are mapped back), against the oracle's own whole-workload
+flows.  The kernels themselves are checked on the GPU by the gpu-marked tests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from synth import recipes
+from tests import cpu_abi_standin as standin
+
+
+def _inputs(wl):
+    from vlm_compression_fac_b300 import pipeline
+    units = pipeline.unit_specs(wl)
+    weights = {}
+    for u in wl.units:
+        weights.setdefault(u.weight, torch.from_numpy(recipes.gen_full_weight(wl, u)))
+    acts = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
+            if s.kind == "act"}
+    grads = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
+             if s.kind == "grad"}
+    return units, weights, acts, grads
+
+
+def _small():
+    return recipes.mini_block(n_tokens=300, d=64, ffn=96, kv=32, seed=5)
+
+
+@pytest.mark.parametrize("heads", [False, True])
+def test_compress_glue(monkeypatch, heads):
+    from vlm_compression_fac_b300 import pipeline
+    ctx = standin.install(monkeypatch)
+    wl = recipes.mini_vlm(n_tokens=200) if heads else _small()
+    units, weights, acts, grads = _inputs(wl)
+    res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                            quant=wl.quant == "int8_token")
+    ref = O.compress_workload(wl)
+    sig = [u.sigma.numpy() for u in res.units]
+    for s_, r in zip(sig, ref["units"]):
+        np.testing.assert_allclose(s_, r.sigma, rtol=1e-5, atol=1e-7 * r.sigma[0])
+    al = O.allocate(sig, [u.m + u.n for u in wl.units], wl.budget, precision="f32")
+    np.testing.assert_array_equal(res.ranks.numpy(), al.ranks)
+    for g, r, u in zip(res.units, ref["units"], wl.units):
+        e = O.whitened_error(recipes.gen_weight(wl, u), g.U.numpy(), g.V.numpy(), r.Sx, r.Sg)
+        opt = float(np.sum(r.sigma[g.rank:] ** 2))
+        assert abs(e - opt) <= 1e-4 * max(opt, 1e-6 * float(np.sum(r.sigma ** 2))), u.name
+
+
+def test_hybrid_glue_matches_the_oracle_flow(monkeypatch):
+    from vlm_compression_fac_b300 import pipeline
+    ctx = standin.install(monkeypatch)
+    wl = _small()
+    units, weights, acts, grads = _inputs(wl)
+    names = [u.name for u in wl.units]
+    pair = (names.index("gate"), names.index("up"))
+    res = pipeline.compress_hybrid_ffn(ctx, units, weights, acts, grads, wl.n_tokens, wl.lam, wl.budget,
+                                       r_temp=8, n_svd=40, pairs=[pair])
+    ref = O.compress_hybrid_ffn(wl, r_temp=8, n_svd=40, pairs=[pair])
+    np.testing.assert_array_equal(res.splits[0]["svd"].numpy(), ref["splits"][0]["svd"])
+    np.testing.assert_array_equal(res.splits[0]["dense"].numpy(), ref["splits"][0]["dense"])
+    assert res.dense_cost == ref["dense_cost"] and res.budget == ref["budget"]
+    assert [(e.kind, e.unit) for e in res.entries] == [(k, i) for k, i, _ in ref["entries"]]
+    for e, (_, _, r) in zip(res.entries, ref["entries"]):
+        np.testing.assert_allclose(e.out.sigma.numpy(), r.sigma, rtol=1e-5, atol=1e-7 * r.sigma[0])
+    sig = [e.out.sigma.numpy() for e in res.entries]
+    al = O.allocate(sig, [e.out.m + e.out.n for e in res.entries], ref["budget"], precision="f32")
+    np.testing.assert_array_equal(res.ranks.numpy(), al.ranks)
+    assert int(res.used.item()) == al.used <= res.budget
+    # the SVD-branch factors reproduce the selected columns' optimum
+    for e, (_, _, r) in zip(res.entries, ref["entries"]):
+        if e.kind != "svd":
+            continue
+        W = recipes.gen_weight(wl, wl.units[e.unit])[:, e.svd_idx.numpy()]
+        err = O.whitened_error(W, e.out.U.numpy(), e.out.V.numpy(), r.Sx, r.Sg)
+        opt = float(np.sum(r.sigma[e.out.rank:] ** 2))
+        assert abs(err - opt) <= 1e-4 * max(opt, 1e-6 * float(np.sum(r.sigma ** 2)))
+
+
+def test_fisher_and_activation_only_glue(monkeypatch):
+    from vlm_compression_fac_b300 import pipeline
+    ctx = standin.install(monkeypatch)
+    wl = _small()
+    units, weights, acts, grads = _inputs(wl)
+    res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                            score="empirical_fisher")
+    keys = [g.scores.numpy() for g in res.units]
+    al = O.allocate_keys(keys, [u.m + u.n for u in wl.units], wl.budget)
+    np.testing.assert_array_equal(res.ranks.numpy(), al.ranks)
+    n_keep = int(al.ranks.sum())
+    for ui, g in enumerate(res.units):
+        want = np.sort(al.order_comp[:n_keep][al.order_unit[:n_keep] == ui])
+        np.testing.assert_array_equal(g.kept.numpy(), want)
+        assert g.U.shape == (g.m, len(want)) and g.V.shape == (len(want), g.n)
+    act = pipeline.compress_activation_only(ctx, units, weights, acts, wl.n_tokens, wl.budget)
+    ref = O.compress_workload_activation_only(wl)
+    np.testing.assert_array_equal(act.ranks.numpy(), ref["alloc"].ranks)
+    for g, r in zip(act.units, ref["units"]):
+        np.testing.assert_allclose(g.U.numpy() @ g.V.numpy(), r["U"] @ r["Vt"], atol=1e-5)

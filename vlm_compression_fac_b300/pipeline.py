@@ -465,6 +465,120 @@ def hybrid_ffn_split(ctx: K.Context, W_gate: torch.Tensor, W_up: torch.Tensor, X
     return svd, dense, err, keys
 
 
+@dataclass
+class HybridEntry:
+    kind: str            # "unit": an ordinary unit; "svd": the SVD-friendly columns of a gate/up unit
+    unit: int            # index into the caller's units
+    out: UnitOut         # spectrum, rank and factors (for "svd": of W[:, svd_idx])
+    svd_idx: Optional[torch.Tensor] = None
+
+
+@dataclass
+class HybridResult:
+    entries: List[HybridEntry]
+    splits: List[dict]   # per (gate, up) pair: "svd" and "dense" channel indices, "errors", "keys"
+    ranks: torch.Tensor  # per entry
+    cut: torch.Tensor
+    used: torch.Tensor
+    budget: int          # the budget left for the low-rank factors after the dense channels
+    dense_cost: int
+
+
+def compress_hybrid_ffn(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch.Tensor],
+                        acts, grads, n_tokens: int, lam: float, budget: int, r_temp: int, n_svd: int,
+                        pairs: Sequence[Sequence[int]], quant: bool = False, tol: float = 1e-6, max_sweeps: int = 30,
+                        stream=None, site_dims: Optional[Dict[str, int]] = None,
+                        act_sites: Optional[Sequence[str]] = None, chunk_tokens: int = 16384) -> HybridResult:
+    """LASER's hybrid FFN inside the global allocation.  Steps 1-4 for every unit; for each
+    (gate, up) pair of unit indices, the temporary factors at rank ``r_temp`` score the hidden
+    channels (hybrid_ffn_split) and the ``n_svd`` SVD-friendly columns of gate and up are
+    whitened again with their block G[S, S] of the gradient factor (gathered by index) and
+    take part in the global allocation as units of their own; the other columns stay dense and
+    their cost (d_model per channel and projection) is taken off the budget first.  Every
+    other unit is allocated as usual; all entries are mapped back with ``unwhiten``."""
+    keep = sorted({units[i].x_site for p in pairs for i in p} | {units[i].g_site for p in pairs for i in p})
+    base = compress(ctx, units, weights, acts, grads, n_tokens, lam=lam, budget=None, quant=quant, tol=tol,
+                    max_sweeps=max_sweeps, stream=stream, site_dims=site_dims, act_sites=act_sites,
+                    chunk_tokens=chunk_tokens, keep_covs=keep, defer_allocation=True)
+    outs = base.units
+    dev = outs[0].sigma.device
+
+    def wview(u: UnitSpec) -> torch.Tensor:
+        return weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
+
+    in_pair = {i for p in pairs for i in p}
+    entries = [HybridEntry("unit", i, outs[i]) for i in range(len(units)) if i not in in_pair]
+    w_of = {id(e.out): wview(units[e.unit]) for e in entries}
+    splits = []
+    dense_cost = 0
+    new_svd: List[HybridEntry] = []
+    for gi, ui in pairs:
+        facs = {}
+        for i in (gi, ui):
+            o, u = outs[i], units[i]
+            U = torch.empty((u.m, max(r_temp, 1)), dtype=torch.float32, device=dev)[:, :r_temp]
+            V = torch.empty((max(r_temp, 1), u.n), dtype=torch.float32, device=dev)[:r_temp]
+            if r_temp > 0:
+                K.unwhiten(ctx, wview(u), o.Sx, o.Sg, o.Sinv, o.sigma, o.vecs, r_temp, U, V, stream=stream)
+            facs[i] = (U, V) if r_temp > 0 else (None, None)
+        ug = units[gi]
+        X = base.covs[ug.x_site][ug.x_off:ug.x_off + ug.m, ug.x_off:ug.x_off + ug.m]
+        svd, dense, err, keys = hybrid_ffn_split(ctx, wview(ug), wview(units[ui]), X, facs[gi], facs[ui], n_svd,
+                                                 stream=stream)
+        splits.append({"gate": gi, "up": ui, "svd": svd, "dense": dense, "errors": err, "keys": keys})
+        for i in (gi, ui):
+            u = units[i]
+            dense_cost += u.m * int(dense.numel())
+            k = int(svd.numel())
+            if k == 0:
+                continue
+            Xi = base.covs[u.x_site][u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m]
+            Gi = base.covs[u.g_site][u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n]
+            W_S = K.gather_rows_cols(ctx, wview(u), col_idx=svd, stream=stream)
+            G_S = K.gather_rows_cols(ctx, Gi, row_idx=svd, col_idx=svd, stream=stream)
+            s_ = min(u.m, k)
+            Sx = torch.empty((u.m, u.m), dtype=torch.float32, device=dev)
+            Sg = torch.empty((k, k), dtype=torch.float32, device=dev)
+            Sinv = torch.empty((s_, s_), dtype=torch.float32, device=dev)
+            Wt = torch.empty((u.m, k), dtype=torch.float32, device=dev)
+            K.whiten(ctx, Xi, G_S, W_S, Sx, Sg, Sinv, Wt, stream=stream)
+            e = HybridEntry("svd", i, UnitOut(u.name + ".svd", u.m, k, K.kf_gram_side(u.m, k), Sx, Sg, Sinv, Wt),
+                            svd_idx=svd)
+            w_of[id(e.out)] = W_S
+            new_svd.append(e)
+    by_s: Dict[int, List[HybridEntry]] = {}
+    for e in new_svd:
+        by_s.setdefault(min(e.out.m, e.out.n), []).append(e)
+    for s_, grp in by_s.items():
+        for e in grp:
+            e.out.sigma = torch.empty(s_, dtype=torch.float32, device=dev)
+            e.out.vecs = torch.empty((s_, s_), dtype=torch.float32, device=dev)
+        sw = torch.zeros(len(grp), dtype=torch.int32, device=dev)
+        K.whitened_svd(ctx, [e.out.Wt for e in grp], [e.out.sigma for e in grp], [e.out.vecs for e in grp],
+                       sweeps=sw, tol=tol, max_sweeps=max_sweeps, stream=stream)
+        for e, v in zip(grp, sw.cpu().tolist()):
+            e.out.sweeps = int(v)
+    entries += new_svd
+
+    lens = [min(e.out.m, e.out.n) for e in entries]
+    sig = torch.cat([e.out.sigma for e in entries])
+    off = torch.tensor([0] + list(_cumsum(lens)), dtype=torch.int64, device=dev)
+    cost = torch.tensor([e.out.m + e.out.n for e in entries], dtype=torch.int64, device=dev)
+    ranks = torch.empty(len(entries), dtype=torch.int32, device=dev)
+    cut = torch.empty(2, dtype=torch.float32, device=dev)
+    used = torch.zeros(1, dtype=torch.int64, device=dev)
+    left = max(int(budget) - dense_cost, 0)
+    K.score_and_allocate(ctx, sig, off, cost, left, ranks, cut=cut, used=used, stream=stream)
+    for e, r in zip(entries, ranks.cpu().tolist()):
+        o = e.out
+        o.rank = int(r)
+        o.U = torch.empty((o.m, max(o.rank, 1)), dtype=torch.float32, device=dev)[:, :o.rank]
+        o.V = torch.empty((max(o.rank, 1), o.n), dtype=torch.float32, device=dev)[:o.rank]
+        if o.rank > 0:
+            K.unwhiten(ctx, w_of[id(o)], o.Sx, o.Sg, o.Sinv, o.sigma, o.vecs, o.rank, o.U, o.V, stream=stream)
+    return HybridResult(entries, splits, ranks, cut, used, left, dense_cost)
+
+
 def _cumsum(xs):
     t = 0
     for x in xs:
