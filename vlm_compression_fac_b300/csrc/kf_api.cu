@@ -204,8 +204,9 @@ kf_status kf_finalize_covariance(kf_ctx* ctx, float* cov, int64_t ldc, int64_t d
                                  kf_stream_t stream) {
   KF_TRY(need(ctx && cov, "kf_finalize_covariance: null pointer"));
   KF_TRY(need(d > 0 && ldc >= d && n_tokens > 0 && lambda >= 0.f, "kf_finalize_covariance: sizes"));
-  static unsigned slot = 0;
-  float* scratch = reinterpret_cast<float*>(reinterpret_cast<char*>(ctx->d_status) + 64) + (slot++ % FINAL_SLOTS);
+  static std::atomic<unsigned> slot{0};
+  float* scratch =
+      reinterpret_cast<float*>(reinterpret_cast<char*>(ctx->d_status) + 64) + (slot.fetch_add(1) % FINAL_SLOTS);
   return launch_finalize(cov, ldc, d, n_tokens, lambda, scratch, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -432,12 +432,11 @@ int64_t count_tiles(const TcGemm& g, int64_t ntm, int64_t ntn) {
 
 template <bool AM, bool BM_>
 kf_status launch_tc(const TcMaps& maps, const TcArgs& a, int64_t ntiles, cudaStream_t st) {
-  static bool attr_set = false;  // per instantiation; benign race (idempotent)
-  if (!attr_set) {
-    KF_CUDA(cudaFuncSetAttribute(tc_gemm_kernel<AM, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(SMEM_BYTES)));
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per instantiation and device
+  KF_TRY(set_attr_once(attr_done, [] {
+    return check_cuda(cudaFuncSetAttribute(tc_gemm_kernel<AM, BM_>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(SMEM_BYTES)), "tc_gemm smem attribute");
+  }));
   tc_gemm_kernel<AM, BM_><<<unsigned(ntiles), 320, SMEM_BYTES, st>>>(maps, a); note_launch();
   return check_cuda(cudaGetLastError(), "tc_gemm launch");
 }

@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <atomic>
 #include <string>
 #include <vector>
 
@@ -63,6 +64,20 @@ kf_status check_cuda(cudaError_t e, const char* what);
     if (_s != KF_OK) return _s;             \
   } while (0)
 #define KF_CUDA(expr) KF_TRY(::kf::check_cuda((expr), #expr))
+
+// A kernel's large shared-memory opt-in is an attribute per device: `done` records, for each
+// device below 64, that `set()` has succeeded there; it is called on the current device until
+// then (devices from 64 up: on every call).  Concurrent first calls both set it (idempotent).
+template <typename F>
+kf_status set_attr_once(std::atomic<unsigned long long>& done, F&& set) {
+  int dev = 0;
+  KF_CUDA(cudaGetDevice(&dev));
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return KF_OK;
+  KF_TRY(set());
+  if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return KF_OK;
+}
 
 // Bump allocator over a caller workspace (256-byte aligned slices).
 struct Carve {

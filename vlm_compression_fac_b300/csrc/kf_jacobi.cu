@@ -992,11 +992,11 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   const int64_t total_tasks = int64_t(per_u) * nu;
   if (total_tasks > 0x7fffffff) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: too many Jacobi tasks");
   const int apply_grid = int(total_tasks < int64_t(ctx->sm_count) * 2 ? total_tasks : int64_t(ctx->sm_count) * 2);
-  static bool attr = false;
-  if (!attr) {
-    KF_CUDA(cudaFuncSetAttribute(jac_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(apply_smem)));
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  KF_TRY(set_attr_once(attr_done, [&] {
+    return check_cuda(cudaFuncSetAttribute(jac_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(apply_smem)), "jac_apply smem attribute");
+  }));
   const int max_inner = KF_JAC_MAX_INNER;
   int sweeps_run = 0;
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[1], st));
@@ -1045,13 +1045,13 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   if (sort_smem > 227 * 1024) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: s too large for the in-CTA sort");
   const size_t eig_smem = size_t(2) * RW * (RW + 1) * sizeof(float);
   const size_t rot_smem = size_t(RW * RW + RW * 64) * sizeof(float);
-  static bool sattr = false;
-  if (!sattr) {
+  static std::atomic<unsigned long long> sattr_done{0};
+  KF_TRY(set_attr_once(sattr_done, [&]() -> kf_status {
     KF_CUDA(cudaFuncSetAttribute(sort_desc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024));
     KF_CUDA(cudaFuncSetAttribute(win_eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(eig_smem)));
     KF_CUDA(cudaFuncSetAttribute(win_rotate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(rot_smem)));
-    sattr = true;
-  }
+    return KF_OK;
+  }));
   const int64_t lyM = bf.lyM, R = bf.R;
   const int nwin = bf.nwin;
   KF_CUDA(cudaMemsetAsync(bf.Y, 0, sizeof(float) * size_t(nu) * s * lyM, st));
