@@ -226,7 +226,8 @@ KF_API kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_prob
  *
  * sigma:      device, the units' spectra concatenated; unit u owns
  *             sigma[seg_offset[u] .. seg_offset[u+1]) in descending order.
- * seg_offset: device int64[n_units + 1]; cost: device int64[n_units] (m_u + n_u).
+ * seg_offset: device int64[n_units + 1]; cost: device int64[n_units] (m_u + n_u; every cost
+ *             must be >= 0, so that the kept components form a prefix of the sorted list).
  * mode:       KF_KEY_HALF_SIGMA2: key 0.5f * (sigma * sigma);
  *             KF_KEY_PER_PARAM:  that divided by (float)cost[u];
  *             KF_KEY_ENERGY_RATIO: (sigma * sigma) / (sum of the unit's sigma^2);

@@ -260,12 +260,11 @@ __global__ void __launch_bounds__(SCAN_T) scan_i64_kernel(long long* __restrict_
   }
 }
 
-// Per item: inclusive prefix; items within budget are kept (kcount = max kept index + 1).
+// Per item: the inclusive prefix sum of the costs in sorted order.
 __global__ void __launch_bounds__(SCAN_T) cut_kernel(const unsigned long long* __restrict__ keys,
                                                      const int64_t* __restrict__ off, const int64_t* __restrict__ cost,
                                                      int n_units, int64_t n, const long long* __restrict__ bexcl,
-                                                     long long budget, long long* __restrict__ prefix,
-                                                     unsigned long long* __restrict__ kcount) {
+                                                     long long* __restrict__ prefix) {
   __shared__ long long ws[32];
   const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
   long long c = 0;
@@ -290,17 +289,44 @@ __global__ void __launch_bounds__(SCAN_T) cut_kernel(const unsigned long long* _
   }
   __syncthreads();
   const long long incl = x + (w > 0 ? ws[w - 1] : 0) + bexcl[blockIdx.x];
-  if (i < n) {
-    prefix[i] = incl;
-    if (incl <= budget) atomicMax(kcount, static_cast<unsigned long long>(i + 1));
-  }
+  if (i < n) prefix[i] = incl;
 }
 
+// kcount = the length of the kept prefix: the largest k with prefix[k - 1] <= budget.  The
+// costs are non-negative, so the prefix sums never decrease and a binary search finds it
+// (one thread, about log2(n) reads).
+__global__ void kcount_kernel(const long long* __restrict__ prefix, int64_t n, long long budget,
+                              unsigned long long* __restrict__ kcount) {
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo + 1) / 2;
+    if (prefix[mid - 1] <= budget) lo = mid; else hi = mid - 1;
+  }
+  *kcount = static_cast<unsigned long long>(lo);
+}
+
+// ranks[u] += the kept components of unit u.  With at most RANKS_SMEM_UNITS units each
+// block counts in shared memory and adds its nonzero counts once; beyond that, one global
+// atomic per component.
+constexpr int RANKS_SMEM_UNITS = 8192;
 __global__ void ranks_kernel(const unsigned long long* __restrict__ keys, const int64_t* __restrict__ off,
                              int n_units, const unsigned long long* __restrict__ kcount, int* __restrict__ ranks) {
+  extern __shared__ int rcount[];
+  const bool local = n_units <= RANKS_SMEM_UNITS;  // uniform over the grid
+  if (local) {
+    for (int u = threadIdx.x; u < n_units; u += blockDim.x) rcount[u] = 0;
+    __syncthreads();
+  }
   const int64_t k = int64_t(*kcount);
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x)
-    atomicAdd(&ranks[unit_of(off, n_units, int64_t(uint32_t(keys[i])))], 1);
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x) {
+    const int u = unit_of(off, n_units, int64_t(uint32_t(keys[i])));
+    if (local) atomicAdd(&rcount[u], 1); else atomicAdd(&ranks[u], 1);
+  }
+  if (local) {
+    __syncthreads();
+    for (int u = threadIdx.x; u < n_units; u += blockDim.x)
+      if (rcount[u]) atomicAdd(&ranks[u], rcount[u]);
+  }
 }
 
 // keep[id] = 1 for the components of the kept prefix (the mask was cleared before).
@@ -442,10 +468,12 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   KF_CUDA(cudaGetLastError());
   scan_i64_kernel<<<1, SCAN_T, 0, st>>>(b.bsum, nb); note_launch();
   KF_CUDA(cudaGetLastError());
-  KF_CUDA(cudaMemsetAsync(b.kcount, 0, sizeof(unsigned long long), st));
-  cut_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, budget, b.prefix, b.kcount); note_launch();
+  cut_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, b.prefix); note_launch();
   KF_CUDA(cudaGetLastError());
-  ranks_kernel<<<grid_cap(n, 256), 256, 0, st>>>(src, off, n_units, b.kcount, ranks); note_launch();
+  kcount_kernel<<<1, 1, 0, st>>>(b.prefix, n, budget, b.kcount); note_launch();
+  KF_CUDA(cudaGetLastError());
+  const size_t rsmem = n_units <= RANKS_SMEM_UNITS ? sizeof(int) * size_t(n_units > 0 ? n_units : 1) : 0;
+  ranks_kernel<<<grid_cap(n, 256), 256, rsmem, st>>>(src, off, n_units, b.kcount, ranks); note_launch();
   KF_CUDA(cudaGetLastError());
   if (keep) {
     KF_CUDA(cudaMemsetAsync(keep, 0, size_t(n), st));
