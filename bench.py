@@ -390,6 +390,7 @@ def run_kfsvd(args):
         "phases_ms": {k: round(v / K_, 3) for k, v in phases.items()},
         "svd_profile": svd_prof, "ranks": [int(x) for x in res.ranks.cpu().tolist()],
         "jacobi_sweeps": [int(u.sweeps) for u in res.units],
+        "units_larger_than_dense": res.larger_than_dense(),
         "roofline": roof, "kernels": kern, "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
         "cpu_baseline": cpu,
     }

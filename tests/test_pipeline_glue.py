@@ -99,3 +99,19 @@ def test_fisher_and_activation_only_glue(monkeypatch):
     np.testing.assert_array_equal(act.ranks.numpy(), ref["alloc"].ranks)
     for g, r in zip(act.units, ref["units"]):
         np.testing.assert_allclose(g.U.numpy() @ g.V.numpy(), r["U"] @ r["Vt"], atol=1e-5)
+
+
+def test_units_larger_than_dense_are_reported(monkeypatch):
+    """A generous budget lets the allocation keep more than a unit's dense size,
+    r (m + n) > m n; the result names those units."""
+    from vlm_compression_fac_b300 import pipeline
+    ctx = standin.install(monkeypatch)
+    wl = _small()
+    units, weights, acts, grads = _inputs(wl)
+    total = sum(u.m * u.n for u in wl.units)
+    res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=2 * total)
+    big = res.larger_than_dense()
+    want = [u.name for u, r in zip(wl.units, res.ranks.tolist()) if r * (u.m + u.n) > u.m * u.n]
+    assert big == want and len(big) > 0
+    res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget // 4)
+    assert res.larger_than_dense() == []

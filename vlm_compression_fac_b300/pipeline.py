@@ -75,6 +75,11 @@ class Result:
     used: torch.Tensor
     timings: Dict[str, float] = field(default_factory=dict)
 
+    def larger_than_dense(self) -> List[str]:
+        """Units whose kept factors hold more parameters than the dense weight, r (m + n) > m n.
+        The allocation allows this (there is no dense fallback in the path); it is reported."""
+        return [u.name for u in self.units if int(u.rank) * (u.m + u.n) > u.m * u.n]
+
 
 RowsFn = Callable[[str, int, int], torch.Tensor]
 
