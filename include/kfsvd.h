@@ -232,9 +232,11 @@ KF_API kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_prob
  *             KF_KEY_PER_PARAM:  that divided by (float)cost[u];
  *             KF_KEY_ENERGY_RATIO: (sigma * sigma) / (sum of the unit's sigma^2);
  *             KF_FIXED_RANK:     ranks[u] = min(fixed_rank[u], length of unit u).
- * The keys are sorted descending (ties: lower unit, then lower component index first) by
- * a device LSD radix sort on 64-bit (~key_bits << 32 | component id) words; the prefix
- * sum of costs in that order is cut at the longest prefix with sum <= budget.
+ * The keys are sorted descending (ties: lower unit, then lower component index first): the
+ * 64-bit words (~key_bits << 32 | component id) are built in id order and sorted by a stable
+ * device LSD radix sort over the score word (four 8-bit passes), which leaves equal scores in
+ * id order; the prefix sum of costs in that order is cut at the longest prefix with
+ * sum <= budget.
  * ranks:      device int32[n_units] out: kept components per unit.
  * cut:        device float[2] out (may be NULL): score of the last kept and of the first
  *             dropped component (NaN where there is none).
