@@ -124,3 +124,86 @@ def test_a_rank_failing_before_the_exchange_is_seen_by_its_peer():
     got = _run(2, [16, 8, 24], 7, fail_rank=1)
     assert got[1][0] == "error" and "planted failure" in got[1][1]
     assert got[0][0] == "error"   # the all-gather ended with an error instead of waiting forever
+
+
+def _sharded_worker(rank, world, port, out_q):
+    import datetime
+    import torch
+    import torch.distributed as dist
+    from synth import recipes
+    from tests import cpu_abi_standin as standin
+    from vlm_compression_fac_b300 import kfsvd, pipeline
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
+    try:
+        for name in standin.NAMES:            # this process only: the library calls run on the oracle
+            setattr(kfsvd, name, getattr(standin, name))
+        ctx = standin._Ctx()
+        wl = recipes.mini_block(n_tokens=300, d=64, ffn=96, kv=32, seed=5)
+        units = pipeline.unit_specs(wl)
+        weights = {}
+        for u in wl.units:
+            weights.setdefault(u.weight, torch.from_numpy(recipes.gen_full_weight(wl, u)))
+        acts = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
+                if s.kind == "act"}
+        grads = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
+                 if s.kind == "grad"}
+        mine, outs, ranks, cut, used = shard.compress_sharded(ctx, units, weights, acts, grads, wl.n_tokens,
+                                                              wl.lam, wl.budget)
+        prods = {i: (o.U @ o.V).numpy().tobytes() for i, o in zip(mine, outs)}
+        out_q.put((rank, "ok", (list(mine), ranks.numpy().tolist(), int(used.item()), prods)))
+    except Exception as e:
+        out_q.put((rank, "error", repr(e)))
+    finally:
+        try:
+            dist.destroy_process_group()
+        except Exception:
+            pass
+
+
+def test_compress_sharded_matches_one_process(monkeypatch):
+    """The sharded driver over two gloo ranks, with the library calls replaced by the oracle
+    stand-in in each rank: the ranks agree on the allocation, every unit is mapped back by
+    exactly one rank, and the result equals the single-process pipeline's."""
+    import torch
+    from synth import recipes
+    from tests import cpu_abi_standin as standin
+    from vlm_compression_fac_b300 import pipeline
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_sharded_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(2):
+        rank, status, payload = q.get(timeout=300)
+        got[rank] = (status, payload)
+    for p in procs:
+        p.join(timeout=60)
+        if p.is_alive():
+            p.kill()
+    for r in range(2):
+        assert got[r][0] == "ok", got[r][1]
+    (m0, r0, u0, p0), (m1, r1, u1, p1) = got[0][1], got[1][1]
+    assert r0 == r1 and u0 == u1
+    assert sorted(m0 + m1) == list(range(7)) and not set(m0) & set(m1)
+    # the same workload in one process
+    c = standin.install(monkeypatch)
+    wl = recipes.mini_block(n_tokens=300, d=64, ffn=96, kv=32, seed=5)
+    units = pipeline.unit_specs(wl)
+    weights = {}
+    for u in wl.units:
+        weights.setdefault(u.weight, torch.from_numpy(recipes.gen_full_weight(wl, u)))
+    acts = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
+            if s.kind == "act"}
+    grads = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
+             if s.kind == "grad"}
+    res = pipeline.compress(c, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget)
+    assert res.ranks.tolist() == r0 and int(res.used.item()) == u0
+    prods = dict(p0)
+    prods.update(p1)
+    for i, o in enumerate(res.units):
+        np.testing.assert_array_equal(np.frombuffer(prods[i], dtype=np.float32).reshape(o.m, o.n),
+                                      (o.U @ o.V).numpy())
