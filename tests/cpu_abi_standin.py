@@ -104,21 +104,22 @@ def score_and_allocate_keys(ctx, keys, seg_offset, cost, budget, ranks, keep=Non
 
 
 def unwhiten(ctx, W, Sx, Sg, Sinv, sigma, vecs, r, U, V, workspace=None, stream=None):
+    # Like the library, reads only the Gram-side factor and its inverse (the other factor may
+    # have been released): right side U = W S_g V~_r, V = V~_r^T S_g^-1; left side
+    # U = S_x^-1 U~_r Sigma_r, V = Sigma_r^-1 U~_r^T S_x W.
     if r == 0:
         return
     m, n = W.shape
     Wd = _np(W)
-    sx, sg = _np(Sx), _np(Sg)
-    Wt = O.whiten(Wd, sx, sg)
     s = _np(sigma)[:r]
     Q = _np(vecs)[:, :r]
-    if kf_gram_side(m, n) == 0:          # Q = right singular vectors of W~
-        Ut = Wt @ Q / s[None, :]
-        Vt = Q
-    else:                                # Q = left singular vectors
-        Ut = Q
-        Vt = Wt.T @ Q / s[None, :]
-    u_, v_ = O.unwhiten(sx, sg, Ut, s, Vt, r)
+    inv = _np(Sinv)
+    if kf_gram_side(m, n) == 0:
+        sg = _np(Sg)
+        u_, v_ = Wd @ sg @ Q, Q.T @ inv
+    else:
+        sx = _np(Sx)
+        u_, v_ = inv @ (Q * s[None, :]), (Q.T @ sx @ Wd) / s[:, None]
     _put(U, u_)
     _put(V, v_)
 

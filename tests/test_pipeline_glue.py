@@ -115,3 +115,35 @@ def test_units_larger_than_dense_are_reported(monkeypatch):
     assert big == want and len(big) > 0
     res = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget // 4)
     assert res.larger_than_dense() == []
+
+
+@pytest.mark.parametrize("score", [None, "empirical_fisher"])
+def test_streamed_groups_match_resident_rows(monkeypatch, score):
+    """Rows produced on demand in uneven token chunks, units processed block by block with the
+    covariances released after each block, quantised activation sites: the same spectra,
+    ranks and factors as with every site's rows resident and one group."""
+    from vlm_compression_fac_b300 import pipeline
+    ctx = standin.install(monkeypatch)
+    wl = recipes.decoder_blocks(2, 64, 96, 32, 250, 0.4, 17, "two_blocks", quant="int8_token")
+    units, weights, acts, grads = _inputs(wl)
+    one = pipeline.compress(ctx, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                            quant=True, score=score)
+
+    def rows(name, t0, t1):
+        return torch.from_numpy(recipes.gen_stream(wl, wl.sites[name], t0, t1))
+
+    blocks = sorted({u.block for u in wl.units})
+    groups = [[i for i, u in enumerate(wl.units) if u.block == b] for b in blocks]
+    streamed = pipeline.compress(ctx, units, weights, rows, None, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                                 quant=True, score=score, site_dims={n: s.d for n, s in wl.sites.items()},
+                                 act_sites=[n for n, s in wl.sites.items() if s.kind == "act"], groups=groups,
+                                 chunk_tokens=97, keep_covs=False, keep_whitened=False)
+    # the covariances are held in float32 between chunks (as in the library), so chunking moves
+    # the sums by float32 roundings: compare against sigma_max and max |U V|
+    assert streamed.ranks.tolist() == one.ranks.tolist()
+    for a, b in zip(streamed.units, one.units):
+        sb = b.sigma.numpy()
+        np.testing.assert_allclose(a.sigma.numpy(), sb, rtol=0, atol=1e-5 * sb[0])
+        pb = (b.U @ b.V).numpy()
+        np.testing.assert_allclose((a.U @ a.V).numpy(), pb, rtol=0, atol=1e-4 * np.abs(pb).max())
+    assert streamed.covs == {}
