@@ -64,3 +64,32 @@ def test_invalid_arguments_fail_before_any_launch():
         assert st in (K.KF_ERR_CUDA, K.KF_ERR_UNSUPPORTED, K.KF_ERR_INVALID)
     else:
         L.kf_destroy(h)
+
+
+def test_every_compute_call_rejects_a_null_context():
+    """Each entry point's argument check runs on the host before any CUDA call: with a null
+    context every compute call returns KF_ERR_INVALID and names itself in kf_last_error."""
+    from vlm_compression_fac_b300 import kfsvd as K
+    L = K.lib()
+    calls = {
+        "fake_quant_rows": (None, None, 0, 4, 8, 8, None, None),
+        "whiten": (None,) + (None, 8, 8, None, 8, 8, None, 0, 8, 0, None, 8, None, 8, None, 8, None, 8, None, 0, None),
+        "whitened_svd": (None, 1, None, 1e-6, 30, None, 0, None),
+        "score_and_allocate_weighted": (None, None, None, None, 1, 0, 0, 3, None, None, None, None, None, 0, None),
+        "score_and_allocate_keys": (None, None, None, None, 1, 0, 0, None, None, None, None, None, 0, None),
+        "empirical_fisher_accumulate": (None, None, 0, 8, None, 0, 8, 4, 8, 8, None, 8, None, 8, 8, None, None, 0,
+                                        None),
+        "unwhiten": (None, None, 0, 8, 8, 8, None, 8, None, 8, None, 8, None, None, 8, 1, None, 1, None, 8, None, 0,
+                     None),
+        "activation_covariance": (None, None, 8, 8, None, 0, 8, 8, None, 8, None, 0, None),
+        "activation_eig": (None, 1, None, 1e-6, 30, None, 0, None),
+        "activation_factors": (None, None, 0, 8, 8, 8, None, 8, 1, None, 1, None, 8, None, 0, None),
+        "channel_errors": (None, None, 0, 8, 8, 8, None, 1, None, 8, 1, None, 8, None, None, None, 0, None),
+        "gather_rows_cols": (None, None, 0, 8, 8, 8, None, 1, None, 1, None, 1, None),
+        "compact_mask": (None, None, 4, 1, None, None, None),
+    }
+    for name, args in calls.items():
+        st = getattr(L, name)(*args)
+        assert st == K.KF_ERR_INVALID, name
+        msg = L.kf_last_error()
+        assert name.encode() in msg and b"null context" in msg, (name, msg)
