@@ -197,3 +197,33 @@ def test_llama7b_block_activation_only_fullsize(ctx):
             assert np.all(resid <= 1e-3 * lam[0]), (g.name, float(resid.max() / lam[0]))
             opt = trC - float(np.sum(lam))
         assert abs(loss - opt) <= 1e-3 * max(opt, 1e-3 * trC), (g.name, loss, opt)
+
+
+def test_activation_only_streamed_blocks(ctx):
+    """The route with rows generated on demand in token chunks and the units processed block by
+    block (two decoder blocks, INT8 fake-quantised activations): the same checks as the
+    resident case against the oracle."""
+    from synth import device
+    from vlm_compression_fac_b300 import pipeline
+    wl = recipes.decoder_blocks(2, 256, 328, 128, 900, 0.4, 31, "two_blocks_qaw", quant="int8_token")
+    units = pipeline.unit_specs(wl)
+    weights = device.weights_on_device(wl, torch)
+    blocks = sorted({u.block for u in wl.units})
+    groups = [[i for i, u in enumerate(wl.units) if u.block == b] for b in blocks]
+    res = pipeline.compress_activation_only(ctx, units, weights, device.rows_fn(wl, torch), wl.n_tokens, wl.budget,
+                                            quant=True, site_dims={n: s.d for n, s in wl.sites.items()},
+                                            groups=groups, chunk_tokens=256)
+    ctx.sync_status()
+    ref = O.compress_workload_activation_only(wl)
+    sig_g = [g.sigma.cpu().numpy() for g in res.units]
+    for g, r, sg in zip(res.units, ref["units"], sig_g):
+        assert np.max(np.abs(sg - r["sigma"])) <= 1e-3 * r["sigma"][0], g.name
+    costs = [u.m + u.n for u in wl.units]
+    al = O.allocate([s[:min(u.m, u.n)] for s, u in zip(sig_g, wl.units)], costs, wl.budget, precision="f32")
+    np.testing.assert_array_equal(res.ranks.cpu().numpy(), al.ranks)
+    for g, r, u in zip(res.units, ref["units"], wl.units):
+        A = O.fake_quant_int8_token(recipes.gen_stream(wl, wl.sites[u.x_site], 0, wl.n_tokens))
+        loss = O.activation_loss(A[:, u.x_off:u.x_off + u.m], r["W"], g.U.cpu().numpy(), g.V.cpu().numpy())
+        opt = float(np.sum(r["sigma"][g.rank:] ** 2))
+        tot = float(np.sum(r["sigma"] ** 2))
+        assert abs(loss - opt) <= 1e-3 * max(opt, 1e-3 * tot), (g.name, loss, opt)
