@@ -329,6 +329,11 @@ KF_API kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t 
  * tensor cores with U and V split into hi + lo bfloat16 planes (about 3e-5 relative per
  * projection); the squares and sums are float64, in a fixed order (deterministic).
  * ---------------------------------------------------------------------------------- */
+/* empirical_fisher_finalize: keys[i] = (float)(score_sum[i] / (2 n_tokens)) for i < n (IEEE
+ * float64 division, rounded to nearest float32): the scores as float32 sort keys for
+ * score_and_allocate_keys, n_tokens the calibration tokens accumulated. */
+KF_API kf_status empirical_fisher_finalize(kf_ctx* ctx, const double* score_sum, int64_t n, int64_t n_tokens,
+                                           float* keys, kf_stream_t stream);
 KF_API size_t empirical_fisher_workspace_size(int64_t m, int64_t n, int32_t r);
 KF_API kf_status empirical_fisher_accumulate(kf_ctx* ctx, const void* act, kf_dtype act_dtype, int64_t lda,
                                              const void* grad, kf_dtype grad_dtype, int64_t ldg,

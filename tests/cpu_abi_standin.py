@@ -159,6 +159,10 @@ def empirical_fisher_accumulate(ctx, act, grad, U, V, score_sum, workspace=None,
     _put(score_sum, _np(score_sum) + np.sum(P * P * Q * Q, axis=0))
 
 
+def empirical_fisher_finalize(ctx, score_sum, n_tokens, keys, stream=None):
+    _put(keys, (_np(score_sum) / (2.0 * n_tokens)).astype(np.float32))
+
+
 def activation_covariance(ctx, X, W, C, workspace=None, stream=None):
     Wd = _np(W)
     _put(C, Wd.T @ _np(X) @ Wd)
@@ -181,7 +185,7 @@ def activation_factors(ctx, W, vecs, r, U, V, workspace=None, stream=None):
     _put(V, v_)
 
 
-NAMES = ["fake_quant_rows", "empirical_fisher_accumulate", "activation_covariance", "activation_eig",
+NAMES = ["fake_quant_rows", "empirical_fisher_accumulate", "empirical_fisher_finalize", "activation_covariance", "activation_eig",
          "activation_factors", "kf_gram_side", "kfac_accumulate", "kf_finalize_covariance", "whiten",
          "whitened_svd", "score_and_allocate", "score_and_allocate_keys", "unwhiten", "channel_errors",
          "compact_mask", "gather_rows_cols"]

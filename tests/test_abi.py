@@ -87,6 +87,7 @@ def test_every_compute_call_rejects_a_null_context():
         "channel_errors": (None, None, 0, 8, 8, 8, None, 1, None, 8, 1, None, 8, None, None, None, 0, None),
         "gather_rows_cols": (None, None, 0, 8, 8, 8, None, 1, None, 1, None, 1, None),
         "compact_mask": (None, None, 4, 1, None, None, None),
+        "empirical_fisher_finalize": (None, None, 4, 10, None, None),
     }
     for name, args in calls.items():
         st = getattr(L, name)(*args)

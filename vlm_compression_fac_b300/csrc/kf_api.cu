@@ -401,6 +401,15 @@ kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_problem* pr
                  reinterpret_cast<cudaStream_t>(stream), false);
 }
 
+kf_status empirical_fisher_finalize(kf_ctx* ctx, const double* score_sum, int64_t n, int64_t n_tokens, float* keys,
+                                    kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "empirical_fisher_finalize: null context"));
+  KF_TRY(need(n >= 0 && n_tokens > 0, "empirical_fisher_finalize: sizes"));
+  if (n == 0) return KF_OK;
+  KF_TRY(need(score_sum && keys, "empirical_fisher_finalize: null pointer"));
+  return launch_fisher_finalize(score_sum, n, n_tokens, keys, reinterpret_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------- index plumbing
 kf_status gather_rows_cols(kf_ctx* ctx, const void* src, kf_dtype dtype, int64_t lds, int64_t src_rows,
                            int64_t src_cols, const int64_t* row_idx, int64_t rows, const int64_t* col_idx, int64_t cols,

@@ -154,6 +154,7 @@ kf_status launch_gather2d(const void* src, kf_dtype dt, int64_t lds, int64_t src
                           int* status, cudaStream_t st);
 kf_status launch_compact_mask(const unsigned char* mask, int64_t n, int want, int64_t* idx, int64_t* count,
                               cudaStream_t st);
+kf_status launch_fisher_finalize(const double* sum, int64_t n, int64_t n_tokens, float* keys, cudaStream_t st);
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,
                           float* scratch, cudaStream_t st);
 kf_status launch_copy(const float* src, int64_t lds, float* dst, int64_t ldd, int64_t rows,

@@ -236,6 +236,13 @@ __global__ void __launch_bounds__(1024) compact_mask_kernel(const unsigned char*
   if (t == 0) *count = base;
 }
 
+// keys[i] = float(sum[i] / (2 N)): IEEE float64 division, then round to nearest float32.
+__global__ void fisher_finalize_kernel(const double* __restrict__ sum, int64_t n, double two_n,
+                                       float* __restrict__ keys) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x)
+    keys[i] = __double2float_rn(sum[i] / two_n);
+}
+
 // Sum of the diagonal in float64, fixed order (one CTA).
 __global__ void diag_mean_kernel(const float* __restrict__ C, int64_t ldc, int64_t d,
                                  int64_t n_tokens, float lambda, float* __restrict__ out) {
@@ -408,6 +415,12 @@ kf_status launch_compact_mask(const unsigned char* mask, int64_t n, int want, in
                               cudaStream_t st) {
   compact_mask_kernel<<<1, 1024, 0, st>>>(mask, n, want, idx, count); note_launch();
   return check_cuda(cudaGetLastError(), "compact_mask launch");
+}
+
+kf_status launch_fisher_finalize(const double* sum, int64_t n, int64_t n_tokens, float* keys, cudaStream_t st) {
+  if (n <= 0) return KF_OK;
+  fisher_finalize_kernel<<<grid_for(n), 256, 0, st>>>(sum, n, 2.0 * double(n_tokens), keys); note_launch();
+  return check_cuda(cudaGetLastError(), "fisher_finalize launch");
 }
 
 kf_status launch_finalize(float* C, int64_t ldc, int64_t d, int64_t n_tokens, float lambda,

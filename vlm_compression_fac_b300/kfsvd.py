@@ -33,7 +33,7 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "whitened_svd_workspace_size", "whitened_svd",
             "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_weighted",
             "score_and_allocate_keys", "score_and_allocate_noalloc",
-            "empirical_fisher_workspace_size", "empirical_fisher_accumulate",
+            "empirical_fisher_workspace_size", "empirical_fisher_accumulate", "empirical_fisher_finalize",
             "unwhiten_workspace_size", "unwhiten",
             "activation_covariance_workspace_size", "activation_covariance", "activation_eig_workspace_size",
             "activation_eig", "activation_factors_workspace_size", "activation_factors",
@@ -90,6 +90,7 @@ _SIGS = {
     "score_and_allocate_weighted": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_keys": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
+    "empirical_fisher_finalize": (_I32, [_P, _P, _I64, _I64, _P, _P]),
     "empirical_fisher_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "empirical_fisher_accumulate": (_I32, [_P, _P, _I32, _I64, _P, _I32, _I64, _I64, _I64, _I64, _P, _I64, _P,
                                            _I64, _I32, _P, _P, _SZ, _P]),
@@ -313,6 +314,12 @@ def score_and_allocate_keys(ctx: Context, keys, seg_offset, cost, budget: int, r
     _check(lib().score_and_allocate_keys(ctx.handle, _ptr(keys), _ptr(seg_offset), _ptr(cost), n_units, n, int(budget),
                                          _ptr(ranks), _ptr(keep), _ptr(cut), _ptr(used), _ptr(ws), wsb,
                                          _stream(stream)))
+
+
+def empirical_fisher_finalize(ctx: Context, score_sum, n_tokens: int, keys, stream=None):
+    """keys (float32) = score_sum (float64) / (2 n_tokens), rounded to float32."""
+    _check(lib().empirical_fisher_finalize(ctx.handle, _ptr(score_sum), int(score_sum.numel()), int(n_tokens),
+                                           _ptr(keys), _stream(stream)))
 
 
 def empirical_fisher_workspace_size(m: int, n: int, r: int) -> int:

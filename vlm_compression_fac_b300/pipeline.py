@@ -311,7 +311,9 @@ def _fisher_allocation(ctx, units, outs, weights, rows_fn, quant_sites, n_tokens
             mark("fisher<")
             K.empirical_fisher_accumulate(ctx, a, g, Ua, Va, acc, stream=stream)
             mark("fisher>")
-        keys.append((acc / (2.0 * n_tokens)).to(torch.float32))
+        k_ = torch.empty(s, dtype=torch.float32, device=dev)
+        K.empirical_fisher_finalize(ctx, acc, n_tokens, k_, stream=stream)
+        keys.append(k_)
         full.append((Ua, Va))
     mark("score")
     keys_t = torch.cat(keys)
