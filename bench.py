@@ -57,6 +57,10 @@ def parse():
     ap.add_argument("--tokens", type=int, default=None,
                     help="calibration tokens per site (default: the workload's 131072); a smaller N "
                          "keeps every matrix shape and is meant for profiler captures")
+    ap.add_argument("--workloads", default="all",
+                    help="comma-separated extra workloads timed once each after the main line, at N=1 on "
+                         "rank 0: single_linear, llama70b_block, llama7b_model, vlm; 'all' (default) or "
+                         "'none'")
     return ap.parse_args()
 
 
@@ -134,16 +138,17 @@ def cost_tail(m, n):
 JAC_APPLY_TRAFFIC = 1.5967e9
 
 
-# Algorithmic bytes per component of one score_and_allocate call: sigma read (4) and key
-# written (8); four stable radix passes over the score word, each reading and writing the
-# 8-byte key (4 x 16); one read of the sorted keys for the cost prefix and the cut (8).
+# ALGORITHMIC bytes per component of one score_and_allocate call (a model of the minimum
+# traffic, not measured DRAM bytes): sigma read (4) and key written (8); four stable radix
+# passes over the score word, each reading and writing the 8-byte key (4 x 16); one read of
+# the sorted keys for the cost prefix and the cut (8).
 ALLOC_BYTES_PER_KEY = 12 + 4 * 16 + 8
 
 
 def alloc_scaled(ctx, torch, K, hbm_peak, log2n=28, unit_len=1 << 17, reps=5):
     """score_and_allocate over 2^log2n components (units of unit_len descending values, m + n
     = 2 unit_len each, budget half of everything), timed with CUDA events on the launching
-    stream after two warm-up calls."""
+    stream after two warm-up calls.  ``achieved`` is algorithmic bytes per second."""
     n = 1 << log2n
     n_units = n // unit_len
     g = torch.Generator(device="cuda")
@@ -177,7 +182,135 @@ def alloc_scaled(ctx, torch, K, hbm_peak, log2n=28, unit_len=1 << 17, reps=5):
     torch.cuda.empty_cache()
     return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(gbs / hbm_peak, 4), "ms": round(ms, 3), "components": n, "units": n_units,
-            "kept": kept, "bytes_per_key": ALLOC_BYTES_PER_KEY, "peak_kind": "HBM copy, of measured"}
+            "kept": kept, "algorithmic_bytes_per_key": ALLOC_BYTES_PER_KEY, "peak_kind": "HBM copy, of measured"}
+
+
+def fp32_peak_probe(ctx, torch, K, iters=1 << 19):
+    """FP32 FMA roof of this device, measured: the library's probe kernel (every SM's FMA pipes
+    busy with independent fma chains) timed with CUDA events on the launching stream; best of
+    three after a warm-up launch."""
+    sink = torch.zeros(8, dtype=torch.float32, device="cuda")
+    st = torch.cuda.current_stream()
+    K.kf_fp32_fma_probe(ctx, 1 << 12, sink, stream=st)
+    torch.cuda.synchronize()
+    best = 0.0
+    for _ in range(3):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        f = K.kf_fp32_fma_probe(ctx, iters, sink, stream=st)
+        e1.record(st)
+        torch.cuda.synchronize()
+        best = max(best, f / (e0.elapsed_time(e1) / 1e3) / 1e12)
+    return best
+
+
+def streaming_kernels(ctx, torch, K, hbm_peak, reps=5):
+    """The HBM-bound streaming steps on a VLM-sized stream (147456 tokens x 3584 bf16
+    channels, 1.06 GB, larger than L2): the seeded generator's device twin (writes 2 B per
+    element) and the per-token INT8 fake quantisation of quantisation-aware whitening (reads 2 B
+    and writes 2 B per element), each timed with CUDA events over `reps` launches."""
+    from synth import device, recipes
+    wl = recipes.vlm()
+    site = wl.sites["lm.b0.attn_in"]
+    N, d = wl.n_tokens, site.d
+    st = torch.cuda.current_stream()
+    out = {}
+    rows = device.stream_on_device(wl, site, 0, N, torch)
+    q = torch.empty_like(rows)
+    K.fake_quant_rows(ctx, rows, q, stream=st)
+    torch.cuda.synchronize()
+    for name, fn, nbytes in (("synthetic generator (libkfsynth, 2 B written per element)",
+                              lambda: device.stream_on_device(wl, site, 0, N, torch), 2 * N * d),
+                             ("fake_quant_kernel (INT8 per token, 2 B read + 2 B written per element)",
+                              lambda: K.fake_quant_rows(ctx, rows, q, stream=st), 4 * N * d)):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gbs / hbm_peak, 4), "ms": round(ms, 3), "elements": N * d,
+                     "peak_kind": "HBM copy, of measured"}
+    ctx.sync_status()
+    del rows, q
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_workloads(ctx, torch, K, names, fp32_peak):
+    """One end-to-end pass of each named workload through the streaming pipeline (calibration
+    rows generated on the device chunk by chunk, the way a data loader feeds them; blocks one
+    after another for the multi-block workloads), with wall-clock seconds, the pipeline's phase
+    times from CUDA events, and the SM clocks sampled during the pass."""
+    from synth import device, recipes
+    from vlm_compression_fac_b300 import pipeline
+    makers = {"single_linear": recipes.single_linear, "llama70b_block": recipes.llama70b_block,
+              "llama7b_model": recipes.llama7b_model, "vlm": recipes.vlm}
+    out = {}
+    for name in names:
+        wl = makers[name]()
+        units = pipeline.unit_specs(wl)
+        weights = device.weights_on_device(wl, torch)
+        groups = None
+        if len({u.block for u in wl.units}) > 1:
+            groups = [[i for i, u in enumerate(wl.units) if u.block == b] for b in sorted({u.block for u in wl.units})]
+        st = torch.cuda.current_stream()
+        ev = []
+
+        def mark(tag):
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(st)
+            ev.append((tag, e))
+
+        torch.cuda.synchronize()
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        t0 = time.perf_counter()
+        mark("start")
+        res = pipeline.compress(ctx, units, weights, device.rows_fn(wl, torch), None, wl.n_tokens, lam=wl.lam,
+                                budget=None if wl.fixed_rank is not None else wl.budget, fixed_rank=wl.fixed_rank,
+                                quant=wl.quant == "int8_token", site_dims={n: s.d for n, s in wl.sites.items()},
+                                act_sites=[n for n, s in wl.sites.items() if s.kind == "act"], groups=groups,
+                                chunk_tokens=32768, keep_covs=False, keep_whitened=False, sync_timer=mark)
+        ctx.sync_status()
+        torch.cuda.synchronize()
+        secs = time.perf_counter() - t0
+        clk = clocks.stop()
+        ph, syrk_ms, prev = {}, 0.0, ev[0][1]
+        open_s = None
+        for tag, e in ev[1:]:
+            if tag == "syrk<":
+                open_s = e
+                continue
+            if tag == "syrk>":
+                syrk_ms += open_s.elapsed_time(e)
+                continue
+            ph[tag] = ph.get(tag, 0.0) + prev.elapsed_time(e)
+            prev = e
+        blocks = len({u.block for u in wl.units})
+        svd_ms = ph.get("whiten", 0.0) + ph.get("svd", 0.0)
+        out[name] = {
+            "workload": "%s: %d units, N=%d per site%s, %s" % (
+                wl.name, len(wl.units), wl.n_tokens, ", INT8 per-token fake-quantised activations"
+                if wl.quant == "int8_token" else "", "fixed r=%d" % wl.fixed_rank if wl.fixed_rank is not None
+                else "rho=%.2f global" % wl.rho),
+            "seconds_end_to_end": round(secs, 3),
+            "calib_tokens_per_s": round(wl.n_tokens * blocks / (ph.get("kfac", 0.0) / 1e3), 1),
+            "syrk_ms": round(syrk_ms, 2),
+            "layers_per_s": round(len(wl.units) / (svd_ms / 1e3), 3) if svd_ms > 0 else None,
+            "phases_ms": {k: round(v, 2) for k, v in ph.items()},
+            "ranks_sum": int(res.ranks.sum().item()), "used": int(res.used.item()),
+            "budget": None if wl.fixed_rank is not None else int(wl.budget),
+            "sweeps_max": max(u.sweeps for u in res.units), "clocks": clk,
+            "inputs": "calibration rows generated on the device by the seeded generator inside the timed pass"}
+        del res, weights
+        torch.cuda.empty_cache()
+    return out
 
 
 def syrk_flops(n_tokens, d):
@@ -333,7 +466,10 @@ def run_kfsvd(args):
     pk = peaks() or {}
     bf16_peak = pk.get("bf16_tflops_sustained", 1400.0)
     sm_max = (clk or {}).get("sm_max_mhz") or pk.get("sm_max_mhz", 2032.0)
-    fp32_peak = 148 * 128 * 2 * sm_max * 1e6 / 1e12
+    n_sm = torch.cuda.get_device_properties(local).multi_processor_count
+    fp32_derived = n_sm * 128 * 2 * sm_max * 1e6 / 1e12
+    fp32_measured = fp32_peak_probe(ctx, torch, K)
+    fp32_peak = fp32_measured
     sites = list(acts.values()) + list(grads.values())
     syrk_total_flops = sum(syrk_flops(wl.n_tokens, t.shape[1]) for t in sites) * K_
     syrk_tf = syrk_total_flops / (syrk_ms / 1e3) / 1e12 if syrk_ms > 0 else 0.0
@@ -349,7 +485,8 @@ def run_kfsvd(args):
             "launches_per_step": apply_launches // K_,
             "avg_launch_ms": round(apply_ms / max(apply_launches, 1), 4),
             "traffic": JAC_APPLY_TRAFFIC,
-            "peak_kind": "FP32 FFMA: 148 SMs x 128 lanes x 2 flop x max SM clock (derived)"},
+            "peak_kind": "FP32 FFMA, measured by the library's FMA probe kernel (derived %d SMs x 128 lanes x 2 "
+                         "flop x %.0f MHz = %.1f TFLOP/s)" % (n_sm, sm_max, fp32_derived)},
         "jac_solve_kernel (Jacobi pair problems)": {
             "bound": "latency", "ms_per_step": round(solve_ms / K_, 3),
             "launches_per_step": apply_launches // K_},
@@ -364,7 +501,12 @@ def run_kfsvd(args):
             "frac": round(f_tf / bf16_peak, 4), "ms_per_step": round(fisher_ms / K_, 3),
             "calls_per_step": n_fisher // K_, "peak_kind": "bf16 dense, sustained, of measured"}
     if not args.no_alloc_scaled:
-        kern["score_and_allocate (2^28 components)"] = alloc_scaled(ctx, torch, K, pk.get("hbm_gbs", 6400.0))
+        kern["score_and_allocate (2^28 components, 2048 units of 2^17)"] = alloc_scaled(ctx, torch, K,
+                                                                                       pk.get("hbm_gbs", 6400.0))
+        kern["score_and_allocate (2^28 components, 65536 units of 4096)"] = alloc_scaled(
+            ctx, torch, K, pk.get("hbm_gbs", 6400.0), unit_len=4096)
+    if rank == 0 and world == 1:
+        kern.update(streaming_kernels(ctx, torch, K, pk.get("hbm_gbs", 6400.0)))
     dom = max(("tc_gemm_kernel (covariance SYRK)", syrk_ms), ("jac_apply_kernel (Jacobi rotations)", apply_ms),
               key=lambda kv: kv[1])[0]
     roof = {k: v for k, v in kern[dom].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
@@ -375,6 +517,16 @@ def run_kfsvd(args):
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1 and not swift:
         cpu = oracle_sample(wl, sample_tokens=1024)
+        cpu["single_linear_in_full"] = oracle_single_linear()
+
+    # ---------------- the other workloads, one pass each (N=1, rank 0)
+    wls = None
+    names = [] if args.workloads == "none" else (
+        ["single_linear", "llama70b_block", "llama7b_model", "vlm"] if args.workloads == "all"
+        else [x for x in args.workloads.split(",") if x])
+    if names and rank == 0 and world == 1:
+        K.kf_svd_profile_enable(ctx, False)
+        wls = run_workloads(ctx, torch, K, names, fp32_peak)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K_,
@@ -392,7 +544,9 @@ def run_kfsvd(args):
         "jacobi_sweeps": [int(u.sweeps) for u in res.units],
         "units_larger_than_dense": res.larger_than_dense(),
         "roofline": roof, "kernels": kern, "clocks": clk, "e2e": e2e, "gpu_launches": int(launches),
-        "cpu_baseline": cpu,
+        "cpu_baseline": cpu, "fp32_peak_tflops": {"measured": round(fp32_measured, 2),
+                                                  "derived": round(fp32_derived, 2), "sm_count": n_sm},
+        "workloads": wls,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -439,6 +593,20 @@ def oracle_sample(wl, sample_tokens=1024, tail_unit="q"):
                       "SVD/unwhiten tail of unit %s (%.1f s, scaled by the tail cost model to all %d units); "
                       "extrapolated step %.1f s" % (sample_tokens, wl.n_tokens, len(wl.sites), t_cov, tail_unit,
                                                     t_tail, len(wl.units), est)}
+
+
+def oracle_single_linear():
+    """The fp64 oracle over the whole single 256 x 512 layer workload (2048 float32 tokens,
+    rank 64), in full: no sample, no extrapolation."""
+    import oracle as O
+    from synth import recipes
+    wl = recipes.single_linear()
+    t0 = time.perf_counter()
+    O.compress_workload(wl)
+    secs = time.perf_counter() - t0
+    return {"value": round(wl.n_tokens / secs, 1), "unit": "tokens/s", "seconds": round(secs, 3),
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": "the whole single_linear workload (256x512 float32 layer, N=2048, r=64), not extrapolated"}
 
 
 def run_reference(args):

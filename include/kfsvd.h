@@ -96,6 +96,22 @@ KF_API uint64_t kf_launch_count(void);
  * for KF_ERR_NO_CONVERGENCE, the wait site for KF_ERR_TIMEOUT. */
 KF_API kf_status kf_sync_status(kf_ctx* ctx, kf_stream_t stream, int32_t* info);
 
+/* Limit, in nanoseconds of device wall-clock time, of each wait inside the tensor-core
+ * pipeline (a stage of operands arriving, an accumulator being consumed) for later calls on
+ * this context; 0 restores the default of 4 s.  A wait that runs out records KF_ERR_TIMEOUT
+ * (info = wait site) in the status word, and the kernel stops issuing work, waits for what
+ * it already started (on the 4 s limit), releases its tensor memory and returns; its output
+ * is then incomplete.  The context stays usable: the next call with a long enough limit
+ * computes normally.  A short limit is for testing the failure path. */
+KF_API kf_status kf_set_wait_limit(kf_ctx* ctx, uint64_t limit_ns);
+
+/* Measurement aid: launches a kernel that keeps every FP32 FMA pipe of the device busy
+ * (8 CTAs of 256 threads per SM, 16 independent fma chains per thread, `iters` steps) and
+ * returns in *flops the flops it executes (2 per fma); the caller times the launch on
+ * `stream` with CUDA events to measure the FP32 SIMT roof of the Gram and Jacobi kernels.
+ * sink: device float[8], written only in a case that does not occur (keeps the work live). */
+KF_API kf_status kf_fp32_fma_probe(kf_ctx* ctx, int64_t iters, float* sink, double* flops, kf_stream_t stream);
+
 /* Side whose Gram matrix the spectrum is taken from: KF_SIDE_RIGHT (W~^T W~, n x n) when
  * d_out <= d_in, else KF_SIDE_LEFT (W~ W~^T, m x m). */
 KF_API kf_side kf_gram_side(int64_t m, int64_t n);
@@ -279,12 +295,40 @@ KF_API kf_status score_and_allocate_keys(kf_ctx* ctx, const float* keys, const i
                                          int64_t* used, void* workspace, size_t workspace_bytes,
                                          kf_stream_t stream);
 
+/* score_and_allocate_hybrid - sort-and-truncate on Swift-SVD's hybrid score (section B,
+ * Dynamic Rank Allocation Strategy: s_i = beta_i^alpha (log(e + eps*_{k,i}))^(1 - alpha),
+ * combining the layer's end-to-end importance beta_i with the closed-form loss eps*_{k,i} of
+ * the layer truncated to rank k).  Keyed per component: component k (0-based) of unit u gets
+ * the unit's score at rank k, with eps*_k = sum_{j >= k} sigma_j^2 the energy the truncation
+ * drops (float64, summed one term at a time from the unit's last component upward), key =
+ * (float)(beta_u^alpha * pow(log(e + eps*_k), 1 - alpha)) in float64; the keys are sorted
+ * descending (ties: lower unit, then lower component) and cut at the budget as in
+ * score_and_allocate, so the next component always goes to the unit whose current
+ * truncation scores highest.  eps*_k never increases along a unit, so neither do its keys
+ * and the kept set is a prefix of its spectrum (ranks[u] components).
+ * importance: device float[n_units] (beta; NULL means 1 for every unit; a value that is not
+ *             positive gives the unit keys 0).
+ * alpha:      in [0, 1] (KF_ERR_INVALID otherwise): 1 ranks units by beta alone, 0 by the
+ *             residual loss alone.  The grid search over alpha and the retention ratio that the
+ *             paper runs on validation data is the caller's.
+ * sigma, seg_offset, cost, ranks, cut, used and the workspace as for score_and_allocate; the
+ * scale of sigma matters (eps* enters through log(e + eps*)). */
+KF_API kf_status score_and_allocate_hybrid(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset,
+                                           const int64_t* cost, int32_t n_units, int64_t n_components,
+                                           int64_t budget, const float* importance, double alpha,
+                                           int32_t* ranks, float* cut, int64_t* used, void* workspace,
+                                           size_t workspace_bytes, kf_stream_t stream);
+
 /* score_and_allocate_noalloc - score_and_allocate for callers that cannot allocate device
  * memory: for example a host framework that has already handed all device memory to its own
  * pool, or a caller that must not trigger a device allocation (which may synchronise the
  * device) in the middle of a job.  It takes no workspace and allocates nothing: its scratch
- * is a 25 MiB array placed in device memory when the library is loaded, held on every GPU
- * that loads the library until the process exits.  The papers have no counterpart; this is
+ * is a 25 MiB file-scope device array of the library, held on every GPU that uses it until
+ * the process exits.  With CUDA's lazy module loading (the default) the array is reserved
+ * on a device when the library's allocation code is first used there: the first launch of
+ * any allocation kernel (score_and_allocate and its variants) or this call's first address
+ * lookup.  A caller that must not allocate after some point should make one call (of this
+ * entry point or of score_and_allocate) on each device before it.  The papers have no counterpart; this is
  * a packaging variant of (5a) with identical results.
  * Limit: n_components <= 1048576 (2^20); larger calls return KF_ERR_UNSUPPORTED before any
  * launch.  The first call on a device looks up the array's device address (once per
@@ -295,6 +339,15 @@ KF_API kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma, con
                                             const int64_t* cost, int32_t n_units, int64_t n_components,
                                             int64_t budget, kf_alloc_mode mode, const int32_t* fixed_rank,
                                             int32_t* ranks, float* cut, int64_t* used, kf_stream_t stream);
+
+/* kf_hybrid_ffn_budget - LASER's hybrid FFN budget: the parameters left for the low-rank
+ * factors once the dense channels are paid for, max(budget - dense_cost, 0), with
+ * dense_cost = sum_i d_model[i] n_dense[i] over the dense projections (a dense channel of a
+ * gate or up projection keeps its d_model weights) written to *dense_cost (may be NULL).
+ * Host arrays of n entries; returns -1 (message in kf_last_error) for a negative n or entry,
+ * or a null array with n > 0.  Host arithmetic, no device work. */
+KF_API int64_t kf_hybrid_ffn_budget(int64_t budget, int32_t n, const int64_t* d_model, const int64_t* n_dense,
+                                    int64_t* dense_cost);
 
 /* ------------------------------------------------------------------------------------
  * (5b) unwhiten - rank-r factors in the original space.

@@ -17,7 +17,9 @@ in float64 (numpy/LAPACK routines serve as textbook steps).  Sources:
             singular pair until the parameter budget is reached).
   [Swift]   "Swift-SVD: Theoretical Optimality Meets Practical Efficiency in Low-Rank LLM
             Compression", section 2A (closed form W_k = W V_k V_k^T; incremental
-            covariance aggregation; one eigendecomposition of the aggregated covariance).
+            covariance aggregation; one eigendecomposition of the aggregated covariance)
+            and section B (hybrid scoring of layer importance and closed-form loss for the
+            dynamic rank allocation).
 
 Readings where the pages are silent: W is d_in x d_out (y = x W);
 X = A^T A / N and G = Gr^T Gr / N uncentred, each damped by lam * mean(diag); the
@@ -35,6 +37,7 @@ closed forms, the pages' identities, brute force or hand-worked values; none is
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass
 from typing import Dict, List, Optional, Sequence
 
@@ -256,6 +259,54 @@ def allocate_keys(keys: Sequence[np.ndarray], costs: Sequence[int], budget: int)
     nxt = float(scores[order[n_keep]]) if n_keep < len(order) else float("nan")
     used = int(prefix[n_keep - 1]) if n_keep > 0 else 0
     return Allocation(ranks, cut, nxt, used, units[order], comps[order], scores[order])
+
+
+def swift_residual_losses(sigma: np.ndarray) -> List[float]:
+    """[Swift] 2A/B: the closed-form loss of a unit truncated to rank k is the energy of the
+    components it drops, eps*_k = sum_{j >= k} sigma_j^2 (k = 0 .. len - 1, 0-based sigma).
+    Summed in float64 from the last component upward, one term at a time (the square of a
+    float32 value is exact in float64), so that the sum order is fixed."""
+    s = [float(np.float32(x)) for x in sigma]
+    eps = [0.0] * len(s)
+    acc = 0.0
+    for j in range(len(s) - 1, -1, -1):
+        acc = acc + s[j] * s[j]
+        eps[j] = acc
+    return eps
+
+
+def swift_hybrid_keys(sigma: np.ndarray, beta: float, alpha: float) -> np.ndarray:
+    """[Swift] B, hybrid scoring s_i = beta_i^alpha (log(e + eps*_{k,i}))^(1 - alpha) as a
+    sort-and-truncate key per component: component k (0-based) of unit i gets the unit's
+    score at rank k, i.e. while it holds the k components before it, so the next component
+    always goes to the unit whose current truncation scores highest (keys sorted
+    descending).  eps*_k is non-increasing in k, so every unit's keys are too and the kept
+    set is a prefix of its spectrum.  beta_i (the unit's end-to-end importance) and alpha in
+    [0, 1] are the caller's; a beta that is not positive gives the unit keys 0.  Each key is
+    evaluated in float64 with the C library's log and pow and rounded once to float32."""
+    eps = swift_residual_losses(sigma)
+    b = float(np.float32(beta))      # the importance is given as a float32 per unit
+    if not (b > 0.0):
+        return np.zeros(len(eps), dtype=np.float32)
+    bw = math.pow(b, float(alpha))
+    out = np.empty(len(eps), dtype=np.float32)
+    for k, e in enumerate(eps):
+        out[k] = np.float32(bw * math.pow(math.log(math.e + e), 1.0 - float(alpha)))
+    return out
+
+
+def allocate_swift_hybrid(sigmas: Sequence[np.ndarray], costs: Sequence[int], budget: int,
+                          betas: Sequence[float], alpha: float) -> Allocation:
+    """Global sort-and-truncate ([UniRank] 2.1's procedure) on [Swift] B's hybrid keys."""
+    return allocate_keys([swift_hybrid_keys(s, b, alpha) for s, b in zip(sigmas, betas)], costs, budget)
+
+
+def hybrid_ffn_budget(budget: int, d_model: Sequence[int], n_dense: Sequence[int]) -> int:
+    """[LASER] hybrid FFN: the parameter budget left for the low-rank factors once the dense
+    channels are paid for, max(budget - sum_p d_model_p n_dense_p, 0); each dense channel of a
+    gate or up projection keeps its d_model weights (one entry per projection)."""
+    left = int(budget) - sum(int(a) * int(b) for a, b in zip(d_model, n_dense))
+    return max(left, 0)
 
 
 # --------------------------------------------------------------- the objective

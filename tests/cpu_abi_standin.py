@@ -86,6 +86,29 @@ def score_and_allocate(ctx, sigma, seg_offset, cost, budget, ranks, mode=0, fixe
         cut.copy_(torch.tensor([al.cut_score, al.next_score], dtype=torch.float32))
 
 
+def _put_alloc(al, ranks, cut, used):
+    ranks.copy_(torch.tensor(al.ranks, dtype=torch.int32))
+    if used is not None:
+        used.fill_(int(al.used))
+    if cut is not None:
+        cut.copy_(torch.tensor([al.cut_score, al.next_score], dtype=torch.float32))
+
+
+def score_and_allocate_weighted(ctx, sigma, seg_offset, cost, budget, ranks, mode=3, unit_weight=None, cut=None,
+                                used=None, workspace=None, stream=None):
+    segs = _segments(sigma, seg_offset)
+    key = {0: O.KEY_HALF_SIGMA2, 1: O.KEY_PER_PARAM, 3: O.KEY_ENERGY_RATIO}[mode]
+    w = None if unit_weight is None else unit_weight.cpu().tolist()
+    _put_alloc(O.allocate(segs, cost.cpu().tolist(), int(budget), key, precision="f32", weights=w), ranks, cut, used)
+
+
+def score_and_allocate_hybrid(ctx, sigma, seg_offset, cost, budget, ranks, alpha, importance=None, cut=None,
+                              used=None, workspace=None, stream=None):
+    segs = _segments(sigma, seg_offset)
+    b = [1.0] * len(segs) if importance is None else importance.cpu().tolist()
+    _put_alloc(O.allocate_swift_hybrid(segs, cost.cpu().tolist(), int(budget), b, alpha), ranks, cut, used)
+
+
 def score_and_allocate_keys(ctx, keys, seg_offset, cost, budget, ranks, keep=None, cut=None, used=None,
                             workspace=None, stream=None):
     segs = [np.maximum(s.astype(np.float32), 0) for s in _segments(keys, seg_offset)]
@@ -187,7 +210,8 @@ def activation_factors(ctx, W, vecs, r, U, V, workspace=None, stream=None):
 
 NAMES = ["fake_quant_rows", "empirical_fisher_accumulate", "empirical_fisher_finalize", "activation_covariance", "activation_eig",
          "activation_factors", "kf_gram_side", "kfac_accumulate", "kf_finalize_covariance", "whiten",
-         "whitened_svd", "score_and_allocate", "score_and_allocate_keys", "unwhiten", "channel_errors",
+         "whitened_svd", "score_and_allocate", "score_and_allocate_keys", "score_and_allocate_weighted",
+         "score_and_allocate_hybrid", "unwhiten", "channel_errors",
          "compact_mask", "gather_rows_cols"]
 
 

@@ -12,7 +12,7 @@ HEADER = os.path.join(ROOT, "include", "kfsvd.h")
 
 def declared_symbols():
     txt = open(HEADER).read()
-    return sorted(set(re.findall(r"^KF_API [^(]*?\b([a-z_]+)\(", txt, flags=re.M)))
+    return sorted(set(re.findall(r"^KF_API [^(]*?\b([a-z_][a-z_0-9]*)\(", txt, flags=re.M)))
 
 
 def test_header_declares_the_five_steps():
@@ -88,9 +88,27 @@ def test_every_compute_call_rejects_a_null_context():
         "gather_rows_cols": (None, None, 0, 8, 8, 8, None, 1, None, 1, None, 1, None),
         "compact_mask": (None, None, 4, 1, None, None, None),
         "empirical_fisher_finalize": (None, None, 4, 10, None, None),
+        "score_and_allocate_hybrid": (None, None, None, None, 1, 0, 0, None, 0.5, None, None, None, None, 0, None),
+        "kf_set_wait_limit": (None, 1000),
     }
     for name, args in calls.items():
         st = getattr(L, name)(*args)
         assert st == K.KF_ERR_INVALID, name
         msg = L.kf_last_error()
         assert name.encode() in msg and b"null context" in msg, (name, msg)
+
+
+def test_hybrid_allocation_and_budget_reject_bad_arguments_on_the_host():
+    """score_and_allocate_hybrid checks alpha in [0, 1] before any launch; the hybrid FFN budget
+    is host arithmetic in the library (equal to the oracle's statement of it)."""
+    import oracle as O
+    from vlm_compression_fac_b300 import kfsvd as K
+    L = K.lib()
+    h = ctypes.c_void_p(1)   # never dereferenced: the alpha check comes first
+    st = L.score_and_allocate_hybrid(h, None, None, None, 1, 0, 0, None, 1.5, None, None, None, None, 0, None)
+    assert st == K.KF_ERR_INVALID and b"alpha" in L.kf_last_error()
+    for budget, dm, nd in ((1000, [64, 64], [3, 3]), (100, [64, 64], [3, 3]), (7, [], []), (10 ** 12, [4096] * 4,
+                                                                                            [1000, 2000, 0, 7])):
+        assert K.kf_hybrid_ffn_budget(budget, dm, nd) == O.hybrid_ffn_budget(budget, dm, nd)
+    with pytest.raises(K.KfsvdError):
+        K.kf_hybrid_ffn_budget(10, [64], [-1])

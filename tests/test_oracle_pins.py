@@ -534,3 +534,110 @@ def test_hybrid_ffn_flow_accounting_and_limits():
     none = O.compress_hybrid_ffn(wl, r_temp=8, n_svd=0)
     assert all(kind == "unit" for kind, _, _ in none["entries"])
     assert {names[i] for _, i, _ in none["entries"]} == set(names) - {"gate", "up"}
+
+
+def test_swift_hybrid_keys_hand_case():
+    """Swift-SVD B hybrid scoring as per-component keys, on a hand-worked case
+    (tests/golden/swift_hybrid_hand.json): the keys, and the sort-and-truncate over them."""
+    g = json.load(open(os.path.join(GOLD, "swift_hybrid_hand.json")))
+    for s, b, want in zip(g["sigmas"], g["betas"], g["keys"]):
+        got = O.swift_hybrid_keys(np.array(s, dtype=np.float32), b, g["alpha"])
+        assert got.dtype == np.float32
+        np.testing.assert_allclose(got.astype(np.float64), want, rtol=1e-7, atol=0)
+    for c in g["cases"]:
+        al = O.allocate_swift_hybrid([np.array(s, np.float32) for s in g["sigmas"]], g["costs"], c["budget"],
+                                     g["betas"], g["alpha"])
+        assert list(al.ranks) == c["ranks"] and al.used == c["used"]
+        for got, want in ((al.cut_score, c["cut"]), (al.next_score, c["next"])):
+            if want is None:
+                assert np.isnan(got)
+            else:
+                assert abs(got - want) <= 1e-7 * abs(want)
+
+
+def test_swift_residual_loss_is_the_truncation_loss():
+    """eps*_k (Swift-SVD B's closed-form loss at rank k) equals the whitened error of the
+    rank-k factors mapped back, ||S_x (W - U_k V_k) S_g||^2 (Swift-SVD 2A / LASER 1 optimum),
+    for every k, and is non-increasing with eps*_0 = ||W~||_F^2."""
+    A, Gr, W, X, G = _tiny_problem(m=6, n=5, N=40, seed=3)
+    Sx, Sg = O.cholesky_factors(X, G)
+    Ut, s, Vt = O.whitened_svd(O.whiten(W, Sx, Sg))
+    s32 = s.astype(np.float32)
+    eps = O.swift_residual_losses(s32)
+    assert all(eps[k] >= eps[k + 1] for k in range(len(eps) - 1))
+    for k in range(len(s)):
+        U, V = O.unwhiten(Sx, Sg, Ut, s, Vt, k)
+        e = O.whitened_error(W, U, V, Sx, Sg)
+        assert abs(eps[k] - e) <= 1e-6 * eps[0] + 1e-12, k
+    assert abs(eps[0] - float(np.sum(O.whiten(W, Sx, Sg) ** 2))) <= 1e-6 * eps[0]
+
+
+def test_swift_hybrid_limits_and_monotone_keys():
+    """alpha = 1: the key is beta alone, so units are filled whole in decreasing beta (ties to
+    the lower unit).  alpha = 0: the key is log(e + eps*), a monotone map of the residual
+    loss, so the allocation equals sorting by eps* itself.  Any alpha: keys non-increasing
+    along a unit (the kept set is a prefix); beta <= 0 gives keys 0."""
+    r = np.random.default_rng(31)
+    sigs = [np.sort(r.gamma(1.0, 1.0, k)).astype(np.float32)[::-1].copy() for k in (6, 9, 4)]
+    costs = [11, 15, 7]
+    betas = [0.5, 2.0, 1.0]
+    total = sum(c * len(s) for c, s in zip(costs, sigs))
+    for budget in (0, 40, 100, 160, total):
+        al = O.allocate_swift_hybrid(sigs, costs, budget, betas, 1.0)
+        want, left = [0, 0, 0], budget
+        for u in (1, 2, 0):
+            k = min(len(sigs[u]), left // costs[u])
+            want[u] = k
+            if k < len(sigs[u]):
+                break
+            left -= k * costs[u]
+        assert list(al.ranks) == want, (budget, list(al.ranks), want)
+        a0 = O.allocate_swift_hybrid(sigs, costs, budget, betas, 0.0)
+        e0 = O.allocate_keys([np.array(O.swift_residual_losses(s)) for s in sigs], costs, budget)
+        assert list(a0.ranks) == list(e0.ranks)
+    for alpha in (0.0, 0.3, 0.7, 1.0):
+        for s, b in zip(sigs, betas):
+            k = O.swift_hybrid_keys(s, b, alpha)
+            assert np.all(np.diff(k.astype(np.float64)) <= 0)
+    assert not np.any(O.swift_hybrid_keys(sigs[0], 0.0, 0.5))
+    assert not np.any(O.swift_hybrid_keys(sigs[0], -1.0, 0.5))
+
+
+def test_swift_hybrid_allocation_is_the_greedy_next_component_rule():
+    """The sort-and-truncate over the hybrid keys is the greedy process the reading states:
+    repeatedly give the next component to the unit whose current truncation has the highest
+    hybrid score (recomputed from the dropped components' energy), ties to the lower unit, and
+    stop at the first component that would overflow the budget."""
+    r = np.random.default_rng(44)
+    for trial in range(20):
+        nu = int(r.integers(1, 5))
+        sigs = [np.sort(r.gamma(0.7, 1.0, int(r.integers(1, 7)))).astype(np.float32)[::-1].copy()
+                for _ in range(nu)]
+        costs = [int(r.integers(1, 9)) for _ in range(nu)]
+        betas = [float(r.uniform(0.1, 3.0)) for _ in range(nu)]
+        alpha = float(r.uniform(0.0, 1.0))
+        budget = int(r.integers(0, 60))
+        held, spent = [0] * nu, 0
+        while True:
+            best, bu = None, -1
+            for u in range(nu):
+                if held[u] == len(sigs[u]):
+                    continue
+                rest = sum(float(x) * float(x) for x in sigs[u][held[u]:].astype(np.float64))
+                sc = float(np.float32(betas[u] ** alpha * np.log(np.e + rest) ** (1.0 - alpha)))
+                if best is None or sc > best:
+                    best, bu = sc, u
+            if bu < 0 or spent + costs[bu] > budget:
+                break
+            held[bu] += 1
+            spent += costs[bu]
+        al = O.allocate_swift_hybrid(sigs, costs, budget, betas, alpha)
+        assert list(al.ranks) == held and al.used == spent, trial
+
+
+def test_hybrid_ffn_budget():
+    """LASER hybrid FFN: the dense channels' parameters come off the budget first (d_model
+    weights per dense channel and projection); never below zero."""
+    assert O.hybrid_ffn_budget(1000, [64, 64], [3, 3]) == 1000 - 384
+    assert O.hybrid_ffn_budget(100, [64, 64], [3, 3]) == 0
+    assert O.hybrid_ffn_budget(500, [], []) == 500

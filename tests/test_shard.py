@@ -126,7 +126,7 @@ def test_a_rank_failing_before_the_exchange_is_seen_by_its_peer():
     assert got[0][0] == "error"   # the all-gather ended with an error instead of waiting forever
 
 
-def _sharded_worker(rank, world, port, out_q):
+def _sharded_worker(rank, world, port, out_q, opts=None):
     import datetime
     import torch
     import torch.distributed as dist
@@ -150,7 +150,7 @@ def _sharded_worker(rank, world, port, out_q):
         grads = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
                  if s.kind == "grad"}
         mine, outs, ranks, cut, used = shard.compress_sharded(ctx, units, weights, acts, grads, wl.n_tokens,
-                                                              wl.lam, wl.budget)
+                                                              wl.lam, wl.budget, **(opts or {}))
         prods = {i: (o.U @ o.V).numpy().tobytes() for i, o in zip(mine, outs)}
         out_q.put((rank, "ok", (list(mine), ranks.numpy().tolist(), int(used.item()), prods)))
     except Exception as e:
@@ -162,10 +162,17 @@ def _sharded_worker(rank, world, port, out_q):
             pass
 
 
-def test_compress_sharded_matches_one_process(monkeypatch):
+SHARD_OPTS = [None, {"mode": 1}, {"score": "energy_ratio", "unit_weights": [0.5, 1.0, 2.0, 1.5, 0.7, 1.2, 0.9]},
+              {"score": "swift_hybrid", "unit_weights": [1.0, 2.0, 0.5, 1.0, 3.0, 1.0, 0.25], "alpha": 0.4}]
+
+
+@pytest.mark.parametrize("opts", SHARD_OPTS, ids=["half_sigma2", "per_param", "energy_ratio", "swift_hybrid"])
+def test_compress_sharded_matches_one_process(monkeypatch, opts):
     """The sharded driver over two gloo ranks, with the library calls replaced by the oracle
     stand-in in each rank: the ranks agree on the allocation, every unit is mapped back by
-    exactly one rank, and the result equals the single-process pipeline's."""
+    exactly one rank, and the result equals the single-process pipeline's, for every
+    allocation key the sharded driver offers (the options reach the global allocation; unit
+    weights are indexed over all units, not over a rank's share)."""
     import torch
     from synth import recipes
     from tests import cpu_abi_standin as standin
@@ -173,7 +180,7 @@ def test_compress_sharded_matches_one_process(monkeypatch):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_sharded_worker, args=(r, 2, port, q)) for r in range(2)]
+    procs = [ctx.Process(target=_sharded_worker, args=(r, 2, port, q, opts)) for r in range(2)]
     for p in procs:
         p.start()
     got = {}
@@ -200,10 +207,21 @@ def test_compress_sharded_matches_one_process(monkeypatch):
             if s.kind == "act"}
     grads = {n: torch.from_numpy(recipes.gen_stream(wl, s, 0, wl.n_tokens)) for n, s in wl.sites.items()
              if s.kind == "grad"}
-    res = pipeline.compress(c, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget)
+    res = pipeline.compress(c, units, weights, acts, grads, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                            **(opts or {}))
     assert res.ranks.tolist() == r0 and int(res.used.item()) == u0
     prods = dict(p0)
     prods.update(p1)
     for i, o in enumerate(res.units):
         np.testing.assert_array_equal(np.frombuffer(prods[i], dtype=np.float32).reshape(o.m, o.n),
                                       (o.U @ o.V).numpy())
+
+
+def test_compress_sharded_rejects_what_it_cannot_do():
+    from vlm_compression_fac_b300 import shard as S
+    with pytest.raises(ValueError):
+        S.compress_sharded(None, [], {}, {}, {}, 10, 0.01, 100, score="empirical_fisher")
+    with pytest.raises(ValueError):
+        S.compress_sharded(None, [object()], {}, {}, {}, 10, 0.01, 100, unit_weights=[1.0, 2.0])
+    with pytest.raises(ValueError):
+        S.compress_sharded(None, [], {}, {}, {}, 10, 0.01, None)

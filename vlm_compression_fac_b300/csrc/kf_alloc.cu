@@ -37,6 +37,7 @@ __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_un
 // by the unit's energy sum sigma^2), times the unit's weight when weights are given (a
 // weight that is negative or not a number counts as 0).  float32, one rounding per operation.
 constexpr int MODE_GIVEN_KEYS = 100;  // internal: the caller's keys, as given
+constexpr int MODE_SWIFT_HYBRID = 101;  // internal: Swift-SVD B hybrid keys built from sigma
 
 __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off,
                                   const int64_t* __restrict__ cost, int n_units, int64_t n, int mode,
@@ -62,6 +63,36 @@ __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t
     }
     const unsigned bits = ~__float_as_uint(sc);
     keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(uint32_t(g));
+  }
+}
+
+// Swift-SVD B: the closed-form loss of unit u truncated to rank k is the energy it drops,
+// eps[g] = sum of sigma^2 from component g to the end of the unit (float64, one term at a
+// time from the unit's last component upward: the square of a float32 value is exact in
+// float64, so the sum order alone fixes the result).  One thread per unit.
+__global__ void swift_eps_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off, int n_units,
+                                 double* __restrict__ eps) {
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
+    double acc = 0.0;
+    for (int64_t g = off[u + 1] - 1; g >= off[u]; --g) {
+      const double v = sigma[g];
+      acc = acc + v * v;
+      eps[g] = acc;
+    }
+  }
+}
+
+// Swift-SVD B hybrid score as a key per component: component k of unit u gets the unit's
+// score at rank k, beta_u^alpha * (log(e + eps_k))^(1 - alpha), in float64 rounded once to
+// float32 (beta not positive or not a number: key 0).
+__global__ void swift_keys_kernel(const double* __restrict__ eps, const int64_t* __restrict__ off, int n_units,
+                                  int64_t n, const float* __restrict__ beta, double alpha, float* __restrict__ keys) {
+  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += int64_t(gridDim.x) * blockDim.x) {
+    const int u = unit_of(off, n_units, g);
+    const float b = beta ? beta[u] : 1.f;
+    float k = 0.f;
+    if (b > 0.f) k = float(pow(double(b), alpha) * pow(log(2.718281828459045 + eps[g]), 1.0 - alpha));
+    keys[g] = k;
   }
 }
 
@@ -405,6 +436,7 @@ size_t alloc_carve(Carve& cv, int64_t n, int64_t n_energy, AllocBufs& b) {
 }  // namespace
 
 int alloc_mode_given_keys() { return MODE_GIVEN_KEYS; }
+int alloc_mode_swift_hybrid() { return MODE_SWIFT_HYBRID; }
 
 size_t alloc_workspace(int64_t n, int64_t n_energy) {
   Carve cv(nullptr, 0, true);
@@ -415,7 +447,7 @@ size_t alloc_workspace(int64_t n, int64_t n_energy) {
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
                     int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
                     int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st,
-                    unsigned char* keep) {
+                    unsigned char* keep, double alpha) {
   (void)ctx;
   KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
   if (mode == KF_FIXED_RANK) {
@@ -431,8 +463,21 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
     unit_energy_kernel<<<unsigned(n_units), 256, 0, st>>>(sigma, off, b.energy); note_launch();
     KF_CUDA(cudaGetLastError());
   }
-  build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), weight, b.energy,
-                                                      b.ka); note_launch();
+  if (int(mode) == MODE_SWIFT_HYBRID) {
+    // eps (float64) in the second key buffer and the float keys in the prefix buffer: both
+    // are free until the first radix scatter and the cost prefix respectively.
+    double* eps = reinterpret_cast<double*>(b.kb);
+    float* hk = reinterpret_cast<float*>(b.prefix);
+    swift_eps_kernel<<<unsigned((n_units + 127) / 128), 128, 0, st>>>(sigma, off, n_units, eps); note_launch();
+    KF_CUDA(cudaGetLastError());
+    swift_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(eps, off, n_units, n, weight, alpha, hk); note_launch();
+    KF_CUDA(cudaGetLastError());
+    build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(hk, off, cost, n_units, n, MODE_GIVEN_KEYS, nullptr,
+                                                        nullptr, b.ka); note_launch();
+  } else {
+    build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), weight, b.energy,
+                                                        b.ka); note_launch();
+  }
   KF_CUDA(cudaGetLastError());
   // The keys are built in id order and every pass is stable, so sorting by the score word
   // alone (the upper 32 bits, four 8-bit passes) leaves equal scores in id order: the same
@@ -554,5 +599,5 @@ extern "C" kf_status score_and_allocate_noalloc(kf_ctx* ctx, const float* sigma,
   void* scratch = nullptr;
   KF_TRY(noalloc_scratch(ctx->device, &scratch));
   return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, nullptr, ranks, cut,
-                   used, scratch, NOALLOC_SCRATCH_BYTES, st, nullptr);
+                   used, scratch, NOALLOC_SCRATCH_BYTES, st, nullptr, 0.0);
 }

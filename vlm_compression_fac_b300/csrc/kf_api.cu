@@ -17,8 +17,9 @@ size_t alloc_workspace(int64_t n, int64_t n_energy);
 kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const int64_t* cost, int32_t n_units,
                     int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
                     int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st,
-                    unsigned char* keep);
+                    unsigned char* keep, double alpha);
 int alloc_mode_given_keys();
+int alloc_mode_swift_hybrid();
 }  // namespace kf
 
 using namespace kf;
@@ -113,6 +114,18 @@ void kf_destroy(kf_ctx* ctx) {
   if (ctx->d_status) cudaFree(ctx->d_status);
   if (ctx->h_flag) cudaFreeHost(ctx->h_flag);
   delete ctx;
+}
+
+kf_status kf_fp32_fma_probe(kf_ctx* ctx, int64_t iters, float* sink, double* flops, kf_stream_t stream) {
+  if (!ctx) return fail(KF_ERR_INVALID, "kf_fp32_fma_probe: null context");
+  if (iters <= 0 || !sink || !flops) return fail(KF_ERR_INVALID, "kf_fp32_fma_probe: arguments");
+  return launch_ffma_probe(ctx->sm_count, iters, sink, flops, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kf_status kf_set_wait_limit(kf_ctx* ctx, uint64_t limit_ns) {
+  if (!ctx) return fail(KF_ERR_INVALID, "kf_set_wait_limit: null context");
+  ctx->wait_ns = limit_ns ? static_cast<unsigned long long>(limit_ns) : 4000000000ull;
+  return KF_OK;
 }
 
 kf_status kf_sync_status(kf_ctx* ctx, kf_stream_t stream, int32_t* info) {
@@ -650,7 +663,7 @@ kf_status allocate_common(kf_ctx* ctx, const char* who, const float* sigma, cons
     return KF_OK;
   }
   return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget, mode, fixed_rank, weight, ranks, cut,
-                   used, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+                   used, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr, 0.0);
 }
 }  // namespace
 
@@ -691,7 +704,50 @@ kf_status score_and_allocate_keys(kf_ctx* ctx, const float* keys, const int64_t*
   }
   return alloc_run(ctx, keys, seg_offset, cost, n_units, n_components, budget,
                    static_cast<kf_alloc_mode>(alloc_mode_given_keys()), nullptr, nullptr, ranks, cut, used, workspace,
-                   workspace_bytes, st, keep);
+                   workspace_bytes, st, keep, 0.0);
+}
+
+kf_status score_and_allocate_hybrid(kf_ctx* ctx, const float* sigma, const int64_t* seg_offset, const int64_t* cost,
+                                    int32_t n_units, int64_t n_components, int64_t budget, const float* importance,
+                                    double alpha, int32_t* ranks, float* cut, int64_t* used, void* workspace,
+                                    size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "score_and_allocate_hybrid: null context"));
+  KF_TRY(need(n_units > 0 && n_components >= 0, "score_and_allocate_hybrid: sizes"));
+  KF_TRY(need(n_components < (int64_t(1) << 32), "score_and_allocate_hybrid: at most 2^32 - 1 components"));
+  KF_TRY(need(alpha >= 0.0 && alpha <= 1.0, "score_and_allocate_hybrid: alpha must lie in [0, 1]"));
+  KF_TRY(need(seg_offset && cost && ranks && (sigma != nullptr || n_components == 0),
+              "score_and_allocate_hybrid: null pointer"));
+  if (workspace_bytes < alloc_workspace(n_components > 0 ? n_components : 1, 0))
+    return fail(KF_ERR_WORKSPACE, "score_and_allocate_hybrid: workspace too small");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (n_components == 0) {
+    KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
+    if (used) KF_CUDA(cudaMemsetAsync(used, 0, sizeof(int64_t), st));
+    if (cut) KF_CUDA(cudaMemsetAsync(cut, 0xFF, 2 * sizeof(float), st));
+    return KF_OK;
+  }
+  return alloc_run(ctx, sigma, seg_offset, cost, n_units, n_components, budget,
+                   static_cast<kf_alloc_mode>(alloc_mode_swift_hybrid()), nullptr, importance, ranks, cut, used,
+                   workspace, workspace_bytes, st, nullptr, alpha);
+}
+
+int64_t kf_hybrid_ffn_budget(int64_t budget, int32_t n, const int64_t* d_model, const int64_t* n_dense,
+                             int64_t* dense_cost) {
+  if (n < 0 || (n > 0 && (!d_model || !n_dense))) {
+    fail(KF_ERR_INVALID, "kf_hybrid_ffn_budget: sizes or null pointer");
+    return -1;
+  }
+  int64_t cost = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (d_model[i] < 0 || n_dense[i] < 0) {
+      fail(KF_ERR_INVALID, "kf_hybrid_ffn_budget: negative entry");
+      return -1;
+    }
+    cost += d_model[i] * n_dense[i];
+  }
+  if (dense_cost) *dense_cost = cost;
+  const int64_t left = budget - cost;
+  return left > 0 ? left : 0;
 }
 
 // ----------------------------------------------------------------------- (5b)

@@ -13,9 +13,12 @@
 // enter as bfloat16 hi/lo splits.  TC_LOWER visits only the tiles that touch the lower
 // triangle (the covariance SYRK X += A^T A) and writes only i >= j.
 //
-// Every mbarrier wait is bounded (wall-clock limit read from %globaltimer); on expiry the
-// thread records KF_ERR_TIMEOUT in the device status word, the CTA drains what it issued
-// (again bounded), frees its tensor memory and returns.
+// Every mbarrier wait is bounded (wall-clock limit read from %globaltimer; the pipeline
+// waits use the context's limit, 4 s unless set otherwise); on expiry the thread records
+// KF_ERR_TIMEOUT in the device status word and the CTA stops issuing work.  Before it frees
+// its tensor memory and returns, the CTA always waits, on the long 4 s limit, for the last
+// TMA loads it issued and for every MMA it issued, so nothing it started is still writing
+// shared or tensor memory when it exits.
 #include "kf_internal.cuh"
 
 #include <cstring>
@@ -29,7 +32,7 @@ constexpr uint32_t B_BYTES = TBN * TBK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;  // stages + alignment + barriers
 constexpr uint32_t TMEM_COLS = 256;
-constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s
+constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s: default and drain limit
 constexpr int SUPER_M = 8, SUPER_N = 4;
 
 struct TcMaps {
@@ -46,6 +49,7 @@ struct TcArgs {
   int64_t kcb;   // k-blocks per accumulation chunk (0: the whole K range)
   int64_t ntm, ntn;
   int* status;
+  unsigned long long wait_ns;  // limit of the pipeline waits
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -75,12 +79,13 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false if the limit expired.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = now_ns();
   uint32_t spins = 0;
   while (!mbar_try(bar, parity)) {
-    if ((++spins & 255u) == 0 && now_ns() - t0 > WAIT_LIMIT_NS) return false;
+    if ((++spins & 255u) == 0 && now_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
           for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
             const int s = int(it % STAGES);
             const uint32_t ph = uint32_t((it / STAGES) & 1);
-            if (!mbar_wait(empty0 + 8 * s, ph ^ 1u)) {
+            if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, g.wait_ns)) {
               raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_EMPTY);
               atomicExch(&abort_flag, 1);
             }
@@ -249,12 +254,12 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
         }
       }
     producer_done:
-      // After an abort, every issued stage must still land before the CTA may exit.
-      if (*(volatile int*)&abort_flag) {
-        for (int64_t j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
-          if (!mbar_wait(full0 + 8 * int(j % STAGES), uint32_t((j / STAGES) & 1)))
-            raise_status(g.status, KF_ERR_TIMEOUT, WAIT_DRAIN);
-        }
+      // Every issued load must land before the CTA may exit, also when another thread gives
+      // up after this one has finished issuing: wait for the last STAGES loads (one per
+      // stage; earlier ones were consumed).  Without an abort they have landed already.
+      for (int64_t j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
+        if (!mbar_wait(full0 + 8 * int(j % STAGES), uint32_t((j / STAGES) & 1)))
+          raise_status(g.status, KF_ERR_TIMEOUT, WAIT_DRAIN);
       }
     }
   } else if (warp == 1) {
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
       for (int64_t c = 0; c < nchunks; ++c) {
         const int b = int(c & 1);
         if (c >= 2 && !*(volatile int*)&abort_flag) {
-          if (!mbar_wait(acce0 + 8 * b, uint32_t(((c >> 1) - 1) & 1))) {
+          if (!mbar_wait(acce0 + 8 * b, uint32_t(((c >> 1) - 1) & 1), g.wait_ns)) {
             raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
             atomicExch(&abort_flag, 1);
           }
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
           for (int64_t kb = kb0; kb < kb1; ++kb, ++it) {
             const int s = int(it % STAGES);
             const uint32_t ph = uint32_t((it / STAGES) & 1);
-            if (!mbar_wait(full0 + 8 * s, ph)) {
+            if (!mbar_wait(full0 + 8 * s, ph, g.wait_ns)) {
               raise_status(g.status, KF_ERR_TIMEOUT, WAIT_TMA_FULL);
               atomicExch(&abort_flag, 1);
             }
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
     bool all_ok = true;
     for (int64_t c = 0; c < nchunks; ++c) {
       const int b = int(c & 1);
-      bool ok = mbar_wait(accf0 + 8 * b, uint32_t((c >> 1) & 1));
+      bool ok = mbar_wait(accf0 + 8 * b, uint32_t((c >> 1) & 1), g.wait_ns);
       if (!ok) {
         raise_status(g.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
         atomicExch(&abort_flag, 1);
@@ -462,6 +467,7 @@ kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st) {
   a.kcb = g.kchunk > 0 ? (g.kchunk + TBK - 1) / TBK : 0;
   a.ntm = (g.M + TBM - 1) / TBM; a.ntn = (g.N + TBN - 1) / TBN;
   a.status = ctx->d_status;
+  a.wait_ns = ctx->wait_ns;
   const int64_t ntiles = count_tiles(g, a.ntm, a.ntn);
   if (ntiles > 0x7fffffff) return fail(KF_ERR_UNSUPPORTED, "tc_gemm: too many tiles");
   const bool am = g.a[0].mn_major, bm = g.b[0].mn_major;

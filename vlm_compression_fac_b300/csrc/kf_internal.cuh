@@ -39,6 +39,7 @@ struct kf_ctx {
   int* d_status = nullptr;          // int32[4] on the device: code, info, Jacobi flag, spare
   int* h_flag = nullptr;            // pinned host int: the Jacobi convergence poll
   kf::PFN_encodeTiled encode = nullptr;
+  unsigned long long wait_ns = 4000000000ull;  // limit of the tensor-core pipeline waits
   // whitened_svd profile (events on the caller's stream; flop counter at d_status + 4)
   bool prof_enabled = false;
   bool prof_valid = false;
@@ -135,6 +136,7 @@ struct TcGemm {
 kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st);
 
 // ------------------------------------------------------------ small kernels
+kf_status launch_ffma_probe(int sm_count, int64_t iters, float* sink, double* flops, cudaStream_t st);
 kf_status launch_fake_quant(const void* in, kf_dtype dt, int64_t rows, int64_t d, int64_t ld,
                             __nv_bfloat16* out, cudaStream_t st);
 kf_status launch_split_bf16(const float* in, int64_t rows, int64_t d, int64_t ld,

@@ -337,7 +337,32 @@ unsigned grid_for(int64_t n, int per = 256) {
   return unsigned(b);
 }
 
+// Peak probe of the FP32 FMA pipes: 16 independent fma chains per thread (enough to cover
+// the pipe latency at 8 resident CTAs of 256 threads per SM), the result kept live by a
+// store that depends on it.
+__global__ void __launch_bounds__(256) ffma_probe_kernel(int64_t iters, float* __restrict__ sink) {
+  float a[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) a[j] = float(threadIdx.x) * 1e-7f + float(j);
+  const float x = 0.9999f + 1e-9f * float(threadIdx.x), y = 1e-6f;
+  for (int64_t i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) a[j] = fmaf(a[j], x, y);
+  }
+  float t = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t += a[j];
+  if (t == 1234.5f) sink[blockIdx.x & 7] = t;
+}
+
 }  // namespace
+
+kf_status launch_ffma_probe(int sm_count, int64_t iters, float* sink, double* flops, cudaStream_t st) {
+  const unsigned blocks = unsigned(sm_count) * 8u;
+  ffma_probe_kernel<<<blocks, 256, 0, st>>>(iters, sink); note_launch();
+  *flops = double(blocks) * 256.0 * double(iters) * 16.0 * 2.0;
+  return check_cuda(cudaGetLastError(), "ffma_probe launch");
+}
 
 kf_status launch_fake_quant(const void* in, kf_dtype dt, int64_t rows, int64_t d, int64_t ld,
                             __nv_bfloat16* out, cudaStream_t st) {

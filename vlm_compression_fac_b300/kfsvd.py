@@ -32,7 +32,8 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "whiten_workspace_size", "whiten", "kf_svd_profile_enable", "kf_svd_profile_read",
             "whitened_svd_workspace_size", "whitened_svd",
             "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_weighted",
-            "score_and_allocate_keys", "score_and_allocate_noalloc",
+            "score_and_allocate_keys", "score_and_allocate_noalloc", "score_and_allocate_hybrid",
+            "kf_set_wait_limit", "kf_hybrid_ffn_budget", "kf_fp32_fma_probe",
             "empirical_fisher_workspace_size", "empirical_fisher_accumulate", "empirical_fisher_finalize",
             "unwhiten_workspace_size", "unwhiten",
             "activation_covariance_workspace_size", "activation_covariance", "activation_eig_workspace_size",
@@ -90,6 +91,11 @@ _SIGS = {
     "score_and_allocate_weighted": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_keys": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "score_and_allocate_noalloc": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _I32, _P, _P, _P, _P, _P]),
+    "score_and_allocate_hybrid": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _P, ctypes.c_double, _P, _P, _P, _P,
+                                         _SZ, _P]),
+    "kf_set_wait_limit": (_I32, [_P, ctypes.c_uint64]),
+    "kf_fp32_fma_probe": (_I32, [_P, _I64, _P, ctypes.POINTER(ctypes.c_double), _P]),
+    "kf_hybrid_ffn_budget": (_I64, [_I64, _I32, _P, _P, _P]),
     "empirical_fisher_finalize": (_I32, [_P, _P, _I64, _I64, _P, _P]),
     "empirical_fisher_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "empirical_fisher_accumulate": (_I32, [_P, _P, _I32, _I64, _P, _I32, _I64, _I64, _I64, _I64, _P, _I64, _P,
@@ -195,6 +201,36 @@ class Context:
         if st != KF_OK:
             raise KfsvdError(st, (lib().kf_last_error() or b"").decode())
         return info.value
+
+
+def kf_fp32_fma_probe(ctx: Context, iters: int, sink, stream=None) -> float:
+    """Launches the FP32 FMA peak probe on ``stream``; returns the flops of the launch (the
+    caller times it).  ``sink``: a float32 device tensor of 8 elements."""
+    f = ctypes.c_double(0.0)
+    _check(lib().kf_fp32_fma_probe(ctx.handle, int(iters), _ptr(sink), ctypes.byref(f), _stream(stream)))
+    return float(f.value)
+
+
+def kf_set_wait_limit(ctx: Context, limit_ns: int):
+    """Limit (ns) of each tensor-core pipeline wait for later calls on ctx; 0 = the 4 s default."""
+    _check(lib().kf_set_wait_limit(ctx.handle, int(limit_ns)))
+
+
+def kf_hybrid_ffn_budget(budget: int, d_model: Sequence[int], n_dense: Sequence[int], with_cost: bool = False):
+    """Parameters left for the low-rank factors after the dense FFN channels (host arithmetic
+    in the library): max(budget - dense_cost, 0), dense_cost = sum d_model[i] n_dense[i];
+    ``with_cost`` returns (left, dense_cost)."""
+    k = len(d_model)
+    if len(n_dense) != k:
+        raise ValueError("kf_hybrid_ffn_budget: d_model and n_dense need the same length")
+    a = (ctypes.c_int64 * max(k, 1))(*[int(x) for x in d_model])
+    b = (ctypes.c_int64 * max(k, 1))(*[int(x) for x in n_dense])
+    c = ctypes.c_int64(0)
+    v = int(lib().kf_hybrid_ffn_budget(int(budget), k, ctypes.cast(a, ctypes.c_void_p),
+                                       ctypes.cast(b, ctypes.c_void_p), ctypes.byref(c)))
+    if v < 0:
+        raise KfsvdError(KF_ERR_INVALID, (lib().kf_last_error() or b"").decode())
+    return (v, int(c.value)) if with_cost else v
 
 
 def kf_launch_count() -> int:
@@ -314,6 +350,18 @@ def score_and_allocate_keys(ctx: Context, keys, seg_offset, cost, budget: int, r
     _check(lib().score_and_allocate_keys(ctx.handle, _ptr(keys), _ptr(seg_offset), _ptr(cost), n_units, n, int(budget),
                                          _ptr(ranks), _ptr(keep), _ptr(cut), _ptr(used), _ptr(ws), wsb,
                                          _stream(stream)))
+
+
+def score_and_allocate_hybrid(ctx: Context, sigma, seg_offset, cost, budget: int, ranks, alpha: float,
+                              importance=None, cut=None, used=None, workspace=None, stream=None):
+    """Sort-and-truncate on Swift-SVD's hybrid score beta^alpha log(e + eps*_k)^(1 - alpha), one
+    key per component (``importance``: float32 device tensor of the units' beta, or None)."""
+    n_units = int(cost.numel())
+    n = int(sigma.numel()) if sigma is not None else 0
+    ws, wsb = _ws(score_and_allocate_workspace_size(n, n_units), workspace, ranks.device)
+    _check(lib().score_and_allocate_hybrid(ctx.handle, _ptr(sigma), _ptr(seg_offset), _ptr(cost), n_units, n,
+                                           int(budget), _ptr(importance), float(alpha), _ptr(ranks), _ptr(cut),
+                                           _ptr(used), _ptr(ws), wsb, _stream(stream)))
 
 
 def empirical_fisher_finalize(ctx: Context, score_sum, n_tokens: int, keys, stream=None):

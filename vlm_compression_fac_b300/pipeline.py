@@ -20,6 +20,7 @@ need are released, so that workloads far larger than device memory stream throug
 """
 from __future__ import annotations
 
+import contextlib
 from dataclasses import dataclass, field
 from typing import Callable, Dict, List, Optional, Sequence, Union
 
@@ -90,6 +91,48 @@ def unit_specs(wl) -> List[UnitSpec]:
             for u in wl.units]
 
 
+SCORES = (None, "half_sigma2", "energy_ratio", "empirical_fisher", "swift_hybrid")
+
+
+def _on_stream(stream):
+    """Every library call of a driver runs on ``stream`` and so must the torch operations
+    between them (zero fills, slicing, concatenation, the caching allocator's reuse): the
+    drivers run under ``torch.cuda.stream(stream)``.  ``stream`` is a torch.cuda.Stream (or
+    an ExternalStream wrapping a foreign handle) or None for the current stream."""
+    if stream is None:
+        return contextlib.nullcontext()
+    if not isinstance(stream, torch.cuda.Stream):
+        raise TypeError("stream must be a torch.cuda.Stream (torch.cuda.ExternalStream for a raw handle) or None")
+    return torch.cuda.stream(stream)
+
+
+def _allocate(ctx, sig, off, cost, budget, ranks, cut, used, stream, score=None, mode=K.KF_KEY_HALF_SIGMA2,
+              fixed_rank=None, unit_weights=None, alpha=None):
+    """The global allocation call for the scores that need no second pass over the rows:
+    1/2 sigma^2 (``mode`` may pick the per-parameter key), a fixed rank, UniRank's energy ratio
+    times ``unit_weights`` (I_l), or Swift-SVD's hybrid score with ``unit_weights`` as the
+    layer importance beta and ``alpha``."""
+    dev = ranks.device
+    w = None if unit_weights is None else torch.tensor([float(x) for x in unit_weights], dtype=torch.float32,
+                                                        device=dev)
+    if w is not None and w.numel() != ranks.numel():
+        raise ValueError("unit_weights: one weight per unit expected")
+    if score == "energy_ratio":
+        K.score_and_allocate_weighted(ctx, sig, off, cost, int(budget), ranks, mode=K.KF_KEY_ENERGY_RATIO,
+                                      unit_weight=w, cut=cut, used=used, stream=stream)
+    elif score == "swift_hybrid":
+        if alpha is None:
+            raise ValueError("score 'swift_hybrid' needs alpha")
+        K.score_and_allocate_hybrid(ctx, sig, off, cost, int(budget), ranks, float(alpha), importance=w, cut=cut,
+                                    used=used, stream=stream)
+    elif fixed_rank is not None:
+        fr = torch.full((ranks.numel(),), int(fixed_rank), dtype=torch.int32, device=dev)
+        K.score_and_allocate(ctx, sig, off, cost, 0, ranks, mode=K.KF_FIXED_RANK, fixed_rank=fr, cut=cut,
+                             used=used, stream=stream)
+    else:
+        K.score_and_allocate(ctx, sig, off, cost, int(budget), ranks, mode=mode, cut=cut, used=used, stream=stream)
+
+
 def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch.Tensor],
              acts: Union[Dict[str, torch.Tensor], RowsFn], grads: Union[Dict[str, torch.Tensor], RowsFn, None],
              n_tokens: int, lam: float = 1e-2, budget: Optional[int] = None, fixed_rank: Optional[int] = None,
@@ -99,7 +142,7 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
              groups: Optional[Sequence[Sequence[int]]] = None, chunk_tokens: int = 16384,
              keep_covs: Union[bool, Sequence[str]] = True, keep_whitened: bool = True,
              score: Optional[str] = None, unit_weights: Optional[Sequence[float]] = None,
-             defer_allocation: bool = False) -> Result:
+             defer_allocation: bool = False, alpha: Optional[float] = None) -> Result:
     """Runs the five steps.
 
     ``acts``/``grads``: dicts of resident (n_tokens x d) device tensors, or ``acts`` a callable
@@ -115,7 +158,12 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     layer importance) or "empirical_fisher" (LASER: each component's contribution to the
     empirical-Fisher loss, 1/2 mean_t (a_t . u_i)^2 (g_t . v_i)^2, from a second pass over the
     calibration rows with every component mapped back; the kept set of a unit is then any
-    subset, and its factors are the kept columns of U and rows of V).
+    subset, and its factors are the kept columns of U and rows of V), or "swift_hybrid"
+    (Swift-SVD's hybrid score beta^alpha log(e + eps*_k)^(1 - alpha) per component, with
+    ``unit_weights`` the layers' importance beta and ``alpha`` in [0, 1]).
+    ``stream``: a torch.cuda.Stream or None; the whole driver runs on it.  Device-side
+    failures (a non-positive Cholesky pivot, Jacobi not converged, a wait that gave up) are
+    raised as KfsvdError at the host read of the ranks.
     ``defer_allocation``: stop after the spectra (steps 1-4) and return the units with their
     sigma, vecs and the factors the unwhitening reads (ranks, cut and used are None); the
     sharded driver allocates over every rank's spectra and then maps back with ``_finish``.
@@ -124,11 +172,20 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
     pass) and around every kfac_accumulate and empirical_fisher_accumulate call ("syrk<",
     "syrk>", "fisher<", "fisher>"), so a caller can record CUDA events there.
     """
-    if score not in (None, "half_sigma2", "energy_ratio", "empirical_fisher"):
+    if score not in SCORES:
         raise ValueError("compress: unknown score %r" % (score,))
-    if score in ("energy_ratio", "empirical_fisher") and (budget is None or fixed_rank is not None) \
+    if score in ("energy_ratio", "empirical_fisher", "swift_hybrid") and (budget is None or fixed_rank is not None) \
             and not defer_allocation:
         raise ValueError("compress: score %r needs a budget and no fixed rank" % (score,))
+    with _on_stream(stream):
+        return _compress(ctx, units, weights, acts, grads, n_tokens, lam, budget, fixed_rank, mode, quant, tol,
+                         max_sweeps, stream, sync_timer, site_dims, act_sites, groups, chunk_tokens, keep_covs,
+                         keep_whitened, score, unit_weights, defer_allocation, alpha)
+
+
+def _compress(ctx, units, weights, acts, grads, n_tokens, lam, budget, fixed_rank, mode, quant, tol, max_sweeps,
+              stream, sync_timer, site_dims, act_sites, groups, chunk_tokens, keep_covs, keep_whitened, score,
+              unit_weights, defer_allocation, alpha) -> Result:
     mark = sync_timer or (lambda _name: None)
     dev = next(iter(weights.values())).device
     if callable(acts):
@@ -233,6 +290,7 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
         mark("svd")
 
     if defer_allocation:
+        ctx.sync_status(stream)
         for o, sw_ in zip(outs, sweeps_dev.cpu().tolist()):
             o.sweeps = int(sw_)
         return Result(outs, all_covs, None, None, None)
@@ -249,23 +307,14 @@ def compress(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict[str, torch
         qsites = quant_sites if quant else set()
         return _fisher_allocation(ctx, units, outs, weights, rows_fn, qsites, n_tokens, chunk_tokens, int(budget),
                                   off, cost, ranks, cut, used, sweeps_dev, all_covs, stream, mark)
-    if score == "energy_ratio":
-        w = None if unit_weights is None else torch.tensor(list(unit_weights), dtype=torch.float32, device=dev)
-        K.score_and_allocate_weighted(ctx, sig, off, cost, int(budget), ranks, mode=K.KF_KEY_ENERGY_RATIO,
-                                      unit_weight=w, cut=cut, used=used, stream=stream)
-        return _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, stream, mark)
-    if fixed_rank is not None:
-        fr = torch.full((len(outs),), int(fixed_rank), dtype=torch.int32, device=dev)
-        K.score_and_allocate(ctx, sig, off, cost, 0, ranks, mode=K.KF_FIXED_RANK, fixed_rank=fr, cut=cut,
-                             used=used, stream=stream)
-    else:
-        K.score_and_allocate(ctx, sig, off, cost, int(budget), ranks, mode=mode, cut=cut, used=used,
-                             stream=stream)
+    _allocate(ctx, sig, off, cost, budget, ranks, cut, used, stream, score=score, mode=mode, fixed_rank=fixed_rank,
+              unit_weights=unit_weights, alpha=alpha)
     return _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, stream, mark)
 
 
 def _finish(ctx, units, outs, weights, ranks, cut, used, sweeps_dev, all_covs, stream, mark) -> Result:
     dev = ranks.device
+    ctx.sync_status(stream)
     ranks_h = ranks.cpu().tolist()
     sweeps_h = sweeps_dev.cpu().tolist()
     mark("allocate")
@@ -319,6 +368,7 @@ def _fisher_allocation(ctx, units, outs, weights, rows_fn, quant_sites, n_tokens
     keys_t = torch.cat(keys)
     keep = torch.empty(keys_t.numel(), dtype=torch.uint8, device=dev)
     K.score_and_allocate_keys(ctx, keys_t, off, cost, budget, ranks, keep=keep, cut=cut, used=used, stream=stream)
+    ctx.sync_status(stream)
     ranks_h = ranks.cpu().tolist()
     sweeps_h = sweeps_dev.cpu().tolist()
     mark("allocate")
@@ -363,8 +413,15 @@ def compress_activation_only(ctx: K.Context, units: Sequence[UnitSpec], weights:
     (activation_covariance), the eigenpairs in batches of equal n (activation_eig); then one
     global sort-and-truncate on 1/2 sigma^2 over the first min(m, n) components of every
     unit (score_and_allocate) and the factors U = W V_k, V = V_k^T (activation_factors).
-    ``acts`` and ``groups`` as for ``compress``; ``sync_timer`` tags: "kfac", "cov", "eig"
-    per group, "allocate", "factors", and "syrk<"/"syrk>" around every kfac_accumulate."""
+    ``acts``, ``groups`` and ``stream`` as for ``compress``; ``sync_timer`` tags: "kfac", "cov",
+    "eig" per group, "allocate", "factors", and "syrk<"/"syrk>" around every kfac_accumulate."""
+    with _on_stream(stream):
+        return _compress_activation_only(ctx, units, weights, acts, n_tokens, budget, quant, tol, max_sweeps, stream,
+                                         sync_timer, site_dims, groups, chunk_tokens, keep_cov)
+
+
+def _compress_activation_only(ctx, units, weights, acts, n_tokens, budget, quant, tol, max_sweeps, stream, sync_timer,
+                              site_dims, groups, chunk_tokens, keep_cov) -> Result:
     mark = sync_timer or (lambda _name: None)
     dev = next(iter(weights.values())).device
     if callable(acts):
@@ -429,6 +486,7 @@ def compress_activation_only(ctx: K.Context, units: Sequence[UnitSpec], weights:
     cut = torch.empty(2, dtype=torch.float32, device=dev)
     used = torch.zeros(1, dtype=torch.int64, device=dev)
     K.score_and_allocate(ctx, sig, off, cost, int(budget), ranks, cut=cut, used=used, stream=stream)
+    ctx.sync_status(stream)
     ranks_h = ranks.cpu().tolist()
     sweeps_h = sweeps_dev.cpu().tolist()
     mark("allocate")
@@ -503,6 +561,13 @@ def compress_hybrid_ffn(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict
     take part in the global allocation as units of their own; the other columns stay dense and
     their cost (d_model per channel and projection) is taken off the budget first.  Every
     other unit is allocated as usual; all entries are mapped back with ``unwhiten``."""
+    with _on_stream(stream):
+        return _compress_hybrid_ffn(ctx, units, weights, acts, grads, n_tokens, lam, budget, r_temp, n_svd, pairs,
+                                    quant, tol, max_sweeps, stream, site_dims, act_sites, chunk_tokens)
+
+
+def _compress_hybrid_ffn(ctx, units, weights, acts, grads, n_tokens, lam, budget, r_temp, n_svd, pairs, quant, tol,
+                         max_sweeps, stream, site_dims, act_sites, chunk_tokens) -> HybridResult:
     keep = sorted({units[i].x_site for p in pairs for i in p} | {units[i].g_site for p in pairs for i in p})
     base = compress(ctx, units, weights, acts, grads, n_tokens, lam=lam, budget=None, quant=quant, tol=tol,
                     max_sweeps=max_sweeps, stream=stream, site_dims=site_dims, act_sites=act_sites,
@@ -517,7 +582,8 @@ def compress_hybrid_ffn(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict
     entries = [HybridEntry("unit", i, outs[i]) for i in range(len(units)) if i not in in_pair]
     w_of = {id(e.out): wview(units[e.unit]) for e in entries}
     splits = []
-    dense_cost = 0
+    dense_dm: List[int] = []     # per dense projection: d_model and its dense channel count
+    dense_n: List[int] = []
     new_svd: List[HybridEntry] = []
     for gi, ui in pairs:
         facs = {}
@@ -535,7 +601,8 @@ def compress_hybrid_ffn(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict
         splits.append({"gate": gi, "up": ui, "svd": svd, "dense": dense, "errors": err, "keys": keys})
         for i in (gi, ui):
             u = units[i]
-            dense_cost += u.m * int(dense.numel())
+            dense_dm.append(u.m)
+            dense_n.append(int(dense.numel()))
             k = int(svd.numel())
             if k == 0:
                 continue
@@ -574,8 +641,9 @@ def compress_hybrid_ffn(ctx: K.Context, units: Sequence[UnitSpec], weights: Dict
     ranks = torch.empty(len(entries), dtype=torch.int32, device=dev)
     cut = torch.empty(2, dtype=torch.float32, device=dev)
     used = torch.zeros(1, dtype=torch.int64, device=dev)
-    left = max(int(budget) - dense_cost, 0)
+    left, dense_cost = K.kf_hybrid_ffn_budget(int(budget), dense_dm, dense_n, with_cost=True)
     K.score_and_allocate(ctx, sig, off, cost, left, ranks, cut=cut, used=used, stream=stream)
+    ctx.sync_status(stream)
     for e, r in zip(entries, ranks.cpu().tolist()):
         o = e.out
         o.rank = int(r)

@@ -78,15 +78,29 @@ def gather_spectra(local: Dict[int, torch.Tensor], lens: Sequence[int], parts: S
     return full
 
 
-def compress_sharded(ctx, units, weights, acts, grads, n_tokens: int, lam: float, budget: int, group=None,
-                     work: Optional[Sequence[float]] = None, **kw):
+def compress_sharded(ctx, units, weights, acts, grads, n_tokens: int, lam: float, budget: Optional[int],
+                     group=None, work: Optional[Sequence[float]] = None, score: Optional[str] = None,
+                     mode: Optional[int] = None, fixed_rank: Optional[int] = None,
+                     unit_weights: Optional[Sequence[float]] = None, alpha: Optional[float] = None, **kw):
     """The whole path over all ranks of ``group``: this rank runs steps 1-4 for its share of the
     units (``pipeline.compress`` with the allocation deferred), the spectra are all-gathered,
     every rank runs the same allocation over all units, and each maps back its own units.
+    The allocation options are those of ``pipeline.compress`` and mean the same here:
+    ``score`` (1/2 sigma^2, "energy_ratio" or "swift_hybrid"), ``mode`` (the per-parameter
+    key), ``fixed_rank``, ``unit_weights`` (one per unit of ``units``, global order) and
+    ``alpha``.  LASER's empirical-Fisher score needs a second pass over every unit's rows
+    before the global sort and is not offered here (ValueError).  Any other keyword goes to
+    ``pipeline.compress`` for steps 1-4.
     Returns (this rank's unit indices, their pipeline.UnitOut, the global ranks tensor,
     cut, used)."""
     from . import kfsvd as K
     from . import pipeline
+    if score not in (None, "half_sigma2", "energy_ratio", "swift_hybrid"):
+        raise ValueError("compress_sharded: score %r is not supported across ranks" % (score,))
+    if unit_weights is not None and len(unit_weights) != len(units):
+        raise ValueError("compress_sharded: unit_weights needs one weight per unit")
+    if (budget is None) == (fixed_rank is None) or (fixed_rank is not None and score not in (None, "half_sigma2")):
+        raise ValueError("compress_sharded: give a budget or a fixed rank (the latter with the default score)")
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
     w = list(work) if work is not None else [unit_work(u.m, u.n, n_tokens) for u in units]
@@ -103,7 +117,9 @@ def compress_sharded(ctx, units, weights, acts, grads, n_tokens: int, lam: float
     ranks = torch.empty(len(units), dtype=torch.int32, device=dev)
     cut = torch.empty(2, dtype=torch.float32, device=dev)
     used = torch.zeros(1, dtype=torch.int64, device=dev)
-    K.score_and_allocate(ctx, full, off, cost, int(budget), ranks, cut=cut, used=used)
+    pipeline._allocate(ctx, full, off, cost, 0 if budget is None else int(budget), ranks, cut, used, None,
+                       score=score, mode=K.KF_KEY_HALF_SIGMA2 if mode is None else int(mode), fixed_rank=fixed_rank,
+                       unit_weights=unit_weights, alpha=alpha)
     local_ranks = ranks[torch.tensor(mine, dtype=torch.int64, device=dev)] if mine else ranks[:0]
     sweeps = torch.tensor([o.sweeps for o in outs.units], dtype=torch.int32, device=dev)
     res = pipeline._finish(ctx, [units[i] for i in mine], outs.units, weights, local_ranks, cut, used, sweeps, {},
