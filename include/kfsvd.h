@@ -190,7 +190,9 @@ KF_API kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, con
  * problem of the call has converged.
  * For each problem: C = W~^T W~ (KF_SIDE_RIGHT) or W~ W~^T (KF_SIDE_LEFT) in float32;
  * C = Q Lambda Q^T by blocked parallel cyclic Jacobi (32-wide blocks, round-robin pairing,
- * every 64 x 64 pair problem diagonalised in shared memory) until every block pair has
+ * one sweep of plane rotations per 64 x 64 pair problem in shared memory, the block rotations
+ * applied to C and Q on the tensor cores with every float32 operand as three bfloat16 planes,
+ * float32-accurate) until every block pair has
  * |c_pq| <= tol * sqrt(c_pp c_qq) (or below a float32 rounding floor).  The vectors are then
  * sorted by their Rayleigh values ||W~ q|| / ||q|| (evaluated on W~ itself, not on C) and
  * refined by two passes of windowed Rayleigh-Ritz: every window of 128 consecutive vectors
@@ -218,10 +220,14 @@ typedef struct {
 typedef struct {
   float gram_ms, jacobi_ms, rayleigh_ms, refine_ms;  /* refine: windowed refinement + final sort */
   int64_t jacobi_steps;          /* solve + apply launch pairs issued */
-  double jacobi_apply_flops;     /* executed multiply-add flops of the rotation products */
+  double jacobi_apply_flops;     /* executed tensor-core flops of the rotation products (bfloat16 plane products,
+                                    2 M N K per MMA) */
   float jacobi_solve_ms;         /* summed device time of the pair-solve launches */
   float jacobi_apply_ms;         /* summed device time of the rotation-apply launches */
   int64_t jacobi_apply_launches; /* number of rotation-apply launches timed */
+  double jacobi_apply_bytes;     /* algorithmic bytes of the rotation apply: C and Qt read and written once per
+                                    executed task (a C super-tile moves 64 KB in and 64 or 128 KB out, a Qt
+                                    panel 32 KB in and out) */
 } kf_svd_profile;
 
 /* Enables (1) or disables (0) recording of the profile by later whitened_svd calls. */

@@ -36,12 +36,6 @@ constexpr int64_t ACC_CHUNK = 8192;  // tokens per preprocessing chunk (float32 
 #define KF_SYRK_KCHUNK 2048
 #endif
 constexpr int64_t SYRK_KCHUNK = KF_SYRK_KCHUNK;
-// The same bound for the whitening / unwhitening products (mixed-sign sums of up to 28672
-// terms per pass, several passes per output).
-#ifndef KF_PRODUCT_KCHUNK
-#define KF_PRODUCT_KCHUNK 1024
-#endif
-constexpr int64_t PRODUCT_KCHUNK = KF_PRODUCT_KCHUNK;
 constexpr int FINAL_SLOTS = 1024;
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -226,92 +220,12 @@ kf_status kf_finalize_covariance(kf_ctx* ctx, float* cov, int64_t ldc, int64_t d
 // --------------------------------------------------------------------- (2)+(3)
 namespace {
 
-// A matrix operand for the tensor-core engine: bfloat16 planes whose sum is the value
-// (one plane for bfloat16 data; two (hi + lo, 16 significant bits) or three (the full 24-bit
-// float32 significand) for float32 data), 16-byte aligned rows.
-struct Planes {
-  const __nv_bfloat16* p[3];
-  int64_t ld;
-  int n;  // 1, 2 or 3
-};
-
-// Room for the planes of a rows x cols operand.
-struct PlaneBuf {
-  __nv_bfloat16* p[3] = {nullptr, nullptr, nullptr};
-  int64_t ld = 0;
-  int n = 0;
-};
-PlaneBuf take_planes(Carve& cv, int64_t rows, int64_t cols, int nplanes) {
-  PlaneBuf b;
-  b.ld = round_up(cols, 8);
-  b.n = nplanes;
-  for (int i = 0; i < nplanes; ++i) b.p[i] = cv.take<__nv_bfloat16>(size_t(rows) * b.ld);
-  return b;
-}
-
-// float32 rows x cols (ld) -> the buffer's planes (two or three).
-kf_status split_f32(const float* in, int64_t ld, int64_t rows, int64_t cols, const PlaneBuf& b, Planes* out,
-                    cudaStream_t st) {
-  if (b.n == 3) {
-    KF_TRY(launch_split3_bf16(in, rows, cols, ld, b.p[0], b.p[1], b.p[2], b.ld, st));
-  } else {
-    KF_TRY(launch_split_bf16(in, rows, cols, ld, b.p[0], b.p[1], b.ld, st));
-  }
-  *out = Planes{{b.p[0], b.p[1], b.n == 3 ? b.p[2] : nullptr}, b.ld, b.n};
-  return KF_OK;
-}
-
-// A caller matrix (bfloat16 or float32) as planes: bfloat16 rows that are already aligned
-// are used in place; other bfloat16 rows are copied to an aligned plane; float32 is split.
-kf_status as_planes(const void* in, kf_dtype dt, int64_t ld, int64_t rows, int64_t cols, const PlaneBuf& b,
-                    Planes* out, cudaStream_t st) {
-  if (dt == KF_F32) return split_f32(static_cast<const float*>(in), ld, rows, cols, b, out, st);
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(in);
-  if ((reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ld % 8) == 0) {
-    *out = Planes{{x, nullptr, nullptr}, ld, 1};
-    return KF_OK;
-  }
-  KF_TRY(launch_copy_bf16(x, rows, cols, ld, b.p[0], b.ld, st));
-  *out = Planes{{b.p[0], nullptr, nullptr}, b.ld, 1};
-  return KF_OK;
-}
-
-// D (M x N float32, ldd) = A B on the tensor cores, A and B given as planes: every cross
-// term A_i B_j with i + j < max(A.n, B.n) (0-based), i.e. all terms down to the last plane's
-// weight; the omitted terms are below the rounding of the planes themselves.  Up to three
-// terms run in one launch, further terms accumulate in a second one.
-// a_mn / b_mn: the operand is stored MN-major (A as K x M rows, B as K x N rows).
-kf_status tc_product(kf_ctx* ctx, int64_t M, int64_t N, int64_t K, const Planes& A, bool a_mn, const Planes& B,
-                     bool b_mn, int krange, float* D, int64_t ldd, cudaStream_t st) {
-  const int L = A.n > B.n ? A.n : B.n;
-  TcOperand ta[9], tb[9];
-  int nt = 0;
-  for (int i = 0; i < A.n; ++i)
-    for (int j = 0; j < B.n; ++j)
-      if (i + j < L) {
-        ta[nt] = TcOperand{A.p[i], A.ld, a_mn};
-        tb[nt] = TcOperand{B.p[j], B.ld, b_mn};
-        ++nt;
-      }
-  for (int t0 = 0; t0 < nt; t0 += 3) {
-    TcGemm g{};
-    g.M = M; g.N = N; g.K = K;
-    g.D = D; g.ldd = ldd; g.accumulate = t0 > 0; g.sched = TC_FULL; g.krange = krange;
-    g.kchunk = PRODUCT_KCHUNK;
-    g.npass = nt - t0 < 3 ? nt - t0 : 3;
-    for (int p = 0; p < g.npass; ++p) {
-      g.a[p] = ta[t0 + p];
-      g.b[p] = tb[t0 + p];
-    }
-    KF_TRY(tc_gemm(ctx, g, st));
-  }
-  return KF_OK;
-}
-
 struct WhitenBufs {
   float *dinv, *T, *tt;
   PlaneBuf w, sg, t, sx;
   int64_t ldT;
+  char *cws, *tws;          // Cholesky trailing-update planes; triangular-inverse doubling levels
+  size_t cws_bytes, tws_bytes;
 };
 
 size_t whiten_carve(Carve& cv, int64_t m, int64_t n, bool w_f32, WhitenBufs& b) {
@@ -320,6 +234,10 @@ size_t whiten_carve(Carve& cv, int64_t m, int64_t n, bool w_f32, WhitenBufs& b) 
   b.ldT = round_up(n, 8);
   b.T = cv.take<float>(size_t(m) * b.ldT);
   b.tt = cv.take<float>(trtri_tmp_floats(mx));
+  b.cws_bytes = chol_workspace_bytes(mx);
+  b.cws = cv.take<char>(b.cws_bytes);
+  b.tws_bytes = trtri_workspace_bytes(m < n ? m : n);
+  b.tws = cv.take<char>(b.tws_bytes);
   b.w = take_planes(cv, m, n, w_f32 ? 3 : 1);
   b.sg = take_planes(cv, n, n, 3);
   b.t = take_planes(cv, m, n, 3);
@@ -356,9 +274,9 @@ kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const floa
   // S_x = chol_lower(X)^T  (and S_x^-1 for the left Gram side)
   if (!(flags & KF_REUSE_SX)) {
     KF_TRY(launch_copy(X, ldx, Sx, ldsx, m, m, false, st));
-    KF_TRY(cholesky_lower(ctx, Sx, ldsx, m, b.dinv, st));
+    KF_TRY(cholesky_lower(ctx, Sx, ldsx, m, b.dinv, b.cws, b.cws_bytes, st));
     if (side == KF_SIDE_LEFT && !(flags & KF_REUSE_SINV)) {
-      KF_TRY(trtri_lower(ctx, Sx, ldsx, m, b.dinv, Sinv, ldsi, b.tt, st));   // L_x^-1
+      KF_TRY(trtri_lower(ctx, Sx, ldsx, m, b.dinv, Sinv, ldsi, b.tt, b.tws, b.tws_bytes, st));   // L_x^-1
       KF_TRY(launch_transpose_inplace(Sinv, ldsi, m, st));                   // S_x^-1 = L_x^-T
     }
     KF_TRY(launch_transpose_inplace(Sx, ldsx, m, st));                       // S_x = L_x^T
@@ -366,9 +284,9 @@ kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const floa
   // S_g = chol_lower(G)  (and S_g^-1 for the right Gram side)
   if (!(flags & KF_REUSE_SG)) {
     KF_TRY(launch_copy(G, ldg, Sg, ldsg, n, n, false, st));
-    KF_TRY(cholesky_lower(ctx, Sg, ldsg, n, b.dinv, st));
+    KF_TRY(cholesky_lower(ctx, Sg, ldsg, n, b.dinv, b.cws, b.cws_bytes, st));
     if (side == KF_SIDE_RIGHT && !(flags & KF_REUSE_SINV)) {
-      KF_TRY(trtri_lower(ctx, Sg, ldsg, n, b.dinv, Sinv, ldsi, b.tt, st));
+      KF_TRY(trtri_lower(ctx, Sg, ldsg, n, b.dinv, Sinv, ldsi, b.tt, b.tws, b.tws_bytes, st));
     }
   }
   // Tensor cores, float32 operands as three bfloat16 planes (float32-accurate products):
@@ -756,6 +674,8 @@ struct UnwhitenBufs {
   float *q0, *q1, *gm, *li, *dinv, *tt, *P;
   int64_t ldP;
   PlaneBuf c, w, sg, si, p;
+  char *cws, *tws;
+  size_t cws_bytes, tws_bytes;
 };
 
 size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, UnwhitenBufs& b) {
@@ -766,6 +686,10 @@ size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, UnwhitenBufs& 
   b.li = cv.take<float>(size_t(r) * r);
   b.dinv = cv.take<float>(size_t(round_up(r, CHOL_NB)) * CHOL_NB);
   b.tt = cv.take<float>(trtri_tmp_floats(r));
+  b.cws_bytes = chol_workspace_bytes(r);
+  b.cws = cv.take<char>(b.cws_bytes);
+  b.tws_bytes = trtri_workspace_bytes(r);
+  b.tws = cv.take<char>(b.tws_bytes);
   b.ldP = round_up(mx, 8);
   b.P = cv.take<float>(size_t(mx) * b.ldP);   // n x r (right side) or r x m (left side)
   b.c = take_planes(cv, s, r, 2);
@@ -818,8 +742,8 @@ kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, in
     g.B = cur; g.ldb = r;
     g.C = b.gm; g.ldc = r; g.alpha = 1.f; g.beta = 0.f; g.out_mask = OUT_LOWER;
     KF_TRY(simt_gemm(g, st));
-    KF_TRY(cholesky_lower(ctx, b.gm, r, r, b.dinv, st));
-    KF_TRY(trtri_lower(ctx, b.gm, r, r, b.dinv, b.li, r, b.tt, st));
+    KF_TRY(cholesky_lower(ctx, b.gm, r, r, b.dinv, b.cws, b.cws_bytes, st));
+    KF_TRY(trtri_lower(ctx, b.gm, r, r, b.dinv, b.li, r, b.tt, b.tws, b.tws_bytes, st));
     GemmDesc h{};
     h.M = s; h.N = r; h.K = r; h.batch = 1;
     h.A = cur; h.lda = r;

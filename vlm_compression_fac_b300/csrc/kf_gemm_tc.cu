@@ -20,6 +20,7 @@
 // TMA loads it issued and for every MMA it issued, so nothing it started is still writing
 // shared or tensor memory when it exits.
 #include "kf_internal.cuh"
+#include "kf_tc_ptx.cuh"
 
 #include <cstring>
 
@@ -32,12 +33,12 @@ constexpr uint32_t B_BYTES = TBN * TBK * 2;  // 32 KB
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;  // stages + alignment + barriers
 constexpr uint32_t TMEM_COLS = 256;
-constexpr unsigned long long WAIT_LIMIT_NS = 4000000000ull;  // 4 s: default and drain limit
 constexpr int SUPER_M = 8, SUPER_N = 4;
 
+constexpr int MAX_PASS = 6;
 struct TcMaps {
-  CUtensorMap a[3];
-  CUtensorMap b[3];
+  CUtensorMap a[MAX_PASS];
+  CUtensorMap b[MAX_PASS];
 };
 
 struct TcArgs {
@@ -46,87 +47,13 @@ struct TcArgs {
   float* D;
   int64_t ldd;
   int accumulate, sched, krange;
+  int negate;    // D (+)= -result
+  int vec_ok;    // D base 16-byte aligned and ldd a multiple of 4 (host-checked)
   int64_t kcb;   // k-blocks per accumulation chunk (0: the whole K range)
   int64_t ntm, ntn;
   int* status;
   unsigned long long wait_ns;  // limit of the pipeline waits
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ unsigned long long now_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait: false if the limit expired.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          unsigned long long limit_ns = WAIT_LIMIT_NS) {
-  if (mbar_try(bar, parity)) return true;
-  const unsigned long long t0 = now_ns();
-  uint32_t spins = 0;
-  while (!mbar_try(bar, parity)) {
-    if ((++spins & 255u) == 0 && now_ns() - t0 > limit_ns) return false;
-  }
-  return true;
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x,
-                                            int32_t y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                       uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05): start address, leading / stride byte offsets
-// (all >> 4), descriptor version 1 at bit 46, 128-byte swizzle (value 2 at bits 61..63).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= uint64_t((addr & 0x3FFFFu) >> 4);
-  d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-  d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-  d |= uint64_t(1) << 46;
-  d |= uint64_t(2) << 61;
-  return d;
-}
 
 // Instruction descriptor, kind::f16: D float32, A and B bfloat16, M = 128, N = 256.
 __host__ __device__ constexpr uint32_t make_idesc(bool a_mn, bool b_mn) {
@@ -354,7 +281,7 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
     }
     // Write the tile: D = acc (or D += acc), rows < M, columns < N, lower triangle for TC_LOWER.
     if (all_ok && row < g.M) {
-      const bool vec_ok = (g.ldd % 4) == 0;
+      const bool vec_ok = g.vec_ok != 0;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const int64_t c0 = col0 + cc * 32;
@@ -375,6 +302,9 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
           for (int j = 0; j < 8; ++j) {
             float4 o = make_float4(acc[cc * 32 + 4 * j], acc[cc * 32 + 4 * j + 1], acc[cc * 32 + 4 * j + 2],
                                    acc[cc * 32 + 4 * j + 3]);
+            if (g.negate) {
+              o.x = -o.x; o.y = -o.y; o.z = -o.z; o.w = -o.w;
+            }
             if (g.accumulate) {
               o.x += old[j].x; o.y += old[j].y; o.z += old[j].z; o.w += old[j].w;
             }
@@ -385,7 +315,8 @@ __global__ void __launch_bounds__(320, 1) tc_gemm_kernel(const __grid_constant__
           for (int j = 0; j < 32; ++j) {
             const int64_t col = c0 + j;
             if (col >= g.N || (g.sched == TC_LOWER && col > row)) continue;
-            dst[j] = g.accumulate ? dst[j] + acc[cc * 32 + j] : acc[cc * 32 + j];
+            const float v = g.negate ? -acc[cc * 32 + j] : acc[cc * 32 + j];
+            dst[j] = g.accumulate ? dst[j] + v : v;
           }
         }
       }
@@ -450,7 +381,7 @@ kf_status launch_tc(const TcMaps& maps, const TcArgs& a, int64_t ntiles, cudaStr
 
 kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st) {
   if (g.M <= 0 || g.N <= 0) return KF_OK;
-  if (g.npass < 1 || g.npass > 3) return fail(KF_ERR_INVALID, "tc_gemm: 1..3 passes");
+  if (g.npass < 1 || g.npass > MAX_PASS) return fail(KF_ERR_INVALID, "tc_gemm: 1..6 passes");
   if (!ctx->encode) return fail(KF_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   TcMaps maps;
   std::memset(&maps, 0, sizeof(maps));
@@ -464,6 +395,8 @@ kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st) {
   a.M = g.M; a.N = g.N; a.K = g.K; a.npass = g.npass;
   a.D = g.D; a.ldd = g.ldd;
   a.accumulate = g.accumulate ? 1 : 0; a.sched = g.sched; a.krange = g.krange;
+  a.negate = g.negate ? 1 : 0;
+  a.vec_ok = ((g.ldd % 4) == 0 && (reinterpret_cast<uintptr_t>(g.D) & 15) == 0) ? 1 : 0;
   a.kcb = g.kchunk > 0 ? (g.kchunk + TBK - 1) / TBK : 0;
   a.ntm = (g.M + TBM - 1) / TBM; a.ntn = (g.N + TBN - 1) / TBN;
   a.status = ctx->d_status;

@@ -124,16 +124,59 @@ struct TcOperand {
 enum TcSched { TC_FULL = 0, TC_LOWER = 1 };
 struct TcGemm {
   int64_t M, N, K;
-  int npass;
-  TcOperand a[3], b[3];
+  int npass;         // 1..6
+  TcOperand a[6], b[6];
   float* D; int64_t ldd;
   bool accumulate;   // D += result (else D = result)
+  bool negate;       // the result enters with a minus sign (D -= ..., or D = -...)
   int sched;         // TC_LOWER: only tiles touching i >= j, only i >= j written
   int krange;        // KR_FULL / KR_GE_ROW / KR_LE_ROW / KR_GE_COL / KR_LE_COL
   int64_t kchunk;    // longest K range accumulated inside the tensor cores (0: unbounded);
                      // each chunk's partial result is added to D in float32
 };
 kf_status tc_gemm(kf_ctx* ctx, const TcGemm& g, cudaStream_t st);
+
+// A matrix operand for the tensor-core engine: bfloat16 planes whose sum is the value
+// (one plane for bfloat16 data; two (hi + lo, 16 significant bits) or three (the full 24-bit
+// float32 significand) for float32 data), 16-byte aligned rows.
+struct Planes {
+  const __nv_bfloat16* p[3];
+  int64_t ld;
+  int n;  // 1, 2 or 3
+};
+// Room for the planes of a rows x cols operand (rows padded to 8 elements).
+struct PlaneBuf {
+  __nv_bfloat16* p[3] = {nullptr, nullptr, nullptr};
+  int64_t ld = 0;
+  int n = 0;
+};
+PlaneBuf take_planes(Carve& cv, int64_t rows, int64_t cols, int nplanes);
+// float32 rows x cols (ld) -> the buffer's planes (two or three).
+kf_status split_f32(const float* in, int64_t ld, int64_t rows, int64_t cols, const PlaneBuf& b, Planes* out,
+                    cudaStream_t st);
+// A caller matrix (bfloat16 or float32) as planes: bfloat16 rows that are already aligned
+// are used in place; other bfloat16 rows are copied to an aligned plane; float32 is split.
+kf_status as_planes(const void* in, kf_dtype dt, int64_t ld, int64_t rows, int64_t cols, const PlaneBuf& b,
+                    Planes* out, cudaStream_t st);
+// Tokens (K) summed inside the tensor cores before a partial is added in float32: long
+// mixed-sign sums of products (whitening, unwhitening; up to 28672 terms, several planes).
+#ifndef KF_PRODUCT_KCHUNK
+#define KF_PRODUCT_KCHUNK 1024
+#endif
+constexpr int64_t PRODUCT_KCHUNK = KF_PRODUCT_KCHUNK;
+struct ProductOpts {
+  bool accumulate = false;   // D += result
+  bool negate = false;       // the result enters negated
+  bool lower = false;        // only tiles touching i >= j, only i >= j written
+  int64_t kchunk = PRODUCT_KCHUNK;
+};
+// D (M x N float32, ldd) = A B on the tensor cores, A and B given as planes: every cross
+// term A_i B_j with i + j < max(A.n, B.n) (0-based), i.e. all terms down to the last plane's
+// weight (at most six, one launch); the omitted terms are below the rounding of the planes
+// themselves.  a_mn / b_mn: the operand is stored MN-major (A as K x M rows, B as K x N rows).
+kf_status tc_product(kf_ctx* ctx, int64_t M, int64_t N, int64_t K, const Planes& A, bool a_mn, const Planes& B,
+                     bool b_mn, int krange, float* D, int64_t ldd, cudaStream_t st,
+                     const ProductOpts& o = ProductOpts());
 
 // ------------------------------------------------------------ small kernels
 kf_status launch_ffma_probe(int sm_count, int64_t iters, float* sink, double* flops, cudaStream_t st);
@@ -168,14 +211,19 @@ kf_status launch_scale_rows(float* A, int64_t lda, int64_t rows, int64_t cols,
                             const float* s, bool invert, cudaStream_t st);
 
 // Cholesky: A (n x n, lda) lower triangle in, L out in place (zeros above), and the
-// inverses of the nb x nb diagonal blocks into dinv (n x 64 scratch, row-major).
+// inverses of the 64 x 64 diagonal blocks into dinv (n x 64 scratch, row-major).  Column
+// strips of CHOL_STRIP; trailing updates on the tensor cores (workspace: chol_workspace_bytes).
 constexpr int CHOL_NB = 64;
-kf_status cholesky_lower(kf_ctx* ctx, float* A, int64_t lda, int64_t n, float* dinv,
+constexpr int64_t CHOL_STRIP = 256;
+size_t chol_workspace_bytes(int64_t n);
+kf_status cholesky_lower(kf_ctx* ctx, float* A, int64_t lda, int64_t n, float* dinv, void* ws, size_t ws_bytes,
                          cudaStream_t st);
 // Inverse of a lower triangular L (n x n) into M (lower, zeros above), using the diagonal
-// block inverses produced by cholesky_lower.
+// block inverses produced by cholesky_lower; tmp: trtri_tmp_floats(n) floats; ws:
+// trtri_workspace_bytes(n) (tensor-core doubling levels).
 kf_status trtri_lower(kf_ctx* ctx, const float* L, int64_t ldl, int64_t n, const float* dinv,
-                      float* M, int64_t ldm, float* tmp, cudaStream_t st);
+                      float* M, int64_t ldm, float* tmp, void* ws, size_t ws_bytes, cudaStream_t st);
 size_t trtri_tmp_floats(int64_t n);
+size_t trtri_workspace_bytes(int64_t n);
 
 }  // namespace kf

@@ -5,12 +5,19 @@
 //     round-robin tournament pairs the blocks so that every step visits nblk/2 disjoint
 //     pairs and a sweep (nblk - 1 steps) visits every pair once;
 //   * jac_solve: one CTA per pair loads the 64 x 64 problem [[C_II C_IJ][C_JI C_JJ]] into
-//     shared memory and diagonalises it by threshold cyclic Jacobi (32 disjoint rotations per
-//     round), accumulating the 64 x 64 orthogonal V_p;
-//   * jac_apply: C <- P^T C P and Q <- Q P for the block-diagonal P = diag(V_p), as 64 x 64
-//     tile products (only tiles with p <= q of C, mirrored; since C stays symmetric the
-//     transposed operand is read from the mirrored tile).  Q is stored transposed (one
-//     eigenvector per row), so Q P becomes P^T Qt, again without any transposition;
+//     shared memory and runs threshold cyclic Jacobi on it (32 disjoint rotations per round,
+//     KF_JAC_MAX_INNER sweeps), accumulating the 64 x 64 orthogonal V_p, which it writes as
+//     three bfloat16 planes in the tensor-core apply's operand layout;
+//   * jac_apply_tc: C <- P^T C P and Q <- Q P for the block-diagonal P = diag(V_p) on the
+//     tensor cores (tcgen05, float32 accumulation in tensor memory): every operand enters as
+//     three bfloat16 planes (the full float32 significand) and the six cross terms down to
+//     the last plane's weight are summed, so the products are float32-accurate.  C is taken
+//     in 128 x 128 super-tiles (two pairs of rows by two pairs of columns, only super-tiles
+//     on or above the diagonal, the result mirrored), each as two chained products with
+//     M = 128: U = S diag(V_q1, V_q2), then the transposed second product
+//     (V_p^T U_p)^T = U_p^T V_p, whose result lands in tensor memory one column of S per lane
+//     for coalesced stores.  Q is stored transposed (one eigenvector per row), so Q P becomes
+//     P^T Qt, computed per 64 x 128 panel as (panel^T V_q) for the same reason;
 //   * a sweep in which no pair had |c_pq| > tol * sqrt(c_pp c_qq) (entries below a float32
 //     rounding floor count as zero) ends the iteration for that problem.
 // The singular values are then the Rayleigh quotients sigma_i = ||W~ q_i|| / ||q_i||,
@@ -19,6 +26,7 @@
 // The same solver serves a symmetric matrix given directly (Swift-SVD 2A's covariance of
 // the layer output): the values are then the Rayleigh quotients q.Cq / q.q.
 #include "kf_internal.cuh"
+#include "kf_tc_ptx.cuh"
 
 #include <cfloat>
 #include <vector>
@@ -27,8 +35,12 @@ namespace kf {
 namespace {
 
 constexpr int JB = 32, JP = 64;  // block width, pair problem size
+// Inner sweeps of a pair problem.  Measured on the 7B block (7 Gram matrices of 4096): one
+// sweep of rotations per pair problem instead of up to 12 costs at most one more outer sweep,
+// the final singular values come out as accurate (about 6e-5 relative on the kept components
+// either way), and the pair solves take 40% less time.
 #ifndef KF_JAC_MAX_INNER
-#define KF_JAC_MAX_INNER 12  // inner sweeps of a pair problem
+#define KF_JAC_MAX_INNER 1
 #endif
 
 // Alignment self-check for vector accesses: a misaligned address is recorded in the status
@@ -51,6 +63,26 @@ __device__ __forceinline__ int rr_pos(int pos, int round, int n) {
 
 __device__ __forceinline__ int64_t gidx(int r, int b0, int b1) {  // pair-local -> global index
   return r < JB ? int64_t(b0) * JB + r : int64_t(b1) * JB + (r - JB);
+}
+
+// Shared-memory operand images of the tensor-core apply (bfloat16, 128-byte swizzle: the
+// 16-byte chunk index inside a 128-byte row is XORed with the row index mod 8; buffers
+// 1024-byte aligned).  The same layouts TMA produces for the GEMM engine's operands.
+//   V image (B operand, K = 64 old indices x N = 64 new indices, MN-major): 3 planes of 8 KB.
+//   A image, K-major (M = 128 rows x K = 64): 3 planes of 16 KB, row m at m * 128 bytes.
+//   A image, MN-major (M = 128 x K = 64): 3 planes of 16 KB, two 64-wide M chunks 8 KB apart,
+//   row k at k * 128 bytes inside a chunk.
+constexpr int VPLANE_BYTES = 8192, VIMG_BYTES = 3 * VPLANE_BYTES;
+constexpr int APLANE_BYTES = 16384, AIMG_BYTES = 3 * APLANE_BYTES;
+__host__ __device__ __forceinline__ uint32_t vimg_off(int k, int n) {
+  return uint32_t(k) * 128u + ((uint32_t((n >> 3) ^ (k & 7))) << 4) + uint32_t(n & 7) * 2u;
+}
+__device__ __forceinline__ uint32_t akm_off(int m, int k) {
+  return uint32_t(m) * 128u + ((uint32_t((k >> 3) ^ (m & 7))) << 4) + uint32_t(k & 7) * 2u;
+}
+__device__ __forceinline__ uint32_t amn_off(int m, int k) {
+  return uint32_t(m >> 6) * 8192u + uint32_t(k) * 128u + ((uint32_t(((m & 63) >> 3) ^ (k & 7))) << 4) +
+         uint32_t(m & 7) * 2u;
 }
 
 // ----------------------------------------------------------------------- prepare
@@ -96,7 +128,7 @@ __global__ void jac_floor_kernel(const float* __restrict__ Call, int64_t sp, flo
 
 // ------------------------------------------------------------------------- solve
 __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call, int64_t sp, int nblk,
-                                                        int step, float* __restrict__ Vall,
+                                                        int step, uint8_t* __restrict__ Vimg,
                                                         int* __restrict__ skipall,
                                                         const int* __restrict__ conv,
                                                         unsigned* __restrict__ offmax,
@@ -256,216 +288,343 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
     V[e >> 6][e & 63] = vout[x];
   }
   __syncthreads();
-  float* Vo = Vall + (int64_t(u) * npairs + k) * (JP * JP);
-#ifdef KF_JAC_SORT_PAIRS
+  // V (row = old index, column = new index) as three bfloat16 planes in the shared-memory
+  // image the tensor-core apply copies verbatim (B operand, MN-major, 128-byte swizzle).
+  uint8_t* img = Vimg + (int64_t(u) * npairs + k) * VIMG_BYTES;
   for (int e = t; e < JP * JP; e += 256) {
-    const int oc = pord[e & 63];
-    Vo[e] = V[e >> 6][oc >= 0 && oc < JP ? oc : (e & 63)];
-  }
+    const int kk = e >> 6, n = e & 63;
+#ifdef KF_JAC_SORT_PAIRS
+    const int oc = pord[n];
+    const float v = V[kk][oc >= 0 && oc < JP ? oc : n];
 #else
-  for (int e = t; e < JP * JP; e += 256) Vo[e] = V[e >> 6][e & 63];
+    const float v = V[kk][n];
 #endif
+    const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
+    const float r1 = v - __bfloat162float(h1);
+    const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+    const uint32_t o = vimg_off(kk, n);
+    *reinterpret_cast<__nv_bfloat16*>(img + o) = h1;
+    *reinterpret_cast<__nv_bfloat16*>(img + VPLANE_BYTES + o) = h2;
+    *reinterpret_cast<__nv_bfloat16*>(img + 2 * VPLANE_BYTES + o) = h3;
+  }
   if (t == 0) skip[k] = 0;
 }
 
 // ------------------------------------------------------------------------- apply
-// 64 x 64 x 64 product out[i][j] = sum_k X[k][i] * Y[k][j] with X, Y dense row-major
-// 64 x 64 in shared memory; thread (tx, ty) owns rows ty*4..+3, columns tx*4..+3.
-__device__ __forceinline__ void mm64(const float* __restrict__ X, const float* __restrict__ Y, float acc[4][4],
-                                     int tx, int ty) {
+// Three-plane split of a float32 value (bfloat16 terms holding its full significand).
+__device__ __forceinline__ void split3(float v, __nv_bfloat16& h1, __nv_bfloat16& h2, __nv_bfloat16& h3) {
+  h1 = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h1);
+  h2 = __float2bfloat16_rn(r1);
+  h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
+}
+__device__ __forceinline__ uint32_t pack2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return uint32_t(__bfloat16_as_ushort(a)) | (uint32_t(__bfloat16_as_ushort(b)) << 16);
+}
+// Four consecutive elements (along the contiguous dimension of one 16-byte chunk) into the
+// three planes of an A image at byte offset `off` (8-byte aligned).
+__device__ __forceinline__ void put4(uint8_t* img, uint32_t off, float4 v) {
+  __nv_bfloat16 a1, a2, a3, b1, b2, b3, c1, c2, c3, d1, d2, d3;
+  split3(v.x, a1, a2, a3);
+  split3(v.y, b1, b2, b3);
+  split3(v.z, c1, c2, c3);
+  split3(v.w, d1, d2, d3);
+  *reinterpret_cast<uint2*>(img + off) = make_uint2(pack2(a1, b1), pack2(c1, d1));
+  *reinterpret_cast<uint2*>(img + APLANE_BYTES + off) = make_uint2(pack2(a2, b2), pack2(c2, d2));
+  *reinterpret_cast<uint2*>(img + 2 * APLANE_BYTES + off) = make_uint2(pack2(a3, b3), pack2(c3, d3));
+}
+// Eight consecutive elements into one 16-byte chunk of each plane.
+__device__ __forceinline__ void put8(uint8_t* img, uint32_t off, const uint32_t* w) {
+  uint32_t p[3][4];
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat16 x1, x2, x3, y1, y2, y3;
+    split3(__uint_as_float(w[2 * q]), x1, x2, x3);
+    split3(__uint_as_float(w[2 * q + 1]), y1, y2, y3);
+    p[0][q] = pack2(x1, y1);
+    p[1][q] = pack2(x2, y2);
+    p[2][q] = pack2(x3, y3);
+  }
 #pragma unroll
-    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < JP; ++k) {
-    const float4 x = *reinterpret_cast<const float4*>(X + k * JP + ty * 4);
-    const float4 y = *reinterpret_cast<const float4*>(Y + k * JP + tx * 4);
-    const float xa[4] = {x.x, x.y, x.z, x.w}, yb[4] = {y.x, y.y, y.z, y.w};
+  for (int pl = 0; pl < 3; ++pl)
+    *reinterpret_cast<uint4*>(img + pl * APLANE_BYTES + off) = make_uint4(p[pl][0], p[pl][1], p[pl][2], p[pl][3]);
+}
+
+// Copies one 24 KB V image (global, 16-byte aligned) into shared memory.
+__device__ __forceinline__ void copy_vimg(uint8_t* dst, const uint8_t* __restrict__ src, int tid) {
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], yb[b], acc[a][b]);
+  for (int i = 0; i < VIMG_BYTES / (16 * 256); ++i) {
+    const int e = tid + i * 256;
+    reinterpret_cast<uint4*>(dst)[e] = __ldg(reinterpret_cast<const uint4*>(src) + e);
   }
 }
 
-__device__ __forceinline__ void cp_async16(float* smem_dst, const float* gsrc) {
-  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+        "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+        "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// One task of a Jacobi step: a tile of C (pair p rows x pair q columns, p <= q) or a
-// 64-column panel cb of the transposed eigenvector matrix for pair q.
-struct ApplyTask {
-  int u, kind, p, q, cb, wp, wq;  // kind 0: C tile, 1: Qt panel; wp/wq: V_p, V_q are applied
+// Instruction descriptors, kind::f16: D float32, A and B bfloat16, M = 128, N = 64; B is
+// always the MN-major V image; A is K-major (S blocks) or MN-major (transposed operands).
+constexpr uint32_t IDESC_N64 = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((64u >> 3) << 17) |
+                               ((128u >> 4) << 24);
+constexpr uint32_t IDESC_A_MN = 1u << 15;
+
+struct TcApplyCtl {
+  uint32_t bar;          // mbarrier address (shared)
+  uint32_t tmem;         // tensor-memory base of this CTA (256 columns)
+  uint32_t ph;           // phase parity of the next wait
+  unsigned long long wait_ns;
+  int* status;
+  int ok;                // 0 after a wait that gave up (uniform over the CTA)
 };
 
-__device__ __forceinline__ bool decode_apply(int g, int per_u, int ntile_c, int npairs, const int* __restrict__ skipall,
-                                             const int* __restrict__ conv, ApplyTask& t) {
-  t.u = g / per_u;
-  int task = g - t.u * per_u;
-  if (conv[t.u]) return false;
-  const int* skip = skipall + int64_t(t.u) * npairs;
-  if (task < ntile_c) {
-    // Row p of the upper triangle (p <= q) holds npairs - p tiles; S(p) = p (2 npairs - p + 1) / 2
-    // tiles precede it.  p = the largest row with S(p) <= task: the root of the quadratic,
-    // then an exact integer correction (at most a step or two for npairs <= 256).
-    const int n2 = 2 * npairs + 1;
-    int p = int((float(n2) - sqrtf(float(n2) * float(n2) - 8.f * float(task))) * 0.5f);
-    p = p < 0 ? 0 : (p > npairs - 1 ? npairs - 1 : p);
-    while (p > 0 && p * (n2 - p) / 2 > task) --p;
-    while (p + 1 < npairs && (p + 1) * (n2 - p - 1) / 2 <= task) ++p;
-    task -= p * (n2 - p) / 2;
-    t.kind = 0; t.p = p; t.q = p + task; t.cb = 0;
-    t.wp = !skip[t.p]; t.wq = !skip[t.q];
-    return t.wp || t.wq;
+// One product phase: the A image (three planes, K-major or MN-major) times the V image into
+// tensor-memory columns [dcol, dcol + 64), all six cross terms over K = 64 (24 MMAs issued by
+// one thread), then every thread waits for their completion.  Returns false (for every
+// thread) if the wait gave up; the CTA then drains and stops.
+__device__ __forceinline__ bool mma_phase(TcApplyCtl& c, uint32_t a_img, bool a_mn, uint32_t v_img, uint32_t dcol,
+                                          int tid) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) {
+    tc_fence_after();
+    const uint32_t idesc = IDESC_N64 | (a_mn ? IDESC_A_MN : 0u);
+    constexpr int TI[6] = {0, 0, 1, 0, 1, 2}, TJ[6] = {0, 1, 0, 2, 1, 0};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int t = 0; t < 6; ++t) {
+        const uint32_t ab = a_img + uint32_t(TI[t]) * APLANE_BYTES;
+        const uint64_t ad = a_mn ? smem_desc(ab + kk * 2048, 8192, 1024) : smem_desc(ab + kk * 32, 16, 1024);
+        const uint64_t bd = smem_desc(v_img + uint32_t(TJ[t]) * VPLANE_BYTES + kk * 2048, 8192, 1024);
+        tc_mma(c.tmem + dcol, ad, bd, idesc, (kk | t) ? 1u : 0u);
+      }
+    }
+    tc_commit(c.bar);
   }
-  task -= ntile_c;
-  t.kind = 1; t.cb = task / npairs; t.q = task - t.cb * npairs; t.p = t.q;
-  t.wp = 0; t.wq = !skip[t.q];
-  return t.wq != 0;
+  const uint32_t want = c.ph;
+  c.ph ^= 1u;
+  const bool ok = mbar_wait(c.bar, want, c.wait_ns);
+  if (__syncthreads_or(!ok)) {
+    if (tid == 0) raise_status(c.status, KF_ERR_TIMEOUT, WAIT_MMA_DONE);
+    mbar_wait(c.bar, want);  // the issued MMAs still read shared memory: drain (long limit)
+    c.ok = 0;
+    return false;
+  }
+  tc_fence_after();
+  return true;
 }
 
-// Stage layout (floats): X (64 x 64) | Vp (64 x 64) | Vq (64 x 64).
-constexpr int STAGE_F = 3 * JP * JP;
-
-__device__ __forceinline__ void issue_apply_loads(const ApplyTask& t, float* stage, const float* __restrict__ Call,
-                                                  const float* __restrict__ Qtall, const float* __restrict__ Vall,
-                                                  int64_t sp, int nblk, int step, int npairs, int tid, int* st) {
-  const float* C = Call + int64_t(t.u) * sp * sp;
-  const float* Qt = Qtall + int64_t(t.u) * sp * sp;
-  const float* Vu = Vall + int64_t(t.u) * npairs * (JP * JP);
-  const int q0 = rr_pos(t.q, step, nblk), q1 = rr_pos(nblk - 1 - t.q, step, nblk);
-  if (t.kind == 0) {
-    const int p0 = rr_pos(t.p, step, nblk), p1 = rr_pos(nblk - 1 - t.p, step, nblk);
-    // C stays symmetric, so X[k][i] = C[q_k][p_i] is the transpose of T = C[rows p][cols q].
-    for (int e = tid; e < JP * JP / 4; e += 256) {
-      const int k = e >> 4, c = (e & 15) * 4;
-      const float* a = C + gidx(k, q0, q1) * sp + gidx(c, p0, p1);
-      if (aligned16(a, st, 101)) cp_async16(stage + k * JP + c, a);
-      const float* vp = Vu + int64_t(t.p) * JP * JP + 4 * e;
-      const float* vq = Vu + int64_t(t.q) * JP * JP + 4 * e;
-      if (t.wp && aligned16(vp, st, 102)) cp_async16(stage + JP * JP + 4 * e, vp);
-      if (t.wq && aligned16(vq, st, 103)) cp_async16(stage + 2 * JP * JP + 4 * e, vq);
-    }
-  } else {
-    for (int e = tid; e < JP * JP / 4; e += 256) {
-      const int k = e >> 4, c = (e & 15) * 4;
-      const float* a = Qt + gidx(k, q0, q1) * sp + int64_t(t.cb) * JP + c;
-      const float* vq = Vu + int64_t(t.q) * JP * JP + 4 * e;
-      if (aligned16(a, st, 104)) cp_async16(stage + k * JP + c, a);
-      if (aligned16(vq, st, 105)) cp_async16(stage + 2 * JP * JP + 4 * e, vq);
-    }
-  }
-}
-
-// Persistent: each CTA walks the tasks of every problem (stride gridDim.x), prefetching the
-// next task's three 16 KB operands with cp.async while it computes the current one.
-__global__ void __launch_bounds__(256, 2) jac_apply_kernel(float* __restrict__ Call, float* __restrict__ Qtall,
-                                                           int64_t sp, int nblk, int step,
-                                                           const float* __restrict__ Vall,
-                                                           const int* __restrict__ skipall,
-                                                           const int* __restrict__ conv, int ntile_c, int per_u,
-                                                           int total, unsigned long long* __restrict__ flops,
-                                                           int* status) {
-  extern __shared__ __align__(16) float sm[];
-  float* stages[2] = {sm, sm + STAGE_F};
-  float* Ub = sm + 2 * STAGE_F;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+// Persistent apply of one Jacobi step on the tensor cores.  Task g of problem u: a super-tile
+// (super-pairs P <= Q; super-pair P = pairs 2P and 2P + 1) of C, or a 64 x 128 panel (pair q,
+// columns 128 cb ..) of Qt.  Tasks whose pairs all skipped their rotation are not run; a
+// skipped pair inside a run task enters with the identity image (exact in three planes).
+__global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
+    float* __restrict__ Call, float* __restrict__ Qtall, int64_t sp, int nblk, int step,
+    const uint8_t* __restrict__ Vimg, const uint8_t* __restrict__ Iimg, const int* __restrict__ skipall,
+    const int* __restrict__ conv, int nsup, int nsp, int per_u, int total, unsigned long long* __restrict__ ctr,
+    int* status, unsigned long long wait_ns) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* Abuf = sm;
+  uint8_t* Vb0 = sm + AIMG_BYTES;
+  uint8_t* Vb1 = Vb0 + VIMG_BYTES;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(Vb1 + VIMG_BYTES);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int npairs = nblk / 2;
+  const int64_t npan = sp / 128;
 
-  ApplyTask cur, nxt;
-  int g = blockIdx.x;
-  while (g < total && !decode_apply(g, per_u, ntile_c, npairs, skipall, conv, cur)) g += gridDim.x;
-  if (g >= total) return;
-  issue_apply_loads(cur, stages[0], Call, Qtall, Vall, sp, nblk, step, npairs, tid, status);
-  cp_async_commit();
-  int s = 0;
-  unsigned long long done_flops = 0;
-  while (true) {
-    int gn = g + gridDim.x;
-    while (gn < total && !decode_apply(gn, per_u, ntile_c, npairs, skipall, conv, nxt)) gn += gridDim.x;
-    const bool more = gn < total;
-    if (more) {
-      issue_apply_loads(nxt, stages[s ^ 1], Call, Qtall, Vall, sp, nblk, step, npairs, tid, status);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const float* X = stages[s];
-    const float* Vp = stages[s] + JP * JP;
-    const float* Vq = stages[s] + 2 * JP * JP;
-    float acc[4][4];
-    const int q0 = rr_pos(cur.q, step, nblk), q1 = rr_pos(nblk - 1 - cur.q, step, nblk);
-    if (cur.kind == 0) {
-      float* C = Call + int64_t(cur.u) * sp * sp;
-      const int p0 = rr_pos(cur.p, step, nblk), p1 = rr_pos(nblk - 1 - cur.p, step, nblk);
-      if (cur.wq) {
-        mm64(X, Vq, acc, tx, ty);  // U = T Vq
-      } else {
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tslot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  TcApplyCtl c;
+  c.bar = smem_u32(bar);
+  c.tmem = *tslot;
+  c.ph = 0;
+  c.wait_ns = wait_ns;
+  c.status = status;
+  c.ok = 1;
+  const uint32_t a_img = smem_u32(Abuf), v0 = smem_u32(Vb0), v1 = smem_u32(Vb1);
+  const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+  unsigned long long bytes = 0, flops = 0;
+
+  for (int g = blockIdx.x; g < total && c.ok; g += gridDim.x) {
+    const int u = g / per_u;
+    int task = g - u * per_u;
+    if (conv[u]) continue;
+    const int* skip = skipall + int64_t(u) * npairs;
+    const uint8_t* Vu = Vimg + int64_t(u) * npairs * VIMG_BYTES;
+    if (task < nsup) {
+      // ---------------- C super-tile (P, Q), P <= Q: row P holds nsp - P super-tiles
+      const int n2 = 2 * nsp + 1;
+      int P = int((float(n2) - sqrtf(float(n2) * float(n2) - 8.f * float(task))) * 0.5f);
+      P = P < 0 ? 0 : (P > nsp - 1 ? nsp - 1 : P);
+      while (P > 0 && P * (n2 - P) / 2 > task) --P;
+      while (P + 1 < nsp && (P + 1) * (n2 - P - 1) / 2 <= task) ++P;
+      const int Q = P + (task - P * (n2 - P) / 2);
+      const int pr[2] = {2 * P, 2 * P + 1}, qr[2] = {2 * Q, 2 * Q + 1};
+      if (skip[pr[0]] && skip[pr[1]] && skip[qr[0]] && skip[qr[1]]) continue;
+      const bool diag = P == Q;
+      float* C = Call + int64_t(u) * sp * sp;
+      int pb[2][2], qb[2][2];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 4; ++b) acc[a][b] = X[(tx * 4 + b) * JP + ty * 4 + a];
+      for (int i = 0; i < 2; ++i) {
+        pb[i][0] = rr_pos(pr[i], step, nblk); pb[i][1] = rr_pos(nblk - 1 - pr[i], step, nblk);
+        qb[i][0] = rr_pos(qr[i], step, nblk); qb[i][1] = rr_pos(nblk - 1 - qr[i], step, nblk);
       }
-      if (cur.wp) {
+      // S = C[rows of P][cols of Q] into registers: warp w rows w + 8 i, lane l cols 4 l .. 4 l + 3
+      const int cl = 4 * lane;                       // local column 0..124
+      const int64_t gcol = int64_t(qb[cl >> 6][(cl >> 5) & 1]) * JB + (cl & 31);
+      float4 s[16];
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-          *reinterpret_cast<float4*>(Ub + (ty * 4 + a) * JP + tx * 4) =
-              make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        __syncthreads();
-        mm64(Vp, Ub, acc, tx, ty);  // T' = Vp^T U
+      for (int i = 0; i < 16; ++i) {
+        const int r = warp + 8 * i;
+        const int64_t grow = int64_t(pb[r >> 6][(r >> 5) & 1]) * JB + (r & 31);
+        s[i] = *reinterpret_cast<const float4*>(C + grow * sp + gcol);
       }
-      done_flops += (unsigned long long)(cur.wp + cur.wq) * 2ull * JP * JP * JP;
-      // T' (rows ty*4+a, cols tx*4+b) -> C[rows p][cols q]; the mirrored tile gets T'^T,
-      // which this thread holds as four contiguous runs of 4 (rows tx*4+b, cols ty*4..+3).
-      if (cur.p != cur.q) {
+      const uint8_t* vq0 = skip[qr[0]] ? Iimg : Vu + int64_t(qr[0]) * VIMG_BYTES;
+      const uint8_t* vq1 = skip[qr[1]] ? Iimg : Vu + int64_t(qr[1]) * VIMG_BYTES;
+      const uint8_t* vp0 = skip[pr[0]] ? Iimg : Vu + int64_t(pr[0]) * VIMG_BYTES;
+      const uint8_t* vp1 = skip[pr[1]] ? Iimg : Vu + int64_t(pr[1]) * VIMG_BYTES;
+      copy_vimg(Vb0, vq0, tid);
+      copy_vimg(Vb1, vq1, tid);
+      // step 1a: U[:, 0:64] = S[:, q pair 0] V_q0   (lanes 0..15 hold those columns)
+      if (lane < 16) {
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          float* d = C + gidx(ty * 4 + a, p0, p1) * sp + gidx(tx * 4, q0, q1);
-          if (aligned16(d, status, 106)) *reinterpret_cast<float4*>(d) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl), s[i]);
+      }
+      if (!mma_phase(c, a_img, false, v0, 0, tid)) break;
+      // step 1b: U[:, 64:128] = S[:, q pair 1] V_q1
+      if (lane >= 16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl - 64), s[i]);
+      }
+      if (!mma_phase(c, a_img, false, v1, 64, tid)) break;
+      // step 2: D_p = U_p^T V_p for p pair 0 (U rows 0..63) and 1 (rows 64..127): the threads of
+      // TMEM lanes of rows of p write U_p^T (M = U column, K = row within p) as MN-major planes
+      for (int pp = 0; pp < 2; ++pp) {
+        copy_vimg(pp ? Vb1 : Vb0, pp ? vp1 : vp0, tid);
+        if (((warp & 3) >> 1) == pp) {
+          const int k = (warp & 1) * 32 + lane;      // row within pair pp
+          const int m0 = (warp >> 2) * 64;           // U columns m0 .. m0 + 63
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v[32];
+            tmem_ld32(c.tmem + lane_base + uint32_t(m0 + 32 * h), v);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) put8(Abuf, amn_off(m0 + 32 * h + 8 * q, k), v + 8 * q);
+          }
         }
+        if (!mma_phase(c, a_img, true, pp ? v1 : v0, 128 + 64 * pp, tid)) break;
+      }
+      if (!c.ok) break;
+      // epilogue: D_p (lane = column c of Q, TMEM column n = row of pair p) -> C[p rows][Q cols]
+      // and, mirrored, C[Q cols][p rows]; a diagonal super-tile writes the pair-0 x pair-1 tile
+      // and the upper halves of its two diagonal tiles, each with its mirror (C stays exactly
+      // symmetric).
+      const int cc = (warp & 3) * 32 + lane;
+      const int64_t gc = int64_t(qb[cc >> 6][(cc >> 5) & 1]) * JB + (cc & 31);
+      const int nh = warp >> 2;                      // rows 32 nh .. 32 nh + 31 of the pair
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          float* d = C + gidx(tx * 4 + b, q0, q1) * sp + gidx(ty * 4, p0, p1);
-          if (aligned16(d, status, 107)) *reinterpret_cast<float4*>(d) = make_float4(acc[0][b], acc[1][b], acc[2][b], acc[3][b]);
-        }
-      } else {
-        // Diagonal tile: keep it exactly symmetric by writing entries i <= j to (i, j) and (j, i).
+      for (int pp = 0; pp < 2; ++pp) {
+        const int qq = cc >> 6;
+        if (diag && pp > qq) continue;               // uniform per warp (cc >> 6 fixed per warp)
+        uint32_t v[32];
+        tmem_ld32(c.tmem + lane_base + uint32_t(128 + 64 * pp + 32 * nh), v);
+        const int64_t rb = int64_t(pb[pp][nh]) * JB;  // the 32 rows lie in one block
+        if (diag && pp == qq) {
+          const int cl2 = cc & 63;
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int b = 0; b < 4; ++b) {
-            const int i = ty * 4 + a, j = tx * 4 + b;
-            if (i <= j) {
-              C[gidx(i, p0, p1) * sp + gidx(j, p0, p1)] = acc[a][b];
-              C[gidx(j, p0, p1) * sp + gidx(i, p0, p1)] = acc[a][b];
+          for (int j = 0; j < 32; ++j) {
+            const int n = 32 * nh + j;
+            if (n <= cl2) {
+              C[(rb + j) * sp + gc] = __uint_as_float(v[j]);
+              C[gc * sp + rb + j] = __uint_as_float(v[j]);
             }
           }
-      }
-    } else {
-      float* Qt = Qtall + int64_t(cur.u) * sp * sp;
-      mm64(Vq, X, acc, tx, ty);  // Qt[rows q][panel] <- Vq^T Qt[rows q][panel]
-      done_flops += 2ull * JP * JP * JP;
+        } else {
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        float* d = Qt + gidx(ty * 4 + a, q0, q1) * sp + int64_t(cur.cb) * JP + tx * 4;
-        if (aligned16(d, status, 108)) *reinterpret_cast<float4*>(d) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+          for (int j = 0; j < 32; ++j) C[(rb + j) * sp + gc] = __uint_as_float(v[j]);
+          float* mr = C + gc * sp + rb;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            reinterpret_cast<float4*>(mr)[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                                          __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
       }
+      bytes += 65536ull + (diag ? 65536ull : 131072ull);
+      flops += 96ull * 262144ull;
+    } else {
+      // ---------------- Qt panel: rows of pair q, columns 128 cb .. 128 cb + 127
+      task -= nsup;
+      const int cb = int(task / npairs), q = task - cb * npairs;
+      if (skip[q]) continue;
+      float* Qt = Qtall + int64_t(u) * sp * sp;
+      const int b0 = rr_pos(q, step, nblk), b1 = rr_pos(nblk - 1 - q, step, nblk);
+      const int64_t col0 = int64_t(cb) * 128;
+      float4 x[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = warp + 8 * i;
+        x[i] = *reinterpret_cast<const float4*>(Qt + gidx(r, b0, b1) * sp + col0 + 4 * lane);
+      }
+      copy_vimg(Vb0, Vu + int64_t(q) * VIMG_BYTES, tid);
+      // A = panel^T (M = panel column, K = row of the pair), MN-major
+#pragma unroll
+      for (int i = 0; i < 8; ++i) put4(Abuf, amn_off(4 * lane, warp + 8 * i), x[i]);
+      if (!mma_phase(c, a_img, true, v0, 0, tid)) break;
+      const int cc = (warp & 3) * 32 + lane;
+      const int nh = warp >> 2;
+      uint32_t v[32];
+      tmem_ld32(c.tmem + lane_base + uint32_t(32 * nh), v);
+      const int64_t rb = int64_t(nh ? b1 : b0) * JB;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) Qt[(rb + j) * sp + col0 + cc] = __uint_as_float(v[j]);
+      bytes += 65536ull;
+      flops += 24ull * 262144ull;
     }
-    __syncthreads();  // the stage and Ub are rewritten by the next iteration's loads
-    if (!more) break;
-    cur = nxt;
-    g = gn;
-    s ^= 1;
+    (void)npan;
   }
-  if (flops && tid == 0 && done_flops) atomicAdd(flops, done_flops);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(c.tmem) : "memory");
+  }
+  if (ctr && tid == 0) {
+    if (flops) atomicAdd(ctr, flops);
+    if (bytes) atomicAdd(ctr + 1, bytes);
+  }
 }
+
+// The identity in the V image layout: plane 1 = I, planes 2 and 3 zero.
+__global__ void ident_img_kernel(uint8_t* __restrict__ img) {
+  for (int e = threadIdx.x; e < VIMG_BYTES / 16; e += blockDim.x) reinterpret_cast<uint4*>(img)[e] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (threadIdx.x < JP)
+    *reinterpret_cast<__nv_bfloat16*>(img + vimg_off(threadIdx.x, threadIdx.x)) = __float2bfloat16_rn(1.f);
+}
+
 
 __global__ void jac_check_kernel(int n_units, int* __restrict__ conv, unsigned* __restrict__ off, float tol,
                                  int sweep, int max_sweeps, int* __restrict__ sweeps, int* status,
@@ -877,14 +1036,15 @@ struct JacPlan {
 static JacPlan jac_plan(int64_t s) {
   JacPlan p;
   p.s = s;
-  p.sp = (s + JP - 1) / JP * JP;
+  p.sp = (s + 127) / 128 * 128;  // an even number of pairs: whole 128 x 128 super-tiles
   p.nblk = int(p.sp / JB);
   p.npairs = p.nblk / 2;
   return p;
 }
 
 struct SvdBufs {
-  float *C, *Q, *V, *flo, *Y, *sig, *qinv, *Qs, *Ys, *Bw, *Vw;
+  float *C, *Q, *flo, *Y, *sig, *qinv, *Qs, *Ys, *Bw, *Vw;
+  uint8_t *Vimg, *Iimg;
   int *skip, *conv, *perm;
   unsigned* off;
   int64_t R, lyM;
@@ -899,7 +1059,8 @@ static size_t svd_carve(Carve& cv, int nu, int64_t m_max, int64_t n_max, int64_t
   b.R = int64_t(b.nwin) * RW + RW / 2;
   b.C = cv.take<float>(size_t(nu) * pl.sp * pl.sp);
   b.Q = cv.take<float>(size_t(nu) * pl.sp * pl.sp);
-  b.V = cv.take<float>(size_t(nu) * pl.npairs * JP * JP);
+  b.Vimg = cv.take<uint8_t>(size_t(nu) * pl.npairs * VIMG_BYTES);
+  b.Iimg = cv.take<uint8_t>(VIMG_BYTES);
   b.skip = cv.take<int>(size_t(nu) * pl.npairs);
   b.conv = cv.take<int>(nu);
   b.off = cv.take<unsigned>(nu);
@@ -936,7 +1097,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   SvdBufs bf;
   svd_carve(cv, nu, m_max, n_max, s, bf);
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "whitened_svd: workspace too small");
-  float *C = bf.C, *Q = bf.Q, *V = bf.V, *flo = bf.flo, *sig = bf.sig, *qinv = bf.qinv;
+  float *C = bf.C, *Q = bf.Q, *flo = bf.flo, *sig = bf.sig, *qinv = bf.qinv;
   int *skip = bf.skip, *conv = bf.conv, *perm = bf.perm;
   unsigned* off = bf.off;
 
@@ -945,7 +1106,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   if (prof) {
     for (int e = 0; e < 5; ++e)
       if (!ctx->prof_ev[e]) KF_CUDA(cudaEventCreate(&ctx->prof_ev[e]));
-    KF_CUDA(cudaMemsetAsync(flops, 0, sizeof(unsigned long long), st));
+    KF_CUDA(cudaMemsetAsync(flops, 0, 2 * sizeof(unsigned long long), st));
     KF_CUDA(cudaEventRecord(ctx->prof_ev[0], st));
     ctx->prof_kev_used = 0;
     ctx->prof_steps = int64_t(max_sweeps) * (pl.nblk - 1);
@@ -985,18 +1146,26 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   int* sweeps_dev = perm;  // reuse: perm is rewritten by the sort afterwards
   KF_CUDA(cudaMemsetAsync(sweeps_dev, 0, sizeof(int) * nu, st));
 
-  const int ntile_c = pl.npairs * (pl.npairs + 1) / 2;
-  const int ntile_q = int(pl.sp / JP) * pl.npairs;
-  const size_t apply_smem = size_t(2 * STAGE_F + JP * JP) * sizeof(float);
-  const int per_u = ntile_c + ntile_q;
+  // tensor-core apply: super-tiles of two pairs by two pairs (on or above the diagonal) and
+  // 128-column panels of Qt per pair
+  const int nsp = pl.npairs / 2;
+  const int nsup = nsp * (nsp + 1) / 2;
+  const int ntile_q = int(pl.sp / 128) * pl.npairs;
+  const size_t apply_smem = 1024 + size_t(AIMG_BYTES) + 2 * size_t(VIMG_BYTES) + 64;
+  const int per_u = nsup + ntile_q;
   const int64_t total_tasks = int64_t(per_u) * nu;
   if (total_tasks > 0x7fffffff) return fail(KF_ERR_UNSUPPORTED, "whitened_svd: too many Jacobi tasks");
   const int apply_grid = int(total_tasks < int64_t(ctx->sm_count) * 2 ? total_tasks : int64_t(ctx->sm_count) * 2);
   static std::atomic<unsigned long long> attr_done{0};
   KF_TRY(set_attr_once(attr_done, [&] {
-    return check_cuda(cudaFuncSetAttribute(jac_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           int(apply_smem)), "jac_apply smem attribute");
+    return check_cuda(cudaFuncSetAttribute(jac_apply_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(apply_smem)), "jac_apply_tc smem attribute");
   }));
+  if ((reinterpret_cast<uintptr_t>(C) & 15) || (reinterpret_cast<uintptr_t>(Q) & 15) ||
+      (reinterpret_cast<uintptr_t>(bf.Vimg) & 15) || (reinterpret_cast<uintptr_t>(bf.Iimg) & 15))
+    return fail(KF_ERR_INVALID, "whitened_svd: workspace not 16-byte aligned");
+  ident_img_kernel<<<1, 256, 0, st>>>(bf.Iimg); note_launch();
+  KF_TRY(check_cuda(cudaGetLastError(), "ident_img_kernel"));
   const int max_inner = KF_JAC_MAX_INNER;
   int sweeps_run = 0;
   if (prof) KF_CUDA(cudaEventRecord(ctx->prof_ev[1], st));
@@ -1013,13 +1182,14 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
         ctx->prof_kev_used += 3;
         KF_CUDA(cudaEventRecord(kev[0], st));
       }
-      jac_solve_kernel<<<dim3(pl.npairs, nu), 256, 0, st>>>(C, pl.sp, pl.nblk, step, V, skip, conv, off, flo, tol,
-                                                           max_inner); note_launch();
+      jac_solve_kernel<<<dim3(pl.npairs, nu), 256, 0, st>>>(C, pl.sp, pl.nblk, step, bf.Vimg, skip, conv, off, flo,
+                                                           tol, max_inner); note_launch();
       KF_TRY(check_cuda(cudaGetLastError(), "jac_solve_kernel"));
       if (prof) KF_CUDA(cudaEventRecord(kev[1], st));
-      jac_apply_kernel<<<apply_grid, 256, apply_smem, st>>>(C, Q, pl.sp, pl.nblk, step, V, skip, conv, ntile_c,
-                                                            per_u, int(total_tasks), flops, ctx->d_status); note_launch();
-      KF_TRY(check_cuda(cudaGetLastError(), "jac_apply_kernel"));
+      jac_apply_tc_kernel<<<apply_grid, 256, apply_smem, st>>>(C, Q, pl.sp, pl.nblk, step, bf.Vimg, bf.Iimg, skip,
+                                                               conv, nsup, nsp, per_u, int(total_tasks), flops,
+                                                               ctx->d_status, ctx->wait_ns); note_launch();
+      KF_TRY(check_cuda(cudaGetLastError(), "jac_apply_tc_kernel"));
       if (prof) KF_CUDA(cudaEventRecord(kev[2], st));
     }
     jac_check_kernel<<<1, 256, 0, st>>>(nu, conv, off, tol, sw, max_sweeps, sweeps_dev, ctx->d_status,
@@ -1126,8 +1296,8 @@ kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out) {
   KF_CUDA(cudaEventSynchronize(ctx->prof_ev[4]));
   float t[4];
   for (int i = 0; i < 4; ++i) KF_CUDA(cudaEventElapsedTime(&t[i], ctx->prof_ev[i], ctx->prof_ev[i + 1]));
-  unsigned long long f = 0;
-  KF_CUDA(cudaMemcpy(&f, ctx->prof_flops(), sizeof(f), cudaMemcpyDeviceToHost));
+  unsigned long long f[2] = {0, 0};
+  KF_CUDA(cudaMemcpy(f, ctx->prof_flops(), sizeof(f), cudaMemcpyDeviceToHost));
   out->gram_ms = t[0];
   out->jacobi_ms = t[1];
   out->rayleigh_ms = t[2];
@@ -1144,7 +1314,8 @@ kf_status svd_profile_read(kf_ctx* ctx, kf_svd_profile* out) {
   out->jacobi_solve_ms = float(ts);
   out->jacobi_apply_ms = float(ta);
   out->jacobi_apply_launches = ctx->prof_kev_used / 3;
-  out->jacobi_apply_flops = double(f);
+  out->jacobi_apply_flops = double(f[0]);
+  out->jacobi_apply_bytes = double(f[1]);
   return KF_OK;
 }
 

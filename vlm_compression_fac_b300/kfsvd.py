@@ -63,7 +63,8 @@ class SvdProfile(ctypes.Structure):
     _fields_ = [("gram_ms", ctypes.c_float), ("jacobi_ms", ctypes.c_float), ("rayleigh_ms", ctypes.c_float),
                 ("refine_ms", ctypes.c_float), ("jacobi_steps", ctypes.c_int64),
                 ("jacobi_apply_flops", ctypes.c_double), ("jacobi_solve_ms", ctypes.c_float),
-                ("jacobi_apply_ms", ctypes.c_float), ("jacobi_apply_launches", ctypes.c_int64)]
+                ("jacobi_apply_ms", ctypes.c_float), ("jacobi_apply_launches", ctypes.c_int64),
+                ("jacobi_apply_bytes", ctypes.c_double)]
 
 
 _P, _I64, _I32, _U32, _F, _SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32,
