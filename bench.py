@@ -131,11 +131,12 @@ def cost_tail(m, n):
     return m * n * s + (m ** 3 + n ** 3) / 3.0 + m * m * n + m * n * n
 
 
-# DRAM bytes (read + written) of one jac_apply_kernel launch that executes every task of a
-# step (7 problems of 4096, early sweep): ncu, dram__bytes_read.sum + dram__bytes_write.sum,
-# 715.9 MB + 880.8 MB.  The algorithmic bytes of such a launch are 7 x 14 B x 4096^2 = 1.64 GB
-# (half of C read, all of C and Q written, Q read).  Later launches skip converged pairs.
-JAC_APPLY_TRAFFIC = 1.5967e9
+# DRAM bytes (read + written, ncu dram__bytes_read.sum + dram__bytes_write.sum) of one
+# jac_apply_tc_kernel launch that runs every task of a step (7 problems of 4096): None until a
+# capture of the current kernel is summarised under profiles/.  The algorithmic bytes of such
+# a launch are 7 x 14 B x 4096^2 = 1.64 GB (C read once on or above the diagonal, written in
+# full; Qt read and written once); later launches skip tasks whose pairs all converged.
+JAC_APPLY_TRAFFIC = None
 
 
 # ALGORITHMIC bytes per component of one score_and_allocate call (a model of the minimum
@@ -368,7 +369,7 @@ def run_kfsvd(args):
     # ---------------- timed region (device-resident inputs)
     phases = {k: 0.0 for k in (("kfac", "cov", "eig", "allocate", "factors") if swift else
                                ("kfac", "whiten", "svd", "score", "allocate", "unwhiten"))}
-    syrk_ms, jac_ms, jac_flops, svd_prof = 0.0, 0.0, 0.0, None
+    syrk_ms, jac_ms, jac_flops, jac_bytes, svd_prof = 0.0, 0.0, 0.0, 0.0, None
     fisher_ms, n_fisher = 0.0, 0
     apply_ms, solve_ms, apply_launches = 0.0, 0.0, 0
     n_syrk = 0
@@ -390,6 +391,7 @@ def run_kfsvd(args):
         p = K.kf_svd_profile_read(ctx)
         jac_ms += p["jacobi_ms"]
         jac_flops += p["jacobi_apply_flops"]
+        jac_bytes += p["jacobi_apply_bytes"]
         apply_ms += p["jacobi_apply_ms"]
         solve_ms += p["jacobi_solve_ms"]
         apply_launches += p["jacobi_apply_launches"]
@@ -474,19 +476,25 @@ def run_kfsvd(args):
     syrk_total_flops = sum(syrk_flops(wl.n_tokens, t.shape[1]) for t in sites) * K_
     syrk_tf = syrk_total_flops / (syrk_ms / 1e3) / 1e12 if syrk_ms > 0 else 0.0
     apply_tf = jac_flops / (apply_ms / 1e3) / 1e12 if apply_ms > 0 else 0.0
+    apply_gbs = jac_bytes / (apply_ms / 1e3) / 1e9 if apply_ms > 0 else 0.0
+    hbm_peak = pk.get("hbm_gbs", 6400.0)
+    bf16_burst = pk.get("bf16_tflops", 1800.0)
     kern = {
         "tc_gemm_kernel (covariance SYRK)": {
             "bound": "tensor", "achieved": round(syrk_tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
             "frac": round(syrk_tf / bf16_peak, 4), "ms_per_step": round(syrk_ms / K_, 3),
             "launches_per_step": n_syrk // K_, "peak_kind": "bf16 dense, sustained, of measured"},
-        "jac_apply_kernel (Jacobi rotations)": {
-            "bound": "alu", "achieved": round(apply_tf, 2), "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
-            "frac": round(apply_tf / fp32_peak, 4), "ms_per_step": round(apply_ms / K_, 3),
+        "jac_apply_tc_kernel (Jacobi rotations, tcgen05)": {
+            "bound": "hbm", "achieved": round(apply_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(apply_gbs / hbm_peak, 4), "ms_per_step": round(apply_ms / K_, 3),
             "launches_per_step": apply_launches // K_,
             "avg_launch_ms": round(apply_ms / max(apply_launches, 1), 4),
+            "algorithmic_bytes_per_step": round(jac_bytes / K_),
             "traffic": JAC_APPLY_TRAFFIC,
-            "peak_kind": "FP32 FFMA, measured by the library's FMA probe kernel (derived %d SMs x 128 lanes x 2 "
-                         "flop x %.0f MHz = %.1f TFLOP/s)" % (n_sm, sm_max, fp32_derived)},
+            "tensor_tflops_executed": round(apply_tf, 2),
+            "tensor_frac_of_bf16_burst": round(apply_tf / bf16_burst, 4),
+            "peak_kind": "HBM copy, of measured; algorithmic bytes = C and Qt read and written once per executed "
+                         "task"},
         "jac_solve_kernel (Jacobi pair problems)": {
             "bound": "latency", "ms_per_step": round(solve_ms / K_, 3),
             "launches_per_step": apply_launches // K_},
@@ -507,8 +515,8 @@ def run_kfsvd(args):
             ctx, torch, K, pk.get("hbm_gbs", 6400.0), unit_len=4096)
     if rank == 0 and world == 1:
         kern.update(streaming_kernels(ctx, torch, K, pk.get("hbm_gbs", 6400.0)))
-    dom = max(("tc_gemm_kernel (covariance SYRK)", syrk_ms), ("jac_apply_kernel (Jacobi rotations)", apply_ms),
-              key=lambda kv: kv[1])[0]
+    dom = max(("tc_gemm_kernel (covariance SYRK)", syrk_ms),
+              ("jac_apply_tc_kernel (Jacobi rotations, tcgen05)", apply_ms), key=lambda kv: kv[1])[0]
     roof = {k: v for k, v in kern[dom].items() if k in ("bound", "achieved", "peak", "unit", "frac", "traffic")}
     roof["kernel"] = dom
     roof.setdefault("traffic", None)

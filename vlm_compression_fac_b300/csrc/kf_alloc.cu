@@ -39,10 +39,13 @@ __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_un
 constexpr int MODE_GIVEN_KEYS = 100;  // internal: the caller's keys, as given
 constexpr int MODE_SWIFT_HYBRID = 101;  // internal: Swift-SVD B hybrid keys built from sigma
 
+// The low word of a key is the component id, or, when no caller needs ids (no keep mask), the
+// unit index: the sort orders by the score word only and is stable, so equal scores stay in
+// id order either way, and every later pass needs only the unit (its cost, its rank count).
 __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off,
                                   const int64_t* __restrict__ cost, int n_units, int64_t n, int mode,
                                   const float* __restrict__ weight, const float* __restrict__ energy,
-                                  unsigned long long* __restrict__ keys) {
+                                  unsigned long long* __restrict__ keys, int low_is_unit) {
   for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += int64_t(gridDim.x) * blockDim.x) {
     const int u = unit_of(off, n_units, g);
     const float s = sigma[g];
@@ -62,7 +65,8 @@ __global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t
       sc = (w > 0.f) ? __fmul_rn(w, sc) : 0.f;  // also maps a NaN weight to 0
     }
     const unsigned bits = ~__float_as_uint(sc);
-    keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(uint32_t(g));
+    const uint32_t low = low_is_unit ? uint32_t(u) : uint32_t(g);
+    keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(low);
   }
 }
 
@@ -199,52 +203,90 @@ __global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__
   }
 }
 
+// Stable scatter of one 4096-key tile: every key's rank among the tile's keys of its digit
+// (rounds of 256 keys in index order; per-warp digit counts by warp match, then across the 8
+// warps in warp order), the key stored at that position of the tile's digit-ordered copy in
+// shared memory, then the copy written out so that consecutive threads write consecutive
+// addresses of one digit's run (coalesced).  The tile's digit counts come from the scanned
+// (digit, tile) histogram: count[d] = base of the next tile (or digit) minus this base.
 __global__ void __launch_bounds__(RT) scatter_kernel(const unsigned long long* __restrict__ in,
                                                      unsigned long long* __restrict__ out, int64_t n, int shift,
                                                      int ntiles, const unsigned* __restrict__ hist) {
   __shared__ unsigned base[256];
+  __shared__ unsigned start[256];   // the digit's first position in the tile's ordered copy
   __shared__ unsigned run[256];
-  __shared__ unsigned wcnt[RT / 32][256];
-  __shared__ unsigned woff[RT / 32][256];
+  __shared__ unsigned wcnt[RT / 32][256];   // per-warp digit counts, then (in place) offsets
+  __shared__ unsigned long long tk[TILE];
+  __shared__ unsigned wsum[RT / 32];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  base[t] = hist[int64_t(t) * ntiles + blockIdx.x];
-  run[t] = 0;
   const int64_t tile0 = int64_t(blockIdx.x) * TILE;
+  const int tile_n = int(n - tile0 < TILE ? n - tile0 : TILE);
+  {
+    const int64_t hi = int64_t(t) * ntiles + blockIdx.x;
+    base[t] = hist[hi];
+    const unsigned nxt = (blockIdx.x + 1 < ntiles) ? hist[hi + 1] : (t + 1 < 256 ? hist[int64_t(t + 1) * ntiles] : unsigned(n));
+    const unsigned cnt = nxt - base[t];
+    // exclusive scan of the 256 counts (one per thread) -> start
+    unsigned x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    unsigned pre = 0;
+    for (int ww = 0; ww < w; ++ww) pre += wsum[ww];
+    start[t] = pre + x - cnt;
+    run[t] = 0;
+  }
   for (int r = 0; r < RI; ++r) {
     for (int x = lane; x < 256; x += 32) wcnt[w][x] = 0;
     __syncthreads();
-    const int64_t g = tile0 + int64_t(r) * RT + t;
-    const bool valid = g < n;
-    const unsigned long long k = valid ? in[g] : 0ull;
+    const int li = r * RT + t;
+    const bool valid = li < tile_n;
+    const unsigned long long k = valid ? in[tile0 + li] : 0ull;
     const unsigned d = valid ? unsigned((k >> shift) & 255u) : 256u;
     const unsigned peers = __match_any_sync(0xffffffffu, d);
     const unsigned lt = peers & ((1u << lane) - 1u);
     const unsigned rank = __popc(lt);
     if (valid && lt == 0) wcnt[w][d] = __popc(peers);
     __syncthreads();
-    {  // per digit: offsets of each warp within this round, in warp order
+    {  // per digit: offsets of each warp within this round, in warp order (in place)
       unsigned acc = run[t];
       for (int ww = 0; ww < RT / 32; ++ww) {
-        woff[ww][t] = acc;
-        acc += wcnt[ww][t];
+        const unsigned c = wcnt[ww][t];
+        wcnt[ww][t] = acc;
+        acc += c;
       }
       run[t] = acc;
     }
     __syncthreads();
-    if (valid) out[base[d] + woff[w][d] + rank] = k;
+    if (valid) tk[start[d] + wcnt[w][d] + rank] = k;
     __syncthreads();
   }
+  for (int i = t; i < tile_n; i += RT) {
+    const unsigned long long k = tk[i];
+    const unsigned d = unsigned((k >> shift) & 255u);
+    out[base[d] + (unsigned(i) - start[d])] = k;
+  }
+}
+
+__device__ __forceinline__ int key_unit(unsigned long long k, const int64_t* __restrict__ off, int n_units,
+                                        int low_is_unit) {
+  return low_is_unit ? int(uint32_t(k)) : unit_of(off, n_units, int64_t(uint32_t(k)));
 }
 
 // Inclusive prefix sums of the sorted components' costs, per 1024-item block.
 __global__ void __launch_bounds__(SCAN_T) cost_block_sum_kernel(const unsigned long long* __restrict__ keys,
                                                                 const int64_t* __restrict__ off,
                                                                 const int64_t* __restrict__ cost, int n_units,
-                                                                int64_t n, long long* __restrict__ bsum) {
+                                                                int64_t n, long long* __restrict__ bsum,
+                                                                int low_is_unit) {
   __shared__ long long red[SCAN_T / 32];
   const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
   long long c = 0;
-  if (i < n) c = cost[unit_of(off, n_units, int64_t(uint32_t(keys[i])))];
+  if (i < n) c = cost[key_unit(keys[i], off, n_units, low_is_unit)];
 #pragma unroll
   for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
@@ -295,11 +337,11 @@ __global__ void __launch_bounds__(SCAN_T) scan_i64_kernel(long long* __restrict_
 __global__ void __launch_bounds__(SCAN_T) cut_kernel(const unsigned long long* __restrict__ keys,
                                                      const int64_t* __restrict__ off, const int64_t* __restrict__ cost,
                                                      int n_units, int64_t n, const long long* __restrict__ bexcl,
-                                                     long long* __restrict__ prefix) {
+                                                     long long* __restrict__ prefix, int low_is_unit) {
   __shared__ long long ws[32];
   const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
   long long c = 0;
-  if (i < n) c = cost[unit_of(off, n_units, int64_t(uint32_t(keys[i])))];
+  if (i < n) c = cost[key_unit(keys[i], off, n_units, low_is_unit)];
   long long x = c;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
@@ -341,7 +383,8 @@ __global__ void kcount_kernel(const long long* __restrict__ prefix, int64_t n, l
 // atomic per component.
 constexpr int RANKS_SMEM_UNITS = 8192;
 __global__ void ranks_kernel(const unsigned long long* __restrict__ keys, const int64_t* __restrict__ off,
-                             int n_units, const unsigned long long* __restrict__ kcount, int* __restrict__ ranks) {
+                             int n_units, const unsigned long long* __restrict__ kcount, int* __restrict__ ranks,
+                             int low_is_unit) {
   extern __shared__ int rcount[];
   const bool local = n_units <= RANKS_SMEM_UNITS;  // uniform over the grid
   if (local) {
@@ -350,7 +393,7 @@ __global__ void ranks_kernel(const unsigned long long* __restrict__ keys, const 
   }
   const int64_t k = int64_t(*kcount);
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < k; i += int64_t(gridDim.x) * blockDim.x) {
-    const int u = unit_of(off, n_units, int64_t(uint32_t(keys[i])));
+    const int u = key_unit(keys[i], off, n_units, low_is_unit);
     if (local) atomicAdd(&rcount[u], 1); else atomicAdd(&ranks[u], 1);
   }
   if (local) {
@@ -459,6 +502,7 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   alloc_carve(cv, n, mode == KF_KEY_ENERGY_RATIO ? n_units : 0, b);
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "score_and_allocate: workspace too small");
   const int ntiles = int((n + TILE - 1) / TILE);
+  const int low_is_unit = keep ? 0 : 1;
   if (mode == KF_KEY_ENERGY_RATIO) {
     unit_energy_kernel<<<unsigned(n_units), 256, 0, st>>>(sigma, off, b.energy); note_launch();
     KF_CUDA(cudaGetLastError());
@@ -473,10 +517,10 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
     swift_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(eps, off, n_units, n, weight, alpha, hk); note_launch();
     KF_CUDA(cudaGetLastError());
     build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(hk, off, cost, n_units, n, MODE_GIVEN_KEYS, nullptr,
-                                                        nullptr, b.ka); note_launch();
+                                                        nullptr, b.ka, low_is_unit); note_launch();
   } else {
     build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), weight, b.energy,
-                                                        b.ka); note_launch();
+                                                        b.ka, low_is_unit); note_launch();
   }
   KF_CUDA(cudaGetLastError());
   // The keys are built in id order and every pass is stable, so sorting by the score word
@@ -509,16 +553,19 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   }
   // src now holds the sorted keys.
   const int64_t nb = (n + SCAN_T - 1) / SCAN_T;
-  cost_block_sum_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum); note_launch();
+  cost_block_sum_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, low_is_unit);
+  note_launch();
   KF_CUDA(cudaGetLastError());
   scan_i64_kernel<<<1, SCAN_T, 0, st>>>(b.bsum, nb); note_launch();
   KF_CUDA(cudaGetLastError());
-  cut_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, b.prefix); note_launch();
+  cut_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, b.prefix, low_is_unit);
+  note_launch();
   KF_CUDA(cudaGetLastError());
   kcount_kernel<<<1, 1, 0, st>>>(b.prefix, n, budget, b.kcount); note_launch();
   KF_CUDA(cudaGetLastError());
   const size_t rsmem = n_units <= RANKS_SMEM_UNITS ? sizeof(int) * size_t(n_units > 0 ? n_units : 1) : 0;
-  ranks_kernel<<<grid_cap(n, 256), 256, rsmem, st>>>(src, off, n_units, b.kcount, ranks); note_launch();
+  ranks_kernel<<<grid_cap(n, 256), 256, rsmem, st>>>(src, off, n_units, b.kcount, ranks, low_is_unit);
+  note_launch();
   KF_CUDA(cudaGetLastError());
   if (keep) {
     KF_CUDA(cudaMemsetAsync(keep, 0, size_t(n), st));

@@ -26,7 +26,11 @@ using namespace kf;
 
 namespace {
 
-constexpr int64_t ACC_CHUNK = 8192;  // tokens per preprocessing chunk (float32 / QAW input)
+constexpr int64_t ACC_CHUNK = 8192;   // tokens per preprocessing chunk of float32 input (two planes)
+// Tokens per fake-quantised chunk: each chunk is one SYRK launch, which reads and writes the
+// whole d x d float32 accumulator once, so chunks are long (at d = 18944 one pass over the
+// accumulator moves 2.9 GB; over 32768 tokens the chunk's own rows are 1.2 GB).
+constexpr int64_t QAW_CHUNK = 32768;
 // Tokens accumulated inside the tensor cores before the partial sum is added to the float32
 // covariance in global memory.  The tensor cores' float32 accumulation loses accuracy on
 // long sums of positive terms: the error of a diagonal entry grows about linearly with the
@@ -141,7 +145,7 @@ kf_status kf_sync_status(kf_ctx* ctx, kf_stream_t stream, int32_t* info) {
 size_t kfac_accumulate_workspace_size(kf_dtype dtype, kf_quant quant, int64_t d) {
   const int64_t dp = round_up(d > 0 ? d : 1, 8);
   if (dtype == KF_BF16 && quant == KF_QUANT_NONE) return 0;
-  if (quant == KF_QUANT_INT8_TOKEN) return size_t(ACC_CHUNK) * dp * 2 + 256;
+  if (quant == KF_QUANT_INT8_TOKEN) return size_t(QAW_CHUNK) * dp * 2 + 256;
   return size_t(2) * ACC_CHUNK * dp * 2 + 512;  // float32: hi and lo planes
 }
 
@@ -169,11 +173,12 @@ kf_status kfac_accumulate(kf_ctx* ctx, const void* act, kf_dtype dtype, int64_t 
     return tc_gemm(ctx, g, st);
   }
   const int64_t dp = round_up(d, 8);
+  const int64_t chunk = quant == KF_QUANT_INT8_TOKEN ? QAW_CHUNK : ACC_CHUNK;
   Carve cv(workspace, workspace_bytes, false);
-  __nv_bfloat16* p0 = cv.take<__nv_bfloat16>(size_t(ACC_CHUNK) * dp);
-  __nv_bfloat16* p1 = quant == KF_QUANT_NONE ? cv.take<__nv_bfloat16>(size_t(ACC_CHUNK) * dp) : nullptr;
-  for (int64_t t0 = 0; t0 < n_tokens; t0 += ACC_CHUNK) {
-    const int64_t rows = n_tokens - t0 < ACC_CHUNK ? n_tokens - t0 : ACC_CHUNK;
+  __nv_bfloat16* p0 = cv.take<__nv_bfloat16>(size_t(chunk) * dp);
+  __nv_bfloat16* p1 = quant == KF_QUANT_NONE ? cv.take<__nv_bfloat16>(size_t(chunk) * dp) : nullptr;
+  for (int64_t t0 = 0; t0 < n_tokens; t0 += chunk) {
+    const int64_t rows = n_tokens - t0 < chunk ? n_tokens - t0 : chunk;
     const char* src = static_cast<const char*>(act) + size_t(t0) * ld * elem_size(dtype);
     g.K = rows;
     if (quant == KF_QUANT_INT8_TOKEN) {

@@ -35,6 +35,7 @@ namespace kf {
 namespace {
 
 constexpr int JB = 32, JP = 64;  // block width, pair problem size
+constexpr size_t JAC_SOLVE_SMEM = size_t(2 * JP * (JP + 2) + JP * (JP + 1)) * sizeof(float);
 // Inner sweeps of a pair problem.  Measured on the 7B block (7 Gram matrices of 4096): one
 // sweep of rotations per pair problem instead of up to 12 costs at most one more outer sweep,
 // the final singular values come out as accurate (about 6e-5 relative on the kept components
@@ -136,8 +137,12 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
                                                         int max_inner) {
   // Row stride JP + 2: the 32 couplings A[p][q] that one rotation round reads lie on an
   // anti-diagonal (p + q constant), which a stride of JP + 1 would put in a single bank.
-  __shared__ float A[JP][JP + 2];
-  __shared__ float V[JP][JP + 1];
+  // Two copies of A: a round reads the current one and writes every entry of the next, so a
+  // round needs a single barrier (JAC_SOLVE_SMEM bytes of dynamic shared memory).
+  extern __shared__ float jsm[];
+  float (*A)[JP + 2] = reinterpret_cast<float (*)[JP + 2]>(jsm);
+  float (*An)[JP + 2] = reinterpret_cast<float (*)[JP + 2]>(jsm + JP * (JP + 2));
+  float (*V)[JP + 1] = reinterpret_cast<float (*)[JP + 1]>(jsm + 2 * JP * (JP + 2));
   __shared__ float red[8];
 
   const int k = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
       // identical in every warp (same inputs), so the branch is uniform over the CTA
       if (!__any_sync(0xffffffffu, act)) continue;
       rotated = 1;
-      __syncthreads();  // every warp has read the entries this round rewrites
+      // every entry of An is written: block (j, lane) covers rows p_j, q_j x columns p, q
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         const int j = warp + 8 * x;
@@ -214,22 +219,23 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
         const float cj = __shfl_sync(0xffffffffu, c, j), sj = __shfl_sync(0xffffffffu, sn, j);
         const int actj = __shfl_sync(0xffffffffu, act, j);
         if (j == lane) {
-          if (act) {
-            A[p][p] = a - td;
-            A[q][q] = b + td;
-            A[p][q] = 0.f;
-            A[q][p] = 0.f;
-          }
+          An[p][p] = act ? a - td : a;
+          An[q][q] = act ? b + td : b;
+          An[p][q] = act ? 0.f : d;
+          An[q][p] = act ? 0.f : A[q][p];
           continue;
         }
-        if (!actj && !act) continue;
         const float e00 = A[pj][p], e01 = A[pj][q], e10 = A[qj][p], e11 = A[qj][q];
+        if (!actj && !act) {
+          An[pj][p] = e00; An[pj][q] = e01; An[qj][p] = e10; An[qj][q] = e11;
+          continue;
+        }
         const float a1 = e00 * c - e01 * sn, b1 = e00 * sn + e01 * c;
         const float c1 = e10 * c - e11 * sn, d1 = e10 * sn + e11 * c;
-        A[pj][p] = cj * a1 - sj * c1;
-        A[pj][q] = cj * b1 - sj * d1;
-        A[qj][p] = sj * a1 + cj * c1;
-        A[qj][q] = sj * b1 + cj * d1;
+        An[pj][p] = cj * a1 - sj * c1;
+        An[pj][q] = cj * b1 - sj * d1;
+        An[qj][p] = sj * a1 + cj * c1;
+        An[qj][q] = sj * b1 + cj * d1;
       }
       if (act) {
 #pragma unroll
@@ -241,6 +247,9 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
         }
       }
       __syncthreads();
+      float (*tmp)[JP + 2] = A;
+      A = An;
+      An = tmp;
     }
     if (!rotated) break;
   }
@@ -1158,6 +1167,8 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   const int apply_grid = int(total_tasks < int64_t(ctx->sm_count) * 2 ? total_tasks : int64_t(ctx->sm_count) * 2);
   static std::atomic<unsigned long long> attr_done{0};
   KF_TRY(set_attr_once(attr_done, [&] {
+    KF_TRY(check_cuda(cudaFuncSetAttribute(jac_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           int(JAC_SOLVE_SMEM)), "jac_solve smem attribute"));
     return check_cuda(cudaFuncSetAttribute(jac_apply_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            int(apply_smem)), "jac_apply_tc smem attribute");
   }));
@@ -1182,7 +1193,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
         ctx->prof_kev_used += 3;
         KF_CUDA(cudaEventRecord(kev[0], st));
       }
-      jac_solve_kernel<<<dim3(pl.npairs, nu), 256, 0, st>>>(C, pl.sp, pl.nblk, step, bf.Vimg, skip, conv, off, flo,
+      jac_solve_kernel<<<dim3(pl.npairs, nu), 256, JAC_SOLVE_SMEM, st>>>(C, pl.sp, pl.nblk, step, bf.Vimg, skip, conv, off, flo,
                                                            tol, max_inner); note_launch();
       KF_TRY(check_cuda(cudaGetLastError(), "jac_solve_kernel"));
       if (prof) KF_CUDA(cudaEventRecord(kev[1], st));

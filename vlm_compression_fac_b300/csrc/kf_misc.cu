@@ -44,68 +44,115 @@ template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // LASER Methodology 1 (quantisation-aware whitening): symmetric per-token INT8 fake
-// quantisation.  One CTA per token row; float32 arithmetic with IEEE division.
+// quantisation, float32 arithmetic with IEEE division: s = max|row| / 127, q = clamp(rint(x / s),
+// -127, 127), value s q rounded to bfloat16 (a zero row stays zero).  One warp per token row
+// (8 rows per CTA): the row is read once for its maximum and once more (from cache) to
+// quantise; bfloat16 rows with 16-byte aligned rows go 8 elements per access.
+__device__ __forceinline__ float fq_val(float x, float s) {
+  if (!(s > 0.f)) return 0.f;
+  float q = rintf(__fdiv_rn(x, s));
+  q = fminf(fmaxf(q, -127.f), 127.f);
+  return __fmul_rn(s, q);
+}
+
 template <typename T>
-__global__ void __launch_bounds__(256) fake_quant_kernel(const T* __restrict__ in, int64_t d,
-                                                         int64_t ld, __nv_bfloat16* __restrict__ out) {
-  __shared__ float red[8];
-  const int64_t row = blockIdx.x;
+__global__ void __launch_bounds__(256) fake_quant_kernel(const T* __restrict__ in, int64_t rows, int64_t d,
+                                                         int64_t ld, __nv_bfloat16* __restrict__ out, int vec) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
   const T* x = in + row * ld;
-  float m = 0.f;
-  for (int64_t j = threadIdx.x; j < d; j += blockDim.x) m = fmaxf(m, fabsf(to_f(x[j])));
-  m = warp_max(m);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    v = warp_max(v);
-    if (threadIdx.x == 0) red[0] = v;
-  }
-  __syncthreads();
-  const float s = __fdiv_rn(red[0], 127.0f);
   __nv_bfloat16* y = out + row * d;
-  for (int64_t j = threadIdx.x; j < d; j += blockDim.x) {
-    float v = 0.f;
-    if (s > 0.f) {
-      float q = rintf(__fdiv_rn(to_f(x[j]), s));
-      q = fminf(fmaxf(q, -127.f), 127.f);
-      v = __fmul_rn(s, q);
+  float m = 0.f;
+  if (vec) {
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    for (int64_t j = lane; j < d / 8; j += 32) {
+      const uint4 w = xv[j];
+      const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        m = fmaxf(m, fabsf(__uint_as_float(a[q] << 16)));
+        m = fmaxf(m, fabsf(__uint_as_float(a[q] & 0xFFFF0000u)));
+      }
     }
-    y[j] = __float2bfloat16_rn(v);
+  } else {
+    for (int64_t j = lane; j < d; j += 32) m = fmaxf(m, fabsf(to_f(x[j])));
+  }
+  m = warp_max(m);
+  const float s = __fdiv_rn(m, 127.0f);
+  if (vec) {
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    uint4* yv = reinterpret_cast<uint4*>(y);
+    for (int64_t j = lane; j < d / 8; j += 32) {
+      const uint4 w = xv[j];
+      const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const __nv_bfloat16 lo = __float2bfloat16_rn(fq_val(__uint_as_float(a[q] << 16), s));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(fq_val(__uint_as_float(a[q] & 0xFFFF0000u), s));
+        o[q] = uint32_t(__bfloat16_as_ushort(lo)) | (uint32_t(__bfloat16_as_ushort(hi)) << 16);
+      }
+      yv[j] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  } else {
+    for (int64_t j = lane; j < d; j += 32) y[j] = __float2bfloat16_rn(fq_val(to_f(x[j]), s));
   }
 }
 
-__global__ void split_kernel(const float* __restrict__ in, int64_t rows, int64_t d, int64_t ld,
-                             __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo,
-                             int64_t ldo) {
-  const int64_t n = rows * d;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = i / d, c = i - r * d;
-    const float v = in[r * ld + c];
-    const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    hi[r * ldo + c] = h;
-    lo[r * ldo + c] = __float2bfloat16_rn(v - __bfloat162float(h));
-  }
+// Splits of float32 rows into bfloat16 planes: x = hi + lo (16 significant bits) or
+// x = x1 + x2 + x3 (the full 24-bit significand).  2-D grid: blockIdx.y walks the rows,
+// each thread four consecutive columns (one float4 load when the rows allow it).
+__device__ __forceinline__ void split3_val(float v, __nv_bfloat16& h1, __nv_bfloat16& h2, __nv_bfloat16& h3) {
+  h1 = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(h1);
+  h2 = __float2bfloat16_rn(r1);
+  h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
 }
 
-// x = x1 + x2 + x3 with each term a bfloat16 (8 significant bits): together they hold the
-// full 24-bit float32 significand.
-__global__ void split3_kernel(const float* __restrict__ in, int64_t rows, int64_t d, int64_t ld,
-                              __nv_bfloat16* __restrict__ p1, __nv_bfloat16* __restrict__ p2,
-                              __nv_bfloat16* __restrict__ p3, int64_t ldo) {
-  const int64_t n = rows * d;
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = i / d, c = i - r * d;
-    const float v = in[r * ld + c];
-    const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(h1);
-    const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(h2);
-    p1[r * ldo + c] = h1;
-    p2[r * ldo + c] = h2;
-    p3[r * ldo + c] = __float2bfloat16_rn(r2);
+template <int NP>
+__global__ void __launch_bounds__(256) split_planes_kernel(const float* __restrict__ in, int64_t rows, int64_t d,
+                                                           int64_t ld, __nv_bfloat16* __restrict__ p1,
+                                                           __nv_bfloat16* __restrict__ p2,
+                                                           __nv_bfloat16* __restrict__ p3, int64_t ldo, int vec) {
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const float* x = in + r * ld;
+    for (int64_t c = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * 4; c < d;
+         c += int64_t(gridDim.x) * blockDim.x * 4) {
+      float v[4];
+      if (vec && c + 3 < d) {
+        const float4 f = *reinterpret_cast<const float4*>(x + c);
+        v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = c + q < d ? x[c + q] : 0.f;
+      }
+      __nv_bfloat16 h[3][4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (NP == 3) {
+          split3_val(v[q], h[0][q], h[1][q], h[2][q]);
+        } else {
+          h[0][q] = __float2bfloat16_rn(v[q]);
+          h[1][q] = __float2bfloat16_rn(v[q] - __bfloat162float(h[0][q]));
+          h[2][q] = h[1][q];
+        }
+      }
+      __nv_bfloat16* outs[3] = {p1, p2, p3};
+#pragma unroll
+      for (int pl = 0; pl < NP; ++pl) {
+        __nv_bfloat16* y = outs[pl] + r * ldo + c;
+        if (vec && c + 3 < d) {
+          const uint32_t a = uint32_t(__bfloat16_as_ushort(h[pl][0])) | (uint32_t(__bfloat16_as_ushort(h[pl][1])) << 16);
+          const uint32_t b = uint32_t(__bfloat16_as_ushort(h[pl][2])) | (uint32_t(__bfloat16_as_ushort(h[pl][3])) << 16);
+          *reinterpret_cast<uint2*>(y) = make_uint2(a, b);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (c + q < d) y[q] = h[pl][q];
+        }
+      }
+    }
   }
 }
 
@@ -367,25 +414,47 @@ kf_status launch_ffma_probe(int sm_count, int64_t iters, float* sink, double* fl
 kf_status launch_fake_quant(const void* in, kf_dtype dt, int64_t rows, int64_t d, int64_t ld,
                             __nv_bfloat16* out, cudaStream_t st) {
   if (rows <= 0) return KF_OK;
-  if (dt == KF_BF16)
-    fake_quant_kernel<__nv_bfloat16><<<unsigned(rows), 256, 0, st>>>((const __nv_bfloat16*)in, d, ld, out);
-  else
-    fake_quant_kernel<float><<<unsigned(rows), 256, 0, st>>>((const float*)in, d, ld, out);
+  const unsigned blocks = unsigned((rows + 7) / 8);
+  if (dt == KF_BF16) {
+    const int vec = ((reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out)) % 16 == 0 && ld % 8 == 0 &&
+                     d % 8 == 0) ? 1 : 0;
+    fake_quant_kernel<__nv_bfloat16><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)in, rows, d, ld, out, vec);
+  } else {
+    fake_quant_kernel<float><<<blocks, 256, 0, st>>>((const float*)in, rows, d, ld, out, 0);
+  }
   note_launch();
   return check_cuda(cudaGetLastError(), "fake_quant launch");
 }
 
+namespace {
+dim3 split_grid(int64_t rows, int64_t d) {
+  const int64_t gx = (d + 1023) / 1024;
+  const int64_t gy = rows < 65535 ? rows : 65535;
+  return dim3(unsigned(gx < 1 ? 1 : gx), unsigned(gy < 1 ? 1 : gy));
+}
+int split_vec(const float* in, int64_t ld, const void* p1, const void* p2, const void* p3, int64_t ldo) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(in);
+  const uintptr_t o = reinterpret_cast<uintptr_t>(p1) | reinterpret_cast<uintptr_t>(p2) |
+                      reinterpret_cast<uintptr_t>(p3);
+  return (a % 16 == 0 && ld % 4 == 0 && o % 8 == 0 && ldo % 4 == 0) ? 1 : 0;
+}
+}  // namespace
+
 kf_status launch_split_bf16(const float* in, int64_t rows, int64_t d, int64_t ld,
                             __nv_bfloat16* hi, __nv_bfloat16* lo, int64_t ldo, cudaStream_t st) {
   if (rows <= 0 || d <= 0) return KF_OK;
-  split_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, hi, lo, ldo); note_launch();
+  split_planes_kernel<2><<<split_grid(rows, d), 256, 0, st>>>(in, rows, d, ld, hi, lo, lo, ldo,
+                                                              split_vec(in, ld, hi, lo, lo, ldo));
+  note_launch();
   return check_cuda(cudaGetLastError(), "split launch");
 }
 
 kf_status launch_split3_bf16(const float* in, int64_t rows, int64_t d, int64_t ld, __nv_bfloat16* p1,
                              __nv_bfloat16* p2, __nv_bfloat16* p3, int64_t ldo, cudaStream_t st) {
   if (rows <= 0 || d <= 0) return KF_OK;
-  split3_kernel<<<grid_for(rows * d), 256, 0, st>>>(in, rows, d, ld, p1, p2, p3, ldo); note_launch();
+  split_planes_kernel<3><<<split_grid(rows, d), 256, 0, st>>>(in, rows, d, ld, p1, p2, p3, ldo,
+                                                              split_vec(in, ld, p1, p2, p3, ldo));
+  note_launch();
   return check_cuda(cudaGetLastError(), "split3 launch");
 }
 
