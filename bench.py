@@ -314,6 +314,43 @@ def run_workloads(ctx, torch, K, names, fp32_peak):
     return out
 
 
+class SitePrefetch:
+    """Calibration rows for the pipeline's streamed-rows interface, copied from pinned host
+    memory on a side stream one site ahead: while the compute stream accumulates a site's
+    covariance, the next site's rows are already on their way (the copy engine and the
+    tensor cores overlap).  ``order`` is the order in which the pipeline asks for the sites; a
+    site asked for out of that order is copied when asked."""
+
+    def __init__(self, torch, host, order, compute):
+        self.torch = torch
+        self.host = host
+        self.order = list(order)
+        self.compute = compute
+        self.copy = torch.cuda.Stream()
+        self.ready = {}
+        self._start(0)
+
+    def _start(self, i):
+        if i >= len(self.order) or self.order[i] in self.ready:
+            return
+        name = self.order[i]
+        with self.torch.cuda.stream(self.copy):
+            t = self.host[name].to("cuda", non_blocking=True)
+            ev = self.torch.cuda.Event()
+            ev.record(self.copy)
+        self.ready[name] = (t, ev, i)
+
+    def __call__(self, name, t0, t1):
+        if name not in self.ready:
+            self.order.append(name)
+            self._start(len(self.order) - 1)
+        t, ev, i = self.ready.pop(name)
+        self.compute.wait_event(ev)
+        t.record_stream(self.compute)
+        self._start(i + 1)
+        return t[t0:t1]
+
+
 def syrk_flops(n_tokens, d):
     return 2.0 * n_tokens * d * (d + 1) / 2.0
 
@@ -356,6 +393,17 @@ def run_kfsvd(args):
             return pipeline.compress_activation_only(ctx, units, w, a, wl.n_tokens, wl.budget, sync_timer=timer)
         return pipeline.compress(ctx, units, w, a, g, wl.n_tokens, lam=wl.lam, budget=wl.budget, sync_timer=timer,
                                  score=args.score)
+
+    def run_rows(rows, w):
+        """The same step with the calibration rows from a callable (whole sites per call)."""
+        dims = {n: s.d for n, s in wl.sites.items()}
+        if swift:
+            return pipeline.compress_activation_only(ctx, units, w, rows, wl.n_tokens, wl.budget, site_dims=dims,
+                                                     chunk_tokens=wl.n_tokens)
+        return pipeline.compress(ctx, units, w, rows, None, wl.n_tokens, lam=wl.lam, budget=wl.budget,
+                                 score=args.score, site_dims=dims,
+                                 act_sites=[n for n, s in wl.sites.items() if s.kind == "act"],
+                                 chunk_tokens=wl.n_tokens)
 
     def one_step(a, g, w):
         return run(a, g, w, mark)
@@ -444,15 +492,21 @@ def run_kfsvd(args):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        h_rows = dict(h_acts)
+        h_rows.update(h_grads)
+        order = []                  # the order in which the pipeline asks for the sites
+        for u in units:
+            for sn in ((u.x_site,) if swift else (u.x_site, u.g_site)):
+                if sn not in order:
+                    order.append(sn)
         e0.record(stream)
         for _ in range(K_):
-            a = {k: v.to("cuda", non_blocking=True) for k, v in h_acts.items()}
-            g = {k: v.to("cuda", non_blocking=True) for k, v in h_grads.items()}
             w = {k: v.to("cuda", non_blocking=True) for k, v in h_w.items()}
-            r = run(a, g, w)
+            rows = SitePrefetch(torch, h_rows, order, stream)
+            r = run_rows(rows, w)
             outs = [u.U.cpu() for u in r.units] + [u.V.cpu() for u in r.units] + [r.ranks.cpu()]
             out_bytes = sum(o.numel() * o.element_size() for o in outs)
-            del a, g, w, r
+            del w, r, rows
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1)

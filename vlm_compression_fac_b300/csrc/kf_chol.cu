@@ -26,16 +26,16 @@ constexpr int NB = CHOL_NB;
 
 // Factors the nb x nb (nb <= 64) lower block at A in shared memory and writes its lower
 // factor back (zeros above) and the inverse of that factor to dinv (NB columns, row-major).
-// Column j of the factorisation is one phase: every thread reads the pivot and column j
-// (final after the previous barrier), stores its scaled entries of column j into L and
-// updates its entries of the trailing lower triangle; column j is never written in its own
-// phase.  The inverse solves L X = I for all columns at once, one elimination step per phase
-// (rows below k updated with the unscaled row k), scaled by the diagonal at the end.
+// Column j: every thread takes the pivot from a[j][j], the threads of rows below scale
+// column j into L (one IEEE division per entry), then after a barrier the trailing lower
+// triangle gets its rank-1 update from L's column (thread (ty, tx): rows j + 1 + ty + 4 i,
+// column j + 1 + tx).  The inverse solves L X = I for all columns at once: step k scales row
+// k of X, then updates the rows below with it.
 __global__ void __launch_bounds__(256) chol_diag_kernel(float* __restrict__ A, int64_t lda, int nb,
                                                         float* __restrict__ dinv, int* status, int64_t k0) {
   __shared__ float a[NB][NB + 1];
   __shared__ float L[NB][NB + 1];
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, tx = t & 63, ty = t >> 6;
   for (int idx = t; idx < NB * NB; idx += blockDim.x) {
     const int i = idx / NB, j = idx % NB;
     const bool in = i < nb && j < nb && j <= i;
@@ -51,30 +51,28 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(float* __restrict__ A, i
       if (bad) raise_status(status, KF_ERR_NOT_SPD, int(k0 + j));
       L[j][j] = ljj;
     }
-    const int rem = nb - j - 1;
-    for (int i = j + 1 + t; i < nb; i += blockDim.x) L[i][j] = __fdiv_rn(a[i][j], ljj);
-    for (int idx = t; idx < rem * rem; idx += blockDim.x) {
-      const int i = j + 1 + idx / rem, k = j + 1 + idx % rem;
-      if (k <= i) {
-        const float li = __fdiv_rn(a[i][j], ljj), lk = __fdiv_rn(a[k][j], ljj);
-        a[i][k] = fmaf(-li, lk, a[i][k]);
-      }
+    if (t > j && t < nb) L[t][j] = __fdiv_rn(a[t][j], ljj);
+    __syncthreads();
+    const int k = j + 1 + tx;
+    if (k < nb) {
+      const float lk = L[k][j];
+      for (int i = k + ty; i < nb; i += 4) a[i][k] = fmaf(-L[i][j], lk, a[i][k]);
     }
     __syncthreads();
   }
-  // X = L^-1: B = I; step k: B[i][c] -= L[i][k] B[k][c] / L[k][k] for i > k, c <= k; then
-  // X[i][c] = B[i][c] / L[i][i].  `a` holds B (its old contents are no longer needed).
+  // X = L^-1 in `a` (its old contents are no longer needed): start from I; step k:
+  // X[k][c] /= L[k][k] for c <= k, then X[i][c] -= L[i][k] X[k][c] for i > k, c <= k.
   for (int idx = t; idx < NB * NB; idx += blockDim.x) {
     const int i = idx / NB, c = idx % NB;
     a[i][c] = (i == c && i < nb) ? 1.f : 0.f;
   }
   __syncthreads();
-  for (int k = 0; k < nb - 1; ++k) {
-    const float lkk = L[k][k];
-    const int rows = nb - k - 1, cols = k + 1;
-    for (int idx = t; idx < rows * cols; idx += blockDim.x) {
-      const int i = k + 1 + idx / cols, c = idx % cols;
-      a[i][c] = fmaf(-L[i][k], __fdiv_rn(a[k][c], lkk), a[i][c]);
+  for (int k = 0; k < nb; ++k) {
+    if (t <= k) a[k][t] = __fdiv_rn(a[k][t], L[k][k]);
+    __syncthreads();
+    if (tx <= k) {
+      const float xk = a[k][tx];
+      for (int i = k + 1 + ty; i < nb; i += 4) a[i][tx] = fmaf(-L[i][k], xk, a[i][tx]);
     }
     __syncthreads();
   }
@@ -84,7 +82,7 @@ __global__ void __launch_bounds__(256) chol_diag_kernel(float* __restrict__ A, i
   }
   for (int idx = t; idx < nb * NB; idx += blockDim.x) {
     const int i = idx / NB, c = idx % NB;
-    dinv[int64_t(i) * NB + c] = (c < nb && c <= i) ? __fdiv_rn(a[i][c], L[i][i]) : 0.f;
+    dinv[int64_t(i) * NB + c] = (c < nb && c <= i) ? a[i][c] : 0.f;
   }
 }
 

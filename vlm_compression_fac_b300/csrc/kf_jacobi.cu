@@ -192,7 +192,11 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   // so the parameters reach the threads that need them by warp shuffles rather than
   // through shared memory; thread (warp w, lane k) then updates the 2 x 2 blocks (j, k),
   // j = w, w + 8, w + 16, w + 24, and rows w, w + 8, ... of the columns p_k, q_k of V.
+  // The rotation parameters use the fast reciprocal and reciprocal square root: a rotation
+  // only has to be (nearly) orthogonal and to shrink its coupling, and the Newton-Schulz step
+  // below re-orthogonalises the accumulated V before it leaves the kernel.
   const int lane = t & 31, warp = t >> 5;
+  const float tol2 = tol * tol;
   for (int sweep = 0; sweep < max_inner; ++sweep) {
     int rotated = 0;
     for (int r = 0; r < JP - 1; ++r) {
@@ -200,10 +204,10 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
       const float a = A[p][p], b = A[q][q], d = A[p][q];
       float c = 1.f, sn = 0.f, td = 0.f;
       int act = 0;
-      if (fabsf(d) > flo && fabsf(d) > tol * sqrtf(fmaxf(a * b, 0.f))) {
-        const float tau = __fdiv_rn(b - a, 2.f * d);
-        const float tt = copysignf(1.f, tau) / (fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f)));
-        c = 1.0f / sqrtf(fmaf(tt, tt, 1.f));
+      if (fabsf(d) > flo && d * d > tol2 * fmaxf(a * b, 0.f)) {
+        const float tau = (b - a) * __frcp_rn(2.f * d);
+        const float tt = copysignf(__frcp_rn(fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f))), tau);
+        c = rsqrtf(fmaf(tt, tt, 1.f));
         sn = tt * c;
         td = tt * d;
         act = 1;
@@ -360,13 +364,21 @@ __device__ __forceinline__ void put8(uint8_t* img, uint32_t off, const uint32_t*
     *reinterpret_cast<uint4*>(img + pl * APLANE_BYTES + off) = make_uint4(p[pl][0], p[pl][1], p[pl][2], p[pl][3]);
 }
 
-// Copies one 24 KB V image (global, 16-byte aligned) into shared memory.
-__device__ __forceinline__ void copy_vimg(uint8_t* dst, const uint8_t* __restrict__ src, int tid) {
+// Starts the copy of one 24 KB V image (global, 16-byte aligned) into shared memory with
+// cp.async (16 bytes per thread and step) and commits it as one group: the caller waits for
+// the group (cp.async.wait_group) before the MMA phase that reads the image.
+__device__ __forceinline__ void copy_vimg_async(uint8_t* dst, const uint8_t* __restrict__ src, int tid) {
 #pragma unroll
   for (int i = 0; i < VIMG_BYTES / (16 * 256); ++i) {
     const int e = tid + i * 256;
-    reinterpret_cast<uint4*>(dst)[e] = __ldg(reinterpret_cast<const uint4*>(src) + e);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst + 16 * e)), "l"(src + 16 * e)
+                 : "memory");
   }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
@@ -434,10 +446,90 @@ __device__ __forceinline__ bool mma_phase(TcApplyCtl& c, uint32_t a_img, bool a_
   return true;
 }
 
-// Persistent apply of one Jacobi step on the tensor cores.  Task g of problem u: a super-tile
-// (super-pairs P <= Q; super-pair P = pairs 2P and 2P + 1) of C, or a 64 x 128 panel (pair q,
-// columns 128 cb ..) of Qt.  Tasks whose pairs all skipped their rotation are not run; a
-// skipped pair inside a run task enters with the identity image (exact in three planes).
+// A task of the tensor-core apply: a super-tile (super-pairs P <= Q; super-pair P = pairs 2P
+// and 2P + 1) of C, or a 64 x 256 panel (pair q, columns 256 cb ..) of Qt.
+struct TcTask {
+  int kind;  // 0: C super-tile, 1: Qt panel
+  int u, P, Q, q, cb;
+};
+
+// Advances g (in steps of the grid) to the next task that runs and decodes it; false if none
+// is left.  A task runs unless its problem has converged or all its pairs skipped rotation.
+__device__ __forceinline__ bool next_tc_task(int& g, int total, int per_u, int nsup, int nsp, int npairs,
+                                             const int* __restrict__ skipall, const int* __restrict__ conv,
+                                             TcTask& t) {
+  for (; g < total; g += gridDim.x) {
+    const int u = g / per_u;
+    int task = g - u * per_u;
+    if (conv[u]) continue;
+    const int* skip = skipall + int64_t(u) * npairs;
+    if (task < nsup) {
+      // row P of the upper triangle of super-tiles holds nsp - P of them
+      const int n2 = 2 * nsp + 1;
+      int P = int((float(n2) - sqrtf(float(n2) * float(n2) - 8.f * float(task))) * 0.5f);
+      P = P < 0 ? 0 : (P > nsp - 1 ? nsp - 1 : P);
+      while (P > 0 && P * (n2 - P) / 2 > task) --P;
+      while (P + 1 < nsp && (P + 1) * (n2 - P - 1) / 2 <= task) ++P;
+      const int Q = P + (task - P * (n2 - P) / 2);
+      if (skip[2 * P] && skip[2 * P + 1] && skip[2 * Q] && skip[2 * Q + 1]) continue;
+      t.kind = 0; t.u = u; t.P = P; t.Q = Q; t.q = 0; t.cb = 0;
+      return true;
+    }
+    task -= nsup;
+    const int cb = task / npairs, q = task - cb * npairs;
+    if (skip[q]) continue;
+    t.kind = 1; t.u = u; t.P = 0; t.Q = 0; t.q = q; t.cb = cb;
+    return true;
+  }
+  return false;
+}
+
+// Issues the global loads of a task's float32 operand into R (16 float4 per thread): a
+// super-tile's S = C[rows of P][cols of Q] (warp w rows w + 8 i, lane l columns 4 l ..), or a
+// panel's two 128-column halves (rows w + 8 i of the pair, columns 4 l .. of each half).
+__device__ __forceinline__ void load_tc_task(const TcTask& t, float4* R, const float* __restrict__ Call,
+                                             const float* __restrict__ Qtall, int64_t sp, int nblk, int step,
+                                             int warp, int lane) {
+  if (t.kind == 0) {
+    const float* C = Call + int64_t(t.u) * sp * sp;
+    const int cl = 4 * lane, qp = 2 * t.Q + (cl >> 6);
+    const int64_t gcol = int64_t(((cl >> 5) & 1) ? rr_pos(nblk - 1 - qp, step, nblk) : rr_pos(qp, step, nblk)) * JB +
+                         (cl & 31);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int r = warp + 8 * i, pp = 2 * t.P + (r >> 6);
+      const int64_t grow = int64_t(((r >> 5) & 1) ? rr_pos(nblk - 1 - pp, step, nblk) : rr_pos(pp, step, nblk)) * JB +
+                           (r & 31);
+      R[i] = *reinterpret_cast<const float4*>(C + grow * sp + gcol);
+    }
+  } else {
+    const float* Qt = Qtall + int64_t(t.u) * sp * sp;
+    const int b0 = rr_pos(t.q, step, nblk), b1 = rr_pos(nblk - 1 - t.q, step, nblk);
+    const int64_t col0 = int64_t(t.cb) * 256;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (col0 + 128 * h < sp) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = warp + 8 * i;
+          R[8 * h + i] = *reinterpret_cast<const float4*>(Qt + gidx(r, b0, b1) * sp + col0 + 128 * h + 4 * lane);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ const uint8_t* vimg_src(const uint8_t* Vimg, const uint8_t* Iimg, const int* skipall,
+                                                   int u, int npairs, int pair) {
+  return skipall[int64_t(u) * npairs + pair] ? Iimg : Vimg + (int64_t(u) * npairs + pair) * VIMG_BYTES;
+}
+
+// Persistent apply of one Jacobi step on the tensor cores over the tasks above.  Tasks whose
+// pairs all skipped their rotation are not run; a skipped pair inside a run task enters with
+// the identity image (exact in three planes).  Latency hiding inside a CTA: the next task's
+// rows are loaded into registers as soon as the current task has staged its own, and its V
+// images are copied (cp.async) as soon as the current task's last product has completed, so
+// both overlap the current task's remaining products and its stores.
 __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
     float* __restrict__ Call, float* __restrict__ Qtall, int64_t sp, int nblk, int step,
     const uint8_t* __restrict__ Vimg, const uint8_t* __restrict__ Iimg, const int* __restrict__ skipall,
@@ -452,7 +544,6 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int npairs = nblk / 2;
-  const int64_t npan = sp / 128;
 
   if (tid == 0) {
     mbar_init(smem_u32(bar), 1);
@@ -477,22 +568,26 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
   const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
   unsigned long long bytes = 0, flops = 0;
 
-  for (int g = blockIdx.x; g < total && c.ok; g += gridDim.x) {
-    const int u = g / per_u;
-    int task = g - u * per_u;
-    if (conv[u]) continue;
-    const int* skip = skipall + int64_t(u) * npairs;
-    const uint8_t* Vu = Vimg + int64_t(u) * npairs * VIMG_BYTES;
-    if (task < nsup) {
-      // ---------------- C super-tile (P, Q), P <= Q: row P holds nsp - P super-tiles
-      const int n2 = 2 * nsp + 1;
-      int P = int((float(n2) - sqrtf(float(n2) * float(n2) - 8.f * float(task))) * 0.5f);
-      P = P < 0 ? 0 : (P > nsp - 1 ? nsp - 1 : P);
-      while (P > 0 && P * (n2 - P) / 2 > task) --P;
-      while (P + 1 < nsp && (P + 1) * (n2 - P - 1) / 2 <= task) ++P;
-      const int Q = P + (task - P * (n2 - P) / 2);
+  TcTask cur, nxt;
+  float4 R[16];
+  int g = blockIdx.x;
+  bool have = next_tc_task(g, total, per_u, nsup, nsp, npairs, skipall, conv, cur);
+  if (have) {
+    load_tc_task(cur, R, Call, Qtall, sp, nblk, step, warp, lane);
+    if (cur.kind == 0) {
+      copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, cur.u, npairs, 2 * cur.Q), tid);
+      copy_vimg_async(Vb1, vimg_src(Vimg, Iimg, skipall, cur.u, npairs, 2 * cur.Q + 1), tid);
+    } else {
+      copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, cur.u, npairs, cur.q), tid);
+    }
+  }
+  while (have && c.ok) {
+    int g2 = g + gridDim.x;
+    bool have2 = false;
+    if (cur.kind == 0) {
+      // ---------------- C super-tile (P, Q)
+      const int u = cur.u, P = cur.P, Q = cur.Q;
       const int pr[2] = {2 * P, 2 * P + 1}, qr[2] = {2 * Q, 2 * Q + 1};
-      if (skip[pr[0]] && skip[pr[1]] && skip[qr[0]] && skip[qr[1]]) continue;
       const bool diag = P == Q;
       float* C = Call + int64_t(u) * sp * sp;
       int pb[2][2], qb[2][2];
@@ -501,38 +596,28 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
         pb[i][0] = rr_pos(pr[i], step, nblk); pb[i][1] = rr_pos(nblk - 1 - pr[i], step, nblk);
         qb[i][0] = rr_pos(qr[i], step, nblk); qb[i][1] = rr_pos(nblk - 1 - qr[i], step, nblk);
       }
-      // S = C[rows of P][cols of Q] into registers: warp w rows w + 8 i, lane l cols 4 l .. 4 l + 3
-      const int cl = 4 * lane;                       // local column 0..124
-      const int64_t gcol = int64_t(qb[cl >> 6][(cl >> 5) & 1]) * JB + (cl & 31);
-      float4 s[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int r = warp + 8 * i;
-        const int64_t grow = int64_t(pb[r >> 6][(r >> 5) & 1]) * JB + (r & 31);
-        s[i] = *reinterpret_cast<const float4*>(C + grow * sp + gcol);
-      }
-      const uint8_t* vq0 = skip[qr[0]] ? Iimg : Vu + int64_t(qr[0]) * VIMG_BYTES;
-      const uint8_t* vq1 = skip[qr[1]] ? Iimg : Vu + int64_t(qr[1]) * VIMG_BYTES;
-      const uint8_t* vp0 = skip[pr[0]] ? Iimg : Vu + int64_t(pr[0]) * VIMG_BYTES;
-      const uint8_t* vp1 = skip[pr[1]] ? Iimg : Vu + int64_t(pr[1]) * VIMG_BYTES;
-      copy_vimg(Vb0, vq0, tid);
-      copy_vimg(Vb1, vq1, tid);
+      const int cl = 4 * lane;
       // step 1a: U[:, 0:64] = S[:, q pair 0] V_q0   (lanes 0..15 hold those columns)
       if (lane < 16) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl), s[i]);
+        for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl), R[i]);
       }
+      cp_async_wait<0>();
       if (!mma_phase(c, a_img, false, v0, 0, tid)) break;
+      copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, u, npairs, pr[0]), tid);  // during step 1b
       // step 1b: U[:, 64:128] = S[:, q pair 1] V_q1
       if (lane >= 16) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl - 64), s[i]);
+        for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl - 64), R[i]);
       }
       if (!mma_phase(c, a_img, false, v1, 64, tid)) break;
+      // R is free: the next task's rows load during steps 2a, 2b and the stores
+      have2 = next_tc_task(g2, total, per_u, nsup, nsp, npairs, skipall, conv, nxt);
+      if (have2) load_tc_task(nxt, R, Call, Qtall, sp, nblk, step, warp, lane);
+      copy_vimg_async(Vb1, vimg_src(Vimg, Iimg, skipall, u, npairs, pr[1]), tid);  // during step 2a
       // step 2: D_p = U_p^T V_p for p pair 0 (U rows 0..63) and 1 (rows 64..127): the threads of
       // TMEM lanes of rows of p write U_p^T (M = U column, K = row within p) as MN-major planes
       for (int pp = 0; pp < 2; ++pp) {
-        copy_vimg(pp ? Vb1 : Vb0, pp ? vp1 : vp0, tid);
         if (((warp & 3) >> 1) == pp) {
           const int k = (warp & 1) * 32 + lane;      // row within pair pp
           const int m0 = (warp >> 2) * 64;           // U columns m0 .. m0 + 63
@@ -544,9 +629,18 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
             for (int q = 0; q < 4; ++q) put8(Abuf, amn_off(m0 + 32 * h + 8 * q, k), v + 8 * q);
           }
         }
+        if (pp == 0) cp_async_wait<1>(); else cp_async_wait<0>();
         if (!mma_phase(c, a_img, true, pp ? v1 : v0, 128 + 64 * pp, tid)) break;
       }
       if (!c.ok) break;
+      if (have2) {  // both V buffers are free: the next task's first images
+        if (nxt.kind == 0) {
+          copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, 2 * nxt.Q), tid);
+          copy_vimg_async(Vb1, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, 2 * nxt.Q + 1), tid);
+        } else {
+          copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, nxt.q), tid);
+        }
+      }
       // epilogue: D_p (lane = column c of Q, TMEM column n = row of pair p) -> C[p rows][Q cols]
       // and, mirrored, C[Q cols][p rows]; a diagonal super-tile writes the pair-0 x pair-1 tile
       // and the upper halves of its two diagonal tiles, each with its mirror (C stays exactly
@@ -584,36 +678,49 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
       bytes += 65536ull + (diag ? 65536ull : 131072ull);
       flops += 96ull * 262144ull;
     } else {
-      // ---------------- Qt panel: rows of pair q, columns 128 cb .. 128 cb + 127
-      task -= nsup;
-      const int cb = int(task / npairs), q = task - cb * npairs;
-      if (skip[q]) continue;
+      // ---------------- Qt panel: rows of pair q, columns 256 cb .. 256 cb + 255 (the second
+      // 128-column half only where the rows are that long), each half one product
+      const int u = cur.u, q = cur.q;
       float* Qt = Qtall + int64_t(u) * sp * sp;
       const int b0 = rr_pos(q, step, nblk), b1 = rr_pos(nblk - 1 - q, step, nblk);
-      const int64_t col0 = int64_t(cb) * 128;
-      float4 x[8];
+      const int64_t col0 = int64_t(cur.cb) * 256;
+      const int halves = col0 + 128 < sp ? 2 : 1;     // uniform over the CTA
+      bool fine = true;
+      for (int h = 0; h < halves && fine; ++h) {
+        // A = half^T (M = column of the half, K = row of the pair), MN-major
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = warp + 8 * i;
-        x[i] = *reinterpret_cast<const float4*>(Qt + gidx(r, b0, b1) * sp + col0 + 4 * lane);
+        for (int i = 0; i < 8; ++i) put4(Abuf, amn_off(4 * lane, warp + 8 * i), R[8 * h + i]);
+        cp_async_wait<0>();
+        fine = mma_phase(c, a_img, true, v0, 64 * h, tid);
       }
-      copy_vimg(Vb0, Vu + int64_t(q) * VIMG_BYTES, tid);
-      // A = panel^T (M = panel column, K = row of the pair), MN-major
-#pragma unroll
-      for (int i = 0; i < 8; ++i) put4(Abuf, amn_off(4 * lane, warp + 8 * i), x[i]);
-      if (!mma_phase(c, a_img, true, v0, 0, tid)) break;
+      if (!fine) break;
+      have2 = next_tc_task(g2, total, per_u, nsup, nsp, npairs, skipall, conv, nxt);
+      if (have2) {
+        load_tc_task(nxt, R, Call, Qtall, sp, nblk, step, warp, lane);
+        if (nxt.kind == 0) {
+          copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, 2 * nxt.Q), tid);
+          copy_vimg_async(Vb1, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, 2 * nxt.Q + 1), tid);
+        } else {
+          copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, nxt.q), tid);
+        }
+      }
       const int cc = (warp & 3) * 32 + lane;
       const int nh = warp >> 2;
-      uint32_t v[32];
-      tmem_ld32(c.tmem + lane_base + uint32_t(32 * nh), v);
       const int64_t rb = int64_t(nh ? b1 : b0) * JB;
+      for (int h = 0; h < halves; ++h) {
+        uint32_t v[32];
+        tmem_ld32(c.tmem + lane_base + uint32_t(64 * h + 32 * nh), v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) Qt[(rb + j) * sp + col0 + cc] = __uint_as_float(v[j]);
-      bytes += 65536ull;
-      flops += 24ull * 262144ull;
+        for (int j = 0; j < 32; ++j) Qt[(rb + j) * sp + col0 + 128 * h + cc] = __uint_as_float(v[j]);
+      }
+      bytes += 65536ull * uint64_t(halves);
+      flops += 24ull * 262144ull * uint64_t(halves);
     }
-    (void)npan;
+    cur = nxt;
+    have = have2;
+    g = g2;
   }
+  cp_async_wait<0>();  // no copy into this CTA's shared memory may still be in flight at exit
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -1159,7 +1266,7 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
   // 128-column panels of Qt per pair
   const int nsp = pl.npairs / 2;
   const int nsup = nsp * (nsp + 1) / 2;
-  const int ntile_q = int(pl.sp / 128) * pl.npairs;
+  const int ntile_q = int((pl.sp + 255) / 256) * pl.npairs;
   const size_t apply_smem = 1024 + size_t(AIMG_BYTES) + 2 * size_t(VIMG_BYTES) + 64;
   const int per_u = nsup + ntile_q;
   const int64_t total_tasks = int64_t(per_u) * nu;
