@@ -76,6 +76,12 @@ typedef enum { KF_SIDE_RIGHT = 0, KF_SIDE_LEFT = 1 } kf_side;
 #define KF_REUSE_SX 1u
 #define KF_REUSE_SG 2u
 #define KF_REUSE_SINV 4u
+/* whiten() flags: the three bfloat16 planes of S_x (S_g) that the previous whiten() call left
+ * in the same workspace are reused instead of split again.  Valid only when that call had the
+ * same workspace pointer, the same m and n, and the same factor (units that share an input or
+ * output factor, e.g. the attention heads of one layer, taken one after the other). */
+#define KF_REUSE_SX_PLANES 8u
+#define KF_REUSE_SG_PLANES 16u
 
 typedef struct kf_ctx kf_ctx;
 
@@ -178,6 +184,30 @@ KF_API kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, con
                  uint32_t flags, float* Sx, int64_t ldsx, float* Sg, int64_t ldsg, float* Sinv,
                  int64_t ldsi, float* Wt, int64_t ldwt, void* workspace,
                  size_t workspace_bytes, kf_stream_t stream);
+
+/* factor_covariances - step 2 for many factors at once: the Cholesky factor of each damped
+ * covariance and, where asked, the inverse of that factor, each job an independent chain of
+ * launches on one of the context's internal streams (forked from and joined back into
+ * `stream`, so the call is ordered on it like any other).  A group of units then calls
+ * whiten() with KF_REUSE_SX | KF_REUSE_SG | KF_REUSE_SINV.  The factorisations are chains of
+ * small launches (64 x 64 diagonal blocks, panels, tensor-core trailing updates), so running
+ * the chains side by side shortens the step to about the longest chain.
+ * Per job: A (n x n, lda, lower triangle read) the damped factor; S (lds) out: the lower
+ * Cholesky factor L (upper = 0, as S_g) or L^T (upper = 1, as S_x), zeros in the other
+ * triangle; Sinv (ldsi, may be NULL) out: the inverse of S (L^-1 or L^-T).  A non-positive
+ * pivot sets KF_ERR_NOT_SPD as in whiten().  The jobs' outputs must not overlap. */
+typedef struct {
+  const float* A;
+  int64_t lda, n;
+  float* S;
+  int64_t lds;
+  float* Sinv;    /* may be NULL */
+  int64_t ldsi;
+  int32_t upper;
+} kf_factor_job;
+KF_API size_t factor_covariances_workspace_size(int32_t n_jobs, const kf_factor_job* jobs);
+KF_API kf_status factor_covariances(kf_ctx* ctx, int32_t n_jobs, const kf_factor_job* jobs, void* workspace,
+                                    size_t workspace_bytes, kf_stream_t stream);
 
 /* ------------------------------------------------------------------------------------
  * (4) whitened_svd - spectrum of W~ through its Gram matrix.

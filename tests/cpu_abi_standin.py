@@ -46,12 +46,29 @@ def kf_finalize_covariance(ctx, cov, n_tokens, lam, stream=None):
 
 
 def whiten(ctx, X, G, W, Sx, Sg, Sinv, Wt, flags=0, workspace=None, stream=None):
+    # like the library: factors (and the Gram-side inverse) flagged as present are reused
     m, n = W.shape
     sx, sg = O.cholesky_factors(_np(X), _np(G))
-    _put(Sx, sx)
-    _put(Sg, sg)
-    _put(Sinv, np.linalg.inv(sg) if kf_gram_side(m, n) == 0 else np.linalg.inv(sx))
+    if flags & 1:
+        sx = _np(Sx)
+    else:
+        _put(Sx, sx)
+    if flags & 2:
+        sg = _np(Sg)
+    else:
+        _put(Sg, sg)
+    if not flags & 4:
+        _put(Sinv, np.linalg.inv(sg) if kf_gram_side(m, n) == 0 else np.linalg.inv(sx))
     _put(Wt, O.whiten(_np(W), sx, sg))
+
+
+def factor_covariances(ctx, jobs, workspace=None, stream=None):
+    for A, S, Sinv, upper in jobs:
+        L = np.linalg.cholesky(_np(A))
+        F = L.T.copy() if upper else L
+        _put(S, F)
+        if Sinv is not None:
+            _put(Sinv, np.linalg.inv(F))
 
 
 def whitened_svd(ctx, Wts, sigmas, vecs, sweeps=None, tol=1e-6, max_sweeps=30, workspace=None, stream=None):
@@ -208,7 +225,7 @@ def activation_factors(ctx, W, vecs, r, U, V, workspace=None, stream=None):
     _put(V, v_)
 
 
-NAMES = ["fake_quant_rows", "empirical_fisher_accumulate", "empirical_fisher_finalize", "activation_covariance", "activation_eig",
+NAMES = ["factor_covariances", "fake_quant_rows", "empirical_fisher_accumulate", "empirical_fisher_finalize", "activation_covariance", "activation_eig",
          "activation_factors", "kf_gram_side", "kfac_accumulate", "kf_finalize_covariance", "whiten",
          "whitened_svd", "score_and_allocate", "score_and_allocate_keys", "score_and_allocate_weighted",
          "score_and_allocate_hybrid", "unwhiten", "channel_errors",

@@ -90,6 +90,7 @@ def test_every_compute_call_rejects_a_null_context():
         "empirical_fisher_finalize": (None, None, 4, 10, None, None),
         "score_and_allocate_hybrid": (None, None, None, None, 1, 0, 0, None, 0.5, None, None, None, None, 0, None),
         "kf_set_wait_limit": (None, 1000),
+        "factor_covariances": (None, 1, None, None, 0, None),
     }
     for name, args in calls.items():
         st = getattr(L, name)(*args)

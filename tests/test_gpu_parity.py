@@ -155,6 +155,31 @@ def test_whiten(ctx, m, n):
     assert rel_fro(Wt.cpu().numpy(), O.whiten(W, oSx, oSg)) <= 1e-5
 
 
+@pytest.mark.parametrize("sizes", [(320, 704, 192), (1000, 64, 257), (513,)])
+def test_factor_covariances_batched(ctx, sizes):
+    """Step 2 for several factors at once (independent chains on the context's streams):
+    each S = chol_lower(A) or its transpose, and its inverse, against float64 LAPACK on the
+    same damped factors (relative Frobenius 1e-5); sizes below, at and across the 256-wide
+    column strips and the doubling levels of the inverse."""
+    r = np.random.default_rng(sum(sizes))
+    jobs, want = [], []
+    for j, n in enumerate(sizes):
+        B = r.standard_normal((n + 40, n)) * (1.0 / np.sqrt(np.arange(1, n + 1)))
+        A = O.finalize_covariance(O.covariance_sum(B), n + 40, 1e-2).astype(np.float32)
+        upper = j % 2 == 1
+        S = torch.empty((n, n), dtype=torch.float32, device="cuda")
+        Si = torch.empty((n, n), dtype=torch.float32, device="cuda")
+        jobs.append((to_dev(A, torch), S, Si, upper))
+        L = np.linalg.cholesky(A.astype(np.float64))
+        F = L.T if upper else L
+        want.append((F, np.linalg.inv(F)))
+    K().factor_covariances(ctx, jobs)
+    ctx.sync_status()
+    for (A, S, Si, upper), (F, Fi) in zip(jobs, want):
+        assert rel_fro(S.cpu().numpy(), F) <= 1e-5
+        assert rel_fro(Si.cpu().numpy(), Fi) <= 1e-5
+
+
 def test_whiten_not_spd_reports_pivot(ctx):
     X = np.eye(96, dtype=np.float32)
     X[40, 40] = -1.0

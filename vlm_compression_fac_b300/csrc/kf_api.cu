@@ -106,6 +106,10 @@ kf_status kf_create(int device, kf_ctx** out) {
 
 void kf_destroy(kf_ctx* ctx) {
   if (!ctx) return;
+  for (int i = 0; i < kf_ctx::NSTREAMS; ++i)
+    if (ctx->streams[i]) cudaStreamDestroy(ctx->streams[i]);
+  for (int i = 0; i <= kf_ctx::NSTREAMS; ++i)
+    if (ctx->stream_ev[i]) cudaEventDestroy(ctx->stream_ev[i]);
   for (int e = 0; e < 5; ++e)
     if (ctx->prof_ev[e]) cudaEventDestroy(ctx->prof_ev[e]);
   for (cudaEvent_t e : ctx->prof_kev) cudaEventDestroy(e);
@@ -299,11 +303,98 @@ kf_status whiten(kf_ctx* ctx, const float* X, int64_t ldx, int64_t m, const floa
   // output row i needs k >= i).
   Planes pw, psg, pt, psx;
   KF_TRY(as_planes(W, w_dtype, ldw, m, n, b.w, &pw, st));
-  KF_TRY(split_f32(Sg, ldsg, n, n, b.sg, &psg, st));
+  if (flags & KF_REUSE_SG_PLANES) {
+    psg = Planes{{b.sg.p[0], b.sg.p[1], b.sg.p[2]}, b.sg.ld, 3};
+  } else {
+    KF_TRY(split_f32(Sg, ldsg, n, n, b.sg, &psg, st));
+  }
   KF_TRY(tc_product(ctx, m, n, n, pw, false, psg, true, KR_GE_COL, b.T, b.ldT, st));
   KF_TRY(split_f32(b.T, b.ldT, m, n, b.t, &pt, st));
-  KF_TRY(split_f32(Sx, ldsx, m, m, b.sx, &psx, st));
+  if (flags & KF_REUSE_SX_PLANES) {
+    psx = Planes{{b.sx.p[0], b.sx.p[1], b.sx.p[2]}, b.sx.ld, 3};
+  } else {
+    KF_TRY(split_f32(Sx, ldsx, m, m, b.sx, &psx, st));
+  }
   return tc_product(ctx, m, n, m, psx, false, pt, true, KR_GE_ROW, Wt, ldwt, st);
+}
+
+// --------------------------------------------------------- batched factorisation
+namespace {
+struct FactorBufs {
+  float *dinv, *tt;
+  char *cws, *tws;
+  size_t cws_bytes, tws_bytes;
+};
+size_t factor_carve(Carve& cv, int32_t n_jobs, const kf_factor_job* jobs, std::vector<FactorBufs>* out) {
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const int64_t n = jobs[j].n > 0 ? jobs[j].n : 1;
+    FactorBufs b;
+    b.dinv = cv.take<float>(size_t(round_up(n, CHOL_NB)) * CHOL_NB);
+    b.cws_bytes = chol_workspace_bytes(n);
+    b.cws = cv.take<char>(b.cws_bytes);
+    const bool inv = jobs[j].Sinv != nullptr;
+    b.tt = inv ? cv.take<float>(trtri_tmp_floats(n)) : nullptr;
+    b.tws_bytes = inv ? trtri_workspace_bytes(n) : 0;
+    b.tws = inv ? cv.take<char>(b.tws_bytes) : nullptr;
+    if (out) out->push_back(b);
+  }
+  return cv.off;
+}
+
+kf_status ensure_streams(kf_ctx* ctx) {
+  for (int i = 0; i < kf_ctx::NSTREAMS; ++i)
+    if (!ctx->streams[i]) KF_CUDA(cudaStreamCreateWithFlags(&ctx->streams[i], cudaStreamNonBlocking));
+  for (int i = 0; i <= kf_ctx::NSTREAMS; ++i)
+    if (!ctx->stream_ev[i]) KF_CUDA(cudaEventCreateWithFlags(&ctx->stream_ev[i], cudaEventDisableTiming));
+  return KF_OK;
+}
+}  // namespace
+
+size_t factor_covariances_workspace_size(int32_t n_jobs, const kf_factor_job* jobs) {
+  if (n_jobs <= 0 || !jobs) return 0;
+  Carve cv(nullptr, 0, true);
+  return factor_carve(cv, n_jobs, jobs, nullptr) + 256;
+}
+
+kf_status factor_covariances(kf_ctx* ctx, int32_t n_jobs, const kf_factor_job* jobs, void* workspace,
+                             size_t workspace_bytes, kf_stream_t stream) {
+  KF_TRY(need(ctx != nullptr, "factor_covariances: null context"));
+  if (n_jobs == 0) return KF_OK;
+  KF_TRY(need(n_jobs > 0 && jobs, "factor_covariances: jobs"));
+  for (int32_t j = 0; j < n_jobs; ++j) {
+    const kf_factor_job& f = jobs[j];
+    KF_TRY(need(f.A && f.S && f.n > 0 && f.lda >= f.n && f.lds >= f.n && (!f.Sinv || f.ldsi >= f.n),
+                "factor_covariances: job fields"));
+  }
+  Carve cv(workspace, workspace_bytes, false);
+  std::vector<FactorBufs> bufs;
+  factor_carve(cv, n_jobs, jobs, &bufs);
+  if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "factor_covariances: workspace too small");
+  KF_TRY(ensure_streams(ctx));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int used = n_jobs < kf_ctx::NSTREAMS ? n_jobs : kf_ctx::NSTREAMS;
+  // fork: every internal stream starts after the work already queued on the caller's stream
+  KF_CUDA(cudaEventRecord(ctx->stream_ev[kf_ctx::NSTREAMS], st));
+  for (int i = 0; i < used; ++i) KF_CUDA(cudaStreamWaitEvent(ctx->streams[i], ctx->stream_ev[kf_ctx::NSTREAMS], 0));
+  kf_status rc = KF_OK;
+  for (int32_t j = 0; j < n_jobs && rc == KF_OK; ++j) {
+    const kf_factor_job& f = jobs[j];
+    const FactorBufs& b = bufs[size_t(j)];
+    cudaStream_t sj = ctx->streams[j % kf_ctx::NSTREAMS];
+    rc = launch_copy(f.A, f.lda, f.S, f.lds, f.n, f.n, false, sj);
+    if (rc == KF_OK) rc = cholesky_lower(ctx, f.S, f.lds, f.n, b.dinv, b.cws, b.cws_bytes, sj);
+    if (rc == KF_OK && f.Sinv) rc = trtri_lower(ctx, f.S, f.lds, f.n, b.dinv, f.Sinv, f.ldsi, b.tt, b.tws, b.tws_bytes, sj);
+    if (rc == KF_OK && f.upper) {
+      rc = launch_transpose_inplace(f.S, f.lds, f.n, sj);
+      if (rc == KF_OK && f.Sinv) rc = launch_transpose_inplace(f.Sinv, f.ldsi, f.n, sj);
+    }
+  }
+  // join (also after a failed launch, so that the caller's stream never runs ahead of them)
+  for (int i = 0; i < used; ++i) {
+    KF_CUDA(cudaEventRecord(ctx->stream_ev[i], ctx->streams[i]));
+    KF_CUDA(cudaStreamWaitEvent(st, ctx->stream_ev[i], 0));
+  }
+  return rc;
 }
 
 // ------------------------------------------------------------------------ (4)
@@ -679,6 +770,7 @@ struct UnwhitenBufs {
   float *q0, *q1, *gm, *li, *dinv, *tt, *P;
   int64_t ldP;
   PlaneBuf c, w, sg, si, p;
+  PlaneBuf q3, l3;  // CholeskyQR2 operands as three planes
   char *cws, *tws;
   size_t cws_bytes, tws_bytes;
 };
@@ -702,6 +794,8 @@ size_t unwhiten_carve(Carve& cv, int64_t m, int64_t n, int64_t r, UnwhitenBufs& 
   b.sg = take_planes(cv, mx, mx, 2);          // S_g (right) or S_x (left)
   b.si = take_planes(cv, s, s, 2);            // the Gram-side inverse
   b.p = take_planes(cv, mx, mx, 2);           // P as an operand (n x r or r x m)
+  b.q3 = take_planes(cv, s, r, 3);
+  b.l3 = take_planes(cv, r, r, 3);
   return cv.off;
 }
 }  // namespace
@@ -735,26 +829,22 @@ kf_status unwhiten(kf_ctx* ctx, const void* W, kf_dtype w_dtype, int64_t ldw, in
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "unwhiten: workspace too small");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
 
-  // CholeskyQR2 of the r leading Gram-side vectors: twice Q <- Q R^-1 with R^T R = Q^T Q
-  // (float32 SIMT: the Gram of nearly orthonormal columns needs float32 accuracy).
+  // CholeskyQR2 of the r leading Gram-side vectors: twice Q <- Q L^-T with L L^T = Q^T Q.
+  // The Gram of nearly orthonormal columns needs float32 accuracy: both products run on the
+  // tensor cores with three-plane operands (all six cross terms).
   KF_TRY(launch_copy(vecs, ldv, b.q0, r, s, r, false, st));
   float* cur = b.q0;
   float* nxt = b.q1;
   for (int it = 0; it < 2; ++it) {
-    GemmDesc g{};
-    g.M = r; g.N = r; g.K = s; g.batch = 1;
-    g.A = cur; g.lda = r; g.trans_a = true;
-    g.B = cur; g.ldb = r;
-    g.C = b.gm; g.ldc = r; g.alpha = 1.f; g.beta = 0.f; g.out_mask = OUT_LOWER;
-    KF_TRY(simt_gemm(g, st));
+    Planes pq, pl;
+    KF_TRY(split_f32(cur, r, s, r, b.q3, &pq, st));
+    ProductOpts lo;
+    lo.lower = true;
+    KF_TRY(tc_product(ctx, r, r, s, pq, true, pq, true, KR_FULL, b.gm, r, st, lo));  // Q^T Q, lower
     KF_TRY(cholesky_lower(ctx, b.gm, r, r, b.dinv, b.cws, b.cws_bytes, st));
     KF_TRY(trtri_lower(ctx, b.gm, r, r, b.dinv, b.li, r, b.tt, b.tws, b.tws_bytes, st));
-    GemmDesc h{};
-    h.M = s; h.N = r; h.K = r; h.batch = 1;
-    h.A = cur; h.lda = r;
-    h.B = b.li; h.ldb = r; h.trans_b = true; h.krange = KR_LE_COL;  // (L^-1)^T is upper
-    h.C = nxt; h.ldc = r; h.alpha = 1.f; h.beta = 0.f;
-    KF_TRY(simt_gemm(h, st));
+    KF_TRY(split_f32(b.li, r, r, r, b.l3, &pl, st));
+    KF_TRY(tc_product(ctx, s, r, r, pq, false, pl, false, KR_LE_COL, nxt, r, st));   // (L^-1)^T is upper
     float* tmp = cur; cur = nxt; nxt = tmp;
   }
   // The remaining products run on the tensor cores with float32 operands split hi + lo.

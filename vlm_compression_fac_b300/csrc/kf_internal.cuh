@@ -40,6 +40,11 @@ struct kf_ctx {
   int* h_flag = nullptr;            // pinned host int: the Jacobi convergence poll
   kf::PFN_encodeTiled encode = nullptr;
   unsigned long long wait_ns = 4000000000ull;  // limit of the tensor-core pipeline waits
+  // internal streams for independent chains of work inside one call (factor_covariances),
+  // created on first use, joined back into the caller's stream before the call returns
+  static constexpr int NSTREAMS = 8;
+  cudaStream_t streams[NSTREAMS] = {};
+  cudaEvent_t stream_ev[NSTREAMS + 1] = {};
   // whitened_svd profile (events on the caller's stream; flop counter at d_status + 4)
   bool prof_enabled = false;
   bool prof_valid = false;

@@ -1161,6 +1161,7 @@ static JacPlan jac_plan(int64_t s) {
 struct SvdBufs {
   float *C, *Q, *flo, *Y, *sig, *qinv, *Qs, *Ys, *Bw, *Vw;
   uint8_t *Vimg, *Iimg;
+  PlaneBuf wpl, qpl;  // three-plane copies of one problem's W~ (or C) and of its eigenvector rows
   int *skip, *conv, *perm;
   unsigned* off;
   int64_t R, lyM;
@@ -1189,6 +1190,8 @@ static size_t svd_carve(Carve& cv, int nu, int64_t m_max, int64_t n_max, int64_t
   b.Ys = cv.take<float>(size_t(nu) * b.R * b.lyM);
   b.Bw = cv.take<float>(size_t(nu) * b.nwin * RW * RW);
   b.Vw = cv.take<float>(size_t(nu) * b.nwin * RW * RW);
+  b.wpl = take_planes(cv, m_max, n_max, 3);
+  b.qpl = take_planes(cv, s, s, 3);
   return cv.off;
 }
 
@@ -1228,27 +1231,25 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     ctx->prof_steps = int64_t(max_sweeps) * (pl.nblk - 1);
     ctx->prof_valid = true;
   }
-  // Gram of the smaller side, lower triangle, float32 SIMT (accuracy matters here).
+  // Gram of the smaller side, lower triangle, on the tensor cores with W~ as three bfloat16
+  // planes (all six cross terms, float32 accumulation over K chunks of 1024): float32-level
+  // products, as the eigenvalues need.
   for (int i = 0; i < nu; ++i) {
     const kf_svd_problem& p = pr[i];
+    float* Ci = C + int64_t(i) * pl.sp * pl.sp;
     if (sym) {  // the matrix itself
-      KF_TRY(launch_copy(p.Wt, p.ldw, C + int64_t(i) * pl.sp * pl.sp, pl.sp, s, s, false, st));
+      KF_TRY(launch_copy(p.Wt, p.ldw, Ci, pl.sp, s, s, false, st));
       continue;
     }
-    GemmDesc g{};
-    g.M = s; g.N = s; g.batch = 1;
-    g.C = C + int64_t(i) * pl.sp * pl.sp; g.ldc = pl.sp;
-    g.alpha = 1.f; g.beta = 0.f; g.out_mask = OUT_LOWER;
-    if (kf_gram_side(p.m, p.n) == KF_SIDE_RIGHT) {  // W~^T W~
-      g.K = p.m;
-      g.A = p.Wt; g.lda = p.ldw; g.trans_a = true;
-      g.B = p.Wt; g.ldb = p.ldw; g.trans_b = false;
-    } else {  // W~ W~^T
-      g.K = p.n;
-      g.A = p.Wt; g.lda = p.ldw; g.trans_a = false;
-      g.B = p.Wt; g.ldb = p.ldw; g.trans_b = true;
+    Planes pw;
+    KF_TRY(split_f32(p.Wt, p.ldw, p.m, p.n, bf.wpl, &pw, st));
+    ProductOpts o;
+    o.lower = true;
+    if (kf_gram_side(p.m, p.n) == KF_SIDE_RIGHT) {  // W~^T W~: A = W~^T (MN-major), B = W~ (MN-major)
+      KF_TRY(tc_product(ctx, s, s, p.m, pw, true, pw, true, KR_FULL, Ci, pl.sp, st, o));
+    } else {                                        // W~ W~^T: A = W~ (K-major), B = W~^T (K-major)
+      KF_TRY(tc_product(ctx, s, s, p.n, pw, false, pw, false, KR_FULL, Ci, pl.sp, st, o));
     }
-    KF_TRY(simt_gemm(g, st));
   }
   {
     dim3 grid(unsigned((pl.sp * pl.sp + 255) / 256 > 4096 ? 4096 : (pl.sp * pl.sp + 255) / 256), unsigned(nu));
@@ -1349,14 +1350,13 @@ kf_status svd_run(kf_ctx* ctx, int32_t nu, const kf_svd_problem* pr, float tol, 
     const bool right = kf_gram_side(p.m, p.n) == KF_SIDE_RIGHT;
     const int64_t len_y = right ? p.m : p.n;
     float* Yi = bf.Y + int64_t(i) * s * lyM;
-    // Yt = Qt W~^T (right side, y_j = W~ q_j) or Qt W~ (left side, y_j = W~^T q_j)
-    GemmDesc g{};
-    g.M = s; g.N = len_y; g.K = s; g.batch = 1;
-    g.A = Qti; g.lda = pl.sp;
-    g.B = p.Wt; g.ldb = p.ldw; g.trans_b = right;
-    g.C = Yi; g.ldc = lyM;
-    g.alpha = 1.f; g.beta = 0.f;
-    KF_TRY(simt_gemm(g, st));
+    // Yt = Qt W~^T (right side, y_j = W~ q_j) or Qt W~ (left side, y_j = W~^T q_j), on the
+    // tensor cores with both operands as three bfloat16 planes (the images enter sigma at
+    // first order, so they need float32-level products)
+    Planes pq, pw;
+    KF_TRY(split_f32(Qti, pl.sp, s, s, bf.qpl, &pq, st));
+    KF_TRY(split_f32(p.Wt, p.ldw, p.m, p.n, bf.wpl, &pw, st));
+    KF_TRY(tc_product(ctx, s, len_y, s, pq, false, pw, !right, KR_FULL, Yi, lyM, st));
     rayleigh_norms_kernel<<<unsigned(s), 256, 0, st>>>(Yi, lyM, len_y, Qti, pl.sp, s, sig + int64_t(i) * s,
                                                       qinv + int64_t(i) * s, ctx->d_status, int(sym)); note_launch();
     KF_TRY(check_cuda(cudaGetLastError(), "rayleigh_norms_kernel"));

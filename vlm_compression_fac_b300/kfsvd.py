@@ -22,6 +22,7 @@ KF_QUANT_NONE, KF_QUANT_INT8_TOKEN = 0, 1
 KF_KEY_HALF_SIGMA2, KF_KEY_PER_PARAM, KF_FIXED_RANK, KF_KEY_ENERGY_RATIO = 0, 1, 2, 3
 KF_SIDE_RIGHT, KF_SIDE_LEFT = 0, 1
 KF_REUSE_SX, KF_REUSE_SG, KF_REUSE_SINV = 1, 2, 4
+KF_REUSE_SX_PLANES, KF_REUSE_SG_PLANES = 8, 16
 
 STATUS_NAMES = {0: "KF_OK", 1: "KF_ERR_INVALID", 2: "KF_ERR_WORKSPACE", 3: "KF_ERR_CUDA",
                 4: "KF_ERR_NOT_SPD", 5: "KF_ERR_NO_CONVERGENCE", 6: "KF_ERR_TIMEOUT",
@@ -34,6 +35,7 @@ EXPORTED = ["kf_create", "kf_destroy", "kf_last_error", "kf_launch_count", "kf_s
             "score_and_allocate_workspace_size", "score_and_allocate", "score_and_allocate_weighted",
             "score_and_allocate_keys", "score_and_allocate_noalloc", "score_and_allocate_hybrid",
             "kf_set_wait_limit", "kf_hybrid_ffn_budget", "kf_fp32_fma_probe",
+            "factor_covariances_workspace_size", "factor_covariances",
             "empirical_fisher_workspace_size", "empirical_fisher_accumulate", "empirical_fisher_finalize",
             "unwhiten_workspace_size", "unwhiten",
             "activation_covariance_workspace_size", "activation_covariance", "activation_eig_workspace_size",
@@ -57,6 +59,12 @@ class SymProblem(ctypes.Structure):
     _fields_ = [("C", ctypes.c_void_p), ("n", ctypes.c_int64), ("ldc", ctypes.c_int64),
                 ("sigma", ctypes.c_void_p), ("vecs", ctypes.c_void_p), ("ldv", ctypes.c_int64),
                 ("sweeps", ctypes.c_void_p)]
+
+
+class FactorJob(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("lda", ctypes.c_int64), ("n", ctypes.c_int64), ("S", ctypes.c_void_p),
+                ("lds", ctypes.c_int64), ("Sinv", ctypes.c_void_p), ("ldsi", ctypes.c_int64),
+                ("upper", ctypes.c_int32)]
 
 
 class SvdProfile(ctypes.Structure):
@@ -95,6 +103,8 @@ _SIGS = {
     "score_and_allocate_hybrid": (_I32, [_P, _P, _P, _P, _I32, _I64, _I64, _P, ctypes.c_double, _P, _P, _P, _P,
                                          _SZ, _P]),
     "kf_set_wait_limit": (_I32, [_P, ctypes.c_uint64]),
+    "factor_covariances_workspace_size": (_SZ, [_I32, ctypes.POINTER(FactorJob)]),
+    "factor_covariances": (_I32, [_P, _I32, ctypes.POINTER(FactorJob), _P, _SZ, _P]),
     "kf_fp32_fma_probe": (_I32, [_P, _I64, _P, ctypes.POINTER(ctypes.c_double), _P]),
     "kf_hybrid_ffn_budget": (_I64, [_I64, _I32, _P, _P, _P]),
     "empirical_fisher_finalize": (_I32, [_P, _P, _I64, _I64, _P, _P]),
@@ -279,6 +289,22 @@ def whiten(ctx: Context, X, G, W, Sx, Sg, Sinv, Wt, flags: int = 0, workspace=No
     _check(lib().whiten(ctx.handle, _ptr(X), _ld(X), m, _ptr(G), _ld(G), n, _ptr(W), _dtype_code(W), _ld(W),
                         int(flags), _ptr(Sx), _ld(Sx), _ptr(Sg), _ld(Sg), _ptr(Sinv), _ld(Sinv), _ptr(Wt),
                         _ld(Wt), _ptr(ws), wsb, _stream(stream)))
+
+
+def factor_covariances(ctx: Context, jobs: Sequence, workspace=None, stream=None):
+    """Cholesky factors (and optional inverses) of several damped covariances side by side.
+    ``jobs``: tuples (A, S, Sinv or None, upper) of device tensors; S = chol_lower(A) (upper =
+    False) or its transpose (upper = True), Sinv its inverse."""
+    k = len(jobs)
+    if k == 0:
+        return
+    arr = (FactorJob * k)()
+    for i, (A, S, Sinv, upper) in enumerate(jobs):
+        n = int(A.shape[0])
+        arr[i] = FactorJob(_ptr(A), _ld(A), n, _ptr(S), _ld(S), _ptr(Sinv), 0 if Sinv is None else _ld(Sinv),
+                           1 if upper else 0)
+    ws, wsb = _ws(int(lib().factor_covariances_workspace_size(k, arr)), workspace, jobs[0][0].device)
+    _check(lib().factor_covariances(ctx.handle, k, arr, _ptr(ws), wsb, _stream(stream)))
 
 
 def kf_svd_profile_enable(ctx: Context, enable: bool = True):

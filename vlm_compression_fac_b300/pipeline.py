@@ -228,43 +228,60 @@ def _compress(ctx, units, weights, acts, grads, n_tokens, lam, budget, fixed_ran
 
         # ---- steps 2 and 3: factors and whitened weights (a factor is shared by the units
         # that use the same block of the same site)
+        # step 2 for the whole group at once: every distinct factor (S_x = chol(X)^T per input
+        # block, S_g = chol(G) per output block) and the Gram-side inverses, as independent
+        # chains side by side (factor_covariances); the whiten calls below reuse them
         fx: Dict[tuple, torch.Tensor] = {}
         fg: Dict[tuple, torch.Tensor] = {}
         inv_x: Dict[tuple, torch.Tensor] = {}
         inv_g: Dict[tuple, torch.Tensor] = {}
+        want_ix = {(units[i].x_site, units[i].x_off, units[i].m) for i in grp
+                   if K.kf_gram_side(units[i].m, units[i].n) == K.KF_SIDE_LEFT}
+        want_ig = {(units[i].g_site, units[i].g_off, units[i].n) for i in grp
+                   if K.kf_gram_side(units[i].m, units[i].n) == K.KF_SIDE_RIGHT}
+        jobs = []
+        for i in grp:
+            u = units[i]
+            kx, kg = (u.x_site, u.x_off, u.m), (u.g_site, u.g_off, u.n)
+            if kx not in fx:
+                fx[kx] = torch.empty((u.m, u.m), dtype=torch.float32, device=dev)
+                if kx in want_ix:
+                    inv_x[kx] = torch.empty((u.m, u.m), dtype=torch.float32, device=dev)
+                jobs.append((covs[u.x_site][u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m], fx[kx], inv_x.get(kx), True))
+            if kg not in fg:
+                fg[kg] = torch.empty((u.n, u.n), dtype=torch.float32, device=dev)
+                if kg in want_ig:
+                    inv_g[kg] = torch.empty((u.n, u.n), dtype=torch.float32, device=dev)
+                jobs.append((covs[u.g_site][u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n], fg[kg], inv_g.get(kg), False))
+        K.factor_covariances(ctx, jobs, stream=stream)
+        del jobs
+        # step 3: one workspace for the group's whiten calls; consecutive units that share a
+        # factor (and a shape) reuse its bfloat16 planes from the previous call
+        wws = torch.empty(max(K.whiten_workspace_size(units[i].m, units[i].n) for i in grp), dtype=torch.uint8,
+                          device=dev)
+        planes_of = None          # (m, n, x key, g key) of the planes left in wws
         for i in grp:
             u = units[i]
             side = K.kf_gram_side(u.m, u.n)
-            s = min(u.m, u.n)
             kx, kg = (u.x_site, u.x_off, u.m), (u.g_site, u.g_off, u.n)
-            flags = 0
-            if kx in fx:
-                Sx = fx[kx]
-                flags |= K.KF_REUSE_SX
-            else:
-                Sx = fx[kx] = torch.empty((u.m, u.m), dtype=torch.float32, device=dev)
-            if kg in fg:
-                Sg = fg[kg]
-                flags |= K.KF_REUSE_SG
-            else:
-                Sg = fg[kg] = torch.empty((u.n, u.n), dtype=torch.float32, device=dev)
-            invs, key = (inv_x, kx) if side == K.KF_SIDE_LEFT else (inv_g, kg)
-            if key in invs:
-                Sinv = invs[key]
-                flags |= K.KF_REUSE_SINV
-            else:
-                Sinv = invs[key] = torch.empty((s, s), dtype=torch.float32, device=dev)
-                # the Gram-side inverse is produced together with its factor
-                flags &= ~(K.KF_REUSE_SX if side == K.KF_SIDE_LEFT else K.KF_REUSE_SG)
+            flags = K.KF_REUSE_SX | K.KF_REUSE_SG | K.KF_REUSE_SINV
+            Sx, Sg = fx[kx], fg[kg]
+            Sinv = inv_x[kx] if side == K.KF_SIDE_LEFT else inv_g[kg]
             X = covs[u.x_site][u.x_off:u.x_off + u.m, u.x_off:u.x_off + u.m]
             G = covs[u.g_site][u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n]
             W = weights[u.weight][u.row0:u.row0 + u.m, u.col0:u.col0 + u.n]
             Wt = torch.empty((u.m, u.n), dtype=torch.float32, device=dev)
-            K.whiten(ctx, X, G, W, Sx, Sg, Sinv, Wt, flags=flags, stream=stream)
+            if planes_of is not None and planes_of[:2] == (u.m, u.n):
+                if planes_of[2] == kx:
+                    flags |= K.KF_REUSE_SX_PLANES
+                if planes_of[3] == kg:
+                    flags |= K.KF_REUSE_SG_PLANES
+            K.whiten(ctx, X, G, W, Sx, Sg, Sinv, Wt, flags=flags, workspace=wws, stream=stream)
+            planes_of = (u.m, u.n, kx, kg)
             keep_x = keep_whitened or side == K.KF_SIDE_LEFT
             keep_g = keep_whitened or side == K.KF_SIDE_RIGHT
             outs[i] = UnitOut(u.name, u.m, u.n, side, Sx if keep_x else None, Sg if keep_g else None, Sinv, Wt)
-        del fx, fg, inv_x, inv_g
+        del fx, fg, inv_x, inv_g, wws
         if keep_covs is True:
             all_covs.update(covs)
         elif keep_covs:
