@@ -95,8 +95,8 @@ def fake_quant_int8_token(A: np.ndarray) -> np.ndarray:
 def cholesky_factors(X: np.ndarray, G: np.ndarray):
     """S_x = chol_lower(X)^T (upper), S_g = chol_lower(G) (lower).  [LASER] 1: S_x, S_g
     are Cholesky factors of X and G; this orientation gives S_x^T S_x = X, S_g S_g^T = G."""
-    Lx = np.linalg.cholesky(np.asarray(X, dtype=np.float64))
-    Lg = np.linalg.cholesky(np.asarray(G, dtype=np.float64))
+    Lx = sla.cholesky(np.asarray(X, dtype=np.float64), lower=True, check_finite=False)
+    Lg = sla.cholesky(np.asarray(G, dtype=np.float64), lower=True, check_finite=False)
     return Lx.T.copy(), Lg
 
 
@@ -117,7 +117,7 @@ def gram_eigenvalues(Wt: np.ndarray) -> np.ndarray:
     """[Swift] 2A: one eigendecomposition of the Gram matrix of the smaller side."""
     m, n = Wt.shape
     C = Wt.T @ Wt if n <= m else Wt @ Wt.T
-    w = np.linalg.eigh(C)[0]
+    w = np.linalg.eigvalsh(C)   # the eigenvalues alone: the spectrum is all this step returns
     return np.sort(w)[::-1]
 
 

@@ -149,6 +149,7 @@ def _check_units(wl, out, names, oracle_sig):
     idx = {u.name: i for i, u in enumerate(wl.units)}
     worst = 0.0
     problems = []
+    t0 = time.perf_counter()
     for name in names:
         i = idx[name]
         so, (W, Sx, Sg, Wt) = _oracle_sigma(wl, out, i)
@@ -170,6 +171,7 @@ def _check_units(wl, out, names, oracle_sig):
             if e_opt > 1e-12 * float(np.sum(so ** 2)) and abs(e / e_opt - 1.0) > 1e-3:
                 problems.append(("whitened error", name, e, e_opt))
         del W, Sx, Sg, Wt
+    print("%s: %d units checked against the oracle in %.1f s" % (wl.name, len(names), time.perf_counter() - t0))
     assert not problems, problems
     return worst
 
@@ -197,8 +199,10 @@ def _check_ranks_by_margin(wl, out, oracle_sig, delta):
     # recompute the units whose band components lie closest to the cut first
     todo = sorted((i for i in band_units if i not in oracle_sig), key=lambda i: band_units[i])
     done = todo[:MAX_RECHECK_UNITS]
+    t0 = time.perf_counter()
     for i in done:
         oracle_sig[i], _ = _oracle_sigma(wl, out, i)
+    print("%s: %d band units recomputed by the oracle in %.1f s" % (wl.name, len(done), time.perf_counter() - t0))
     left = len(todo) - len(done)
     print("%s: delta %.2e, %d components of %d units in the cut band; oracle spectra for %d of them (%d checked "
           "units, %d recomputed closest to the cut); %d band units keep their GPU spectra (ranks there rest on the "

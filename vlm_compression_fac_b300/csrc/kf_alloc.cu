@@ -126,12 +126,20 @@ __global__ void __launch_bounds__(RT) hist_kernel(const unsigned long long* __re
                                                   int ntiles, unsigned* __restrict__ hist) {
   __shared__ unsigned h[256];
   h[threadIdx.x] = 0;
-  __syncthreads();
   const int64_t base = int64_t(blockIdx.x) * TILE;
   const unsigned lane = threadIdx.x & 31u;
+  // all of this thread's keys are requested before the first is used
+  unsigned long long k[RI];
+#pragma unroll
   for (int i = 0; i < RI; ++i) {
     const int64_t g = base + int64_t(i) * RT + threadIdx.x;
-    const unsigned d = g < n ? unsigned((keys[g] >> shift) & 255u) : 256u;
+    k[i] = g < n ? keys[g] : 0ull;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < RI; ++i) {
+    const int64_t g = base + int64_t(i) * RT + threadIdx.x;
+    const unsigned d = g < n ? unsigned((k[i] >> shift) & 255u) : 256u;
     // one shared atomic per distinct digit of the warp (the leading bytes of the keys are
     // often nearly constant, which would serialise per-key atomics on one bin)
     const unsigned peers = __match_any_sync(0xffffffffu, d);
@@ -203,24 +211,36 @@ __global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__
   }
 }
 
-// Stable scatter of one 4096-key tile: every key's rank among the tile's keys of its digit
-// (rounds of 256 keys in index order; per-warp digit counts by warp match, then across the 8
-// warps in warp order), the key stored at that position of the tile's digit-ordered copy in
-// shared memory, then the copy written out so that consecutive threads write consecutive
-// addresses of one digit's run (coalesced).  The tile's digit counts come from the scanned
-// (digit, tile) histogram: count[d] = base of the next tile (or digit) minus this base.
-__global__ void __launch_bounds__(RT) scatter_kernel(const unsigned long long* __restrict__ in,
+// Stable scatter of one 4096-key tile.  Warp w owns the tile's keys w * WK .. w * WK + WK - 1
+// (WK = TILE / 8; the warp's round r holds keys w * WK + 32 r + lane), so the tile's index
+// order is (warp, round, lane) order.  All keys are loaded first; phase 1 counts each warp's
+// keys per digit (one counter update per distinct digit of a round, by warp match); one pass
+// over the warps per digit turns the counts into each (digit, warp)'s first position in the
+// tile's digit-ordered copy in shared memory; phase 2 puts every key at its warp's running
+// position for its digit plus its rank among the round's equal digits; the copy is then
+// written out so that consecutive threads write consecutive addresses of one digit's run
+// (coalesced).  The tile's digit counts come from the scanned (digit, tile) histogram:
+// count[d] = base of the next tile (or digit) minus this base.
+constexpr int WK = TILE / (RT / 32);
+__global__ void __launch_bounds__(RT, 3) scatter_kernel(const unsigned long long* __restrict__ in,
                                                      unsigned long long* __restrict__ out, int64_t n, int shift,
                                                      int ntiles, const unsigned* __restrict__ hist) {
   __shared__ unsigned base[256];
   __shared__ unsigned start[256];   // the digit's first position in the tile's ordered copy
-  __shared__ unsigned run[256];
-  __shared__ unsigned wcnt[RT / 32][256];   // per-warp digit counts, then (in place) offsets
+  __shared__ unsigned wpos[RT / 32][256];   // per-warp digit counts, then running positions
   __shared__ unsigned long long tk[TILE];
   __shared__ unsigned wsum[RT / 32];
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
   const int64_t tile0 = int64_t(blockIdx.x) * TILE;
   const int tile_n = int(n - tile0 < TILE ? n - tile0 : TILE);
+  unsigned long long key[RI];
+#pragma unroll
+  for (int r = 0; r < RI; ++r) {
+    const int li = w * WK + r * 32 + lane;
+    key[r] = li < tile_n ? in[tile0 + li] : 0ull;
+  }
+  for (int x = lane; x < 256; x += 32) wpos[w][x] = 0;
   {
     const int64_t hi = int64_t(t) * ntiles + blockIdx.x;
     base[t] = hist[hi];
@@ -238,33 +258,38 @@ __global__ void __launch_bounds__(RT) scatter_kernel(const unsigned long long* _
     unsigned pre = 0;
     for (int ww = 0; ww < w; ++ww) pre += wsum[ww];
     start[t] = pre + x - cnt;
-    run[t] = 0;
   }
+  unsigned peers[RI];
+#pragma unroll
   for (int r = 0; r < RI; ++r) {
-    for (int x = lane; x < 256; x += 32) wcnt[w][x] = 0;
-    __syncthreads();
-    const int li = r * RT + t;
-    const bool valid = li < tile_n;
-    const unsigned long long k = valid ? in[tile0 + li] : 0ull;
-    const unsigned d = valid ? unsigned((k >> shift) & 255u) : 256u;
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    const unsigned lt = peers & ((1u << lane) - 1u);
-    const unsigned rank = __popc(lt);
-    if (valid && lt == 0) wcnt[w][d] = __popc(peers);
-    __syncthreads();
-    {  // per digit: offsets of each warp within this round, in warp order (in place)
-      unsigned acc = run[t];
-      for (int ww = 0; ww < RT / 32; ++ww) {
-        const unsigned c = wcnt[ww][t];
-        wcnt[ww][t] = acc;
-        acc += c;
-      }
-      run[t] = acc;
-    }
-    __syncthreads();
-    if (valid) tk[start[d] + wcnt[w][d] + rank] = k;
-    __syncthreads();
+    const bool valid = w * WK + r * 32 + lane < tile_n;
+    const unsigned d = valid ? unsigned((key[r] >> shift) & 255u) : 256u;
+    peers[r] = __match_any_sync(0xffffffffu, d);
+    if (valid && (peers[r] & lt_mask) == 0u) wpos[w][d] += __popc(peers[r]);
+    __syncwarp();
   }
+  __syncthreads();
+  {  // per digit: each warp's first position, in warp order
+    unsigned acc = start[t];
+#pragma unroll
+    for (int ww = 0; ww < RT / 32; ++ww) {
+      const unsigned c = wpos[ww][t];
+      wpos[ww][t] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < RI; ++r) {
+    const bool valid = w * WK + r * 32 + lane < tile_n;
+    const unsigned d = valid ? unsigned((key[r] >> shift) & 255u) : 0u;
+    const unsigned pos = valid ? wpos[w][d] : 0u;
+    if (valid) tk[pos + __popc(peers[r] & lt_mask)] = key[r];
+    __syncwarp();
+    if (valid && (peers[r] & lt_mask) == 0u) wpos[w][d] = pos + __popc(peers[r]);
+    __syncwarp();
+  }
+  __syncthreads();
   for (int i = t; i < tile_n; i += RT) {
     const unsigned long long k = tk[i];
     const unsigned d = unsigned((k >> shift) & 255u);

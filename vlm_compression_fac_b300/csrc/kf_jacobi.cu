@@ -35,7 +35,8 @@ namespace kf {
 namespace {
 
 constexpr int JB = 32, JP = 64;  // block width, pair problem size
-constexpr size_t JAC_SOLVE_SMEM = size_t(2 * JP * (JP + 2) + JP * (JP + 1)) * sizeof(float);
+constexpr int JS = JP + 4;  // row stride of V and of the Newton-Schulz factor in the pair solve
+constexpr size_t JAC_SOLVE_SMEM = size_t(2 * JP * JS) * sizeof(float);
 // Inner sweeps of a pair problem.  Measured on the 7B block (7 Gram matrices of 4096): one
 // sweep of rotations per pair problem instead of up to 12 costs at most one more outer sweep,
 // the final singular values come out as accurate (about 6e-5 relative on the kept components
@@ -128,6 +129,26 @@ __global__ void jac_floor_kernel(const float* __restrict__ Call, int64_t sp, flo
 }
 
 // ------------------------------------------------------------------------- solve
+// The pair problem's 64 indices sit in 64 slots of a circle-method tournament: slot k < 32 is
+// the first index of rotation pair k, slot 32 + k its second.  After every round each slot's
+// contents move one place round the circle (slot 0 stays; 1 -> 32; k -> k - 1 for 2 <= k < 32;
+// 32 + k -> 33 + k for k < 31; 63 -> 31), so that the 63 rounds of a sweep meet every pair of
+// indices once and bring every index back to its starting slot.  The index that starts in
+// slot k < 32 is the pair-local column k (first block), the one in slot 32 + k is 63 - k
+// (second block), which makes round r pair exactly the indices rr_pos(k, r, 64) and
+// rr_pos(63 - k, r, 64).  In shared memory slot k < 32 is row/column k and slot 32 + k is
+// 32 + ((k + 31) & 31): with this placement every load and store of a round, including the
+// moved stores, touches 32 different banks.
+__device__ __forceinline__ int slot_phys(int s) { return s < JB ? s : JB + ((s - JB + JB - 1) & (JB - 1)); }
+__device__ __forceinline__ int slot_next(int s) {
+  if (s == 0) return 0;
+  if (s == 1) return JB;
+  if (s < JB) return s - 1;
+  if (s == JP - 1) return JB - 1;
+  return s + 1;
+}
+__device__ __forceinline__ int index_phys(int x) { return slot_phys(x < JB ? x : JP + JB - 1 - x); }
+
 __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call, int64_t sp, int nblk,
                                                         int step, uint8_t* __restrict__ Vimg,
                                                         int* __restrict__ skipall,
@@ -135,14 +156,12 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
                                                         unsigned* __restrict__ offmax,
                                                         const float* __restrict__ floorv, float tol,
                                                         int max_inner) {
-  // Row stride JP + 2: the 32 couplings A[p][q] that one rotation round reads lie on an
-  // anti-diagonal (p + q constant), which a stride of JP + 1 would put in a single bank.
-  // Two copies of A: a round reads the current one and writes every entry of the next, so a
-  // round needs a single barrier (JAC_SOLVE_SMEM bytes of dynamic shared memory).
+  // Two slot-ordered copies of the 64 x 64 problem (row stride JP): a round reads one and
+  // writes every entry of the other at its moved position, so a round needs one barrier.
+  // The same JAC_SOLVE_SMEM bytes later hold V and the Newton-Schulz factor (stride JS).
   extern __shared__ float jsm[];
-  float (*A)[JP + 2] = reinterpret_cast<float (*)[JP + 2]>(jsm);
-  float (*An)[JP + 2] = reinterpret_cast<float (*)[JP + 2]>(jsm + JP * (JP + 2));
-  float (*V)[JP + 1] = reinterpret_cast<float (*)[JP + 1]>(jsm + 2 * JP * (JP + 2));
+  float* A = jsm;
+  float* An = jsm + JP * JS;
   __shared__ float red[8];
 
   const int k = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
@@ -152,7 +171,7 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   const int b0 = rr_pos(k, step, nblk), b1 = rr_pos(nblk - 1 - k, step, nblk);
   for (int e = t; e < JP * JP; e += 256) {
     const int r = e >> 6, c = e & 63;
-    A[r][c] = C[gidx(r, b0, b1) * sp + gidx(c, b0, b1)];
+    A[index_phys(r) * JP + index_phys(c)] = C[gidx(r, b0, b1) * sp + gidx(c, b0, b1)];
   }
   __syncthreads();
   const float flo = floorv[u];
@@ -160,10 +179,10 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   // Largest relative coupling between the two blocks.
   float m = 0.f;
   for (int e = t; e < JB * JB; e += 256) {
-    const int r = e >> 5, c = JB + (e & 31);
-    const float v = fabsf(A[r][c]);
+    const int r = index_phys(e >> 5), c = index_phys(JB + (e & 31));
+    const float v = fabsf(A[r * JP + c]);
     if (v > flo) {
-      const float den = fmaxf(sqrtf(fmaxf(A[r][r] * A[c][c], 0.f)), flo);
+      const float den = fmaxf(sqrtf(fmaxf(A[r * JP + r] * A[c * JP + c], 0.f)), flo);
       m = fmaxf(m, v / den);
     }
   }
@@ -184,142 +203,170 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
     return;
   }
 
-  for (int e = t; e < JP * JP; e += 256) V[e >> 6][e & 63] = ((e >> 6) == (e & 63)) ? 1.f : 0.f;
-  __syncthreads();
-
-  // Threshold cyclic Jacobi on the 64 x 64 pair problem, 32 disjoint rotations per round.
-  // Every warp computes all 32 rotations of a round (lane l: pair l) from the same entries,
-  // so the parameters reach the threads that need them by warp shuffles rather than
-  // through shared memory; thread (warp w, lane k) then updates the 2 x 2 blocks (j, k),
-  // j = w, w + 8, w + 16, w + 24, and rows w, w + 8, ... of the columns p_k, q_k of V.
-  // The rotation parameters use the fast reciprocal and reciprocal square root: a rotation
-  // only has to be (nearly) orthogonal and to shrink its coupling, and the Newton-Schulz step
-  // below re-orthogonalises the accumulated V before it leaves the kernel.
+  // Threshold cyclic Jacobi, 32 disjoint rotations per round.  Every warp computes all 32
+  // rotations of a round (lane l: pair l) from the same entries, so the parameters reach the
+  // threads that need them by warp shuffles.  Thread (warp w, lane l) updates the 2 x 2 blocks
+  // (pair j, pair l), j = w, w + 8, w + 16, w + 24, and holds rows w, w + 8, ..., w + 56 of the
+  // two columns of V in slots l and 32 + l in registers; V's columns follow the circle by warp
+  // shuffles.  The rotation parameters use the fast reciprocal and reciprocal square root: a
+  // rotation only has to be (nearly) orthogonal and to shrink its coupling, and the
+  // Newton-Schulz step below re-orthogonalises V before it leaves the kernel.
   const int lane = t & 31, warp = t >> 5;
+  const int ct = lane, cb = slot_phys(JB + lane);
+  const int dct = slot_phys(slot_next(lane)), dcb = slot_phys(slot_next(JB + lane));
+  int rt[4], rb[4], drt[4], drb[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int j = warp + 8 * x;
+    rt[x] = j * JP;
+    rb[x] = slot_phys(JB + j) * JP;
+    drt[x] = slot_phys(slot_next(j)) * JP;
+    drb[x] = slot_phys(slot_next(JB + j)) * JP;
+  }
+  float vt[8], vb[8];
+#pragma unroll
+  for (int y = 0; y < 8; ++y) {
+    const int i = warp + 8 * y;
+    vt[y] = (i == lane) ? 1.f : 0.f;
+    vb[y] = (i == JP - 1 - lane) ? 1.f : 0.f;
+  }
   const float tol2 = tol * tol;
   for (int sweep = 0; sweep < max_inner; ++sweep) {
     int rotated = 0;
     for (int r = 0; r < JP - 1; ++r) {
-      const int p = rr_pos(lane, r, JP), q = rr_pos(JP - 1 - lane, r, JP);
-      const float a = A[p][p], b = A[q][q], d = A[p][q];
+      const float a = A[ct * JP + ct], b = A[cb * JP + cb], d = A[ct * JP + cb];
       float c = 1.f, sn = 0.f, td = 0.f;
-      int act = 0;
+      bool act = false;
       if (fabsf(d) > flo && d * d > tol2 * fmaxf(a * b, 0.f)) {
         const float tau = (b - a) * __frcp_rn(2.f * d);
         const float tt = copysignf(__frcp_rn(fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f))), tau);
         c = rsqrtf(fmaf(tt, tt, 1.f));
         sn = tt * c;
         td = tt * d;
-        act = 1;
+        act = true;
       }
-      // identical in every warp (same inputs), so the branch is uniform over the CTA
-      if (!__any_sync(0xffffffffu, act)) continue;
-      rotated = 1;
-      // every entry of An is written: block (j, lane) covers rows p_j, q_j x columns p, q
+      rotated |= __any_sync(0xffffffffu, act);  // the same in every warp
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         const int j = warp + 8 * x;
-        const int pj = __shfl_sync(0xffffffffu, p, j), qj = __shfl_sync(0xffffffffu, q, j);
         const float cj = __shfl_sync(0xffffffffu, c, j), sj = __shfl_sync(0xffffffffu, sn, j);
-        const int actj = __shfl_sync(0xffffffffu, act, j);
         if (j == lane) {
-          An[p][p] = act ? a - td : a;
-          An[q][q] = act ? b + td : b;
-          An[p][q] = act ? 0.f : d;
-          An[q][p] = act ? 0.f : A[q][p];
+          An[drt[x] + dct] = a - td;
+          An[drb[x] + dcb] = b + td;
+          An[drt[x] + dcb] = act ? 0.f : d;
+          An[drb[x] + dct] = act ? 0.f : A[rb[x] + ct];
           continue;
         }
-        const float e00 = A[pj][p], e01 = A[pj][q], e10 = A[qj][p], e11 = A[qj][q];
-        if (!actj && !act) {
-          An[pj][p] = e00; An[pj][q] = e01; An[qj][p] = e10; An[qj][q] = e11;
-          continue;
-        }
+        // an inactive rotation has c = 1, s = 0 and reproduces its entries exactly
+        const float e00 = A[rt[x] + ct], e01 = A[rt[x] + cb], e10 = A[rb[x] + ct], e11 = A[rb[x] + cb];
         const float a1 = e00 * c - e01 * sn, b1 = e00 * sn + e01 * c;
         const float c1 = e10 * c - e11 * sn, d1 = e10 * sn + e11 * c;
-        An[pj][p] = cj * a1 - sj * c1;
-        An[pj][q] = cj * b1 - sj * d1;
-        An[qj][p] = sj * a1 + cj * c1;
-        An[qj][q] = sj * b1 + cj * d1;
+        An[drt[x] + dct] = cj * a1 - sj * c1;
+        An[drt[x] + dcb] = cj * b1 - sj * d1;
+        An[drb[x] + dct] = sj * a1 + cj * c1;
+        An[drb[x] + dcb] = sj * b1 + cj * d1;
       }
-      if (act) {
 #pragma unroll
-        for (int y = 0; y < JP / 8; ++y) {
-          const int i = warp + 8 * y;
-          const float x0 = V[i][p], y0 = V[i][q];
-          V[i][p] = c * x0 - sn * y0;
-          V[i][q] = sn * x0 + c * y0;
-        }
+      for (int y = 0; y < 8; ++y) {
+        const float x0 = vt[y], y0 = vb[y];
+        const float nt = c * x0 - sn * y0, nb = sn * x0 + c * y0;
+        // slot l + 1 -> l, slot 32 + l - 1 -> 32 + l; slot 1 -> 32, slot 63 -> 31, slot 0 stays
+        const float dn = __shfl_down_sync(0xffffffffu, nt, 1);
+        const float up = __shfl_up_sync(0xffffffffu, nb, 1);
+        vt[y] = lane == 0 ? nt : (lane == JB - 1 ? nb : dn);
+        vb[y] = lane == 0 ? dn : up;
       }
       __syncthreads();
-      float (*tmp)[JP + 2] = A;
+      float* tmp = A;
       A = An;
       An = tmp;
     }
     if (!rotated) break;
   }
-  // Rounds without an active rotation have no barrier: every warp must have finished reading
-  // A before it is reused as scratch below.
-  __syncthreads();
-#ifdef KF_JAC_SORT_PAIRS
-  // Order the pair's eigenvectors by eigenvalue, largest first, so that the first block of
-  // the pair receives the larger half of the pair's spectrum.
-  __shared__ int pord[JP];
-  if (t < JP) {
-    const float di = A[t][t];
-    int rank = 0;
-    for (int j = 0; j < JP; ++j) {
-      const float dj = A[j][j];
-      rank += (dj > di) || (dj == di && j < t);
-    }
-    pord[rank] = t;
+  // After whole sweeps every index is back in its starting slot: the vector in slot l is the
+  // new direction l, the one in slot 32 + l the new direction 63 - l.
+  float* V = jsm;               // V[i][n], stride JS (A is no longer needed)
+  float* M = jsm + JP * JS;
+#pragma unroll
+  for (int y = 0; y < 8; ++y) {
+    const int i = warp + 8 * y;
+    V[i * JS + lane] = vt[y];
+    V[i * JS + JP - 1 - lane] = vb[y];
   }
   __syncthreads();
-#endif
   // One Newton-Schulz step V <- V (3I - V^T V) / 2 removes the orthogonality drift that the
-  // rounding of many plane rotations leaves in V (A is free now: the apply step rebuilds C).
-  for (int e = t; e < JP * JP; e += 256) {
-    const int i = e >> 6, j = e & 63;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < JP; ++k) acc = fmaf(V[k][i], V[k][j], acc);
-    A[i][j] = (i == j ? 1.5f : 0.f) - 0.5f * acc;
-  }
-  __syncthreads();
-  float vout[JP * JP / 256];
+  // rounding of many plane rotations leaves in V; each thread computes a 4 x 4 tile of each
+  // product (rows 4 ti .. 4 ti + 3, columns 4 tj .. 4 tj + 3).
+  const int ti = t >> 4, tj = t & 15;
+  float acc[4][4];
 #pragma unroll
-  for (int x = 0; x < JP * JP / 256; ++x) {
-    const int e = t + x * 256, i = e >> 6, j = e & 63;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int k = 0; k < JP; ++k) acc = fmaf(V[i][k], A[k][j], acc);
-    vout[x] = acc;
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 4
+  for (int kk = 0; kk < JP; ++kk) {
+    const float4 p = *reinterpret_cast<const float4*>(V + kk * JS + 4 * ti);
+    const float4 q = *reinterpret_cast<const float4*>(V + kk * JS + 4 * tj);
+    const float pa[4] = {p.x, p.y, p.z, p.w}, qb[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(pa[a], qb[b], acc[a][b]);
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    float4 w;
+    w.x = (4 * ti + a == 4 * tj + 0 ? 1.5f : 0.f) - 0.5f * acc[a][0];
+    w.y = (4 * ti + a == 4 * tj + 1 ? 1.5f : 0.f) - 0.5f * acc[a][1];
+    w.z = (4 * ti + a == 4 * tj + 2 ? 1.5f : 0.f) - 0.5f * acc[a][2];
+    w.w = (4 * ti + a == 4 * tj + 3 ? 1.5f : 0.f) - 0.5f * acc[a][3];
+    *reinterpret_cast<float4*>(M + (4 * ti + a) * JS + 4 * tj) = w;
   }
   __syncthreads();
 #pragma unroll
-  for (int x = 0; x < JP * JP / 256; ++x) {
-    const int e = t + x * 256;
-    V[e >> 6][e & 63] = vout[x];
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 2
+  for (int kk = 0; kk < JP; kk += 4) {
+    float pv[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float4 p = *reinterpret_cast<const float4*>(V + (4 * ti + a) * JS + kk);
+      pv[a][0] = p.x; pv[a][1] = p.y; pv[a][2] = p.z; pv[a][3] = p.w;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 mq = *reinterpret_cast<const float4*>(M + (kk + q) * JS + 4 * tj);
+      const float mb[4] = {mq.x, mq.y, mq.z, mq.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(pv[a][q], mb[b], acc[a][b]);
+    }
   }
-  __syncthreads();
   // V (row = old index, column = new index) as three bfloat16 planes in the shared-memory
-  // image the tensor-core apply copies verbatim (B operand, MN-major, 128-byte swizzle).
+  // image the tensor-core apply copies verbatim (B operand, MN-major, 128-byte swizzle): four
+  // consecutive new indices of one old index are 8 bytes of one 16-byte chunk of each plane.
   uint8_t* img = Vimg + (int64_t(u) * npairs + k) * VIMG_BYTES;
-  for (int e = t; e < JP * JP; e += 256) {
-    const int kk = e >> 6, n = e & 63;
-#ifdef KF_JAC_SORT_PAIRS
-    const int oc = pord[n];
-    const float v = V[kk][oc >= 0 && oc < JP ? oc : n];
-#else
-    const float v = V[kk][n];
-#endif
-    const __nv_bfloat16 h1 = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(h1);
-    const __nv_bfloat16 h2 = __float2bfloat16_rn(r1);
-    const __nv_bfloat16 h3 = __float2bfloat16_rn(r1 - __bfloat162float(h2));
-    const uint32_t o = vimg_off(kk, n);
-    *reinterpret_cast<__nv_bfloat16*>(img + o) = h1;
-    *reinterpret_cast<__nv_bfloat16*>(img + VPLANE_BYTES + o) = h2;
-    *reinterpret_cast<__nv_bfloat16*>(img + 2 * VPLANE_BYTES + o) = h3;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    __nv_bfloat16 h[4][3];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float v = acc[a][b];
+      h[b][0] = __float2bfloat16_rn(v);
+      const float r1 = v - __bfloat162float(h[b][0]);
+      h[b][1] = __float2bfloat16_rn(r1);
+      h[b][2] = __float2bfloat16_rn(r1 - __bfloat162float(h[b][1]));
+    }
+    const uint32_t o = vimg_off(4 * ti + a, 4 * tj);
+#pragma unroll
+    for (int pl = 0; pl < 3; ++pl) {
+      const uint32_t lo = uint32_t(__bfloat16_as_ushort(h[0][pl])) | (uint32_t(__bfloat16_as_ushort(h[1][pl])) << 16);
+      const uint32_t hi = uint32_t(__bfloat16_as_ushort(h[2][pl])) | (uint32_t(__bfloat16_as_ushort(h[3][pl])) << 16);
+      *reinterpret_cast<uint2*>(img + pl * VPLANE_BYTES + o) = make_uint2(lo, hi);
+    }
   }
   if (t == 0) skip[k] = 0;
 }
