@@ -24,6 +24,21 @@ def bf16_dev(x, torch):
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).cuda()
 
 
+def host_weight(wl, unit, torch, cache=None):
+    """The unit's weight block (m x n) with exactly the values of the host generator
+    (recipes.gen_weight), produced by the generator's bit-identical device twin
+    (test_device_generator_matches_host) and copied back: the numpy generator needs minutes
+    for the full-size 70B and VLM weights.  Heads of one matrix share its cached copy."""
+    from synth import device
+    key = unit.weight
+    full = cache.get(key) if cache is not None else None
+    if full is None:
+        full = device.weight_on_device(wl, unit, torch).float().cpu().numpy()
+        if cache is not None and tuple(unit.weight_shape) != (unit.m, unit.n):
+            cache[key] = full
+    return np.ascontiguousarray(full[unit.row0:unit.row0 + unit.m, unit.col0:unit.col0 + unit.n])
+
+
 def moved_components(ranks_gpu, alloc_oracle, sig_oracle):
     """Components on which the GPU's and the oracle's ranks disagree, as
     (unit, component index, relative distance of its oracle score from the oracle's cut)."""

@@ -34,7 +34,7 @@ import pytest
 
 import oracle as O
 from synth import recipes
-from tests.gpu_util import rank_parity
+from tests.gpu_util import host_weight, rank_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -136,7 +136,7 @@ def _oracle_sigma(wl, out, i):
     G = _site_cov(wl, out, u.g_site).astype(np.float64)[u.g_off:u.g_off + u.n, u.g_off:u.g_off + u.n]
     Sx, Sg = O.cholesky_factors(X, G)
     del X, G
-    W = recipes.gen_weight(wl, u).astype(np.float64)
+    W = host_weight(wl, u, torch, out.setdefault("wcache", {})).astype(np.float64)
     Wt = O.whiten(W, Sx, Sg)
     so = np.sqrt(np.maximum(O.gram_eigenvalues(Wt), 0.0))
     return so, (W, Sx, Sg, Wt)

@@ -16,7 +16,7 @@ import pytest
 
 import oracle as O
 from synth import recipes
-from tests.gpu_util import rank_parity, rel_fro
+from tests.gpu_util import host_weight, rank_parity, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -92,7 +92,7 @@ def test_fullsize_spectra_allocation_and_factors(run):
         X = covs[u.x_site].astype(np.float64)
         G = covs[u.g_site].astype(np.float64)
         Sx, Sg = O.cholesky_factors(X, G)
-        W = recipes.gen_weight(wl, u).astype(np.float64)
+        W = host_weight(wl, u, torch).astype(np.float64)
         Wt = O.whiten(W, Sx, Sg)
         assert rel_fro(g["Wt"], Wt) <= 1e-5, u.name
         lam_ = O.gram_eigenvalues(Wt)

@@ -149,7 +149,83 @@ __device__ __forceinline__ int slot_next(int s) {
 }
 __device__ __forceinline__ int index_phys(int x) { return slot_phys(x < JB ? x : JP + JB - 1 - x); }
 
-__global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call, int64_t sp, int nblk,
+// One rotation round of the pair solve (see jac_solve_kernel): reads the slot-ordered matrix
+// A, writes the rotated matrix at the moved slots of An, and rotates and moves this thread's
+// rows of V.  Every warp computes all 32 rotations of the round (lane l: pair l) from the
+// same entries.  The rotation parameters use the hardware's approximate reciprocal and
+// square root: a rotation only has to be (nearly) orthogonal and to shrink its coupling,
+// and the Newton-Schulz step after the sweep re-orthogonalises the accumulated V.  Returns
+// whether any rotation of the round was active (the same in every warp).
+struct RoundMap {
+  int ct, cb, dct, dcb;
+  int rt[4], rb[4], drt[4], drb[4];
+};
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ bool solve_round(const float* __restrict__ A, float* __restrict__ An, float (&vt)[8],
+                                            float (&vb)[8], const RoundMap& q, int lane, int warp, float flo,
+                                            float tol2) {
+  const float a = A[q.ct * JP + q.ct], b = A[q.cb * JP + q.cb], d = A[q.ct * JP + q.cb];
+  float c = 1.f, sn = 0.f, td = 0.f;
+  const bool act = fabsf(d) > flo && d * d > tol2 * fmaxf(a * b, 0.f);
+  if (act) {
+    const float tau = (b - a) * rcp_approx(2.f * d);
+    const float tt = copysignf(rcp_approx(fabsf(tau) + sqrt_approx(fmaf(tau, tau, 1.f))), tau);
+    c = rsqrtf(fmaf(tt, tt, 1.f));
+    sn = tt * c;
+    td = tt * d;
+  }
+  const bool any = __any_sync(0xffffffffu, act);
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const int j = warp + 8 * x;
+    const float cj = __shfl_sync(0xffffffffu, c, j), sj = __shfl_sync(0xffffffffu, sn, j);
+    // an inactive rotation has c = 1, s = 0 and reproduces its entries exactly; the diagonal
+    // block of pair l (j == l) takes its closed form instead (selected, not branched)
+    const float e00 = A[q.rt[x] + q.ct], e01 = A[q.rt[x] + q.cb], e10 = A[q.rb[x] + q.ct], e11 = A[q.rb[x] + q.cb];
+    const float a1 = e00 * c - e01 * sn, b1 = e00 * sn + e01 * c;
+    const float c1 = e10 * c - e11 * sn, d1 = e10 * sn + e11 * c;
+    const bool dg = j == lane;
+    An[q.drt[x] + q.dct] = dg ? a - td : cj * a1 - sj * c1;
+    An[q.drt[x] + q.dcb] = dg ? (act ? 0.f : e01) : cj * b1 - sj * d1;
+    An[q.drb[x] + q.dct] = dg ? (act ? 0.f : e10) : sj * a1 + cj * c1;
+    An[q.drb[x] + q.dcb] = dg ? b + td : sj * b1 + cj * d1;
+  }
+#pragma unroll
+  for (int y = 0; y < 8; ++y) {
+    const float x0 = vt[y], y0 = vb[y];
+    const float nt = c * x0 - sn * y0, nb = sn * x0 + c * y0;
+    // slot l + 1 -> l, slot 32 + l - 1 -> 32 + l; slot 1 -> 32, slot 63 -> 31, slot 0 stays
+    const float dn = __shfl_down_sync(0xffffffffu, nt, 1);
+    const float up = __shfl_up_sync(0xffffffffu, nb, 1);
+    vt[y] = lane == 0 ? nt : (lane == JB - 1 ? nb : dn);
+    vb[y] = lane == 0 ? dn : up;
+  }
+  __syncthreads();
+  return any;
+}
+// One sweep (63 rounds, an odd number: the result ends in B).
+__device__ __forceinline__ bool solve_sweep(float* __restrict__ A, float* __restrict__ B, float (&vt)[8],
+                                            float (&vb)[8], const RoundMap& q, int lane, int warp, float flo,
+                                            float tol2) {
+  bool rotated = false;
+  for (int r = 0; r < (JP - 2) / 2; ++r) {
+    rotated |= solve_round(A, B, vt, vb, q, lane, warp, flo, tol2);
+    rotated |= solve_round(B, A, vt, vb, q, lane, warp, flo, tol2);
+  }
+  rotated |= solve_round(A, B, vt, vb, q, lane, warp, flo, tol2);
+  return rotated;
+}
+
+__global__ void __launch_bounds__(256, 4) jac_solve_kernel(float* __restrict__ Call, int64_t sp, int nblk,
                                                         int step, uint8_t* __restrict__ Vimg,
                                                         int* __restrict__ skipall,
                                                         const int* __restrict__ conv,
@@ -160,8 +236,8 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   // writes every entry of the other at its moved position, so a round needs one barrier.
   // The same JAC_SOLVE_SMEM bytes later hold V and the Newton-Schulz factor (stride JS).
   extern __shared__ float jsm[];
-  float* A = jsm;
-  float* An = jsm + JP * JS;
+  float* const A = jsm;
+  float* const An = jsm + JP * JS;
   __shared__ float red[8];
 
   const int k = blockIdx.x, u = blockIdx.y, t = threadIdx.x;
@@ -203,25 +279,23 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
     return;
   }
 
-  // Threshold cyclic Jacobi, 32 disjoint rotations per round.  Every warp computes all 32
-  // rotations of a round (lane l: pair l) from the same entries, so the parameters reach the
-  // threads that need them by warp shuffles.  Thread (warp w, lane l) updates the 2 x 2 blocks
-  // (pair j, pair l), j = w, w + 8, w + 16, w + 24, and holds rows w, w + 8, ..., w + 56 of the
-  // two columns of V in slots l and 32 + l in registers; V's columns follow the circle by warp
-  // shuffles.  The rotation parameters use the fast reciprocal and reciprocal square root: a
-  // rotation only has to be (nearly) orthogonal and to shrink its coupling, and the
-  // Newton-Schulz step below re-orthogonalises V before it leaves the kernel.
+  // Threshold cyclic Jacobi, 32 disjoint rotations per round (solve_round).  Thread (warp w,
+  // lane l) updates the 2 x 2 blocks (pair j, pair l), j = w, w + 8, w + 16, w + 24, and holds
+  // rows w, w + 8, ..., w + 56 of the two columns of V in slots l and 32 + l in registers; V's
+  // columns follow the circle by warp shuffles.  Every address of a round is fixed per thread.
   const int lane = t & 31, warp = t >> 5;
-  const int ct = lane, cb = slot_phys(JB + lane);
-  const int dct = slot_phys(slot_next(lane)), dcb = slot_phys(slot_next(JB + lane));
-  int rt[4], rb[4], drt[4], drb[4];
+  RoundMap q;
+  q.ct = lane;
+  q.cb = slot_phys(JB + lane);
+  q.dct = slot_phys(slot_next(lane));
+  q.dcb = slot_phys(slot_next(JB + lane));
 #pragma unroll
   for (int x = 0; x < 4; ++x) {
     const int j = warp + 8 * x;
-    rt[x] = j * JP;
-    rb[x] = slot_phys(JB + j) * JP;
-    drt[x] = slot_phys(slot_next(j)) * JP;
-    drb[x] = slot_phys(slot_next(JB + j)) * JP;
+    q.rt[x] = j * JP;
+    q.rb[x] = slot_phys(JB + j) * JP;
+    q.drt[x] = slot_phys(slot_next(j)) * JP;
+    q.drb[x] = slot_phys(slot_next(JB + j)) * JP;
   }
   float vt[8], vb[8];
 #pragma unroll
@@ -232,55 +306,9 @@ __global__ void __launch_bounds__(256) jac_solve_kernel(float* __restrict__ Call
   }
   const float tol2 = tol * tol;
   for (int sweep = 0; sweep < max_inner; ++sweep) {
-    int rotated = 0;
-    for (int r = 0; r < JP - 1; ++r) {
-      const float a = A[ct * JP + ct], b = A[cb * JP + cb], d = A[ct * JP + cb];
-      float c = 1.f, sn = 0.f, td = 0.f;
-      bool act = false;
-      if (fabsf(d) > flo && d * d > tol2 * fmaxf(a * b, 0.f)) {
-        const float tau = (b - a) * __frcp_rn(2.f * d);
-        const float tt = copysignf(__frcp_rn(fabsf(tau) + sqrtf(fmaf(tau, tau, 1.f))), tau);
-        c = rsqrtf(fmaf(tt, tt, 1.f));
-        sn = tt * c;
-        td = tt * d;
-        act = true;
-      }
-      rotated |= __any_sync(0xffffffffu, act);  // the same in every warp
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const int j = warp + 8 * x;
-        const float cj = __shfl_sync(0xffffffffu, c, j), sj = __shfl_sync(0xffffffffu, sn, j);
-        if (j == lane) {
-          An[drt[x] + dct] = a - td;
-          An[drb[x] + dcb] = b + td;
-          An[drt[x] + dcb] = act ? 0.f : d;
-          An[drb[x] + dct] = act ? 0.f : A[rb[x] + ct];
-          continue;
-        }
-        // an inactive rotation has c = 1, s = 0 and reproduces its entries exactly
-        const float e00 = A[rt[x] + ct], e01 = A[rt[x] + cb], e10 = A[rb[x] + ct], e11 = A[rb[x] + cb];
-        const float a1 = e00 * c - e01 * sn, b1 = e00 * sn + e01 * c;
-        const float c1 = e10 * c - e11 * sn, d1 = e10 * sn + e11 * c;
-        An[drt[x] + dct] = cj * a1 - sj * c1;
-        An[drt[x] + dcb] = cj * b1 - sj * d1;
-        An[drb[x] + dct] = sj * a1 + cj * c1;
-        An[drb[x] + dcb] = sj * b1 + cj * d1;
-      }
-#pragma unroll
-      for (int y = 0; y < 8; ++y) {
-        const float x0 = vt[y], y0 = vb[y];
-        const float nt = c * x0 - sn * y0, nb = sn * x0 + c * y0;
-        // slot l + 1 -> l, slot 32 + l - 1 -> 32 + l; slot 1 -> 32, slot 63 -> 31, slot 0 stays
-        const float dn = __shfl_down_sync(0xffffffffu, nt, 1);
-        const float up = __shfl_up_sync(0xffffffffu, nb, 1);
-        vt[y] = lane == 0 ? nt : (lane == JB - 1 ? nb : dn);
-        vb[y] = lane == 0 ? dn : up;
-      }
-      __syncthreads();
-      float* tmp = A;
-      A = An;
-      An = tmp;
-    }
+    // the two buffers' roles are fixed inside each call (constant shared-memory offsets)
+    const bool rotated = (sweep & 1) ? solve_sweep(An, A, vt, vb, q, lane, warp, flo, tol2)
+                                     : solve_sweep(A, An, vt, vb, q, lane, warp, flo, tol2);
     if (!rotated) break;
   }
   // After whole sweeps every index is back in its starting slot: the vector in slot l is the
