@@ -288,7 +288,9 @@ KF_API kf_status whitened_svd(kf_ctx* ctx, int32_t n_problems, const kf_svd_prob
  * 64-bit words (~key_bits << 32 | component id) are built in id order and sorted by a stable
  * device LSD radix sort over the score word (four 8-bit passes), which leaves equal scores in
  * id order; the prefix sum of costs in that order is cut at the longest prefix with
- * sum <= budget.
+ * sum <= budget.  Each pass and the cost prefix are single launches whose 4096-key tiles
+ * chain their offsets by a decoupled look-back; its waits are bounded (4 s), and one that ran
+ * out would be reported as KF_ERR_TIMEOUT by kf_sync_status.
  * ranks:      device int32[n_units] out: kept components per unit.
  * cut:        device float[2] out (may be NULL): score of the last kept and of the first
  *             dropped component (NaN where there is none).

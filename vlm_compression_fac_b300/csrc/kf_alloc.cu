@@ -5,13 +5,20 @@
 //          ascending k is score descending, then lower unit, then lower component index
 //          (ids are assigned in unit order), which makes the order total and deterministic;
 //   sort:  LSD radix sort of the score word, 4 passes of 8 bits (equal scores keep their id
-//          order, since the keys start in id order and every pass is stable); each pass = per-tile digit histogram,
-//          one exclusive scan over (digit, tile), stable scatter (warp match + per-warp
-//          digit counters keep the original order inside a tile);
-//   cut:   inclusive prefix sum of the kept pairs' cost m+n in sorted order; the kept
-//          prefix is every position whose prefix sum is <= budget (costs are positive, so
-//          the walk stops at the first overflow); ranks = kept count per unit.
+//          order, since the keys start in id order and every pass is stable).  The digit
+//          counts of all four passes are taken while the keys are built; each pass is then a
+//          single kernel over 4096-key tiles taken in launch order: a tile counts its digits,
+//          publishes the counts, adds up the counts of the tiles before it (decoupled
+//          look-back) and scatters its keys stably (warp match and per-warp digit counters keep
+//          the original order inside the tile) through a digit-ordered copy in shared memory;
+//   cut:   inclusive prefix sum of the kept pairs' cost m+n in sorted order, by one look-back
+//          scan; the kept prefix is every position whose prefix sum is <= budget (costs are
+//          non-negative, so it is a prefix), found by the tile that holds its end; ranks =
+//          kept count per unit.
+// Every wait of a look-back is bounded: a tile that has not published within the context's
+// wait limit records KF_ERR_TIMEOUT and is counted as empty, so no launch can hang.
 #include "kf_internal.cuh"
+#include "kf_tc_ptx.cuh"
 
 #include <mutex>
 
@@ -21,7 +28,7 @@ namespace {
 constexpr int RT = 256;            // threads per tile
 constexpr int RI = 16;             // keys per thread
 constexpr int TILE = RT * RI;      // 4096 keys per tile
-constexpr int SCAN_T = 1024;
+constexpr int WK = TILE / (RT / 32);  // keys of one warp's contiguous run in a tile
 
 __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_units, int64_t g) {
   int lo = 0, hi = n_units;  // off[lo] <= g < off[hi]
@@ -30,6 +37,16 @@ __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_un
     if (off[mid] <= g) lo = mid; else hi = mid;
   }
   return lo;
+}
+// The unit of component g when the 32 lanes of a warp hold consecutive components from gw on:
+// one binary search for gw (lane 0, broadcast), then each lane walks forward over the (short)
+// list of units that start inside the warp's range.  Every lane of the warp must call it.
+__device__ __forceinline__ int warp_unit_of(const int64_t* __restrict__ off, int n_units, int64_t gw, int64_t g) {
+  int u0 = 0;
+  if ((threadIdx.x & 31) == 0) u0 = unit_of(off, n_units, gw);
+  int u = __shfl_sync(0xffffffffu, u0, 0);
+  while (u + 1 < n_units && off[u + 1] <= g) ++u;
+  return u;
 }
 
 // Key of every component: base score per mode (KF_KEY_HALF_SIGMA2: 0.5 sigma^2;
@@ -42,32 +59,63 @@ constexpr int MODE_SWIFT_HYBRID = 101;  // internal: Swift-SVD B hybrid keys bui
 // The low word of a key is the component id, or, when no caller needs ids (no keep mask), the
 // unit index: the sort orders by the score word only and is stable, so equal scores stay in
 // id order either way, and every later pass needs only the unit (its cost, its rank count).
-__global__ void build_keys_kernel(const float* __restrict__ sigma, const int64_t* __restrict__ off,
-                                  const int64_t* __restrict__ cost, int n_units, int64_t n, int mode,
-                                  const float* __restrict__ weight, const float* __restrict__ energy,
-                                  unsigned long long* __restrict__ keys, int low_is_unit) {
-  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += int64_t(gridDim.x) * blockDim.x) {
-    const int u = unit_of(off, n_units, g);
-    const float s = sigma[g];
-    const float q = __fmul_rn(s, s);
-    float sc;
-    if (mode == MODE_GIVEN_KEYS) {
-      sc = s > 0.f ? s : 0.f;  // a negative or not-a-number key counts as 0
-    } else if (mode == KF_KEY_ENERGY_RATIO) {
-      const float e = energy[u];
-      sc = e > 0.f ? __fdiv_rn(q, e) : 0.f;
-    } else {
-      sc = 0.5f * q;
-      if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
+// The kernel also counts the four 8-bit digits of the score words (ghist[pass][digit]) for
+// the radix passes: consecutive lanes hold consecutive components, whose digits come in runs
+// (a unit's scores are sorted), so each run of equal digits in a warp is added once.
+__global__ void __launch_bounds__(256) build_keys_kernel(const float* __restrict__ sigma,
+                                                         const int64_t* __restrict__ off,
+                                                         const int64_t* __restrict__ cost, int n_units, int64_t n,
+                                                         int mode, const float* __restrict__ weight,
+                                                         const float* __restrict__ energy,
+                                                         unsigned long long* __restrict__ keys, int low_is_unit,
+                                                         unsigned* __restrict__ ghist) {
+  __shared__ unsigned h[4 * 256];
+  for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) h[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  for (int64_t g0 = int64_t(blockIdx.x) * blockDim.x; g0 < n; g0 += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t g = g0 + threadIdx.x;
+    const bool valid = g < n;
+    const int u = warp_unit_of(off, n_units, g0 + (threadIdx.x & ~31), valid ? g : n - 1);
+    unsigned bits = 0;
+    if (valid) {
+      const float s = sigma[g];
+      const float q = __fmul_rn(s, s);
+      float sc;
+      if (mode == MODE_GIVEN_KEYS) {
+        sc = s > 0.f ? s : 0.f;  // a negative or not-a-number key counts as 0
+      } else if (mode == KF_KEY_ENERGY_RATIO) {
+        const float e = energy[u];
+        sc = e > 0.f ? __fdiv_rn(q, e) : 0.f;
+      } else {
+        sc = 0.5f * q;
+        if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
+      }
+      if (weight) {
+        const float w = weight[u];
+        sc = (w > 0.f) ? __fmul_rn(w, sc) : 0.f;  // also maps a NaN weight to 0
+      }
+      bits = ~__float_as_uint(sc);
+      const uint32_t low = low_is_unit ? uint32_t(u) : uint32_t(g);
+      keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(low);
     }
-    if (weight) {
-      const float w = weight[u];
-      sc = (w > 0.f) ? __fmul_rn(w, sc) : 0.f;  // also maps a NaN weight to 0
+    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const unsigned d = (bits >> (8 * b)) & 255u;
+      const unsigned prev = __shfl_up_sync(0xffffffffu, d, 1);
+      const bool head = valid && (lane == 0 || d != prev);
+      const unsigned ends = __ballot_sync(0xffffffffu, head) | ~vmask;  // a run ends at the next head
+      if (head) {
+        const unsigned above = ends & ~((2u << lane) - 1u);
+        const int nxt = above ? __ffs(int(above)) - 1 : 32;
+        atomicAdd(&h[b * 256 + int(d)], unsigned(nxt - lane));
+      }
     }
-    const unsigned bits = ~__float_as_uint(sc);
-    const uint32_t low = low_is_unit ? uint32_t(u) : uint32_t(g);
-    keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(low);
   }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x)
+    if (h[i]) atomicAdd(&ghist[i], h[i]);
 }
 
 // Swift-SVD B: the closed-form loss of unit u truncated to rank k is the energy it drops,
@@ -91,8 +139,10 @@ __global__ void swift_eps_kernel(const float* __restrict__ sigma, const int64_t*
 // float32 (beta not positive or not a number: key 0).
 __global__ void swift_keys_kernel(const double* __restrict__ eps, const int64_t* __restrict__ off, int n_units,
                                   int64_t n, const float* __restrict__ beta, double alpha, float* __restrict__ keys) {
-  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < n; g += int64_t(gridDim.x) * blockDim.x) {
-    const int u = unit_of(off, n_units, g);
+  for (int64_t g0 = int64_t(blockIdx.x) * blockDim.x; g0 < n; g0 += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t g = g0 + threadIdx.x;
+    const int u = warp_unit_of(off, n_units, g0 + (threadIdx.x & ~31u), g < n ? g : n - 1);
+    if (g >= n) continue;
     const float b = beta ? beta[u] : 1.f;
     float k = 0.f;
     if (b > 0.f) k = float(pow(double(b), alpha) * pow(log(2.718281828459045 + eps[g]), 1.0 - alpha));
@@ -122,142 +172,108 @@ __global__ void __launch_bounds__(256) unit_energy_kernel(const float* __restric
   }
 }
 
-__global__ void __launch_bounds__(RT) hist_kernel(const unsigned long long* __restrict__ keys, int64_t n, int shift,
-                                                  int ntiles, unsigned* __restrict__ hist) {
-  __shared__ unsigned h[256];
-  h[threadIdx.x] = 0;
-  const int64_t base = int64_t(blockIdx.x) * TILE;
-  const unsigned lane = threadIdx.x & 31u;
-  // all of this thread's keys are requested before the first is used
-  unsigned long long k[RI];
+// Exclusive scan of each pass's 256 digit counts: gbase[pass][d] = the first sorted position
+// of digit d in that pass.  One CTA of 256 threads per pass.
+__global__ void __launch_bounds__(256) digit_base_kernel(const unsigned* __restrict__ ghist,
+                                                         unsigned* __restrict__ gbase) {
+  __shared__ unsigned wsum[8];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  const unsigned v = ghist[blockIdx.x * 256 + t];
+  unsigned x = v;
 #pragma unroll
-  for (int i = 0; i < RI; ++i) {
-    const int64_t g = base + int64_t(i) * RT + threadIdx.x;
-    k[i] = g < n ? keys[g] : 0ull;
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
+  if (lane == 31) wsum[w] = x;
   __syncthreads();
-#pragma unroll
-  for (int i = 0; i < RI; ++i) {
-    const int64_t g = base + int64_t(i) * RT + threadIdx.x;
-    const unsigned d = g < n ? unsigned((k[i] >> shift) & 255u) : 256u;
-    // one shared atomic per distinct digit of the warp (the leading bytes of the keys are
-    // often nearly constant, which would serialise per-key atomics on one bin)
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    if (d < 256u && (peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&h[d], unsigned(__popc(peers)));
-  }
-  __syncthreads();
-  hist[int64_t(threadIdx.x) * ntiles + blockIdx.x] = h[threadIdx.x];
+  unsigned pre = 0;
+  for (int ww = 0; ww < w; ++ww) pre += wsum[ww];
+  gbase[blockIdx.x * 256 + t] = pre + x - v;
 }
 
-// Multi-CTA exclusive scan of a long uint array in chunks of SCAN_CHUNK: block sums, a scan of
-// the sums, then every chunk rescanned from its base (same result as one sequential scan).
-constexpr int64_t SCAN_CHUNK = 8 * 1024;
-
-__global__ void __launch_bounds__(1024) chunk_sum_u32_kernel(const unsigned* __restrict__ a, int64_t len,
-                                                             unsigned* __restrict__ bsum) {
-  __shared__ unsigned red[32];
-  const int64_t c0 = int64_t(blockIdx.x) * SCAN_CHUNK;
-  unsigned s = 0;
-  for (int64_t i = c0 + threadIdx.x; i < len && i < c0 + SCAN_CHUNK; i += 1024) s += a[i];
-#pragma unroll
-  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned t = 0;
-    for (int w = 0; w < 32; ++w) t += red[w];
-    bsum[blockIdx.x] = t;
-  }
+// Look-back status words, one per (tile, slot): bits 63..62 flag (1: the tile's own count,
+// 2: the inclusive sum through the tile), bits 61..56 the tag of the pass that wrote it (the
+// words are cleared once per call and reused by the passes), bits 55..0 the value.
+constexpr unsigned long long LB_OWN = 1ull << 62, LB_INCL = 2ull << 62;
+constexpr unsigned long long LB_VAL = (1ull << 56) - 1;
+__device__ __forceinline__ void lb_store(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-
-// Exclusive scan of a uint array: CTA b scans [b * chunk, min(len, (b + 1) * chunk)) in steps
-// of SCAN_T, starting from base[b] (or 0 without base).  One CTA with chunk >= len scans the
-// whole array.
-__global__ void __launch_bounds__(SCAN_T) scan_u32_kernel(unsigned* __restrict__ a, int64_t len, int64_t chunk,
-                                                          const unsigned* __restrict__ cbase) {
-  __shared__ unsigned ws[32];
-  __shared__ unsigned carry;
-  if (threadIdx.x == 0) carry = cbase ? cbase[blockIdx.x] : 0u;
-  __syncthreads();
-  const int64_t lo = int64_t(blockIdx.x) * chunk;
-  const int64_t hi = lo + chunk < len ? lo + chunk : len;
-  for (int64_t c0 = lo; c0 < hi; c0 += SCAN_T) {
-    const int64_t i = c0 + threadIdx.x;
-    const unsigned v = i < hi ? a[i] : 0u;
-    unsigned x = v;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
+__device__ __forceinline__ unsigned long long lb_load(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+// Sum of one slot's values over the tiles before `tile` (status word of tile k at
+// st[k * stride]): walks back adding own counts until a tile's inclusive sum is found.  Tiles
+// take their numbers in launch order, so every tile waited on is held by a CTA that is
+// already running; each wait is still bounded by wait_ns (then KF_ERR_TIMEOUT is recorded and
+// the tile counted as empty).
+__device__ unsigned long long lookback(const unsigned long long* st, int64_t stride, int tile,
+                                       unsigned long long tag, unsigned long long wait_ns, int* status) {
+  unsigned long long acc = 0;
+  int k = tile - 1;
+  unsigned long long t0 = 0;
+  while (k >= 0) {
+    const unsigned long long w = lb_load(st + int64_t(k) * stride);
+    if ((w >> 62) != 0 && (w & (63ull << 56)) == tag) {
+      acc += w & LB_VAL;
+      if ((w >> 62) == 2) break;
+      --k;
+      t0 = 0;
+      continue;
     }
-    if (lane == 31) ws[w] = x;
-    __syncthreads();
-    if (w == 0) {
-      unsigned z = ws[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const unsigned y = __shfl_up_sync(0xffffffffu, z, o);
-        if (lane >= o) z += y;
-      }
-      ws[lane] = z;
+    const unsigned long long now = now_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > wait_ns) {
+      raise_status(status, KF_ERR_TIMEOUT, WAIT_LOOKBACK);
+      --k;
+      t0 = 0;
+      continue;
     }
-    __syncthreads();
-    const unsigned incl = x + (w > 0 ? ws[w - 1] : 0u) + carry;
-    if (i < hi) a[i] = incl - v;
-    __syncthreads();
-    if (threadIdx.x == SCAN_T - 1) carry = incl;
-    __syncthreads();
+    __nanosleep(100);
   }
+  return acc;
 }
 
-// Stable scatter of one 4096-key tile.  Warp w owns the tile's keys w * WK .. w * WK + WK - 1
-// (WK = TILE / 8; the warp's round r holds keys w * WK + 32 r + lane), so the tile's index
-// order is (warp, round, lane) order.  All keys are loaded first; phase 1 counts each warp's
-// keys per digit (one counter update per distinct digit of a round, by warp match); one pass
-// over the warps per digit turns the counts into each (digit, warp)'s first position in the
-// tile's digit-ordered copy in shared memory; phase 2 puts every key at its warp's running
-// position for its digit plus its rank among the round's equal digits; the copy is then
-// written out so that consecutive threads write consecutive addresses of one digit's run
-// (coalesced).  The tile's digit counts come from the scanned (digit, tile) histogram:
-// count[d] = base of the next tile (or digit) minus this base.
-constexpr int WK = TILE / (RT / 32);
-__global__ void __launch_bounds__(RT, 3) scatter_kernel(const unsigned long long* __restrict__ in,
-                                                     unsigned long long* __restrict__ out, int64_t n, int shift,
-                                                     int ntiles, const unsigned* __restrict__ hist) {
-  __shared__ unsigned base[256];
+// One radix pass over the score word's byte `pass`, one 4096-key tile per CTA (tile number
+// from a counter, in launch order).  Warp w owns the tile's keys w * WK .. w * WK + WK - 1
+// (the warp's round r holds keys w * WK + 32 r + lane), so the tile's index order is (warp,
+// round, lane) order.  All keys are loaded first; phase 1 counts each warp's keys per digit
+// (one counter update per distinct digit of a round, by warp match); the tile's counts are
+// published and the counts of the tiles before it summed by look-back (thread d for digit d);
+// phase 2 puts every key at its warp's running position for its digit in the tile's
+// digit-ordered copy in shared memory, plus its rank among the round's equal digits; the copy
+// is then written out at gbase[d] + (keys of digit d in earlier tiles) + (rank in the tile),
+// consecutive threads on consecutive addresses of one digit's run (coalesced).
+__global__ void __launch_bounds__(RT, 3) onesweep_kernel(const unsigned long long* __restrict__ in,
+                                                         unsigned long long* __restrict__ out, int64_t n, int pass,
+                                                         const unsigned* __restrict__ gbase,
+                                                         unsigned long long* __restrict__ lbst,
+                                                         unsigned* __restrict__ tile_ctr, int* status,
+                                                         unsigned long long wait_ns) {
   __shared__ unsigned start[256];   // the digit's first position in the tile's ordered copy
+  __shared__ unsigned gpos[256];    // the digit's first position in the output
   __shared__ unsigned wpos[RT / 32][256];   // per-warp digit counts, then running positions
   __shared__ unsigned long long tk[TILE];
   __shared__ unsigned wsum[RT / 32];
+  __shared__ int tile_s;
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int64_t tile0 = int64_t(blockIdx.x) * TILE;
+  if (t == 0) tile_s = int(atomicAdd(tile_ctr, 1u));
+  for (int x = lane; x < 256; x += 32) wpos[w][x] = 0;
+  __syncthreads();
+  const int tile = tile_s;
+  const int shift = 32 + 8 * pass;
+  const int64_t tile0 = int64_t(tile) * TILE;
   const int tile_n = int(n - tile0 < TILE ? n - tile0 : TILE);
   unsigned long long key[RI];
 #pragma unroll
   for (int r = 0; r < RI; ++r) {
     const int li = w * WK + r * 32 + lane;
     key[r] = li < tile_n ? in[tile0 + li] : 0ull;
-  }
-  for (int x = lane; x < 256; x += 32) wpos[w][x] = 0;
-  {
-    const int64_t hi = int64_t(t) * ntiles + blockIdx.x;
-    base[t] = hist[hi];
-    const unsigned nxt = (blockIdx.x + 1 < ntiles) ? hist[hi + 1] : (t + 1 < 256 ? hist[int64_t(t + 1) * ntiles] : unsigned(n));
-    const unsigned cnt = nxt - base[t];
-    // exclusive scan of the 256 counts (one per thread) -> start
-    unsigned x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[w] = x;
-    __syncthreads();
-    unsigned pre = 0;
-    for (int ww = 0; ww < w; ++ww) pre += wsum[ww];
-    start[t] = pre + x - cnt;
   }
   unsigned peers[RI];
 #pragma unroll
@@ -269,7 +285,25 @@ __global__ void __launch_bounds__(RT, 3) scatter_kernel(const unsigned long long
     __syncwarp();
   }
   __syncthreads();
-  {  // per digit: each warp's first position, in warp order
+  // thread t = digit t: the tile's count, published at once; then its place in the tile
+  unsigned cnt = 0;
+#pragma unroll
+  for (int ww = 0; ww < RT / 32; ++ww) cnt += wpos[ww][t];
+  const unsigned long long tag = (unsigned long long)(pass + 1) << 56;
+  unsigned long long* mine = lbst + int64_t(tile) * 256 + t;
+  lb_store(mine, (tile == 0 ? LB_INCL : LB_OWN) | tag | cnt);
+  {
+    unsigned x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[w] = x;
+    __syncthreads();
+    unsigned pre = 0;
+    for (int ww = 0; ww < w; ++ww) pre += wsum[ww];
+    start[t] = pre + x - cnt;
     unsigned acc = start[t];
 #pragma unroll
     for (int ww = 0; ww < RT / 32; ++ww) {
@@ -278,6 +312,12 @@ __global__ void __launch_bounds__(RT, 3) scatter_kernel(const unsigned long long
       acc += c;
     }
   }
+  unsigned long long before = 0;
+  if (tile > 0) {
+    before = lookback(lbst + t, 256, tile, tag, wait_ns, status);
+    lb_store(mine, LB_INCL | tag | (before + cnt));
+  }
+  gpos[t] = gbase[pass * 256 + t] + unsigned(before);
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < RI; ++r) {
@@ -293,7 +333,7 @@ __global__ void __launch_bounds__(RT, 3) scatter_kernel(const unsigned long long
   for (int i = t; i < tile_n; i += RT) {
     const unsigned long long k = tk[i];
     const unsigned d = unsigned((k >> shift) & 255u);
-    out[base[d] + (unsigned(i) - start[d])] = k;
+    out[gpos[d] + (unsigned(i) - start[d])] = k;
   }
 }
 
@@ -301,106 +341,115 @@ __device__ __forceinline__ int key_unit(unsigned long long k, const int64_t* __r
                                         int low_is_unit) {
   return low_is_unit ? int(uint32_t(k)) : unit_of(off, n_units, int64_t(uint32_t(k)));
 }
+__device__ __forceinline__ float key_score(unsigned long long k) { return __uint_as_float(~unsigned(k >> 32)); }
 
-// Inclusive prefix sums of the sorted components' costs, per 1024-item block.
-__global__ void __launch_bounds__(SCAN_T) cost_block_sum_kernel(const unsigned long long* __restrict__ keys,
-                                                                const int64_t* __restrict__ off,
-                                                                const int64_t* __restrict__ cost, int n_units,
-                                                                int64_t n, long long* __restrict__ bsum,
-                                                                int low_is_unit) {
-  __shared__ long long red[SCAN_T / 32];
-  const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
-  long long c = 0;
-  if (i < n) c = cost[key_unit(keys[i], off, n_units, low_is_unit)];
-#pragma unroll
-  for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+// The cost prefix and the cut in one pass over the sorted keys: tile = 4096 keys (16
+// consecutive per thread), the tile's cost total published and the totals of the tiles
+// before it summed by look-back.  The kept prefix is every position whose inclusive cost
+// prefix is <= budget; the one tile whose range of prefixes contains the budget (or the last
+// tile when everything fits, or the first when the budget is negative) writes its length
+// (kcount), the cost it uses and the scores on both sides of the cut.
+__global__ void __launch_bounds__(RT) cost_scan_kernel(const unsigned long long* __restrict__ keys,
+                                                       const int64_t* __restrict__ off,
+                                                       const int64_t* __restrict__ cost, int n_units, int64_t n,
+                                                       long long budget, int low_is_unit,
+                                                       unsigned long long* __restrict__ lbst,
+                                                       unsigned* __restrict__ tile_ctr,
+                                                       unsigned long long* __restrict__ kcount, float* __restrict__ cut,
+                                                       long long* __restrict__ used, int* status,
+                                                       unsigned long long wait_ns) {
+  __shared__ long long wsum[RT / 32];
+  __shared__ long long excl_s;
+  __shared__ int tile_s;
+  __shared__ int kept_w[RT / 32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  if (t == 0) tile_s = int(atomicAdd(tile_ctr, 1u));
   __syncthreads();
-  if (threadIdx.x == 0) {
-    long long s = 0;
-    for (int w = 0; w < SCAN_T / 32; ++w) s += red[w];
-    bsum[blockIdx.x] = s;
-  }
-}
-
-__global__ void __launch_bounds__(SCAN_T) scan_i64_kernel(long long* __restrict__ a, int64_t len) {
-  __shared__ long long ws[32];
-  __shared__ long long carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
-  for (int64_t c0 = 0; c0 < len; c0 += SCAN_T) {
-    const int64_t i = c0 + threadIdx.x;
-    const long long v = i < len ? a[i] : 0;
-    long long x = v;
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int tile = tile_s;
+  const int64_t tile0 = int64_t(tile) * TILE;
+  const int64_t g0 = tile0 + int64_t(t) * RI;
+  long long c[RI];
+  long long sum = 0;
+  if (g0 + RI <= n) {  // 16 consecutive keys: eight 16-byte loads
+    const ulonglong2* kv = reinterpret_cast<const ulonglong2*>(keys + g0);
+    ulonglong2 kk[RI / 2];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) ws[w] = x;
-    __syncthreads();
-    if (w == 0) {
-      long long z = ws[lane];
+    for (int i = 0; i < RI / 2; ++i) kk[i] = kv[i];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, z, o);
-        if (lane >= o) z += y;
-      }
-      ws[lane] = z;
+    for (int i = 0; i < RI / 2; ++i) {
+      c[2 * i] = cost[key_unit(kk[i].x, off, n_units, low_is_unit)];
+      c[2 * i + 1] = cost[key_unit(kk[i].y, off, n_units, low_is_unit)];
     }
-    __syncthreads();
-    const long long incl = x + (w > 0 ? ws[w - 1] : 0) + carry;
-    if (i < len) a[i] = incl - v;
-    __syncthreads();
-    if (threadIdx.x == SCAN_T - 1) carry = incl;
-    __syncthreads();
+  } else {
+#pragma unroll
+    for (int i = 0; i < RI; ++i) {
+      const int64_t g = g0 + i;
+      c[i] = g < n ? cost[key_unit(keys[g], off, n_units, low_is_unit)] : 0;
+    }
   }
-}
-
-// Per item: the inclusive prefix sum of the costs in sorted order.
-__global__ void __launch_bounds__(SCAN_T) cut_kernel(const unsigned long long* __restrict__ keys,
-                                                     const int64_t* __restrict__ off, const int64_t* __restrict__ cost,
-                                                     int n_units, int64_t n, const long long* __restrict__ bexcl,
-                                                     long long* __restrict__ prefix, int low_is_unit) {
-  __shared__ long long ws[32];
-  const int64_t i = int64_t(blockIdx.x) * SCAN_T + threadIdx.x;
-  long long c = 0;
-  if (i < n) c = cost[key_unit(keys[i], off, n_units, low_is_unit)];
-  long long x = c;
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int i = 0; i < RI; ++i) sum += c[i];
+  // exclusive scan of the thread sums over the tile
+  long long x = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const long long y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) ws[w] = x;
+  if (lane == 31) wsum[w] = x;
   __syncthreads();
-  if (w == 0) {
-    long long z = ws[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long y = __shfl_up_sync(0xffffffffu, z, o);
-      if (lane >= o) z += y;
+  long long pre = 0, total = 0;
+  for (int ww = 0; ww < RT / 32; ++ww) {
+    if (ww < w) pre += wsum[ww];
+    total += wsum[ww];
+  }
+  const long long texcl = pre + x - sum;
+  if (t == 0) {
+    unsigned long long* mine = lbst + tile;
+    const unsigned long long tag = 1ull << 56;
+    lb_store(mine, (tile == 0 ? LB_INCL : LB_OWN) | tag | (unsigned long long)total);
+    long long e = 0;
+    if (tile > 0) {
+      e = (long long)lookback(lbst, 1, tile, tag, wait_ns, status);
+      lb_store(mine, LB_INCL | tag | (unsigned long long)(e + total));
     }
-    ws[lane] = z;
+    excl_s = e;
   }
   __syncthreads();
-  const long long incl = x + (w > 0 ? ws[w - 1] : 0) + bexcl[blockIdx.x];
-  if (i < n) prefix[i] = incl;
-}
-
-// kcount = the length of the kept prefix: the largest k with prefix[k - 1] <= budget.  The
-// costs are non-negative, so the prefix sums never decrease and a binary search finds it
-// (one thread, about log2(n) reads).
-__global__ void kcount_kernel(const long long* __restrict__ prefix, int64_t n, long long budget,
-                              unsigned long long* __restrict__ kcount) {
-  int64_t lo = 0, hi = n;
-  while (lo < hi) {
-    const int64_t mid = lo + (hi - lo + 1) / 2;
-    if (prefix[mid - 1] <= budget) lo = mid; else hi = mid - 1;
+  const long long E = excl_s;
+  const int64_t tile_end = tile0 + TILE < n ? tile0 + TILE : n;
+  const bool writer = (E <= budget && budget < E + total) || (tile == 0 && budget < 0) ||
+                      (tile_end == n && E + total <= budget);   // uniform over the CTA
+  if (!writer) return;
+  // kept items of this tile (a prefix of it: the prefix sums do not decrease)
+  int k_t = 0;
+  long long run = E + texcl, last_incl = E + texcl;
+#pragma unroll
+  for (int i = 0; i < RI; ++i) {
+    run += c[i];
+    if (g0 + i < n && run <= budget) {
+      ++k_t;
+      last_incl = run;
+    }
   }
-  *kcount = static_cast<unsigned long long>(lo);
+  int kw = k_t;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) kw += __shfl_xor_sync(0xffffffffu, kw, o);
+  if (lane == 0) kept_w[w] = kw;
+  __syncthreads();
+  int K = 0;
+  for (int ww = 0; ww < RT / 32; ++ww) K += kept_w[ww];
+  const int64_t kc = tile0 + K;
+  // the thread holding the last kept item reports the cost used
+  if (K > 0 && t == (K - 1) / RI && used) *used = last_incl;
+  if (t == 0) {
+    if (K == 0 && used) *used = E;
+    *kcount = static_cast<unsigned long long>(kc);
+    if (cut) {
+      cut[0] = kc > 0 ? key_score(keys[kc - 1]) : __int_as_float(0x7fc00000);
+      cut[1] = kc < n ? key_score(keys[kc]) : __int_as_float(0x7fc00000);
+    }
+  }
 }
 
 // ranks[u] += the kept components of unit u.  With at most RANKS_SMEM_UNITS units each
@@ -436,19 +485,6 @@ __global__ void keep_mask_kernel(const unsigned long long* __restrict__ keys,
     keep[uint32_t(keys[i])] = 1;
 }
 
-__device__ __forceinline__ float key_score(unsigned long long k) { return __uint_as_float(~unsigned(k >> 32)); }
-
-__global__ void finish_kernel(const unsigned long long* __restrict__ keys, const long long* __restrict__ prefix,
-                              int64_t n, const unsigned long long* __restrict__ kcount, float* __restrict__ cut,
-                              long long* __restrict__ used) {
-  const int64_t k = int64_t(*kcount);
-  if (cut) {
-    cut[0] = k > 0 ? key_score(keys[k - 1]) : __int_as_float(0x7fc00000);
-    cut[1] = k < n ? key_score(keys[k]) : __int_as_float(0x7fc00000);
-  }
-  if (used) *used = k > 0 ? prefix[k - 1] : 0;
-}
-
 __global__ void fixed_rank_kernel(const int64_t* __restrict__ off, const int64_t* __restrict__ cost, int n_units,
                                   const int* __restrict__ fixed, int* __restrict__ ranks, float* __restrict__ cut,
                                   long long* __restrict__ used) {
@@ -481,22 +517,28 @@ unsigned grid_cap(int64_t n, int per) {
 
 struct AllocBufs {
   unsigned long long *ka, *kb, *kcount;
-  unsigned *hist, *hsum;
-  long long *bsum, *prefix;
+  unsigned long long *lbst, *lbst2;       // look-back words of the radix passes and of the cost scan
+  unsigned *ghist, *gbase, *ctr;          // digit counts, digit bases, tile counters (4 passes + scan)
+  float* aux;                             // Swift hybrid keys before they become sort keys
   float* energy;
+  unsigned char *clear0, *clear1;         // [clear0, clear1) is zeroed once per call
 };
 
 // n_energy: units whose energy is needed (KF_KEY_ENERGY_RATIO), else 0.
 size_t alloc_carve(Carve& cv, int64_t n, int64_t n_energy, AllocBufs& b) {
   const int64_t ntiles = (n + TILE - 1) / TILE;
-  const int64_t nb = (n + SCAN_T - 1) / SCAN_T;
+  const int64_t nt = ntiles > 0 ? ntiles : 1;
   b.ka = cv.take<unsigned long long>(n > 0 ? n : 1);
   b.kb = cv.take<unsigned long long>(n > 0 ? n : 1);
-  b.hist = cv.take<unsigned>(size_t(256) * (ntiles > 0 ? ntiles : 1));
-  b.hsum = cv.take<unsigned>(size_t((256 * (ntiles > 0 ? ntiles : 1) + SCAN_CHUNK - 1) / SCAN_CHUNK));
-  b.bsum = cv.take<long long>(nb > 0 ? nb : 1);
-  b.prefix = cv.take<long long>(n > 0 ? n : 1);
+  b.lbst = cv.take<unsigned long long>(size_t(256) * nt);
+  b.clear0 = reinterpret_cast<unsigned char*>(b.lbst);
+  b.lbst2 = cv.take<unsigned long long>(size_t(nt));
+  b.ghist = cv.take<unsigned>(4 * 256);
+  b.ctr = cv.take<unsigned>(8);
+  b.clear1 = reinterpret_cast<unsigned char*>(b.ctr + 8);
+  b.gbase = cv.take<unsigned>(4 * 256);
   b.kcount = cv.take<unsigned long long>(1);
+  b.aux = cv.take<float>(n > 0 ? n : 1);
   b.energy = n_energy > 0 ? cv.take<float>(n_energy) : nullptr;
   return cv.off;
 }
@@ -516,7 +558,6 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
                     int64_t n, int64_t budget, kf_alloc_mode mode, const int32_t* fixed, const float* weight,
                     int32_t* ranks, float* cut, int64_t* used, void* ws, size_t ws_bytes, cudaStream_t st,
                     unsigned char* keep, double alpha) {
-  (void)ctx;
   KF_CUDA(cudaMemsetAsync(ranks, 0, sizeof(int32_t) * size_t(n_units), st));
   if (mode == KF_FIXED_RANK) {
     fixed_rank_kernel<<<1, 256, 0, st>>>(off, cost, n_units, fixed, ranks, cut, (long long*)used); note_launch();
@@ -528,25 +569,26 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   if (!cv.fits()) return fail(KF_ERR_WORKSPACE, "score_and_allocate: workspace too small");
   const int ntiles = int((n + TILE - 1) / TILE);
   const int low_is_unit = keep ? 0 : 1;
+  KF_CUDA(cudaMemsetAsync(b.clear0, 0, size_t(b.clear1 - b.clear0), st));
   if (mode == KF_KEY_ENERGY_RATIO) {
     unit_energy_kernel<<<unsigned(n_units), 256, 0, st>>>(sigma, off, b.energy); note_launch();
     KF_CUDA(cudaGetLastError());
   }
   if (int(mode) == MODE_SWIFT_HYBRID) {
-    // eps (float64) in the second key buffer and the float keys in the prefix buffer: both
-    // are free until the first radix scatter and the cost prefix respectively.
+    // eps (float64) in the second key buffer, free until the first radix pass
     double* eps = reinterpret_cast<double*>(b.kb);
-    float* hk = reinterpret_cast<float*>(b.prefix);
     swift_eps_kernel<<<unsigned((n_units + 127) / 128), 128, 0, st>>>(sigma, off, n_units, eps); note_launch();
     KF_CUDA(cudaGetLastError());
-    swift_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(eps, off, n_units, n, weight, alpha, hk); note_launch();
+    swift_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(eps, off, n_units, n, weight, alpha, b.aux); note_launch();
     KF_CUDA(cudaGetLastError());
-    build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(hk, off, cost, n_units, n, MODE_GIVEN_KEYS, nullptr,
-                                                        nullptr, b.ka, low_is_unit); note_launch();
+    build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(b.aux, off, cost, n_units, n, MODE_GIVEN_KEYS, nullptr,
+                                                        nullptr, b.ka, low_is_unit, b.ghist); note_launch();
   } else {
     build_keys_kernel<<<grid_cap(n, 256), 256, 0, st>>>(sigma, off, cost, n_units, n, int(mode), weight, b.energy,
-                                                        b.ka, low_is_unit); note_launch();
+                                                        b.ka, low_is_unit, b.ghist); note_launch();
   }
+  KF_CUDA(cudaGetLastError());
+  digit_base_kernel<<<4, 256, 0, st>>>(b.ghist, b.gbase); note_launch();
   KF_CUDA(cudaGetLastError());
   // The keys are built in id order and every pass is stable, so sorting by the score word
   // alone (the upper 32 bits, four 8-bit passes) leaves equal scores in id order: the same
@@ -554,39 +596,17 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
   unsigned long long* src = b.ka;
   unsigned long long* dst = b.kb;
   for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 32 + pass * 8;
-    hist_kernel<<<ntiles, RT, 0, st>>>(src, n, shift, ntiles, b.hist); note_launch();
-    KF_CUDA(cudaGetLastError());
-    const int64_t hlen = int64_t(256) * ntiles;
-    if (hlen <= SCAN_CHUNK) {
-      scan_u32_kernel<<<1, SCAN_T, 0, st>>>(b.hist, hlen, hlen, nullptr); note_launch();
-      KF_CUDA(cudaGetLastError());
-    } else {
-      const int64_t nch = (hlen + SCAN_CHUNK - 1) / SCAN_CHUNK;
-      chunk_sum_u32_kernel<<<unsigned(nch), 1024, 0, st>>>(b.hist, hlen, b.hsum); note_launch();
-      KF_CUDA(cudaGetLastError());
-      scan_u32_kernel<<<1, SCAN_T, 0, st>>>(b.hsum, nch, nch, nullptr); note_launch();
-      KF_CUDA(cudaGetLastError());
-      scan_u32_kernel<<<unsigned(nch), SCAN_T, 0, st>>>(b.hist, hlen, SCAN_CHUNK, b.hsum); note_launch();
-      KF_CUDA(cudaGetLastError());
-    }
-    scatter_kernel<<<ntiles, RT, 0, st>>>(src, dst, n, shift, ntiles, b.hist); note_launch();
+    onesweep_kernel<<<ntiles, RT, 0, st>>>(src, dst, n, pass, b.gbase, b.lbst, b.ctr + pass, ctx->d_status,
+                                           WAIT_LIMIT_NS); note_launch();
     KF_CUDA(cudaGetLastError());
     unsigned long long* tmp = src;
     src = dst;
     dst = tmp;
   }
   // src now holds the sorted keys.
-  const int64_t nb = (n + SCAN_T - 1) / SCAN_T;
-  cost_block_sum_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, low_is_unit);
+  cost_scan_kernel<<<ntiles, RT, 0, st>>>(src, off, cost, n_units, n, budget, low_is_unit, b.lbst2, b.ctr + 4,
+                                          b.kcount, cut, (long long*)used, ctx->d_status, WAIT_LIMIT_NS);
   note_launch();
-  KF_CUDA(cudaGetLastError());
-  scan_i64_kernel<<<1, SCAN_T, 0, st>>>(b.bsum, nb); note_launch();
-  KF_CUDA(cudaGetLastError());
-  cut_kernel<<<unsigned(nb), SCAN_T, 0, st>>>(src, off, cost, n_units, n, b.bsum, b.prefix, low_is_unit);
-  note_launch();
-  KF_CUDA(cudaGetLastError());
-  kcount_kernel<<<1, 1, 0, st>>>(b.prefix, n, budget, b.kcount); note_launch();
   KF_CUDA(cudaGetLastError());
   const size_t rsmem = n_units <= RANKS_SMEM_UNITS ? sizeof(int) * size_t(n_units > 0 ? n_units : 1) : 0;
   ranks_kernel<<<grid_cap(n, 256), 256, rsmem, st>>>(src, off, n_units, b.kcount, ranks, low_is_unit);
@@ -597,7 +617,6 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
     keep_mask_kernel<<<grid_cap(n, 256), 256, 0, st>>>(src, b.kcount, keep); note_launch();
     KF_CUDA(cudaGetLastError());
   }
-  finish_kernel<<<1, 1, 0, st>>>(src, b.prefix, n, b.kcount, cut, (long long*)used); note_launch();
   return check_cuda(cudaGetLastError(), "allocation launch");
 }
 

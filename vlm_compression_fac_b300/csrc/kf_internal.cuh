@@ -19,7 +19,7 @@ namespace kf {
 enum : int { ST_CODE = 0, ST_INFO = 1 };
 
 // Wait-site codes reported with KF_ERR_TIMEOUT.
-enum : int { WAIT_TMA_EMPTY = 1, WAIT_TMA_FULL = 2, WAIT_MMA_DONE = 3, WAIT_DRAIN = 4 };
+enum : int { WAIT_TMA_EMPTY = 1, WAIT_TMA_FULL = 2, WAIT_MMA_DONE = 3, WAIT_DRAIN = 4, WAIT_LOOKBACK = 5 };
 
 __device__ __forceinline__ void raise_status(int* st, int code, int info) {
   if (atomicCAS(st + ST_CODE, 0, code) == 0) st[ST_INFO] = info;
