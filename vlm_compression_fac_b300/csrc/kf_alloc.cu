@@ -38,13 +38,16 @@ __device__ __forceinline__ int unit_of(const int64_t* __restrict__ off, int n_un
   }
   return lo;
 }
-// The unit of component g when the 32 lanes of a warp hold consecutive components from gw on:
-// one binary search for gw (lane 0, broadcast), then each lane walks forward over the (short)
-// list of units that start inside the warp's range.  Every lane of the warp must call it.
-__device__ __forceinline__ int warp_unit_of(const int64_t* __restrict__ off, int n_units, int64_t gw, int64_t g) {
-  int u0 = 0;
-  if ((threadIdx.x & 31) == 0) u0 = unit_of(off, n_units, gw);
-  int u = __shfl_sync(0xffffffffu, u0, 0);
+// Every CTA of the key builders takes one contiguous range of components (a multiple of 256
+// long) and walks it in steps of its 256 threads; a thread's unit only moves forward, so
+// after one binary search for its first component each step costs at most a few compares.
+__device__ __forceinline__ void chunk_range(int64_t n, int64_t& beg, int64_t& end) {
+  int64_t chunk = (n + gridDim.x - 1) / gridDim.x;
+  chunk = (chunk + 255) & ~int64_t(255);
+  beg = int64_t(blockIdx.x) * chunk;
+  end = beg + chunk < n ? beg + chunk : n;
+}
+__device__ __forceinline__ int advance_unit(const int64_t* __restrict__ off, int n_units, int u, int64_t g) {
   while (u + 1 < n_units && off[u + 1] <= g) ++u;
   return u;
 }
@@ -55,6 +58,30 @@ __device__ __forceinline__ int warp_unit_of(const int64_t* __restrict__ off, int
 // weight that is negative or not a number counts as 0).  float32, one rounding per operation.
 constexpr int MODE_GIVEN_KEYS = 100;  // internal: the caller's keys, as given
 constexpr int MODE_SWIFT_HYBRID = 101;  // internal: Swift-SVD B hybrid keys built from sigma
+
+// Score word of one component (~bits of its float32 score): the same function builds the
+// sort keys and, for the modes whose keys never increase along a unit, counts each unit's
+// kept prefix after the cut.
+__device__ __forceinline__ unsigned score_word(float s, int u, int mode, const int64_t* __restrict__ cost,
+                                               const float* __restrict__ weight,
+                                               const float* __restrict__ energy) {
+  const float q = __fmul_rn(s, s);
+  float sc;
+  if (mode == MODE_GIVEN_KEYS) {
+    sc = s > 0.f ? s : 0.f;  // a negative or not-a-number key counts as 0
+  } else if (mode == KF_KEY_ENERGY_RATIO) {
+    const float e = energy[u];
+    sc = e > 0.f ? __fdiv_rn(q, e) : 0.f;
+  } else {
+    sc = 0.5f * q;
+    if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
+  }
+  if (weight) {
+    const float w = weight[u];
+    sc = (w > 0.f) ? __fmul_rn(w, sc) : 0.f;  // also maps a NaN weight to 0
+  }
+  return ~__float_as_uint(sc);
+}
 
 // The low word of a key is the component id, or, when no caller needs ids (no keep mask), the
 // unit index: the sort orders by the score word only and is stable, so equal scores stay in
@@ -73,29 +100,16 @@ __global__ void __launch_bounds__(256) build_keys_kernel(const float* __restrict
   for (int i = threadIdx.x; i < 4 * 256; i += blockDim.x) h[i] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
-  for (int64_t g0 = int64_t(blockIdx.x) * blockDim.x; g0 < n; g0 += int64_t(gridDim.x) * blockDim.x) {
+  int64_t beg, end;
+  chunk_range(n, beg, end);
+  int u = beg + threadIdx.x < n ? unit_of(off, n_units, beg + threadIdx.x) : 0;
+  for (int64_t g0 = beg; g0 < end; g0 += blockDim.x) {   // the same trip count for the whole CTA
     const int64_t g = g0 + threadIdx.x;
-    const bool valid = g < n;
-    const int u = warp_unit_of(off, n_units, g0 + (threadIdx.x & ~31), valid ? g : n - 1);
+    const bool valid = g < end;
     unsigned bits = 0;
     if (valid) {
-      const float s = sigma[g];
-      const float q = __fmul_rn(s, s);
-      float sc;
-      if (mode == MODE_GIVEN_KEYS) {
-        sc = s > 0.f ? s : 0.f;  // a negative or not-a-number key counts as 0
-      } else if (mode == KF_KEY_ENERGY_RATIO) {
-        const float e = energy[u];
-        sc = e > 0.f ? __fdiv_rn(q, e) : 0.f;
-      } else {
-        sc = 0.5f * q;
-        if (mode == KF_KEY_PER_PARAM) sc = __fdiv_rn(sc, float(cost[u]));
-      }
-      if (weight) {
-        const float w = weight[u];
-        sc = (w > 0.f) ? __fmul_rn(w, sc) : 0.f;  // also maps a NaN weight to 0
-      }
-      bits = ~__float_as_uint(sc);
+      u = advance_unit(off, n_units, u, g);
+      bits = score_word(sigma[g], u, mode, cost, weight, energy);
       const uint32_t low = low_is_unit ? uint32_t(u) : uint32_t(g);
       keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(low);
     }
@@ -139,10 +153,11 @@ __global__ void swift_eps_kernel(const float* __restrict__ sigma, const int64_t*
 // float32 (beta not positive or not a number: key 0).
 __global__ void swift_keys_kernel(const double* __restrict__ eps, const int64_t* __restrict__ off, int n_units,
                                   int64_t n, const float* __restrict__ beta, double alpha, float* __restrict__ keys) {
-  for (int64_t g0 = int64_t(blockIdx.x) * blockDim.x; g0 < n; g0 += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t g = g0 + threadIdx.x;
-    const int u = warp_unit_of(off, n_units, g0 + (threadIdx.x & ~31u), g < n ? g : n - 1);
-    if (g >= n) continue;
+  int64_t beg, end;
+  chunk_range(n, beg, end);
+  int u = beg + threadIdx.x < n ? unit_of(off, n_units, beg + threadIdx.x) : 0;
+  for (int64_t g = beg + threadIdx.x; g < end; g += blockDim.x) {
+    u = advance_unit(off, n_units, u, g);
     const float b = beta ? beta[u] : 1.f;
     float k = 0.f;
     if (b > 0.f) k = float(pow(double(b), alpha) * pow(log(2.718281828459045 + eps[g]), 1.0 - alpha));
@@ -198,29 +213,42 @@ __global__ void __launch_bounds__(256) digit_base_kernel(const unsigned* __restr
 constexpr unsigned long long LB_OWN = 1ull << 62, LB_INCL = 2ull << 62;
 constexpr unsigned long long LB_VAL = (1ull << 56) - 1;
 __device__ __forceinline__ void lb_store(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.volatile.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long lb_load(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.volatile.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 // Sum of one slot's values over the tiles before `tile` (status word of tile k at
-// st[k * stride]): walks back adding own counts until a tile's inclusive sum is found.  Tiles
-// take their numbers in launch order, so every tile waited on is held by a CTA that is
-// already running; each wait is still bounded by wait_ns (then KF_ERR_TIMEOUT is recorded and
-// the tile counted as empty).
+// st[k * stride]): walks back adding own counts until a tile's inclusive sum is found,
+// reading the words of LB_WIN predecessors at a time.  Tiles take their numbers in launch
+// order, so every tile waited on is held by a CTA that is already running; each wait is
+// still bounded by wait_ns (then KF_ERR_TIMEOUT is recorded and the tile counted as empty).
+constexpr int LB_WIN = 8;
 __device__ unsigned long long lookback(const unsigned long long* st, int64_t stride, int tile,
                                        unsigned long long tag, unsigned long long wait_ns, int* status) {
   unsigned long long acc = 0;
   int k = tile - 1;
   unsigned long long t0 = 0;
   while (k >= 0) {
-    const unsigned long long w = lb_load(st + int64_t(k) * stride);
-    if ((w >> 62) != 0 && (w & (63ull << 56)) == tag) {
-      acc += w & LB_VAL;
-      if ((w >> 62) == 2) break;
-      --k;
+    unsigned long long w[LB_WIN];
+#pragma unroll
+    for (int i = 0; i < LB_WIN; ++i) w[i] = k - i >= 0 ? lb_load(st + int64_t(k - i) * stride) : 0ull;
+    int used = 0;
+    bool found = false;
+#pragma unroll
+    for (int i = 0; i < LB_WIN; ++i) {
+      if (found || used < i || k - i < 0) continue;       // stop at the first gap
+      const bool ready = (w[i] >> 62) != 0 && (w[i] & (63ull << 56)) == tag;
+      if (!ready) continue;
+      acc += w[i] & LB_VAL;
+      used = i + 1;
+      found = (w[i] >> 62) == 2;
+    }
+    if (found) break;
+    if (used > 0) {
+      k -= used;
       t0 = 0;
       continue;
     }
@@ -233,7 +261,7 @@ __device__ unsigned long long lookback(const unsigned long long* st, int64_t str
       t0 = 0;
       continue;
     }
-    __nanosleep(100);
+    __nanosleep(64);
   }
   return acc;
 }
@@ -477,6 +505,53 @@ __global__ void ranks_kernel(const unsigned long long* __restrict__ keys, const 
   }
 }
 
+// ranks[u] for keys that never increase along a unit (the sigma-based keys, sigma being in
+// descending order, and the hybrid keys) without reading the kept keys: the kept components
+// of unit u are its leading ones whose key sorts before the last kept key K* =
+// sorted[kcount - 1] (key order: score word, then unit), plus, in K*'s own unit, the kept
+// ones among the components equal to K* (equal keys of one unit keep their id order, and the
+// first kcount - first(K*) of them are kept).  One thread per unit, a binary search over the
+// unit's score words recomputed by the same function that built the keys.
+__global__ void ranks_search_kernel(const float* __restrict__ x, const int64_t* __restrict__ off,
+                                    const int64_t* __restrict__ cost, int n_units, int mode,
+                                    const float* __restrict__ weight, const float* __restrict__ energy,
+                                    const unsigned long long* __restrict__ sorted, int64_t n,
+                                    const unsigned long long* __restrict__ kcount, int* __restrict__ ranks) {
+  __shared__ unsigned long long kstar_s;
+  __shared__ long long eq_s;
+  if (threadIdx.x == 0) {
+    const int64_t kc = int64_t(*kcount);
+    if (kc == 0) {
+      eq_s = -1;
+    } else {
+      const unsigned long long ks = sorted[kc - 1];
+      int64_t lo = 0, hi = kc - 1;  // first position holding ks
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (sorted[mid] < ks) lo = mid + 1; else hi = mid;
+      }
+      kstar_s = ks;
+      eq_s = kc - lo;
+    }
+  }
+  __syncthreads();
+  const long long eq = eq_s;
+  if (eq < 0) return;  // nothing kept: the ranks were cleared before
+  const unsigned hw = unsigned(kstar_s >> 32);
+  const int us = int(uint32_t(kstar_s));
+  for (int u = blockIdx.x * blockDim.x + threadIdx.x; u < n_units; u += gridDim.x * blockDim.x) {
+    int64_t a = off[u], b = off[u + 1];
+    const int64_t base = a;
+    while (a < b) {   // first component that is not kept by its score word
+      const int64_t mid = (a + b) >> 1;
+      const unsigned wd = score_word(x[mid], u, mode, cost, weight, energy);
+      const bool kept = u < us ? wd <= hw : wd < hw;
+      if (kept) a = mid + 1; else b = mid;
+    }
+    ranks[u] = int(a - base + (u == us ? eq : 0));
+  }
+}
+
 // keep[id] = 1 for the components of the kept prefix (the mask was cleared before).
 __global__ void keep_mask_kernel(const unsigned long long* __restrict__ keys,
                                  const unsigned long long* __restrict__ kcount, unsigned char* __restrict__ keep) {
@@ -608,9 +683,21 @@ kf_status alloc_run(kf_ctx* ctx, const float* sigma, const int64_t* off, const i
                                           b.kcount, cut, (long long*)used, ctx->d_status, WAIT_LIMIT_NS);
   note_launch();
   KF_CUDA(cudaGetLastError());
-  const size_t rsmem = n_units <= RANKS_SMEM_UNITS ? sizeof(int) * size_t(n_units > 0 ? n_units : 1) : 0;
-  ranks_kernel<<<grid_cap(n, 256), 256, rsmem, st>>>(src, off, n_units, b.kcount, ranks, low_is_unit);
-  note_launch();
+  // ranks: by a search per unit where its keys never increase along the unit (the ids are
+  // not needed and the keys come from sigma or from the hybrid score), else by counting
+  // the kept keys
+  const bool monotone = low_is_unit && (mode == KF_KEY_HALF_SIGMA2 || mode == KF_KEY_PER_PARAM ||
+                                        mode == KF_KEY_ENERGY_RATIO || int(mode) == MODE_SWIFT_HYBRID);
+  if (monotone) {
+    const bool hyb = int(mode) == MODE_SWIFT_HYBRID;
+    ranks_search_kernel<<<unsigned((n_units + 255) / 256), 256, 0, st>>>(
+        hyb ? b.aux : sigma, off, cost, n_units, hyb ? MODE_GIVEN_KEYS : int(mode), hyb ? nullptr : weight,
+        hyb ? nullptr : b.energy, src, n, b.kcount, ranks); note_launch();
+  } else {
+    const size_t rsmem = n_units <= RANKS_SMEM_UNITS ? sizeof(int) * size_t(n_units > 0 ? n_units : 1) : 0;
+    ranks_kernel<<<grid_cap(n, 256), 256, rsmem, st>>>(src, off, n_units, b.kcount, ranks, low_is_unit);
+    note_launch();
+  }
   KF_CUDA(cudaGetLastError());
   if (keep) {
     KF_CUDA(cudaMemsetAsync(keep, 0, size_t(n), st));
