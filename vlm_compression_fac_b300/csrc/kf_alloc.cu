@@ -103,27 +103,37 @@ __global__ void __launch_bounds__(256) build_keys_kernel(const float* __restrict
   int64_t beg, end;
   chunk_range(n, beg, end);
   int u = beg + threadIdx.x < n ? unit_of(off, n_units, beg + threadIdx.x) : 0;
-  for (int64_t g0 = beg; g0 < end; g0 += blockDim.x) {   // the same trip count for the whole CTA
-    const int64_t g = g0 + threadIdx.x;
-    const bool valid = g < end;
-    unsigned bits = 0;
-    if (valid) {
-      u = advance_unit(off, n_units, u, g);
-      bits = score_word(sigma[g], u, mode, cost, weight, energy);
-      const uint32_t low = low_is_unit ? uint32_t(u) : uint32_t(g);
-      keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(low);
-    }
-    const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  constexpr int BK_UNROLL = 4;   // components per thread and step, their loads issued together
+  for (int64_t g0 = beg; g0 < end; g0 += BK_UNROLL * 256) {   // the same trip count for the whole CTA
+    float sv[BK_UNROLL];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const unsigned d = (bits >> (8 * b)) & 255u;
-      const unsigned prev = __shfl_up_sync(0xffffffffu, d, 1);
-      const bool head = valid && (lane == 0 || d != prev);
-      const unsigned ends = __ballot_sync(0xffffffffu, head) | ~vmask;  // a run ends at the next head
-      if (head) {
-        const unsigned above = ends & ~((2u << lane) - 1u);
-        const int nxt = above ? __ffs(int(above)) - 1 : 32;
-        atomicAdd(&h[b * 256 + int(d)], unsigned(nxt - lane));
+    for (int i = 0; i < BK_UNROLL; ++i) {
+      const int64_t g = g0 + i * 256 + threadIdx.x;
+      sv[i] = g < end ? sigma[g] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < BK_UNROLL; ++i) {
+      const int64_t g = g0 + i * 256 + threadIdx.x;
+      const bool valid = g < end;
+      unsigned bits = 0;
+      if (valid) {
+        u = advance_unit(off, n_units, u, g);
+        bits = score_word(sv[i], u, mode, cost, weight, energy);
+        const uint32_t low = low_is_unit ? uint32_t(u) : uint32_t(g);
+        keys[g] = (static_cast<unsigned long long>(bits) << 32) | static_cast<unsigned long long>(low);
+      }
+      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const unsigned d = (bits >> (8 * b)) & 255u;
+        const unsigned prev = __shfl_up_sync(0xffffffffu, d, 1);
+        const bool head = valid && (lane == 0 || d != prev);
+        const unsigned ends = __ballot_sync(0xffffffffu, head) | ~vmask;  // a run ends at the next head
+        if (head) {
+          const unsigned above = ends & ~((2u << lane) - 1u);
+          const int nxt = above ? __ffs(int(above)) - 1 : 32;
+          atomicAdd(&h[b * 256 + int(d)], unsigned(nxt - lane));
+        }
       }
     }
   }
@@ -266,11 +276,71 @@ __device__ unsigned long long lookback(const unsigned long long* st, int64_t str
   return acc;
 }
 
+// lookback() for one slot per tile, by a whole warp: lane i reads the word of tile k - i, so
+// 32 predecessors are examined per round trip; the nearest inclusive sum ends the walk when
+// every nearer tile has published.  Every lane returns the same sum.
+__device__ unsigned long long warp_lookback(const unsigned long long* st, int tile, unsigned long long tag,
+                                            unsigned long long wait_ns, int* status, int lane) {
+  unsigned long long acc = 0;
+  int k = tile - 1;
+  unsigned long long t0 = 0;
+  while (k >= 0) {
+    const int kk = k - lane;
+    const unsigned long long w = kk >= 0 ? lb_load(st + kk) : (LB_INCL | tag);  // before tile 0: sum 0
+    const bool ready = (w >> 62) != 0 && (w & (63ull << 56)) == tag;
+    const bool incl = ready && (w >> 62) == 2;
+    const unsigned notready = __ballot_sync(0xffffffffu, !ready);
+    const unsigned inclm = __ballot_sync(0xffffffffu, incl);
+    const int first_gap = notready ? __ffs(int(notready)) - 1 : 32;
+    const int first_incl = inclm ? __ffs(int(inclm)) - 1 : 32;
+    if (first_incl < first_gap) {          // lanes 0 .. first_incl all published: done
+      unsigned long long v = (lane <= first_incl && kk >= 0) ? (w & LB_VAL) : 0ull;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      return acc + v;
+    }
+    if (first_gap > 0) {                   // own counts of lanes 0 .. first_gap - 1, go on
+      unsigned long long v = lane < first_gap ? (w & LB_VAL) : 0ull;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      acc += v;
+      k -= first_gap;
+      t0 = 0;
+      continue;
+    }
+    const unsigned long long now = now_ns();   // the nearest predecessor has not published
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > wait_ns) {
+      if (lane == 0) raise_status(status, KF_ERR_TIMEOUT, WAIT_LOOKBACK);
+      --k;
+      t0 = 0;
+      continue;
+    }
+    __nanosleep(64);
+  }
+  return acc;
+}
+
+// The lanes of the warp holding the same 8-bit digit as this lane (itself included; invalid
+// lanes never count): eight ballots, one per bit of the digit.
+__device__ __forceinline__ unsigned digit_peers(unsigned d, bool valid) {
+  unsigned peers = __ballot_sync(0xffffffffu, valid);
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    const bool bit = (d >> b) & 1u;
+    const unsigned m = __ballot_sync(0xffffffffu, bit);
+    peers &= bit ? m : ~m;
+  }
+  return peers;
+}
+
 // One radix pass over the score word's byte `pass`, one 4096-key tile per CTA (tile number
 // from a counter, in launch order).  Warp w owns the tile's keys w * WK .. w * WK + WK - 1
 // (the warp's round r holds keys w * WK + 32 r + lane), so the tile's index order is (warp,
 // round, lane) order.  All keys are loaded first; phase 1 counts each warp's keys per digit
-// (one counter update per distinct digit of a round, by warp match); the tile's counts are
+// (one counter update per distinct digit of a round, the lanes of equal digits found by
+// ballots over the digit's bits); the tile's counts are
 // published and the counts of the tiles before it summed by look-back (thread d for digit d);
 // phase 2 puts every key at its warp's running position for its digit in the tile's
 // digit-ordered copy in shared memory, plus its rank among the round's equal digits; the copy
@@ -307,8 +377,8 @@ __global__ void __launch_bounds__(RT, 3) onesweep_kernel(const unsigned long lon
 #pragma unroll
   for (int r = 0; r < RI; ++r) {
     const bool valid = w * WK + r * 32 + lane < tile_n;
-    const unsigned d = valid ? unsigned((key[r] >> shift) & 255u) : 256u;
-    peers[r] = __match_any_sync(0xffffffffu, d);
+    const unsigned d = unsigned((key[r] >> shift) & 255u);
+    peers[r] = digit_peers(d, valid);
     if (valid && (peers[r] & lt_mask) == 0u) wpos[w][d] += __popc(peers[r]);
     __syncwarp();
   }
@@ -432,16 +502,15 @@ __global__ void __launch_bounds__(RT) cost_scan_kernel(const unsigned long long*
     total += wsum[ww];
   }
   const long long texcl = pre + x - sum;
-  if (t == 0) {
+  if (w == 0) {   // warp 0: publish, then look back 32 predecessors per round trip
     unsigned long long* mine = lbst + tile;
     const unsigned long long tag = 1ull << 56;
-    lb_store(mine, (tile == 0 ? LB_INCL : LB_OWN) | tag | (unsigned long long)total);
-    long long e = 0;
-    if (tile > 0) {
-      e = (long long)lookback(lbst, 1, tile, tag, wait_ns, status);
-      lb_store(mine, LB_INCL | tag | (unsigned long long)(e + total));
+    if (lane == 0) lb_store(mine, (tile == 0 ? LB_INCL : LB_OWN) | tag | (unsigned long long)total);
+    const long long e = tile > 0 ? (long long)warp_lookback(lbst, tile, tag, wait_ns, status, lane) : 0;
+    if (lane == 0) {
+      if (tile > 0) lb_store(mine, LB_INCL | tag | (unsigned long long)(e + total));
+      excl_s = e;
     }
-    excl_s = e;
   }
   __syncthreads();
   const long long E = excl_s;
