@@ -131,12 +131,14 @@ def cost_tail(m, n):
     return m * n * s + (m ** 3 + n ** 3) / 3.0 + m * m * n + m * n * n
 
 
-# DRAM bytes (read + written, ncu dram__bytes_read.sum + dram__bytes_write.sum) of one
-# jac_apply_tc_kernel launch that runs every task of a step (7 problems of 4096): None until a
-# capture of the current kernel is summarised under profiles/.  The algorithmic bytes of such
-# a launch are 7 x 14 B x 4096^2 = 1.64 GB (C read once on or above the diagonal, written in
-# full; Qt read and written once); later launches skip tasks whose pairs all converged.
-JAC_APPLY_TRAFFIC = None
+# DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) of one jac_apply_tc_kernel
+# launch in which every task ran (7 problems of 4096, the 16384-token case, whose Jacobi shapes
+# are those of every N): 728,819,968 read + 908,009,984 written, against 1,651,507,200
+# algorithmic bytes for such a launch (per problem 528 C super-tiles: 64 KB read, 128 KB or
+# on the diagonal 64 KB written; 2048 Qt half-panels: 32 KB read + 32 KB written).  Traffic
+# grows with the tasks a launch runs, so the bench reports it per average launch as this
+# ratio times the launch's algorithmic bytes.
+JAC_APPLY_DRAM_PER_ALG_BYTE = (728819968 + 908009984) / 1651507200
 
 
 # ALGORITHMIC bytes per component of one score_and_allocate call (a model of the minimum
@@ -544,7 +546,7 @@ def run_kfsvd(args):
             "launches_per_step": apply_launches // K_,
             "avg_launch_ms": round(apply_ms / max(apply_launches, 1), 4),
             "algorithmic_bytes_per_step": round(jac_bytes / K_),
-            "traffic": JAC_APPLY_TRAFFIC,
+            "traffic": round(JAC_APPLY_DRAM_PER_ALG_BYTE * jac_bytes / max(apply_launches, 1)),
             "tensor_tflops_executed": round(apply_tf, 2),
             "tensor_frac_of_bf16_burst": round(apply_tf / bf16_burst, 4),
             "peak_kind": "HBM copy, of measured; algorithmic bytes = C and Qt read and written once per executed "
