@@ -562,6 +562,40 @@ __device__ __forceinline__ bool next_tc_task(int& g, int total, int per_u, int n
 // Issues the global loads of a task's float32 operand into R (16 float4 per thread): a
 // super-tile's S = C[rows of P][cols of Q] (warp w rows w + 8 i, lane l columns 4 l ..), or a
 // panel's two 128-column halves (rows w + 8 i of the pair, columns 4 l .. of each half).
+// The rows of task t into R[lo .. hi) only (the registers freed so far).
+__device__ __forceinline__ void load_tc_task_part(const TcTask& t, float4* R, const float* __restrict__ Call,
+                                                  const float* __restrict__ Qtall, int64_t sp, int nblk, int step,
+                                                  int warp, int lane, int lo, int hi) {
+  if (t.kind == 0) {
+    const float* C = Call + int64_t(t.u) * sp * sp;
+    const int cl = 4 * lane, qp = 2 * t.Q + (cl >> 6);
+    const int64_t gcol = int64_t(((cl >> 5) & 1) ? rr_pos(nblk - 1 - qp, step, nblk) : rr_pos(qp, step, nblk)) * JB +
+                         (cl & 31);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < lo || i >= hi) continue;
+      const int r = warp + 8 * i, pp = 2 * t.P + (r >> 6);
+      const int64_t grow = int64_t(((r >> 5) & 1) ? rr_pos(nblk - 1 - pp, step, nblk) : rr_pos(pp, step, nblk)) * JB +
+                           (r & 31);
+      R[i] = *reinterpret_cast<const float4*>(C + grow * sp + gcol);
+    }
+  } else {
+    const float* Qt = Qtall + int64_t(t.u) * sp * sp;
+    const int b0 = rr_pos(t.q, step, nblk), b1 = rr_pos(nblk - 1 - t.q, step, nblk);
+    const int64_t col0 = int64_t(t.cb) * 256;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (col0 + 128 * h < sp) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (8 * h + i < lo || 8 * h + i >= hi) continue;
+          const int r = warp + 8 * i;
+          R[8 * h + i] = *reinterpret_cast<const float4*>(Qt + gidx(r, b0, b1) * sp + col0 + 128 * h + 4 * lane);
+        }
+      }
+    }
+  }
+}
 __device__ __forceinline__ void load_tc_task(const TcTask& t, float4* R, const float* __restrict__ Call,
                                              const float* __restrict__ Qtall, int64_t sp, int nblk, int step,
                                              int warp, int lane) {
@@ -672,23 +706,24 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
         qb[i][0] = rr_pos(qr[i], step, nblk); qb[i][1] = rr_pos(nblk - 1 - qr[i], step, nblk);
       }
       const int cl = 4 * lane;
-      // step 1a: U[:, 0:64] = S[:, q pair 0] V_q0   (lanes 0..15 hold those columns)
+      have2 = next_tc_task(g2, total, per_u, nsup, nsp, npairs, skipall, conv, nxt);
+      // step 1a: U[:, 0:64] = S[:, q pair 0] V_q0   (lanes 0..15 hold those columns); their
+      // registers are then free and start fetching the next task's rows at once
       if (lane < 16) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl), R[i]);
+        if (have2) load_tc_task(nxt, R, Call, Qtall, sp, nblk, step, warp, lane);
       }
       cp_async_wait<0>();
       if (!mma_phase(c, a_img, false, v0, 0, tid)) break;
       copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, u, npairs, pr[0]), tid);  // during step 1b
-      // step 1b: U[:, 64:128] = S[:, q pair 1] V_q1
+      // step 1b: U[:, 64:128] = S[:, q pair 1] V_q1 (lanes 16..31), then their next rows
       if (lane >= 16) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) put4(Abuf, akm_off(warp + 8 * i, cl - 64), R[i]);
+        if (have2) load_tc_task(nxt, R, Call, Qtall, sp, nblk, step, warp, lane);
       }
       if (!mma_phase(c, a_img, false, v1, 64, tid)) break;
-      // R is free: the next task's rows load during steps 2a, 2b and the stores
-      have2 = next_tc_task(g2, total, per_u, nsup, nsp, npairs, skipall, conv, nxt);
-      if (have2) load_tc_task(nxt, R, Call, Qtall, sp, nblk, step, warp, lane);
       copy_vimg_async(Vb1, vimg_src(Vimg, Iimg, skipall, u, npairs, pr[1]), tid);  // during step 2a
       // step 2: D_p = U_p^T V_p for p pair 0 (U rows 0..63) and 1 (rows 64..127): the threads of
       // TMEM lanes of rows of p write U_p^T (M = U column, K = row within p) as MN-major planes
@@ -761,17 +796,19 @@ __global__ void __launch_bounds__(256, 2) jac_apply_tc_kernel(
       const int64_t col0 = int64_t(cur.cb) * 256;
       const int halves = col0 + 128 < sp ? 2 : 1;     // uniform over the CTA
       bool fine = true;
+      have2 = next_tc_task(g2, total, per_u, nsup, nsp, npairs, skipall, conv, nxt);
       for (int h = 0; h < halves && fine; ++h) {
         // A = half^T (M = column of the half, K = row of the pair), MN-major
 #pragma unroll
         for (int i = 0; i < 8; ++i) put4(Abuf, amn_off(4 * lane, warp + 8 * i), R[8 * h + i]);
+        // the registers of this half (of both halves after the last one) fetch the next task
+        if (have2) load_tc_task_part(nxt, R, Call, Qtall, sp, nblk, step, warp, lane, 8 * h,
+                                     h + 1 == halves ? 16 : 8 * h + 8);
         cp_async_wait<0>();
         fine = mma_phase(c, a_img, true, v0, 64 * h, tid);
       }
       if (!fine) break;
-      have2 = next_tc_task(g2, total, per_u, nsup, nsp, npairs, skipall, conv, nxt);
       if (have2) {
-        load_tc_task(nxt, R, Call, Qtall, sp, nblk, step, warp, lane);
         if (nxt.kind == 0) {
           copy_vimg_async(Vb0, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, 2 * nxt.Q), tid);
           copy_vimg_async(Vb1, vimg_src(Vimg, Iimg, skipall, nxt.u, npairs, 2 * nxt.Q + 1), tid);
