@@ -679,9 +679,9 @@ size_t alloc_carve(Carve& cv, int64_t n, int64_t n_energy, AllocBufs& b) {
   b.lbst2 = cv.take<unsigned long long>(size_t(nt));
   b.ghist = cv.take<unsigned>(4 * 256);
   b.ctr = cv.take<unsigned>(8);
-  b.clear1 = reinterpret_cast<unsigned char*>(b.ctr + 8);
+  b.kcount = cv.take<unsigned long long>(1);   // cleared too: 0 unless the cost scan sets it
+  b.clear1 = reinterpret_cast<unsigned char*>(b.kcount + 1);
   b.gbase = cv.take<unsigned>(4 * 256);
-  b.kcount = cv.take<unsigned long long>(1);
   b.aux = cv.take<float>(n > 0 ? n : 1);
   b.energy = n_energy > 0 ? cv.take<float>(n_energy) : nullptr;
   return cv.off;
