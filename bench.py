@@ -620,6 +620,9 @@ def run_kfsvd(args):
 
 
 # ------------------------------------------------------------- oracle arm
+_SAMPLE_WEIGHTS = {}
+
+
 def oracle_sample(wl, sample_tokens=1024, tail_unit="q"):
     """fp64 oracle on a bounded sample of the workload, extrapolated to one full step:
     covariance sums of `sample_tokens` rows of every site (scaled by N / sample_tokens) plus
@@ -643,7 +646,10 @@ def oracle_sample(wl, sample_tokens=1024, tail_unit="q"):
     t_gen = time.perf_counter() - t1
     X = O.finalize_covariance(O.covariance_sum(Ax), 256, wl.lam)
     G = O.finalize_covariance(O.covariance_sum(Ag), 256, wl.lam)
-    W = recipes.gen_weight(wl, u).astype(np.float64)
+    key = (wl.name, u.name)
+    if key not in _SAMPLE_WEIGHTS:   # input generation, outside the timed tail: made once per run
+        _SAMPLE_WEIGHTS[key] = recipes.gen_weight(wl, u).astype(np.float64)
+    W = _SAMPLE_WEIGHTS[key]
     t2 = time.perf_counter()
     Sx, Sg = O.cholesky_factors(X, G)
     Wt = O.whiten(W, Sx, Sg)
