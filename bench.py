@@ -146,6 +146,11 @@ JAC_APPLY_DRAM_PER_ALG_BYTE = (728819968 + 908009984) / 1651507200
 # passes over the score word, each reading and writing the 8-byte key (4 x 16); one read of
 # the sorted keys for the cost prefix and the cut (8).
 ALLOC_BYTES_PER_KEY = 12 + 4 * 16 + 8
+# Measured DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum over every kernel of one
+# call) per component on a 2^24-component call in units of 4096: 766,178,304 read + 437,207,040
+# written.  Below the algorithmic 84 at that size because part of the written keys end in L2
+# (126 MB) before the call finishes; the reads alone are 45.7 B per component.
+ALLOC_DRAM_BYTES_PER_KEY_2E24 = round((766178304 + 437207040) / (1 << 24), 1)
 
 
 def alloc_scaled(ctx, torch, K, hbm_peak, log2n=28, unit_len=1 << 17, reps=5):
@@ -185,7 +190,9 @@ def alloc_scaled(ctx, torch, K, hbm_peak, log2n=28, unit_len=1 << 17, reps=5):
     torch.cuda.empty_cache()
     return {"bound": "hbm", "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(gbs / hbm_peak, 4), "ms": round(ms, 3), "components": n, "units": n_units,
-            "kept": kept, "algorithmic_bytes_per_key": ALLOC_BYTES_PER_KEY, "peak_kind": "HBM copy, of measured"}
+            "kept": kept, "algorithmic_bytes_per_key": ALLOC_BYTES_PER_KEY,
+            "dram_bytes_per_key_measured_at_2e24": ALLOC_DRAM_BYTES_PER_KEY_2E24,
+            "peak_kind": "HBM copy, of measured"}
 
 
 def fp32_peak_probe(ctx, torch, K, iters=1 << 19):
